@@ -1,0 +1,341 @@
+"""Pins for the CPU oracle, against facts that do not come from the oracle.
+
+Each ``check_*`` helper takes the oracle routine under test as an argument so
+that ``test_oracle_mutations.py`` can hand it a deliberately broken copy and
+show that the pin notices.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from sharded_gemm_gb300 import synth
+
+RNG = np.random.default_rng(1234)
+
+
+# ------------------------------------------------------------------ products
+def check_linear_vs_numpy(linear):
+    for (T, K, O) in [(1, 1, 1), (3, 5, 7), (17, 64, 33), (64, 130, 96)]:
+        x = RNG.standard_normal((T, K))
+        w = RNG.standard_normal((O, K))
+        b = RNG.standard_normal(O)
+        ref = np.matmul(x, w.T) + b
+        got = linear(x, w, b)
+        assert got.shape == (T, O)
+        err = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+        assert err <= 1e-12, err
+
+
+def check_matmul_vs_numpy(matmul):
+    for (M, K, N) in [(1, 1, 1), (5, 3, 7), (33, 64, 17), (40, 96, 72)]:
+        X = RNG.standard_normal((M, K))
+        A = RNG.standard_normal((K, N))
+        ref = np.matmul(X, A)
+        got = matmul(X, A)
+        assert got.shape == (M, N)
+        assert np.linalg.norm(got - ref) <= 1e-12 * np.linalg.norm(ref)
+
+
+def test_linear_vs_numpy():
+    check_linear_vs_numpy(oracle.linear)
+
+
+def test_matmul_vs_numpy():
+    check_matmul_vs_numpy(oracle.matmul)
+
+
+def test_linear_small_integers_exact():
+    # Integer-valued operands: every product and partial sum is exact in fp64,
+    # so the result must equal the integer dot products bit for bit.
+    x = np.array([[1, 2, 3], [4, 5, 6]], dtype=np.float64)
+    w = np.array([[1, 0, -1], [2, 1, 0]], dtype=np.float64)
+    b = np.array([10, -10], dtype=np.float64)
+    y = oracle.linear(x, w, b)
+    assert np.array_equal(y, np.array([[1 - 3 + 10, 2 + 2 - 10], [4 - 6 + 10, 8 + 5 - 10]]))
+
+
+# ------------------------------------------------------------------ slicing
+def closed_form_rows(O, S, N, r):
+    """Global row of local row i of shard r: (i // w)*(O/S) + r*w + (i % w)."""
+    w = O // (S * N)
+    return [(i // w) * (O // S) + r * w + (i % w) for i in range(O // N)]
+
+
+def check_shard_closed_form(shard):
+    for (O, C, S, N) in [(8, 3, 1, 2), (12, 2, 3, 2), (24, 5, 3, 4), (16, 1, 2, 8), (6, 4, 1, 1)]:
+        w = RNG.integers(0, 2**16, size=(O, C), dtype=np.uint16)
+        parts = shard(w, 0, S, N)
+        assert len(parts) == N
+        for r in range(N):
+            assert parts[r].dtype == w.dtype
+            assert np.array_equal(parts[r], w[closed_form_rows(O, S, N, r)])
+        # axis -1: the same rule on columns
+        wt = np.ascontiguousarray(w.T)
+        parts = shard(wt, -1, S, N)
+        for r in range(N):
+            assert np.array_equal(parts[r], wt[:, closed_form_rows(O, S, N, r)])
+
+
+def test_shard_closed_form():
+    check_shard_closed_form(oracle.shard)
+
+
+def test_shard_fused_qkv_by_hand():
+    # A fused [Q; K; V] weight with 4 rows each, N = 2: rank 0 holds rows
+    # 0-1 of Q, K and V; rank 1 rows 2-3 of each (segments=3 slicing).
+    w = np.arange(12, dtype=np.uint32)[:, None] * np.uint32(10) + np.arange(2, dtype=np.uint32)
+    p = oracle.shard(w, 0, 3, 2)
+    assert p[0][:, 0].tolist() == [0, 10, 40, 50, 80, 90]
+    assert p[1][:, 0].tolist() == [20, 30, 60, 70, 100, 110]
+
+
+def test_shard_concat_identity():
+    for dt in (np.uint16, np.uint32, np.float32, np.float16):
+        w = RNG.standard_normal((24, 16)).astype(dt) if dt in (np.float32, np.float16) else \
+            RNG.integers(0, 1000, size=(24, 16)).astype(dt)
+        for N in (1, 2, 4, 8):
+            assert np.array_equal(np.concatenate(oracle.shard(w, 0, 1, N), axis=0), w)
+            assert np.array_equal(np.concatenate(oracle.shard(w, 1, 1, N), axis=1), w)
+
+
+def test_shard_bruteforce_tiny():
+    # Every element lands in exactly one shard; within a shard, order follows
+    # (segment, position) of the original.
+    for (L, S, N) in [(4, 1, 2), (6, 3, 2), (12, 2, 3), (8, 2, 2)]:
+        w = np.arange(L, dtype=np.int64)
+        parts = oracle.shard(w, 0, S, N)
+        seen = sorted(v for p in parts for v in p.tolist())
+        assert seen == list(range(L))
+        seg = L // S
+        for r, p in enumerate(parts):
+            for v in p.tolist():
+                assert (v % seg) // (seg // N) == r
+            assert p.tolist() == sorted(p.tolist())
+
+
+def test_shard_not_divisible_raises():
+    with pytest.raises(ValueError):
+        oracle.shard(np.zeros((10, 4)), 0, 3, 2)
+    with pytest.raises(ValueError):
+        oracle.shard(np.zeros((4, 10)), -1, 1, 4)
+
+
+def test_worked_example_shapes(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "worked_example.json")))
+    N = g["N"]
+    cfg = synth.worked()
+    x = oracle.widen(cfg["x"], "f32")
+    assert list(x.shape) == g["x_shape"]
+    w1 = oracle.shard(cfg["w1"], 0, 1, N)
+    b1 = oracle.shard(cfg["b1"], 0, 1, N)
+    assert all(list(p.shape) == g["all_to_sharded"]["weight_slice_shape"] for p in w1)
+    y1 = oracle.all_to_sharded(x, [oracle.widen(p, "f32") for p in w1], [oracle.widen(p, "f32") for p in b1])
+    assert all(list(y.shape) == g["all_to_sharded"]["per_rank_output_shape"] for y in y1)
+    w2 = oracle.shard(cfg["w2"], -1, 1, N)
+    assert all(list(p.shape) == g["sharded_to_all"]["weight_slice_shape"] for p in w2)
+    partials = [oracle.linear(y1[r], oracle.widen(w2[r], "f32")) for r in range(N)]
+    assert all(list(p.shape) == g["sharded_to_all"]["per_rank_partial_shape"] for p in partials)
+    y2 = oracle.sharded_to_all(y1, [oracle.widen(p, "f32") for p in w2], oracle.widen(cfg["b2"], "f32"))
+    assert list(y2.shape) == g["sharded_to_all"]["output_shape"]
+    # and the chain equals the unsharded two-layer model
+    full = oracle.linear(oracle.linear(x, oracle.widen(cfg["w1"], "f32"), oracle.widen(cfg["b1"], "f32")),
+                         oracle.widen(cfg["w2"], "f32"), oracle.widen(cfg["b2"], "f32"))
+    assert np.allclose(y2, full, rtol=0, atol=1e-14)
+
+
+def test_divisibility_message(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "worked_example.json")))["divisibility_error"]
+    with pytest.raises(ValueError) as e:
+        oracle.check_all_to_sharded_dims(g["output_dims"], g["N"])
+    assert str(e.value) == g["message"]
+    oracle.check_all_to_sharded_dims(4096, 8)
+
+
+# ------------------------------------------------------------------ invariants
+def check_col_invariant(all_to_sharded, shard):
+    for (T, K, O, S, N) in [(5, 8, 12, 1, 2), (3, 16, 24, 3, 4), (7, 9, 16, 1, 8)]:
+        x = RNG.standard_normal((T, K))
+        w = RNG.standard_normal((O, K))
+        b = RNG.standard_normal(O)
+        full = np.matmul(x, w.T) + b
+        ys = all_to_sharded(x, shard(w, 0, S, N), shard(b, 0, S, N))
+        for r in range(N):
+            ref = full[:, closed_form_rows(O, S, N, r)]
+            assert np.abs(ys[r] - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
+def check_row_invariant(sharded_to_all, shard):
+    for (T, K, O, N) in [(5, 8, 6, 2), (3, 64, 10, 4), (9, 24, 7, 8), (2, 3, 2, 1)]:
+        x = RNG.standard_normal((T, K))
+        w = RNG.standard_normal((O, K))
+        b = RNG.standard_normal(O)
+        full = np.matmul(x, w.T) + b
+        y = sharded_to_all(shard(x, -1, 1, N), shard(w, -1, 1, N), b)
+        assert np.abs(y - full).max() <= 1e-12 * (1 + np.abs(full).max())
+
+
+def test_col_equals_unsharded():
+    check_col_invariant(oracle.all_to_sharded, oracle.shard)
+
+
+def test_row_equals_unsharded():
+    check_row_invariant(oracle.sharded_to_all, oracle.shard)
+
+
+def test_row_bias_added_once_after_sum():
+    # With zero inputs the partials vanish; the output must be exactly b
+    # (an implementation adding b per shard would give N*b).
+    N = 4
+    x = np.zeros((3, 8))
+    w = RNG.standard_normal((5, 8))
+    b = RNG.standard_normal(5)
+    y = oracle.sharded_to_all(oracle.shard(x, -1, 1, N), oracle.shard(w, -1, 1, N), b)
+    assert np.array_equal(y, np.broadcast_to(b, (3, 5)))
+
+
+def test_pair_equals_unsharded_mlp_small():
+    # Column -> row pair with the intermediate kept sharded (MLX page section 4).
+    T, D, F, N = 6, 16, 24, 4
+    x = RNG.standard_normal((T, D))
+    w1, b1 = RNG.standard_normal((F, D)), RNG.standard_normal(F)
+    w2, b2 = RNG.standard_normal((D, F)), RNG.standard_normal(D)
+    mid = oracle.all_to_sharded(x, oracle.shard(w1, 0, 1, N), oracle.shard(b1, 0, 1, N))
+    y = oracle.sharded_to_all(mid, oracle.shard(w2, -1, 1, N), b2)
+    ref = np.matmul(np.matmul(x, w1.T) + b1, w2.T) + b2
+    assert np.abs(y - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
+# ------------------------------------------------------------------ SUMMA
+def check_summa_q2_identity(summa):
+    # Equations (1) + (2) of the SUMMA page, written out block by block.
+    X = RNG.standard_normal((8, 6))
+    A = RNG.standard_normal((6, 10))
+    Xb, Ab = oracle.blocks(X, 2), oracle.blocks(A, 2)
+    X00, X01, X10, X11 = Xb
+    A00, A01, A10, A11 = Ab
+    expect = [X00 @ A00 + X01 @ A10, X00 @ A01 + X01 @ A11,
+              X10 @ A00 + X11 @ A10, X10 @ A01 + X11 @ A11]
+    got = summa(Xb, Ab, 2)
+    for e, g in zip(expect, got):
+        assert g.shape == e.shape
+        assert np.abs(g - e).max() <= 1e-12 * (1 + np.abs(e).max())
+
+
+def test_summa_q2_identity():
+    check_summa_q2_identity(oracle.summa)
+
+
+def test_summa_q1_is_matmul():
+    X = RNG.standard_normal((7, 5))
+    A = RNG.standard_normal((5, 3))
+    (Y,) = oracle.summa([X], [A], 1)
+    assert np.abs(Y - X @ A).max() <= 1e-12 * np.abs(X @ A).max()
+
+
+def test_summa_identity_x_gives_a_exactly():
+    for q in (1, 2, 4):
+        n = 8 * q
+        X = np.eye(n)
+        A = RNG.standard_normal((n, n))
+        Y = oracle.unblock(oracle.summa(oracle.blocks(X, q), oracle.blocks(A, q), q), q)
+        assert np.array_equal(Y, A)
+
+
+def test_summa_vs_numpy_q4():
+    X = RNG.standard_normal((16, 12))
+    A = RNG.standard_normal((12, 20))
+    Y = oracle.unblock(oracle.summa(oracle.blocks(X, 4), oracle.blocks(A, 4), 4), 4)
+    assert np.abs(Y - X @ A).max() <= 1e-12 * np.abs(X @ A).max()
+
+
+# ------------------------------------------------------------------ 4-bit affine
+def test_pack_order_by_hand():
+    codes = np.array([[1, 2, 3, 4, 5, 6, 7, 8, 15, 0, 0, 0, 0, 0, 0, 9]], dtype=np.uint8)
+    words = oracle.pack_codes(codes)
+    assert words.tolist() == [[0x87654321, 0x9000000F]]
+    assert np.array_equal(oracle.unpack_codes(words, 16), codes)
+
+
+def check_dequant_bruteforce(dequant):
+    rows, K, g = 3, 16, 8
+    packed = RNG.integers(0, 2**32, size=(rows, K // 8), dtype=np.uint64).astype(np.uint32)
+    s = RNG.uniform(0.01, 0.1, size=(rows, K // g)).astype(np.float16)
+    b = RNG.uniform(-0.5, 0.5, size=(rows, K // g)).astype(np.float16)
+    got = dequant(packed, s, b, g)
+    for o in range(rows):
+        for k in range(K):
+            code = (int(packed[o, k // 8]) >> (4 * (k % 8))) & 15
+            want = float(s[o, k // g]) * code + float(b[o, k // g])
+            assert got[o, k] == want
+
+
+def test_dequant_bruteforce():
+    check_dequant_bruteforce(oracle.dequant_affine4)
+
+
+def test_q4_constant_codes_closed_form():
+    # All codes c: y[t, o] = sum_g (s[o,g] c + b[o,g]) * sum_{k in g} x[t, k].
+    T, O, K, g, c = 3, 4, 128, 64, 11
+    packed = np.full((O, K // 8), 0x11111111 * c, dtype=np.uint32)
+    s = RNG.uniform(0.01, 0.1, size=(O, K // g)).astype(np.float16)
+    b = RNG.uniform(-0.5, 0.5, size=(O, K // g)).astype(np.float16)
+    x = RNG.standard_normal((T, K))
+    y = oracle.q4_all_to_sharded(x, [packed], [s], [b], g)[0]
+    xs = x.reshape(T, K // g, g).sum(axis=2)
+    ref = xs @ (s.astype(np.float64) * c + b.astype(np.float64)).T
+    assert np.abs(y - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
+def test_quantize_recovers_exact_grid():
+    # w = b + s*code with s, b exact in fp16 and codes spanning 0..15:
+    # the quantizer must return those codes, that s and that b.
+    s, b = np.float16(0.015625), np.float16(-0.25)
+    codes = RNG.integers(0, 16, size=(2, 64)).astype(np.uint8)
+    codes[:, 0], codes[:, 1] = 0, 15
+    w = (np.float32(b) + np.float32(s) * codes.astype(np.float32)).astype(np.float32)
+    packed, sq, bq = oracle.quantize_affine4(w, 64)
+    assert np.all(sq == s) and np.all(bq == b)
+    assert np.array_equal(oracle.unpack_codes(packed, 64), codes)
+
+
+def test_quantize_roundtrip_bound():
+    w = (RNG.standard_normal((16, 256)) * 0.02).astype(np.float32)
+    packed, s, b = oracle.quantize_affine4(w, 64)
+    what = oracle.dequant_affine4(packed, s, b, 64)
+    sg = np.repeat(s.astype(np.float64), 64, axis=1)
+    mn = np.repeat(w.reshape(16, 4, 64).min(axis=2).astype(np.float64), 64, axis=1)
+    bound = 0.5 * sg + np.abs(np.repeat(b.astype(np.float64), 64, axis=1) - mn) + 1e-6 * np.abs(w)
+    assert np.all(np.abs(what - w) <= bound)
+
+
+def test_quantize_constant_group_uses_unit_scale():
+    w = np.full((1, 64), 0.5, dtype=np.float32)
+    packed, s, b = oracle.quantize_affine4(w, 64)
+    assert float(s[0, 0]) == 1.0 and float(b[0, 0]) == 0.5
+    assert np.all(oracle.unpack_codes(packed, 64) == 0)
+
+
+def test_q4_row_equals_dequant_unsharded():
+    T, O, K, N, g = 2, 6, 512, 4, 64
+    w = (RNG.standard_normal((O, K)) * 0.02).astype(np.float32)
+    x = RNG.standard_normal((T, K))
+    packed, s, b = oracle.quantize_affine4(w, g)
+    what = oracle.dequant_affine4(packed, s, b, g)
+    ref = x @ what.T
+    y = oracle.q4_sharded_to_all(oracle.shard(x, -1, 1, N), oracle.shard(packed, -1, 1, N),
+                                 oracle.shard(s, -1, 1, N), oracle.shard(b, -1, 1, N), g)
+    assert np.abs(y - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
+def test_bf16_widen_exact():
+    bits = np.array([0x3F80, 0xBF80, 0x4049, 0x0000, 0x7F7F], dtype=np.uint16)
+    want = [1.0, -1.0, 3.140625, 0.0, 3.3895313892515355e38]
+    assert oracle.bf16_to_f64(bits).tolist() == want
+
+
+def test_num_threads_positive():
+    assert oracle.num_threads() >= 1

@@ -1,0 +1,72 @@
+"""Plant a mistake in a copy of an oracle routine (on the CPU) and show that
+the corresponding pin in ``test_oracle.py`` fails.  This is evidence that the
+pins can tell a right oracle from a plausible wrong one."""
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle as T
+
+
+def _expect_fail(check, *fns):
+    with pytest.raises(AssertionError):
+        check(*fns)
+
+
+def test_mutation_transposed_operand():
+    # x @ W instead of x @ W.T (only square shapes survive; others must fail)
+    def bad_linear(x, w, b=None):
+        if w.shape[0] != w.shape[1]:
+            return np.zeros((x.shape[0], w.shape[0]))
+        y = x @ w
+        return y if b is None else y + b
+    _expect_fail(T.check_linear_vs_numpy, bad_linear)
+
+
+def test_mutation_dropped_bias():
+    _expect_fail(T.check_linear_vs_numpy, lambda x, w, b=None: oracle.linear(x, w))
+
+
+def test_mutation_shard_wrong_rank():
+    def bad_shard(w, axis, s, n):
+        p = oracle.shard(w, axis, s, n)
+        return p[1:] + p[:1]
+    _expect_fail(T.check_shard_closed_form, bad_shard)
+
+
+def test_mutation_shard_ignores_segments():
+    _expect_fail(T.check_shard_closed_form, lambda w, a, s, n: oracle.shard(w, a, 1, n))
+
+
+def test_mutation_row_bias_per_shard():
+    def bad_row(xs, ws, b=None):
+        tot = sum(oracle.linear(x, w, b) for x, w in zip(xs, ws))
+        return tot
+    _expect_fail(T.check_row_invariant, bad_row, oracle.shard)
+
+
+def test_mutation_col_wrong_index():
+    def bad_col(x, ws, bs=None):
+        return [oracle.linear(x, ws[0], bs[0]) for _ in ws]
+    _expect_fail(T.check_col_invariant, bad_col, oracle.shard)
+
+
+def test_mutation_summa_wrong_block():
+    def bad_summa(Xb, Ab, q):
+        out = []
+        for i in range(q):
+            for j in range(q):
+                out.append(sum(oracle.matmul(Xb[i * q + t], Ab[j * q + t]) for t in range(q)))
+        return out
+    _expect_fail(T.check_summa_q2_identity, bad_summa)
+
+
+def test_mutation_dequant_nibble_order():
+    def bad_dequant(packed, s, b, g):
+        k = s.shape[1] * g
+        codes = np.empty((packed.shape[0], k))
+        for e in range(8):
+            codes[:, e::8] = (packed >> np.uint32(4 * (7 - e))) & 15
+        gi = np.arange(k) // g
+        return s.astype(np.float64)[:, gi] * codes + b.astype(np.float64)[:, gi]
+    _expect_fail(T.check_dequant_bruteforce, bad_dequant)
