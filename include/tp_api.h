@@ -1,0 +1,243 @@
+/*
+ * tp_api.h -- C ABI of the sharded-GEMM library (libtp.so) for one GB300.
+ *
+ * The library runs the sharded matrix multiplies behind tensor-parallel
+ * linear layers.  The N logical shards (the ranks of a tensor-parallel group)
+ * are N separate device buffers on ONE GPU, so the cross-shard reduction of a
+ * row-parallel layer is a fixed-order in-GPU sum, not a collective.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Linear weights are (out, in) row-major and a layer computes
+ *    y = x @ W^T + b ("MLX tensor parallelism guide", section 2.1/2.2).
+ *    SUMMA computes Y = X A with A laid out (K, N) ("ColossalAI 2D tensor
+ *    parallel via SUMMA", SUMMA section).  All matrices are row-major; a
+ *    leading dimension (ld*) is the distance in ELEMENTS between rows.
+ *  - Data pointers are DEVICE pointers owned by the caller; the library never
+ *    frees or keeps them.  Arrays of per-shard pointers (w[r], y[r], ...)
+ *    live in HOST memory and are read during the call only.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and is asynchronous: the call returns before the GPU finishes.
+ *  - Return value: TP_OK (0) or a negative tp_status.  Argument errors are
+ *    detected on the host before anything is launched; on error nothing is
+ *    launched and tp_last_error() returns a message for the calling thread.
+ *  - Bias vectors are float32.  Accumulation is float32 everywhere.
+ *  - The device-side waits of the kernels are bounded; a wait that runs out
+ *    makes the kernel record TP_ERR_TIMEOUT in a device status word and
+ *    return.  tp_query_status() reads (and clears) that word.
+ *  - The library allocates one 4-byte device status word per device on
+ *    first use and caches host-side TMA descriptors; tp_shutdown() frees
+ *    them.  Nothing else is allocated.
+ */
+#ifndef TP_API_H
+#define TP_API_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TP_OK = 0,
+    TP_ERR_INVALID_ARG = -1,   /* null pointer, bad enum, negative size ...   */
+    TP_ERR_NOT_DIVISIBLE = -2, /* a dimension does not split evenly            */
+    TP_ERR_ALIGNMENT = -3,     /* pointer / leading dimension misaligned       */
+    TP_ERR_UNSUPPORTED = -4,   /* valid request this build does not implement  */
+    TP_ERR_CUDA = -5,          /* a CUDA runtime/driver call failed            */
+    TP_ERR_TIMEOUT = -6        /* a bounded device-side wait ran out           */
+} tp_status;
+
+typedef enum { TP_F32 = 0, TP_BF16 = 1, TP_F16 = 2 } tp_dtype;
+
+/* Kernel selection policy (tp_set_policy). */
+typedef enum {
+    TP_POLICY_AUTO = 0, /* tensor-core (tcgen05) kernels where they apply      */
+    TP_POLICY_SIMT = 1  /* plain CUDA-core kernels only (slow cross-check)      */
+} tp_policy;
+
+typedef void *tp_stream_t; /* a cudaStream_t */
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tp_version(void);
+
+/* Message describing the last error returned to the calling thread ("" if none). */
+const char *tp_last_error(void);
+
+/* Synchronizes `stream`, copies the current device's status word into
+ * *device_status (0 = no error, else a tp_status such as TP_ERR_TIMEOUT)
+ * and resets the word to 0.  Returns TP_OK or TP_ERR_CUDA. */
+int tp_query_status(tp_stream_t stream, int *device_status);
+
+/* Selects the kernel family for the calling process (default AUTO).  The SIMT
+ * policy exists to cross-check the tensor-core kernels; it is slow. */
+int tp_set_policy(int policy);
+
+/* Limit, in nanoseconds, of every bounded device-side wait (default 2e9).
+ * Values below 1e6 or above 6e10 are rejected with TP_ERR_INVALID_ARG. */
+int tp_set_wait_limit_ns(int64_t limit_ns);
+
+/* Frees the per-device status words and cached descriptors. */
+int tp_shutdown(void);
+
+/*
+ * a1 -- weight sharding (MLX page, section 3.2, `_shard`; section 3.1
+ * `shard_linear` only reads the original layer).
+ *
+ * Slices a full row-major (rows, cols) array `w` of `elem_bytes`-byte
+ * elements into N shard buffers: along `axis` (0 = rows, 1 or -1 = columns)
+ * the array is split into `segments` equal contiguous parts, each part into N
+ * equal contiguous parts, and shard r receives part r of every segment,
+ * concatenated in segment order.  With L the axis length and
+ * w_len = L / (segments * N), local index i of shard r is global index
+ * (i / w_len) * (L / segments) + r * w_len + (i % w_len).
+ *   axis 0 : shards[r] is (rows / N, cols) row-major;
+ *   axis 1 : shards[r] is (rows, cols / N) row-major.
+ * The copy is bit-exact.  `shards` is a host array of N device pointers to
+ * caller-allocated buffers that must not overlap `w` or each other.
+ * Errors: TP_ERR_NOT_DIVISIBLE if L % (segments * N) != 0 (message
+ * "Cannot shard the output of size L across N devices."); TP_ERR_INVALID_ARG
+ * for a bad axis, segments < 1, N < 1 or N > 64, elem_bytes not in
+ * {1, 2, 4, 8}, or a null pointer.
+ */
+int tp_shard_weight(const void *w, int64_t rows, int64_t cols, int elem_bytes, int axis,
+                    int segments, int N, void *const *shards, tp_stream_t stream);
+
+/*
+ * a2 / a4 -- column-parallel linear, "all-to-sharded" (MLX page, section 2.1
+ * AllToShardedLinear; the pages' Linear1D_Col with gather_output=False, and
+ * the fused-QKV and vocab-parallel LM head of the EnergonAI page, sections 2
+ * and 3).  The contraction dimension is not sharded, so there is no
+ * communication ("sharded matrices" notes, case 1).
+ *
+ * For r = 0..N-1:  y[r] = x @ w[r]^T + bias[r]
+ *   x      (T, K) in_dt, row stride ldx (>= K), replicated input;
+ *   w[r]   (O/N, K) in_dt contiguous: shard r of the (O, K) weight;
+ *   bias   NULL, or a host array of N device pointers to float32 (O/N);
+ *   y[r]   (T, O/N) out_dt, row stride ldy (>= O/N).  For a gathered output
+ *          (vocab-parallel logits) pass y[r] = base + r*(O/N) and ldy = O.
+ * in_dt: TP_BF16 or TP_F16 (tensor cores) or TP_F32 (CUDA cores);
+ * out_dt: TP_F32, TP_BF16 or TP_F16.
+ * Errors: TP_ERR_NOT_DIVISIBLE if O % N != 0, with the message
+ * "Cannot shard the output of size O across N devices."; TP_ERR_INVALID_ARG
+ * for null pointers, T < 0, K < 1, N < 1 or N > 64, ldx < K, ldy < O/N;
+ * TP_ERR_ALIGNMENT if a bf16/f16 x or w[r] is not 16-byte aligned or ldx
+ * is not a multiple of 8.  T = 0 is valid and launches nothing.
+ */
+int tp_all_to_sharded(int N, const void *x, int64_t T, int64_t K, int64_t ldx,
+                      const void *const *w, int64_t O, const void *const *bias,
+                      tp_dtype in_dt, void *const *y, int64_t ldy, tp_dtype out_dt,
+                      tp_stream_t stream);
+
+/*
+ * a3 -- row-parallel linear, "sharded-to-all" (MLX page, section 2.2
+ * ShardedToAllLinear: local matmul, then all_sum over the group, then the
+ * bias; the pages' Linear1D_Row; "sharded matrices" notes, case 3).
+ *
+ * y = (sum over r = 0..N-1, ascending, of x[r] @ w[r]^T) + bias
+ *   x[r]   (T, K/N) in_dt, row stride ldx (>= K/N): shard r of the input;
+ *   w[r]   (O, K/N) in_dt contiguous: shard r of the (O, K) weight, split on
+ *          its last axis;
+ *   bias   NULL or float32 (O), added once, after the sum;
+ *   y      (T, O) out_dt, row stride ldy (>= O).
+ * Every partial x[r] @ w[r]^T is formed in float32 from zero and the
+ * partials are added in ascending r, so the result does not depend on how
+ * the GPU schedules the work.  Partials do not go through device memory.
+ * Errors: TP_ERR_NOT_DIVISIBLE if K % N != 0; otherwise as tp_all_to_sharded.
+ */
+int tp_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K, int64_t ldx,
+                      const void *const *w, int64_t O, const void *bias, tp_dtype in_dt,
+                      void *y, int64_t ldy, tp_dtype out_dt, tp_stream_t stream);
+
+/*
+ * a5 -- SUMMA on a q x q grid ("ColossalAI 2D tensor parallel via SUMMA",
+ * SUMMA section, equations (1) and (2); Matmul_AB_2D).
+ *
+ * Y = X A with X (M, K) and A (K, Ncols) held as q*q blocks, block (i, j) at
+ * index i*q + j:
+ *   X[i*q+j]  (M/q, K/q) in_dt contiguous;
+ *   A[i*q+j]  (K/q, Ncols/q) in_dt contiguous;
+ *   Y[i*q+j]  (M/q, Ncols/q) float32 contiguous, written (not accumulated).
+ * Y_ij = sum over t = 0..q-1 of X_it A_tj, accumulated in float32 in step
+ * order t.  The per-step row and column broadcasts of the distributed
+ * algorithm become reads of the owning block's buffer.
+ * in_dt: TP_BF16, TP_F16 or TP_F32.
+ * Errors: TP_ERR_NOT_DIVISIBLE if q < 1 or M, K or Ncols is not a multiple of
+ * q (the page's grid requires P = q*q processors and block dimensions that
+ * divide evenly); TP_ERR_ALIGNMENT if (for bf16/f16) K/q or Ncols/q is not a
+ * multiple of 8 or a block pointer is not 16-byte aligned; TP_ERR_INVALID_ARG
+ * for null pointers or q > 8.
+ */
+int tp_summa(int q, const void *const *X, const void *const *A, void *const *Y, int64_t M,
+             int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream);
+
+/*
+ * a6 -- affine 4-bit quantization of a float32 weight on the device (MLX
+ * page, section 2.3: group_size 64, bits 4, mode "affine").  Data
+ * preparation, not part of a forward pass.
+ *
+ *   w       (rows, K) float32 row-major;
+ *   wq      (rows, K/8) uint32: 8 codes per word, element k at bits 4*(k%8);
+ *   scales  (rows, K/group_size) float16 (raw 16-bit storage);
+ *   qbias   (rows, K/group_size) float16.
+ * Per group of group_size consecutive elements of a row:
+ *   s = (max - min) / 15 in float32, 1 if that is 0; b = min;
+ *   s and b rounded to float16 (nearest even), s = 1 if it rounds to 0;
+ *   code = clamp(rint((w - b) / s), 0, 15) with float32 operations.
+ * Errors: TP_ERR_UNSUPPORTED if group_size != 64; TP_ERR_NOT_DIVISIBLE if
+ * K % group_size != 0; TP_ERR_INVALID_ARG for null pointers or sizes < 1.
+ */
+int tp_q4_quantize(const float *w, int64_t rows, int64_t K, int group_size, uint32_t *wq,
+                   void *scales, void *qbias, tp_stream_t stream);
+
+/*
+ * a7 -- quantized column-parallel linear (MLX page, section 2.3
+ * QuantizedAllToShardedLinear).
+ *
+ * For r = 0..N-1:  y[r] = x @ What[r]^T + bias[r], where
+ * What[r][o][k] = scales[r][o][k/64] * code(wq[r], o, k) + qbias[r][o][k/64].
+ *   x          (T, K) bfloat16 contiguous;
+ *   wq[r]      (O/N, K/8) uint32;  scales[r], qbias[r] (O/N, K/64) float16;
+ *   bias       NULL or host array of N device pointers to float32 (O/N);
+ *   y[r]       (T, O/N) out_dt, row stride ldy.
+ * Errors: TP_ERR_UNSUPPORTED if group_size != 64; TP_ERR_NOT_DIVISIBLE if
+ * O % N != 0 or K % 64 != 0; TP_ERR_INVALID_ARG / TP_ERR_ALIGNMENT as above.
+ */
+int tp_q4_all_to_sharded(int N, const void *x, int64_t T, int64_t K,
+                         const uint32_t *const *wq, const void *const *scales,
+                         const void *const *qbias, int group_size, int64_t O,
+                         const void *const *bias, void *const *y, int64_t ldy,
+                         tp_dtype out_dt, tp_stream_t stream);
+
+/*
+ * a7 -- quantized row-parallel linear (MLX page, section 2.3
+ * QuantizedShardedToAllLinear: local quantized matmul, then all_sum).
+ *
+ * y = (sum over r ascending of x[r] @ What[r]^T) + bias
+ *   x[r]       (T, K/N) bfloat16 contiguous;
+ *   wq[r]      (O, K/N/8) uint32;  scales[r], qbias[r] (O, K/N/64) float16
+ *              (each shard holds whole groups);
+ *   bias       NULL or float32 (O);   y (T, O) out_dt, row stride ldy.
+ * Errors: TP_ERR_NOT_DIVISIBLE if K % N != 0 or (K/N) % 64 != 0; otherwise
+ * as tp_q4_all_to_sharded.
+ */
+int tp_q4_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K,
+                         const uint32_t *const *wq, const void *const *scales,
+                         const void *const *qbias, int group_size, int64_t O,
+                         const void *bias, void *y, int64_t ldy, tp_dtype out_dt,
+                         tp_stream_t stream);
+
+/*
+ * Fault check of the bounded waits (no counterpart on the pages): launches a
+ * one-block kernel that waits on a shared-memory barrier nothing ever
+ * arrives at, with the given limit (1e6 .. 6e10 ns).  The wait runs out,
+ * the kernel records TP_ERR_TIMEOUT in the status word and returns; the
+ * context stays usable.  Read the result with tp_query_status().
+ */
+int tp_debug_wait_timeout(int64_t limit_ns, tp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_API_H */

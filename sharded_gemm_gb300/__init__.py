@@ -1,0 +1,333 @@
+"""Python binding of libtp.so, the sharded-GEMM C ABI (include/tp_api.h).
+
+Argument marshalling only: every function here checks that the tensors it
+is given can be described to the C ABI (device, dtype, row-major strides),
+passes their device pointers and sizes, and enqueues the call on the current
+torch CUDA stream.  All arithmetic runs in the library's CUDA kernels.  There
+is no fallback: if libtp.so is missing or fails to load, every call raises.
+
+Function names are the C names.  Tensors are torch CUDA tensors; bf16 / f16 /
+f32 map to TP_BF16 / TP_F16 / TP_F32.  4-bit codes are int32 tensors holding
+the uint32 words (8 codes per word, element k at bits 4*(k % 8)); scales and
+quantization biases are float16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtp.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "tp_api.h")
+
+TP_OK, TP_ERR_INVALID_ARG, TP_ERR_NOT_DIVISIBLE, TP_ERR_ALIGNMENT = 0, -1, -2, -3
+TP_ERR_UNSUPPORTED, TP_ERR_CUDA, TP_ERR_TIMEOUT = -4, -5, -6
+TP_F32, TP_BF16, TP_F16 = 0, 1, 2
+TP_POLICY_AUTO, TP_POLICY_SIMT = 0, 1
+
+_lib = None
+
+
+class TPError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("tp error %d: %s" % (code, msg))
+        self.code = code
+        self.msg = msg
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libtp.so (raises RuntimeError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libtp.so is not built (%s); run `python -m sharded_gemm_gb300.build`"
+                               % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+        vpp = ctypes.POINTER(ctypes.c_void_p)
+        sig = {
+            "tp_version": ([], i32),
+            "tp_last_error": ([], ctypes.c_char_p),
+            "tp_query_status": ([vp, ctypes.POINTER(ctypes.c_int)], i32),
+            "tp_set_policy": ([i32], i32),
+            "tp_set_wait_limit_ns": ([i64], i32),
+            "tp_shutdown": ([], i32),
+            "tp_shard_weight": ([vp, i64, i64, i32, i32, i32, i32, vpp, vp], i32),
+            "tp_all_to_sharded": ([i32, vp, i64, i64, i64, vpp, i64, vpp, i32, vpp, i64, i32, vp], i32),
+            "tp_sharded_to_all": ([i32, vpp, i64, i64, i64, vpp, i64, vp, i32, vp, i64, i32, vp], i32),
+            "tp_summa": ([i32, vpp, vpp, vpp, i64, i64, i64, i32, vp], i32),
+            "tp_q4_quantize": ([vp, i64, i64, i32, vp, vp, vp, vp], i32),
+            "tp_q4_all_to_sharded": ([i32, vp, i64, i64, vpp, vpp, vpp, i32, i64, vpp, vpp, i64, i32, vp], i32),
+            "tp_q4_sharded_to_all": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
+            "tp_debug_wait_timeout": ([i64, vp], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/tp_api.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tp_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(rc: int) -> None:
+    if rc != TP_OK:
+        raise TPError(rc, lib().tp_last_error().decode())
+
+
+# ------------------------------------------------------------------ marshalling
+def _torch():
+    import torch
+    return torch
+
+
+def _dt(t) -> int:
+    torch = _torch()
+    m = {torch.float32: TP_F32, torch.bfloat16: TP_BF16, torch.float16: TP_F16}
+    if t.dtype not in m:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+    return m[t.dtype]
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cuda(t, name):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    return t
+
+
+def _rowmajor(t, name):
+    _cuda(t, name)
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError("%s must be 2-D with unit column stride" % name)
+    return t
+
+
+def _contig(t, name):
+    _cuda(t, name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def _ptrs(ts):
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), arr
+
+
+def _common_ld(ts, name):
+    lds = {t.stride(0) if t.shape[0] > 1 else None for t in ts} - {None}
+    if len(lds) > 1:
+        raise ValueError("%s: all shards must share one row stride" % name)
+    return lds.pop() if lds else ts[0].shape[1]
+
+
+# ------------------------------------------------------------------ API
+def tp_version() -> int:
+    return lib().tp_version()
+
+
+def tp_last_error() -> str:
+    return lib().tp_last_error().decode()
+
+
+def tp_set_policy(policy: int) -> None:
+    _check(lib().tp_set_policy(policy))
+
+
+def tp_set_wait_limit_ns(ns: int) -> None:
+    _check(lib().tp_set_wait_limit_ns(ns))
+
+
+def tp_shutdown() -> None:
+    _check(lib().tp_shutdown())
+
+
+def tp_query_status(stream=None) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().tp_query_status(_stream(stream), ctypes.byref(v)))
+    return v.value
+
+
+def tp_debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(lib().tp_debug_wait_timeout(limit_ns, _stream(stream)))
+
+
+def tp_shard_weight(w, axis: int, segments: int, N: int, shards=None, stream=None):
+    """a1: the N rank slices of ``w`` along ``axis`` (bit-exact).
+
+    ``w`` is 2-D (axis 0, 1 or -1) or 1-D (a bias; axis 0 or -1)."""
+    torch = _torch()
+    _contig(w, "w")
+    if w.dim() == 1:
+        if axis not in (0, -1):
+            raise ValueError("a 1-D array can only be sharded along axis 0")
+        w2, ax = w.reshape(-1, 1), 0
+    elif w.dim() == 2:
+        if axis not in (0, 1, -1):
+            raise ValueError("axis must be 0, 1 or -1")
+        w2, ax = w, (0 if axis == 0 else 1)
+    else:
+        raise ValueError("w must be 1-D or 2-D")
+    rows, cols = w2.shape
+    if shards is None:
+        L = rows if ax == 0 else cols
+        shp = (rows // N, cols) if ax == 0 else (rows, cols // N)
+        if L % (segments * N) != 0:
+            shp = (1, 1)  # the library reports the divisibility error
+        shards = [torch.empty(shp, dtype=w.dtype, device=w.device) for _ in range(N)]
+    for i, t in enumerate(shards):
+        _contig(t, "shards[%d]" % i)
+    pp, keep = _ptrs(shards)
+    _check(lib().tp_shard_weight(w2.data_ptr(), rows, cols, w.element_size(), ax, segments, N, pp,
+                                 _stream(stream)))
+    return [t.reshape(-1) for t in shards] if w.dim() == 1 else shards
+
+
+def tp_all_to_sharded(x, w, bias=None, out=None, out_dtype=None, stream=None):
+    """a2/a4: y[r] = x @ w[r].T + bias[r] for every shard r; returns y list.
+
+    ``out`` may be views of one gathered (T, O) buffer (column offset r*O/N)."""
+    torch = _torch()
+    _rowmajor(x, "x")
+    N = len(w)
+    T, K = x.shape
+    On = w[0].shape[0]
+    for i, t in enumerate(w):
+        _contig(t, "w[%d]" % i)
+    if out is None:
+        out = [torch.empty((T, On), dtype=out_dtype or x.dtype, device=x.device) for _ in range(N)]
+    for i, t in enumerate(out):
+        _rowmajor(t, "out[%d]" % i)
+    wp, k1 = _ptrs(w)
+    yp, k2 = _ptrs(out)
+    bp, k3 = (None, None)
+    if bias is not None:
+        for i, t in enumerate(bias):
+            _contig(t, "bias[%d]" % i)
+        bp, k3 = _ptrs(bias)
+    ldx = x.stride(0) if T > 1 else K
+    _check(lib().tp_all_to_sharded(N, x.data_ptr(), T, K, ldx, wp, On * N, bp, _dt(x), yp,
+                                   _common_ld(out, "out"), _dt(out[0]), _stream(stream)))
+    return out
+
+
+def tp_sharded_to_all(x, w, bias=None, out=None, out_dtype=None, stream=None):
+    """a3: y = sum_r x[r] @ w[r].T (ascending r) + bias; returns y."""
+    torch = _torch()
+    N = len(x)
+    for i, t in enumerate(x):
+        _rowmajor(t, "x[%d]" % i)
+    for i, t in enumerate(w):
+        _contig(t, "w[%d]" % i)
+    T, Kn = x[0].shape
+    O = w[0].shape[0]
+    if out is None:
+        out = torch.empty((T, O), dtype=out_dtype or torch.float32, device=x[0].device)
+    _rowmajor(out, "out")
+    if bias is not None:
+        _contig(bias, "bias")
+    xp, k1 = _ptrs(x)
+    wp, k2 = _ptrs(w)
+    ldx = _common_ld(x, "x")
+    ldy = out.stride(0) if T > 1 else O
+    _check(lib().tp_sharded_to_all(N, xp, T, Kn * N, ldx, wp, O,
+                                   None if bias is None else bias.data_ptr(), _dt(x[0]),
+                                   out.data_ptr(), ldy, _dt(out), _stream(stream)))
+    return out
+
+
+def tp_summa(q: int, X, A, Y=None, stream=None):
+    """a5: Y_ij = sum_t X_it A_tj on a q x q grid (blocks indexed i*q+j)."""
+    torch = _torch()
+    for i, t in enumerate(list(X) + list(A)):
+        _contig(t, "block %d" % i)
+    bm, bk = X[0].shape
+    bn = A[0].shape[1]
+    if Y is None:
+        Y = [torch.empty((bm, bn), dtype=torch.float32, device=X[0].device) for _ in range(q * q)]
+    for i, t in enumerate(Y):
+        _contig(t, "Y[%d]" % i)
+    xp, k1 = _ptrs(X)
+    ap, k2 = _ptrs(A)
+    yp, k3 = _ptrs(Y)
+    _check(lib().tp_summa(q, xp, ap, yp, bm * q, bk * q, bn * q, _dt(X[0]), _stream(stream)))
+    return Y
+
+
+def tp_q4_quantize(w, group_size: int = 64, stream=None):
+    """a6: (codes int32 (rows, K/8), scales f16, qbias f16) of a float32 weight."""
+    torch = _torch()
+    _contig(w, "w")
+    rows, K = w.shape
+    wq = torch.empty((rows, max(K // 8, 1)), dtype=torch.int32, device=w.device)
+    sc = torch.empty((rows, max(K // group_size, 1)), dtype=torch.float16, device=w.device)
+    qb = torch.empty_like(sc)
+    _check(lib().tp_q4_quantize(w.data_ptr(), rows, K, group_size, wq.data_ptr(), sc.data_ptr(),
+                                qb.data_ptr(), _stream(stream)))
+    return wq, sc, qb
+
+
+def tp_q4_all_to_sharded(x, wq, scales, qbias, bias=None, out=None, out_dtype=None,
+                         group_size: int = 64, stream=None):
+    """a7 column-parallel: y[r] = x @ What[r].T + bias[r]."""
+    torch = _torch()
+    _contig(x, "x")
+    N = len(wq)
+    T, K = x.shape
+    On = wq[0].shape[0]
+    for lst, nm in ((wq, "wq"), (scales, "scales"), (qbias, "qbias")):
+        for i, t in enumerate(lst):
+            _contig(t, "%s[%d]" % (nm, i))
+    if out is None:
+        out = [torch.empty((T, On), dtype=out_dtype or torch.bfloat16, device=x.device) for _ in range(N)]
+    for i, t in enumerate(out):
+        _rowmajor(t, "out[%d]" % i)
+    qp, k1 = _ptrs(wq)
+    sp, k2 = _ptrs(scales)
+    bq, k3 = _ptrs(qbias)
+    yp, k4 = _ptrs(out)
+    bp, k5 = (None, None)
+    if bias is not None:
+        bp, k5 = _ptrs(bias)
+    _check(lib().tp_q4_all_to_sharded(N, x.data_ptr(), T, K, qp, sp, bq, group_size, On * N, bp, yp,
+                                      _common_ld(out, "out"), _dt(out[0]), _stream(stream)))
+    return out
+
+
+def tp_q4_sharded_to_all(x, wq, scales, qbias, bias=None, out=None, out_dtype=None,
+                         group_size: int = 64, stream=None):
+    """a7 row-parallel: y = sum_r x[r] @ What[r].T (ascending r) + bias."""
+    torch = _torch()
+    N = len(x)
+    for lst, nm in ((x, "x"), (wq, "wq"), (scales, "scales"), (qbias, "qbias")):
+        for i, t in enumerate(lst):
+            _contig(t, "%s[%d]" % (nm, i))
+    T, Kn = x[0].shape
+    O = wq[0].shape[0]
+    if out is None:
+        out = torch.empty((T, O), dtype=out_dtype or torch.float32, device=x[0].device)
+    _rowmajor(out, "out")
+    xp, k1 = _ptrs(x)
+    qp, k2 = _ptrs(wq)
+    sp, k3 = _ptrs(scales)
+    bq, k4 = _ptrs(qbias)
+    ldy = out.stride(0) if T > 1 else O
+    _check(lib().tp_q4_sharded_to_all(N, xp, T, Kn * N, qp, sp, bq, group_size, O,
+                                      None if bias is None else bias.data_ptr(), out.data_ptr(), ldy,
+                                      _dt(out), _stream(stream)))
+    return out

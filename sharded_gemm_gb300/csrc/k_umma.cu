@@ -1,0 +1,614 @@
+// k_umma.cu -- tcgen05 tensor-core GEMM for sm_103a: the column-parallel
+// (all-to-sharded), row-parallel (sharded-to-all) and SUMMA products.
+//
+// One persistent, warp-specialized kernel, one CTA per SM:
+//   warp 0      TMA producer: A tile (128 x 64) and B tile (BN x 64) of bf16/f16
+//               per k-block into a ring of STAGES shared-memory stages, 128-byte
+//               swizzled, completion tracked by mbarrier transaction counts;
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, N=BN,
+//               K=16) into float32 accumulators in TMEM and commits them to
+//               mbarriers;
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator, fixed-order sum of
+//               partials (row-parallel), bias, conversion, global store.
+// A work unit is one output tile of one job.  Within a job, `parts` are the
+// matrix products that make the tile:
+//   chain (SUMMA, column-parallel): all parts accumulate into one TMEM
+//     accumulator in part order (SUMMA's q steps);
+//   partials (row-parallel): every part (rank r) is formed from zero in its
+//     own TMEM buffer, and the epilogue adds the partials in ascending r in
+//     registers, then adds the bias once.  Partials never touch device memory.
+// Swap-AB (T <= 16, decode): the weight rows fill the 128-row MMA dimension,
+// the tokens the N = 16 dimension, and the epilogue stores the transpose.
+// Every mbarrier wait is bounded (see ptx.cuh): a wait that runs out records
+// TP_ERR_TIMEOUT in the status word and the CTA drains its in-flight copies and
+// MMAs, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <string.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "ptx.cuh"
+#include "tp_internal.h"
+
+namespace tp {
+
+constexpr int kMaxMaps = 64;
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
+struct UJob {
+  void *C;
+  const float *bias;
+  int64_t ldc;
+  int rowsA, rowsB;    // extents of the A-operand rows and B-operand rows
+  int part0, nparts;
+  int tilesA, tilesB;
+  int unit_begin;
+};
+
+struct UPart {
+  int16_t amap, bmap;
+  int32_t kblocks;
+};
+
+struct UmmaArgs {
+  CUtensorMap mapA[kMaxMaps];
+  CUtensorMap mapB[kMaxMaps];
+  UJob jobs[kMaxJobs];
+  UPart parts[kMaxParts];
+  int njobs, total_units;
+  int chain, out_dt, vec_ok;
+  uint32_t idesc;
+  int *status;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ int find_job(const UmmaArgs &a, int u) {
+  int j = 0;
+  while (j + 1 < a.njobs && u >= a.jobs[j + 1].unit_begin) ++j;
+  return j;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float x, float y) {
+  __half2 h = __floats2half2_rn(x, y);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Stores CH consecutive output values of one thread (row-major, normal mode).
+template <int CH>
+__device__ __forceinline__ void store_row_chunk(const UmmaArgs &a, const UJob &J, int row, int col0,
+                                                float (&v)[CH]) {
+  if (row >= J.rowsA) return;
+  if (J.bias) {
+#pragma unroll
+    for (int i = 0; i < CH; ++i)
+      if (col0 + i < J.rowsB) v[i] += __ldg(J.bias + col0 + i);
+  }
+  const int64_t base = (int64_t)row * J.ldc + col0;
+  const bool full = a.vec_ok && (col0 + CH <= J.rowsB);
+  if (a.out_dt == TP_F32) {
+    float *C = static_cast<float *>(J.C) + base;
+    if (full && (CH % 4 == 0)) {
+#pragma unroll
+      for (int i = 0; i < CH; i += 4)
+        *reinterpret_cast<float4 *>(C + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < CH; ++i)
+        if (col0 + i < J.rowsB) C[i] = v[i];
+    }
+  } else {
+    uint16_t *C = static_cast<uint16_t *>(J.C) + base;
+    const bool bf = a.out_dt == TP_BF16;
+    if (full && (CH % 8 == 0)) {
+#pragma unroll
+      for (int i = 0; i < CH; i += 8) {
+        uint4 q;
+        q.x = bf ? pack_bf16(v[i], v[i + 1]) : pack_f16(v[i], v[i + 1]);
+        q.y = bf ? pack_bf16(v[i + 2], v[i + 3]) : pack_f16(v[i + 2], v[i + 3]);
+        q.z = bf ? pack_bf16(v[i + 4], v[i + 5]) : pack_f16(v[i + 4], v[i + 5]);
+        q.w = bf ? pack_bf16(v[i + 6], v[i + 7]) : pack_f16(v[i + 6], v[i + 7]);
+        *reinterpret_cast<uint4 *>(C + i) = q;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < CH; ++i)
+        if (col0 + i < J.rowsB)
+          C[i] = bf ? __bfloat16_as_ushort(__float2bfloat16_rn(v[i]))
+                    : __half_as_ushort(__float2half_rn(v[i]));
+    }
+  }
+}
+
+// Swap-AB store: the thread's A row is output column `row`; its values are
+// tokens col0.. of that column.
+template <int CH>
+__device__ __forceinline__ void store_col_chunk(const UmmaArgs &a, const UJob &J, int row, int col0,
+                                                const float (&v)[CH]) {
+  if (row >= J.rowsA) return;
+  const float b = J.bias ? __ldg(J.bias + row) : 0.f;
+#pragma unroll
+  for (int i = 0; i < CH; ++i) {
+    const int t = col0 + i;
+    if (t >= J.rowsB) break;
+    const int64_t idx = (int64_t)t * J.ldc + row;
+    const float x = v[i] + b;
+    if (a.out_dt == TP_F32)
+      static_cast<float *>(J.C)[idx] = x;
+    else if (a.out_dt == TP_BF16)
+      static_cast<uint16_t *>(J.C)[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    else
+      static_cast<uint16_t *>(J.C)[idx] = __half_as_ushort(__float2half_rn(x));
+  }
+}
+
+template <int BN, bool SWAP>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[(BN / 2 < 32) ? BN / 2 : 32]) {
+  constexpr int CH = (BN / 2 < 32) ? BN / 2 : 32;
+  if constexpr (CH == 32) {
+    tmem_ld32(taddr, v);
+  } else {
+    static_assert(CH == 16 || CH == 8, "chunk");
+    if constexpr (CH == 16) {
+      tmem_ld16(taddr, v);
+    } else {
+      uint32_t r[8];
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+            "=r"(r[7])
+          : "r"(taddr));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+    }
+  }
+}
+
+template <int N>
+struct TmemCols {
+  static constexpr int v = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : N <= 256 ? 256 : 512;
+};
+
+template <int BN, bool B_MN, bool SWAP, bool PARTIALS, int STAGES, int NACC>
+__global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_constant__ UmmaArgs a) {
+  constexpr int A_BYTES = BM * BK * 2;
+  constexpr int B_BYTES = BN * BK * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr int TCOLS = TmemCols<NACC * BN>::v;
+  constexpr int HALF = BN / 2;
+  constexpr int CH = HALF < 32 ? HALF : 32;
+  constexpr int NCH = HALF / CH;
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(NACC * BN <= 512, "TMEM capacity");
+
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[NACC], tempty_bar[NACC];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint64_t lim = a.wait_ns;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int s = 0; s < NACC; ++s) {
+      mbar_init(smem_u32(&tfull_bar[s]), 1);
+      mbar_init(smem_u32(&tempty_bar[s]), kEpiWarps);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), TCOLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < kMaxMaps && i < 8; ++i) {
+      prefetch_tmap(&a.mapA[i]);
+      prefetch_tmap(&a.mapB[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_phase[STAGES];
+      bool used[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) used[s] = false;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        const UJob &J = a.jobs[find_job(a, u)];
+        const int local = u - J.unit_begin;
+        const int ta = local % J.tilesA, tb = local / J.tilesA;
+        const int rowA0 = ta * BM, rowB0 = tb * BN;
+        for (int p = 0; ok && p < J.nparts; ++p) {
+          const UPart P = a.parts[J.part0 + p];
+          for (int kb = 0; kb < P.kblocks; ++kb) {
+            if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, lim, a.status, &abort_sh)) {
+              ok = false;
+              break;
+            }
+            const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
+            const uint32_t fb = smem_u32(&full_bar[stage]);
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            tma_load_2d(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
+            if constexpr (B_MN) {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(sb + c * 8192, &a.mapB[P.bmap], fb, rowB0 + c * 64, kb * BK);
+            } else {
+              tma_load_2d(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
+            }
+            used[stage] = true;
+            last_phase[stage] = phase;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Wait (bounded, ignoring the abort flag) for copies still in flight.
+        for (int s = 0; s < STAGES; ++s)
+          if (used[s]) mbar_wait(smem_u32(&full_bar[s]), last_phase[s], lim, a.status, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        const UJob &J = a.jobs[find_job(a, u)];
+        for (int p = 0; ok && p < J.nparts; ++p) {
+          const UPart P = a.parts[J.part0 + p];
+          if (p == 0 || !a.chain) {
+            if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, lim, a.status, &abort_sh)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+          for (int kb = 0; kb < P.kblocks; ++kb) {
+            if (!mbar_wait(smem_u32(&full_bar[stage]), phase, lim, a.status, &abort_sh)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = umma_desc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                       : umma_desc_sw128(sb + kk * 32, 16, 1024);
+              const uint32_t accum = (kb > 0 || kk > 0 || (a.chain && p > 0)) ? 1u : 0u;
+              umma_f16(d, ad, bd, a.idesc, accum);
+            }
+            umma_commit(smem_u32(&empty_bar[stage]));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          if (p == J.nparts - 1 || !a.chain) {
+            umma_commit(smem_u32(&tfull_bar[acc]));
+            if (++acc == NACC) {
+              acc = 0;
+              acc_phase ^= 1;
+            }
+          }
+        }
+      }
+      // All MMAs issued by this thread complete before TMEM is released.
+      umma_commit(smem_u32(&drain_bar));
+      mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int half = ew >> 2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    float sum[PARTIALS ? HALF : 1];
+    for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+      const UJob &J = a.jobs[find_job(a, u)];
+      const int local = u - J.unit_begin;
+      const int ta = local % J.tilesA, tb = local / J.tilesA;
+      const int row = ta * BM + quarter * 32 + lane;
+      const int colb = tb * BN + half * HALF;
+      const int nep = a.chain ? 1 : J.nparts;
+      for (int pe = 0; pe < nep; ++pe) {
+        if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, lim, a.status, &abort_sh)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb_addr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16) +
+                                 (uint32_t)(half * HALF);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          float v[CH];
+          tmem_load_chunk<BN, SWAP>(tb_addr + c * CH, v);
+          tmem_wait_ld();
+          if constexpr (PARTIALS) {
+#pragma unroll
+            for (int i = 0; i < CH; ++i) sum[c * CH + i] = (pe == 0) ? v[i] : sum[c * CH + i] + v[i];
+          } else {
+            if constexpr (SWAP)
+              store_col_chunk<CH>(a, J, row, colb + c * CH, v);
+            else
+              store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+        if (++acc == NACC) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if constexpr (PARTIALS) {
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            float v[CH];
+#pragma unroll
+            for (int i = 0; i < CH; ++i) v[i] = sum[c * CH + i];
+            if constexpr (SWAP)
+              store_col_chunk<CH>(a, J, row, colb + c * CH, v);
+            else
+              store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TCOLS);
+  }
+}
+
+// ====================================================================== host
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_mu;
+
+struct MapKey {
+  uint64_t ptr, inner, outer, stride;
+  uint32_t box0, box1, dt;
+  bool operator==(const MapKey &o) const {
+    return ptr == o.ptr && inner == o.inner && outer == o.outer && stride == o.stride &&
+           box0 == o.box0 && box1 == o.box1 && dt == o.dt;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey &k) const {
+    uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+    h ^= k.inner + 0x7f4a7c15 + (h << 6) + (h >> 2);
+    h ^= k.outer + 0x2545F491 + (h << 6) + (h >> 2);
+    h ^= k.stride + ((uint64_t)k.box0 << 32 | k.box1) + (h << 6) + (h >> 2);
+    return (size_t)(h ^ k.dt);
+  }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+int g_sms[64] = {0};
+
+int get_encoder() {
+  if (g_encode) return TP_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return set_error(TP_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled");
+  g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  return TP_OK;
+}
+
+// 2-D row-major tensor map: `inner` contiguous elements per row, `outer`
+// rows, row stride `ld` elements; box (box0 inner, box1 rows), 128B swizzle.
+int make_map(CUtensorMap *out, const void *ptr, int dt, uint64_t inner, uint64_t outer, uint64_t ld,
+             uint32_t box0, uint32_t box1) {
+  MapKey key{(uint64_t)(uintptr_t)ptr, inner, outer, ld, box0, box1, (uint32_t)dt};
+  {
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return TP_OK;
+    }
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(out, dt == TP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        2, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  if (g_maps.size() > 8192) g_maps.clear();
+  g_maps.emplace(key, *out);
+  return TP_OK;
+}
+
+template <int BN, bool B_MN, bool SWAP, bool PARTIALS, int STAGES, int NACC>
+int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
+  auto kern = umma_gemm_kernel<BN, B_MN, SWAP, PARTIALS, STAGES, NACC>;
+  constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
+    attr_done[dev & 63] = true;
+  }
+  const int grid = args.total_units < sms ? args.total_units : sms;
+  kern<<<grid, kThreads, smem, s>>>(args);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_gemm_kernel launch");
+}
+
+bool al16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+}  // namespace
+
+int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
+  *handled = false;
+  if (p.in_dt != TP_BF16 && p.in_dt != TP_F16) return TP_OK;
+  if (p.b_layout != BL_KMAJOR && p.b_layout != BL_MNMAJOR) return TP_OK;
+  // TMA needs 16-byte aligned bases and row strides; else the CUDA-core path.
+  int64_t maxM = 0;
+  for (int j = 0; j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    if (J.M > INT32_MAX / 2 || J.N > INT32_MAX / 2) return TP_OK;
+    if (J.M > maxM) maxM = J.M;
+    for (int q = 0; q < J.nparts; ++q) {
+      const Part &P = p.parts[J.part0 + q];
+      if (!al16(P.A) || !al16(P.B) || (P.lda % 8) || (P.ldb % 8)) return TP_OK;
+    }
+  }
+  const bool summa = p.b_layout == BL_MNMAJOR;
+  const bool swap = !summa && maxM <= 16;
+  const bool partials = !p.chain;
+  int BN;
+  if (summa)
+    BN = 256;
+  else if (swap)
+    BN = 16;
+  else
+    BN = partials ? 128 : 256;
+
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = get_encoder();
+  if (rc) return rc;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!g_sms[dev & 63]) cudaDeviceGetAttribute(&g_sms[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+  const int sms = g_sms[dev & 63];
+
+  static UmmaArgs args;  // large; guarded by g_mu
+  memset(&args, 0, sizeof(args));
+  int nA = 0, nB = 0;
+  const void *aptr[kMaxMaps], *bptr[kMaxMaps];
+  int64_t units = 0;
+  for (int j = 0; j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    UJob &U = args.jobs[j];
+    U.C = J.C;
+    U.bias = J.bias;
+    U.ldc = J.ldc;
+    U.rowsA = (int)(swap ? J.N : J.M);
+    U.rowsB = (int)(swap ? J.M : J.N);
+    U.part0 = J.part0;
+    U.nparts = J.nparts;
+    U.tilesA = (U.rowsA + BM - 1) / BM;
+    U.tilesB = (U.rowsB + BN - 1) / BN;
+    U.unit_begin = (int)units;
+    units += (int64_t)U.tilesA * U.tilesB;
+    for (int q = 0; q < J.nparts; ++q) {
+      const Part &P = p.parts[J.part0 + q];
+      // operand roles: normal A = activations (M rows), B = weights / SUMMA block
+      const void *opA = swap ? P.B : P.A;
+      const void *opB = swap ? P.A : P.B;
+      const int64_t ldA = swap ? P.ldb : P.lda, ldB = swap ? P.lda : P.ldb;
+      int ia = -1, ib = -1;
+      for (int i = 0; i < nA; ++i)
+        if (aptr[i] == opA) ia = i;
+      for (int i = 0; i < nB; ++i)
+        if (bptr[i] == opB) ib = i;
+      if (ia < 0) {
+        if (nA == kMaxMaps) return TP_OK;
+        rc = make_map(&args.mapA[nA], opA, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsA, (uint64_t)ldA, BK, BM);
+        if (rc) return rc;
+        aptr[nA] = opA;
+        ia = nA++;
+      }
+      if (ib < 0) {
+        if (nB == kMaxMaps) return TP_OK;
+        if (summa)  // B block (K, Nblk) row-major: inner = N
+          rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)U.rowsB, (uint64_t)P.K, (uint64_t)ldB, 64, BK);
+        else
+          rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsB, (uint64_t)ldB, BK, BN);
+        if (rc) return rc;
+        bptr[nB] = opB;
+        ib = nB++;
+      }
+      args.parts[J.part0 + q] = UPart{(int16_t)ia, (int16_t)ib, (int32_t)((P.K + BK - 1) / BK)};
+    }
+  }
+  if (units == 0) {
+    *handled = true;
+    return TP_OK;
+  }
+  if (units > INT32_MAX) return TP_OK;
+  args.njobs = p.njobs;
+  args.total_units = (int)units;
+  args.chain = p.chain;
+  args.out_dt = p.out_dt;
+  const int oe = p.out_dt == TP_F32 ? 4 : 2;
+  int vec = 1;
+  for (int j = 0; j < p.njobs; ++j)
+    if (!al16(p.jobs[j].C) || ((p.jobs[j].ldc * oe) % 16)) vec = 0;
+  args.vec_ok = vec;
+  args.idesc = umma_idesc_f16(p.in_dt == TP_BF16 ? 1u : 0u, summa ? 1u : 0u, BM, (uint32_t)BN);
+  args.status = p.status;
+  args.wait_ns = (uint64_t)p.wait_ns;
+
+  if (summa)
+    rc = launch_config<256, true, false, false, 4, 2>(args, sms, s);
+  else if (swap && partials)
+    rc = launch_config<16, false, true, true, 8, 4>(args, sms, s);
+  else if (swap)
+    rc = launch_config<16, false, true, false, 8, 4>(args, sms, s);
+  else if (partials)
+    rc = launch_config<128, false, false, true, 6, 4>(args, sms, s);
+  else
+    rc = launch_config<256, false, false, false, 4, 2>(args, sms, s);
+  if (rc == TP_OK) *handled = true;
+  return rc;
+}
+
+void umma_shutdown() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_maps.clear();
+}
+
+}  // namespace tp

@@ -1,0 +1,72 @@
+// tp_internal.h -- definitions shared by the translation units of libtp.so.
+//
+// A request of any entry point is lowered to one `Problem`: a list of output
+// matrices ("jobs"), each the sum of one or more matrix products ("parts").
+//   C_j[m][n] = bias_j[n] + sum over parts p of job j of
+//               sum_k A_p[m][k] * B_p(n, k)
+// B_p(n, k) is B_p[n*ldb + k] (layout BL_KMAJOR, a linear weight (out, in)),
+// B_p[k*ldb + n] (BL_MNMAJOR, SUMMA's A block (K, N)), or the dequantized
+// 4-bit weight s[n][k/64]*code(n, k) + b[n][k/64] (BL_Q4).
+// `chain` = 1: the parts of a job accumulate into one float32 sum in part
+// order (SUMMA's q steps).  `chain` = 0: every part is a separate float32
+// partial formed from zero and the partials are added in part order (the
+// row-parallel all_sum over ranks r = 0..N-1).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tp_api.h"
+
+namespace tp {
+
+constexpr int kMaxShards = 64;
+constexpr int kMaxJobs = 64;
+constexpr int kMaxParts = 64;
+
+enum BLayout { BL_KMAJOR = 0, BL_MNMAJOR = 1, BL_Q4 = 2 };
+
+struct Part {
+  const void *A;       // (M, K) row-major, row stride lda
+  const void *B;       // see BLayout
+  const void *scales;  // BL_Q4: float16 (N, K/64)
+  const void *qbias;   // BL_Q4: float16 (N, K/64)
+  int64_t K, lda, ldb;
+};
+
+struct Job {
+  void *C;             // (M, N) out_dt, row stride ldc
+  const float *bias;   // nullable, (N)
+  int64_t M, N, ldc;
+  int part0, nparts;
+};
+
+struct Problem {
+  Job jobs[kMaxJobs];
+  Part parts[kMaxParts];
+  int njobs;
+  int in_dt, out_dt;   // tp_dtype
+  int b_layout;        // BLayout
+  int chain;
+  int *status;         // device status word
+  int64_t wait_ns;     // bound of device-side waits
+};
+
+// ---- shared host state (tp_api.cu)
+int *device_status_word();  // per current device; nullptr on failure
+int64_t wait_limit_ns();
+int set_error(int code, const char *fmt, ...);
+int cuda_error(cudaError_t e, const char *what);
+
+// ---- launchers (each returns TP_OK or a tp_status, error message set)
+int launch_simt(const Problem &p, cudaStream_t s);
+int launch_umma(const Problem &p, cudaStream_t s, bool *handled);
+int launch_q4(const Problem &p, cudaStream_t s, bool *handled);
+int launch_shard(const void *w, int64_t rows, int64_t cols, int elem_bytes, int axis,
+                 int segments, int N, void *const *shards, cudaStream_t s);
+int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void *scales,
+                    void *qbias, cudaStream_t s);
+int launch_debug_wait(int64_t limit_ns, int *status, cudaStream_t s);
+void umma_shutdown();
+
+}  // namespace tp

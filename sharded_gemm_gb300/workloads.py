@@ -1,0 +1,151 @@
+"""The sharded-GEMM workloads as device-resident objects with one ``step()``.
+
+Each class takes host arrays from ``synth`` (or arrays the caller prepared),
+moves them to the GPU once, slices the weights into their N shard buffers
+with ``tp_shard_weight`` (a1), allocates the outputs, and exposes ``step()``:
+one pass of that workload's hot path through the C ABI.  Nothing here does
+arithmetic of its own.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (tp_all_to_sharded, tp_q4_all_to_sharded, tp_q4_quantize, tp_q4_sharded_to_all,
+               tp_shard_weight, tp_sharded_to_all, tp_summa)
+
+
+def to_device(a: np.ndarray, kind: str, device="cuda") -> torch.Tensor:
+    """Host array -> device tensor. kind: 'bf16' (uint16 bits), 'f16', 'f32', 'u32'."""
+    a = np.ascontiguousarray(a)
+    if kind == "bf16":
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    elif kind == "f16":
+        t = torch.from_numpy(a.view(np.float16) if a.dtype == np.uint16 else a.astype(np.float16))
+    elif kind == "f32":
+        t = torch.from_numpy(a.astype(np.float32))
+    elif kind == "u32":
+        t = torch.from_numpy(a.view(np.int32))
+    else:
+        raise ValueError(kind)
+    return t.to(device)
+
+
+def to_host(t: torch.Tensor) -> np.ndarray:
+    """Device tensor -> host float64 (bf16 / f16 / f32 values are exact)."""
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+class MLPPair:
+    """Column-parallel W1 (out dims split on axis 0) feeding row-parallel W2
+    (split on its last axis); the intermediate stays sharded (bf16)."""
+
+    def __init__(self, cfg: dict, device="cuda", mid_dtype=torch.bfloat16, out_dtype=torch.float32):
+        self.N = N = cfg["N"]
+        kind = cfg["dtype"]
+        self.x = to_device(cfg["x"], kind, device)
+        w1 = to_device(cfg["w1"], kind, device)
+        w2 = to_device(cfg["w2"], kind, device)
+        self.w1 = tp_shard_weight(w1, 0, 1, N)
+        self.b1 = tp_shard_weight(to_device(cfg["b1"], "f32", device), 0, 1, N)
+        self.w2 = tp_shard_weight(w2, -1, 1, N)
+        self.b2 = to_device(cfg["b2"], "f32", device)
+        del w1, w2
+        T = self.x.shape[0]
+        if kind == "f32":
+            mid_dtype = torch.float32
+        self.mid = [torch.empty((T, self.w1[0].shape[0]), dtype=mid_dtype, device=device) for _ in range(N)]
+        self.y = torch.empty((T, self.w2[0].shape[0]), dtype=out_dtype, device=device)
+        self.flops = 2.0 * T * (cfg["w1"].shape[0] * cfg["w1"].shape[1] + cfg["w2"].shape[0] * cfg["w2"].shape[1])
+
+    def step(self, x=None, stream=None):
+        tp_all_to_sharded(self.x if x is None else x, self.w1, self.b1, out=self.mid, stream=stream)
+        tp_sharded_to_all(self.mid, self.w2, self.b2, out=self.y, stream=stream)
+        return self.y
+
+
+class Summa:
+    def __init__(self, cfg: dict, q: int, device="cuda"):
+        self.q = q
+        M, K, Nc = cfg["M"], cfg["K"], cfg["Ncols"]
+        X = to_device(cfg["X"], cfg["dtype"], device)
+        A = to_device(cfg["A"], cfg["dtype"], device)
+        bm, bk, bn = M // q, K // q, Nc // q
+        self.X = [X[i * bm:(i + 1) * bm, j * bk:(j + 1) * bk].contiguous() for i in range(q) for j in range(q)]
+        self.A = [A[i * bk:(i + 1) * bk, j * bn:(j + 1) * bn].contiguous() for i in range(q) for j in range(q)]
+        del X, A
+        self.Y = [torch.empty((bm, bn), dtype=torch.float32, device=device) for _ in range(q * q)]
+        self.flops = 2.0 * M * K * Nc
+
+    def step(self, stream=None):
+        return tp_summa(self.q, self.X, self.A, self.Y, stream=stream)
+
+
+class QKV:
+    """Fused QKV (segments=3), row-parallel W_o on x split by columns, and a
+    vocab-parallel LM head whose logits land in one gathered (T, V) buffer."""
+
+    def __init__(self, cfg: dict, device="cuda"):
+        self.N = N = cfg["N"]
+        self.x = to_device(cfg["x"], "bf16", device)
+        T, D, V = self.x.shape[0], cfg["D"], cfg["V"]
+        wq = to_device(cfg["w_qkv"], "bf16", device)
+        self.w_qkv = tp_shard_weight(wq, 0, 3, N)
+        self.b_qkv = tp_shard_weight(to_device(cfg["b_qkv"], "f32", device), 0, 3, N)
+        del wq
+        wo = to_device(cfg["w_o"], "bf16", device)
+        self.w_o = tp_shard_weight(wo, -1, 1, N)
+        self.b_o = to_device(cfg["b_o"], "f32", device)
+        del wo
+        wl = to_device(cfg["w_lm"], "bf16", device)
+        self.w_lm = tp_shard_weight(wl, 0, 1, N)
+        del wl
+        self.qkv = [torch.empty((T, 3 * D // N), dtype=torch.bfloat16, device=device) for _ in range(N)]
+        self.attn_out = torch.empty((T, D), dtype=torch.float32, device=device)
+        self.logits = torch.empty((T, V), dtype=torch.float32, device=device)
+        Vn = V // N
+        self.logit_views = [self.logits[:, r * Vn:(r + 1) * Vn] for r in range(N)]
+        self.x_cols = [self.x[:, r * (D // N):(r + 1) * (D // N)] for r in range(N)]
+        self.flops = 2.0 * T * D * (3 * D + D + V)
+        self.weight_bytes = 2.0 * D * (3 * D + D + V)
+
+    def step(self, stream=None):
+        tp_all_to_sharded(self.x, self.w_qkv, self.b_qkv, out=self.qkv, stream=stream)
+        tp_sharded_to_all(self.x_cols, self.w_o, self.b_o, out=self.attn_out, stream=stream)
+        tp_all_to_sharded(self.x, self.w_lm, None, out=self.logit_views, stream=stream)
+        return self.qkv, self.attn_out, self.logits
+
+
+class Q4Pair:
+    """4-bit affine quantized up (column-parallel) / down (row-parallel) pair.
+
+    ``quantized`` may hold host (codes, scales, biases) for both weights; if
+    absent the float32 source weights are quantized on the device (a6)."""
+
+    def __init__(self, cfg: dict, device="cuda", quantized=None):
+        self.N = N = cfg["N"]
+        self.x = to_device(cfg["x"], "bf16", device)
+        T, D, F = self.x.shape[0], cfg["D"], cfg["F"]
+        if quantized is None:
+            wu = to_device(cfg["w_up"], "f32", device)
+            up = tp_q4_quantize(wu)
+            del wu
+            wd = to_device(cfg["w_down"], "f32", device)
+            down = tp_q4_quantize(wd)
+            del wd
+        else:
+            (uq, us, ub), (dq, ds, db) = quantized
+            up = (to_device(uq, "u32", device), to_device(us, "f16", device), to_device(ub, "f16", device))
+            down = (to_device(dq, "u32", device), to_device(ds, "f16", device), to_device(db, "f16", device))
+        self.up = [tp_shard_weight(a, 0, 1, N) for a in up]
+        self.down = [tp_shard_weight(a, -1, 1, N) for a in down]
+        del up, down
+        self.mid = [torch.empty((T, F // N), dtype=torch.bfloat16, device=device) for _ in range(N)]
+        self.y = torch.empty((T, D), dtype=torch.float32, device=device)
+        self.flops = 2.0 * T * 2 * D * F
+        self.weight_bytes = 2 * D * F * (0.5 + 4.0 / 64)
+
+    def step(self, x=None, stream=None):
+        tp_q4_all_to_sharded(self.x if x is None else x, *self.up, out=self.mid, stream=stream)
+        tp_q4_sharded_to_all(self.mid, *self.down, out=self.y, stream=stream)
+        return self.y

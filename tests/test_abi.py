@@ -1,0 +1,112 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every function
+include/tp_api.h declares, and rejects bad arguments on the host with the
+documented status codes before any CUDA call (so no GPU is needed)."""
+import ctypes
+
+import pytest
+
+import sharded_gemm_gb300 as tp
+from sharded_gemm_gb300 import build as tpbuild
+
+FAKE = 0x10000  # a non-null, 16-byte aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module")
+def L():
+    tpbuild.build()
+    return tp.lib()
+
+
+def _arr(n, v=FAKE):
+    a = (ctypes.c_void_p * n)(*([v] * n))
+    return ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)), a
+
+
+def test_exports_every_declared_symbol(L):
+    names = tp.declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version(L):
+    assert L.tp_version() >= 100
+
+
+def test_all_to_sharded_not_divisible_message(L):
+    w, k1 = _arr(2)
+    y, k2 = _arr(2)
+    rc = L.tp_all_to_sharded(2, FAKE, 4, 2, 2, w, 3, None, tp.TP_F32, y, 2, tp.TP_F32, None)
+    assert rc == tp.TP_ERR_NOT_DIVISIBLE
+    assert tp.tp_last_error() == "Cannot shard the output of size 3 across 2 devices."
+
+
+def test_all_to_sharded_invalid_args(L):
+    w, k1 = _arr(2)
+    y, k2 = _arr(2)
+    assert L.tp_all_to_sharded(0, FAKE, 4, 2, 2, w, 2, None, 0, y, 1, 0, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_all_to_sharded(2, None, 4, 2, 2, w, 2, None, 0, y, 1, 0, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_all_to_sharded(2, FAKE, 4, 2, 1, w, 2, None, 0, y, 1, 0, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_all_to_sharded(2, FAKE, 4, 2, 2, w, 2, None, 7, y, 1, 0, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_all_to_sharded(2, FAKE + 1, 4, 2, 2, w, 2, None, tp.TP_F32, y, 1, 0, None) == tp.TP_ERR_ALIGNMENT
+    wn, k3 = _arr(2, None)
+    assert L.tp_all_to_sharded(2, FAKE, 4, 2, 2, wn, 2, None, 0, y, 1, 0, None) == tp.TP_ERR_INVALID_ARG
+
+
+def test_empty_batch_launches_nothing(L):
+    w, k1 = _arr(2)
+    y, k2 = _arr(2)
+    assert L.tp_all_to_sharded(2, FAKE, 0, 2, 2, w, 2, None, tp.TP_BF16, y, 1, tp.TP_F32, None) == tp.TP_OK
+    x, k3 = _arr(2)
+    assert L.tp_sharded_to_all(2, x, 0, 4, 2, w, 3, None, tp.TP_BF16, FAKE, 3, tp.TP_F32, None) == tp.TP_OK
+
+
+def test_sharded_to_all_not_divisible(L):
+    x, k1 = _arr(4)
+    w, k2 = _arr(4)
+    rc = L.tp_sharded_to_all(4, x, 2, 10, 10, w, 3, None, tp.TP_BF16, FAKE, 3, tp.TP_F32, None)
+    assert rc == tp.TP_ERR_NOT_DIVISIBLE
+
+
+def test_summa_checks(L):
+    b, k = _arr(16)
+    assert L.tp_summa(0, b, b, b, 8, 8, 8, tp.TP_BF16, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert L.tp_summa(3, b, b, b, 8, 9, 9, tp.TP_BF16, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert L.tp_summa(5, b, b, b, 10, 10, 10, tp.TP_BF16, None) == tp.TP_ERR_UNSUPPORTED
+    assert L.tp_summa(2, None, b, b, 8, 8, 8, tp.TP_BF16, None) == tp.TP_ERR_INVALID_ARG
+
+
+def test_shard_weight_checks(L):
+    s, k = _arr(2)
+    assert L.tp_shard_weight(FAKE, 10, 4, 2, 0, 3, 2, s, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert tp.tp_last_error() == "Cannot shard the output of size 10 across 6 devices."
+    assert L.tp_shard_weight(FAKE, 8, 4, 3, 0, 1, 2, s, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_shard_weight(FAKE, 8, 4, 2, 2, 1, 2, s, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_shard_weight(FAKE, 8, 4, 2, 0, 0, 2, s, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_shard_weight(FAKE, 8, 4, 2, 0, 1, 65, s, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_shard_weight(FAKE + 1, 8, 4, 2, 0, 1, 2, s, None) == tp.TP_ERR_ALIGNMENT
+
+
+def test_q4_checks(L):
+    a, k = _arr(8)
+    assert L.tp_q4_quantize(FAKE, 4, 128, 32, FAKE, FAKE, FAKE, None) == tp.TP_ERR_UNSUPPORTED
+    assert L.tp_q4_quantize(FAKE, 4, 100, 64, FAKE, FAKE, FAKE, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert L.tp_q4_all_to_sharded(8, FAKE, 1, 128, a, a, a, 32, 64, None, a, 8, tp.TP_BF16, None) == tp.TP_ERR_UNSUPPORTED
+    assert L.tp_q4_all_to_sharded(8, FAKE, 1, 128, a, a, a, 64, 60, None, a, 8, tp.TP_BF16, None) == tp.TP_ERR_NOT_DIVISIBLE
+    # each shard must hold whole groups: K/N = 96 is not a multiple of 64
+    assert L.tp_q4_sharded_to_all(8, a, 1, 768, a, a, a, 64, 16, None, FAKE, 16, tp.TP_F32, None) == tp.TP_ERR_NOT_DIVISIBLE
+
+
+def test_policy_and_wait_limit_checks(L):
+    assert L.tp_set_policy(7) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_set_policy(tp.TP_POLICY_AUTO) == tp.TP_OK
+    assert L.tp_set_wait_limit_ns(10) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_set_wait_limit_ns(2_000_000_000) == tp.TP_OK
+    assert L.tp_debug_wait_timeout(5, None) == tp.TP_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(tp, "_lib", None)
+    monkeypatch.setattr(tp, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        tp.tp_version()

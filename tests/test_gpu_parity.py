@@ -1,0 +1,295 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Small cases span several tiles with ragged tails in every dimension and run
+under both kernel policies (tensor-core AUTO and the CUDA-core SIMT
+cross-check).  Full-size cases use the workloads' real shapes, in the launch
+configuration the bench times, and compare sampled outputs.
+"""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sharded_gemm_gb300 as tp
+from sharded_gemm_gb300 import build as tpbuild
+from sharded_gemm_gb300 import synth
+from sharded_gemm_gb300.workloads import MLPPair, Q4Pair, QKV, Summa, to_device, to_host
+from gpu_util import bf16, check_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+RNG = np.random.default_rng(2024)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    tpbuild.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+    tp.tp_set_policy(tp.TP_POLICY_AUTO)
+
+
+@pytest.fixture(params=[tp.TP_POLICY_AUTO, tp.TP_POLICY_SIMT], ids=["auto", "simt"])
+def policy(request):
+    tp.tp_set_policy(request.param)
+    yield request.param
+    tp.tp_set_policy(tp.TP_POLICY_AUTO)
+
+
+def _status_ok():
+    assert tp.tp_query_status() == 0
+
+
+def rand_bf16(shape, std=1.0):
+    return synth.f32_to_bf16_bits((RNG.standard_normal(shape) * std).astype(np.float32))
+
+
+# ------------------------------------------------------------------ a1 slicing
+@pytest.mark.parametrize("dtype", [np.uint16, np.uint32, np.float16, np.uint8, np.uint64])
+@pytest.mark.parametrize("axis,S,N,rows,cols", [
+    (0, 1, 4, 8, 12), (0, 3, 2, 12, 6), (1, 1, 8, 5, 16), (-1, 3, 4, 3, 24), (0, 1, 1, 7, 3),
+    (1, 2, 2, 4, 12)])
+def test_shard_weight_bitexact(dtype, axis, S, N, rows, cols):
+    w = RNG.integers(0, 255, size=(rows, cols)).astype(dtype)
+    dev = torch.from_numpy(w.view({1: np.uint8, 2: np.int16, 4: np.int32, 8: np.int64}[w.itemsize])).cuda()
+    got = tp.tp_shard_weight(dev, axis, S, N)
+    ref = oracle.shard(w, axis, S, N)
+    for r in range(N):
+        g = got[r].cpu().numpy().view(dtype)
+        assert g.shape == ref[r].shape
+        assert g.tobytes() == ref[r].tobytes(), r
+
+
+def test_shard_weight_bias_1d():
+    b = RNG.standard_normal(24).astype(np.float32)
+    got = tp.tp_shard_weight(torch.from_numpy(b).cuda(), 0, 3, 4)
+    for g, r in zip(got, oracle.shard(b, 0, 3, 4)):
+        assert g.cpu().numpy().tobytes() == r.tobytes()
+
+
+def test_shard_weight_not_divisible_raises():
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_shard_weight(torch.zeros((10, 4), device="cuda"), 0, 1, 4)
+    assert e.value.code == tp.TP_ERR_NOT_DIVISIBLE
+    assert "Cannot shard the output of size 10 across 4 devices." in e.value.msg
+
+
+# ------------------------------------------------------------------ worked example
+def test_worked_example(policy):
+    cfg = synth.worked()
+    pair = MLPPair(cfg)
+    pair.step()
+    torch.cuda.synchronize()
+    _status_ok()
+    x = oracle.widen(cfg["x"], "f32")
+    w1 = [oracle.widen(p, "f32") for p in oracle.shard(cfg["w1"], 0, 1, 2)]
+    b1 = [oracle.widen(p, "f32") for p in oracle.shard(cfg["b1"], 0, 1, 2)]
+    w2 = [oracle.widen(p, "f32") for p in oracle.shard(cfg["w2"], -1, 1, 2)]
+    ref_mid = oracle.all_to_sharded(x, w1, b1)
+    assert [tuple(m.shape) for m in pair.mid] == [(4, 1), (4, 1)]
+    assert [tuple(w.shape) for w in pair.w1] == [(1, 2), (1, 2)]
+    assert [tuple(w.shape) for w in pair.w2] == [(2, 1), (2, 1)]
+    for r in range(2):
+        check_close(to_host(pair.mid[r]), ref_mid[r], "mid %d" % r)
+    ref = oracle.sharded_to_all([to_host(m) for m in pair.mid], w2, oracle.widen(cfg["b2"], "f32"))
+    check_close(to_host(pair.y), ref, "y")
+    assert np.abs(to_host(pair.y) - ref).max() < 1e-5
+
+
+# ------------------------------------------------------------------ a2 column-parallel
+@pytest.mark.parametrize("T,K,On,N", [(1, 64, 128, 2), (5, 192, 40, 4), (130, 320, 600, 2),
+                                      (300, 200, 264, 3), (17, 512, 256, 8), (256, 128, 512, 1)])
+@pytest.mark.parametrize("out_dt", [torch.bfloat16, torch.float32])
+def test_all_to_sharded(policy, T, K, On, N, out_dt):
+    x = rand_bf16((T, K))
+    w = rand_bf16((On * N, K), 0.05)
+    b = (RNG.standard_normal(On * N) * 0.1).astype(np.float32)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), 0, 1, N)
+    bs = tp.tp_shard_weight(to_device(b, "f32"), 0, 1, N)
+    ys = tp.tp_all_to_sharded(to_device(x, "bf16"), ws, bs, out_dtype=out_dt)
+    _status_ok()
+    ref = oracle.all_to_sharded(bf16(x), [bf16(p) for p in oracle.shard(w, 0, 1, N)],
+                                [p.astype(np.float64) for p in oracle.shard(b, 0, 1, N)])
+    for r in range(N):
+        check_close(to_host(ys[r]), ref[r], "shard %d" % r)
+
+
+def test_all_to_sharded_gathered_output(policy):
+    # vocab-parallel head: every shard writes its columns of one (T, O) buffer
+    T, K, N, On = 70, 256, 4, 300
+    x = rand_bf16((T, K))
+    w = rand_bf16((On * N, K), 0.05)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), 0, 1, N)
+    full = torch.full((T, On * N), float("nan"), device="cuda")
+    views = [full[:, r * On:(r + 1) * On] for r in range(N)]
+    tp.tp_all_to_sharded(to_device(x, "bf16"), ws, None, out=views)
+    _status_ok()
+    check_close(to_host(full), oracle.linear(bf16(x), bf16(w)), "gathered")
+
+
+def test_all_to_sharded_fused_qkv_segments(policy):
+    T, D, N = 33, 256, 4
+    x = rand_bf16((T, D))
+    w = rand_bf16((3 * D, D), 0.05)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), 0, 3, N)
+    ys = tp.tp_all_to_sharded(to_device(x, "bf16"), ws, None, out_dtype=torch.float32)
+    _status_ok()
+    full = oracle.linear(bf16(x), bf16(w))
+    wl = D // N
+    for r in range(N):
+        cols = [s * D + r * wl + i for s in range(3) for i in range(wl)]
+        check_close(to_host(ys[r]), full[:, cols], "qkv shard %d" % r)
+
+
+# ------------------------------------------------------------------ a3 row-parallel
+@pytest.mark.parametrize("T,Kn,O,N", [(1, 64, 256, 2), (5, 96, 40, 4), (130, 320, 300, 4),
+                                      (200, 200, 520, 3), (64, 512, 128, 8), (129, 128, 129, 1)])
+def test_sharded_to_all(policy, T, Kn, O, N):
+    x = rand_bf16((T, Kn * N))
+    w = rand_bf16((O, Kn * N), 0.05)
+    b = (RNG.standard_normal(O) * 0.1).astype(np.float32)
+    xs = tp.tp_shard_weight(to_device(x, "bf16"), -1, 1, N)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), -1, 1, N)
+    y = tp.tp_sharded_to_all(xs, ws, to_device(b, "f32"))
+    _status_ok()
+    ref = oracle.sharded_to_all([bf16(p) for p in oracle.shard(x, -1, 1, N)],
+                                [bf16(p) for p in oracle.shard(w, -1, 1, N)], b.astype(np.float64))
+    check_close(to_host(y), ref, "row")
+
+
+def test_sharded_to_all_strided_input_columns(policy):
+    # W_o style: x split by columns as strided views of one (T, K) buffer
+    T, K, O, N = 48, 512, 192, 8
+    x = rand_bf16((T, K))
+    w = rand_bf16((O, K), 0.05)
+    xd = to_device(x, "bf16")
+    views = [xd[:, r * (K // N):(r + 1) * (K // N)] for r in range(N)]
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), -1, 1, N)
+    y = tp.tp_sharded_to_all(views, ws, None, out_dtype=torch.bfloat16)
+    _status_ok()
+    check_close(to_host(y), oracle.linear(bf16(x), bf16(w)), "strided row")
+
+
+def test_mlp_pair_small(policy):
+    cfg = synth.mlp(seed=3, T=150, D=256, F=688, N=4, bias_std=0.1)
+    pair = MLPPair(cfg)
+    pair.step()
+    _status_ok()
+    x = bf16(cfg["x"])
+    ref_mid = oracle.all_to_sharded(x, [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, 4)],
+                                    [p.astype(np.float64) for p in oracle.shard(cfg["b1"], 0, 1, 4)])
+    mids = [to_host(m) for m in pair.mid]
+    for r in range(4):
+        check_close(mids[r], ref_mid[r], "mid %d" % r)
+    w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, 4)]
+    check_close(to_host(pair.y), oracle.sharded_to_all(mids, w2, cfg["b2"].astype(np.float64)), "y (layer)")
+    chain = oracle.linear(oracle.linear(x, bf16(cfg["w1"]), cfg["b1"]), bf16(cfg["w2"]), cfg["b2"])
+    check_close(to_host(pair.y), chain, "y (end to end)")
+
+
+# ------------------------------------------------------------------ a5 SUMMA
+@pytest.mark.parametrize("q,M,K,Nc", [(1, 128, 128, 256), (2, 272, 320, 528), (4, 512, 256, 1024),
+                                      (2, 48, 64, 48), (4, 544, 544, 544)])
+def test_summa(policy, q, M, K, Nc):
+    cfg = synth.summa(seed=5, M=M, K=K, Ncols=Nc)
+    s = Summa(cfg, q)
+    s.step()
+    _status_ok()
+    Xb = [bf16(b) for b in oracle.blocks(cfg["X"], q)]
+    Ab = [bf16(b) for b in oracle.blocks(cfg["A"], q)]
+    ref = oracle.summa(Xb, Ab, q)
+    for b in range(q * q):
+        check_close(to_host(s.Y[b]), ref[b], "block %d" % b)
+
+
+def test_summa_identity_x_returns_a(policy):
+    q, n = 2, 256
+    X = synth.f32_to_bf16_bits(np.eye(n, dtype=np.float32))
+    A = rand_bf16((n, n))
+    s = Summa(dict(M=n, K=n, Ncols=n, dtype="bf16", X=X, A=A), q)
+    s.step()
+    _status_ok()
+    got = oracle.unblock([to_host(y) for y in s.Y], q)
+    assert np.array_equal(got, bf16(A))
+
+
+# ------------------------------------------------------------------ a6 / a7 4-bit
+@pytest.mark.parametrize("rows,K", [(1, 64), (37, 512), (256, 1024)])
+def test_quantize_bitexact(rows, K):
+    w = (RNG.standard_normal((rows, K)) * 0.02).astype(np.float32)
+    w[0, :64] = 0.25                 # constant group -> unit scale
+    if K >= 192:
+        w[0, 64:128] = np.float32(1e-9) * np.arange(64, dtype=np.float32)   # scale rounds to 0 in f16
+        w[0, 128:192] = np.float32(1e-7) * np.arange(64, dtype=np.float32)  # f16-subnormal scale
+    wq, sc, qb = tp.tp_q4_quantize(torch.from_numpy(w).cuda())
+    rq, rs, rb = oracle.quantize_affine4(w, 64)
+    assert wq.cpu().numpy().view(np.uint32).tobytes() == rq.tobytes()
+    assert sc.cpu().numpy().tobytes() == rs.tobytes()
+    assert qb.cpu().numpy().tobytes() == rb.tobytes()
+
+
+def _q4_host(rows, K, seed):
+    w = (np.random.default_rng(seed).standard_normal((rows, K)) * 0.02).astype(np.float32)
+    return oracle.quantize_affine4(w, 64)
+
+
+@pytest.mark.parametrize("T,K,On,N", [(1, 256, 128, 2), (16, 512, 200, 4), (40, 1024, 136, 8), (256, 128, 64, 1)])
+def test_q4_all_to_sharded(policy, T, K, On, N):
+    x = rand_bf16((T, K))
+    pq, ps, pb = _q4_host(On * N, K, T + K)
+    shards = [tp.tp_shard_weight(to_device(a, k), 0, 1, N) for a, k in ((pq, "u32"), (ps, "f16"), (pb, "f16"))]
+    ys = tp.tp_q4_all_to_sharded(to_device(x, "bf16"), *shards, out_dtype=torch.float32)
+    _status_ok()
+    ref = oracle.q4_all_to_sharded(bf16(x), oracle.shard(pq, 0, 1, N), oracle.shard(ps, 0, 1, N),
+                                   oracle.shard(pb, 0, 1, N), 64)
+    for r in range(N):
+        check_close(to_host(ys[r]), ref[r], "q4 col shard %d" % r)
+
+
+@pytest.mark.parametrize("T,Kn,O,N", [(1, 128, 256, 2), (16, 64, 130, 8), (33, 256, 72, 4), (256, 192, 128, 2)])
+def test_q4_sharded_to_all(policy, T, Kn, O, N):
+    x = rand_bf16((T, Kn * N))
+    pq, ps, pb = _q4_host(O, Kn * N, O + Kn)
+    b = (RNG.standard_normal(O) * 0.1).astype(np.float32)
+    xs = tp.tp_shard_weight(to_device(x, "bf16"), -1, 1, N)
+    shards = [tp.tp_shard_weight(to_device(a, k), -1, 1, N) for a, k in ((pq, "u32"), (ps, "f16"), (pb, "f16"))]
+    y = tp.tp_q4_sharded_to_all(xs, *shards, bias=to_device(b, "f32"))
+    _status_ok()
+    ref = oracle.q4_sharded_to_all([bf16(p) for p in oracle.shard(x, -1, 1, N)], oracle.shard(pq, -1, 1, N),
+                                   oracle.shard(ps, -1, 1, N), oracle.shard(pb, -1, 1, N), 64, b.astype(np.float64))
+    check_close(to_host(y), ref, "q4 row")
+
+
+# ------------------------------------------------------------------ determinism, faults
+def _digest(ts):
+    h = hashlib.sha256()
+    for t in ts:
+        h.update(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
+def test_repeat_runs_bit_identical(policy):
+    cfg = synth.mlp(seed=11, T=260, D=512, F=1376, N=4)
+    pair = MLPPair(cfg)
+    digests = set()
+    for _ in range(5):
+        pair.y.fill_(0)
+        pair.step()
+        digests.add(_digest(pair.mid + [pair.y]))
+    _status_ok()
+    assert len(digests) == 1
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    tp.tp_debug_wait_timeout(50_000_000)
+    assert tp.tp_query_status() == tp.TP_ERR_TIMEOUT
+    assert tp.tp_query_status() == 0  # the word was cleared
+    # the context is still usable
+    x = to_device(rand_bf16((8, 64)), "bf16")
+    w = [to_device(rand_bf16((16, 64)), "bf16")]
+    y = tp.tp_all_to_sharded(x, w, None, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_query_status() == 0
+    assert torch.isfinite(y[0]).all()
