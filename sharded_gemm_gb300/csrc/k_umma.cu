@@ -62,7 +62,7 @@ struct UmmaArgs {
   CUtensorMap mapB[kMaxMaps];
   UJob jobs[kMaxJobs];
   UPart parts[kMaxParts];
-  int njobs, total_units;
+  int njobs, total_units, nmapA, nmapB;
   int chain, out_dt, vec_ok;
   uint32_t idesc;
   int *status;
@@ -220,10 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < kMaxMaps && i < 8; ++i) {
-      prefetch_tmap(&a.mapA[i]);
-      prefetch_tmap(&a.mapB[i]);
-    }
+    for (int i = 0; i < a.nmapA && i < 8; ++i) prefetch_tmap(&a.mapA[i]);
+    for (int i = 0; i < a.nmapB && i < 8; ++i) prefetch_tmap(&a.mapB[i]);
   }
   tc_fence_before();
   __syncthreads();
@@ -580,6 +578,8 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   }
   if (units > INT32_MAX) return TP_OK;
   args.njobs = p.njobs;
+  args.nmapA = nA;
+  args.nmapB = nB;
   args.total_units = (int)units;
   args.chain = p.chain;
   args.out_dt = p.out_dt;

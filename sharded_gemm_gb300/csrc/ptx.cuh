@@ -58,14 +58,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase with `parity` of barrier `bar` completes.  Gives up
-// after `limit_ns` of wall time, or as soon as *abort (shared memory) is set
-// by another thread of the CTA.  On giving up by time it records
-// TP_ERR_TIMEOUT (-6) in *status (first error wins) and sets *abort.
-// Returns true if the phase completed.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                       int *status, volatile int *abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: spins with try_wait until the phase completes,
+// `limit_ns` of wall time passes, or *abort (shared memory) is set by another
+// thread of the CTA.  Running out of time records TP_ERR_TIMEOUT (-6) in
+// *status (first error wins) and sets *abort.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                            int *status, volatile int *abort) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -78,6 +76,14 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t l
       }
     }
   }
+}
+
+// Waits until the phase with `parity` of barrier `bar` completes (bounded, see
+// mbar_wait_slow).  Returns true if the phase completed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                          int *status, volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, limit_ns, status, abort);
 }
 
 // ------------------------------------------------------------------ TMA
