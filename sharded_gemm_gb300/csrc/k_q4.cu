@@ -1,7 +1,33 @@
-// k_q4.cu -- 4-bit affine (group 64) kernels: a6 device quantizer, and the
-// dispatch of the dequant-fused linears (a7).
+// k_q4.cu -- 4-bit affine (group 64) kernels: the a6 device quantizer and the
+// dequant-fused tensor-core linears of a7.
+//
+// q4_umma_kernel builds the WEIGHT operand of tcgen05.mma in tensor memory:
+// converter warps read the packed codes that TMA brought into shared memory,
+// expand them in registers and write them to TMEM with tcgen05.st; the MMA
+// takes A from TMEM and the activations x (B, K-major, 128B-swizzled) from
+// shared memory.  Weight rows fill the M = 128 dimension, tokens the N
+// dimension (swap-AB), and the epilogue stores the transpose.
+//
+// Decode (T <= 16): the codes enter the MMA as the exact integers 0..15
+// (bf16), one TMEM partial D_g per 64-element group g, and the epilogue forms
+//   y[t][o] = sum_g ( s[o][g] * D_g[o][t] + b[o][g] * X_g[t] ),
+//   X_g[t] = sum_{k in g} x[t][k],
+// in float32.  Lane 31 of every 32-lane quarter of the tile is a row of ones,
+// so the tensor core computes X_g alongside D_g (124 weight rows per tile).
+// Prefill (T > 16): the converter writes the dequantized values
+// s*q + b (float32, rounded once to bf16) and the groups accumulate in one
+// TMEM accumulator.
+// Small-T tiles are split over CTAs by K (rank by rank for the row-parallel
+// layer); each split's float32 partial goes to a workspace slot and the CTA
+// that arrives last at the tile's counter adds the slots in split order (rank
+// order), then the bias once.  No CTA ever waits for another.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <string.h>
 
+#include <mutex>
+
+#include "ptx.cuh"
 #include "tp_internal.h"
 
 namespace tp {
@@ -73,11 +99,720 @@ int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void 
   return e == cudaSuccess ? TP_OK : cuda_error(e, "quantize kernel launch");
 }
 
-int launch_q4(const Problem &p, cudaStream_t s, bool *handled) {
+// ====================================================================== q4 tcgen05
+namespace {
+
+constexpr int kQThreads = 14 * 32;  // producer, MMA, 8 converter warps, 4 epilogue warps
+
+struct Q4Part {
+  const uint16_t *sc, *qb;  // float16 bits, (rows, groups)
+  int groups;               // K / 64
+  int16_t cmap, xmap;
+  int nchunk, chunk_groups;
+};
+
+struct Q4Job {
+  void *C;
+  const float *bias;
+  int64_t ldc;
+  int rows, T;
+  int part0, nparts;
+  int tiles, ntiles, splits;
+  int unit_begin;
+  int cnt_base;
+  int64_t ws_base;  // first partial slot of this job (slot = 128 x 16 floats)
+};
+
+struct Q4Args {
+  CUtensorMap cmaps[kMaxParts];
+  CUtensorMap xmaps[kMaxParts];
+  Q4Job jobs[kMaxJobs];
+  Q4Part parts[kMaxParts];
+  int njobs, total_units, ncm, nxm;
+  int out_dt;
+  uint32_t idesc;
+  float *ws;
+  int *cnt;
+  int *status;
+  uint64_t wait_ns;
+};
+
+template <bool DECODE>
+struct Q4Cfg;
+template <>
+struct Q4Cfg<true> {
+  static constexpr int BN = 16, GS = 4, STAGES = 8, NA = 8, ND = 8, ROWS = 124;
+  static constexpr int CODES_BYTES = 16384, XBOX = 2048, X_BYTES = 4 * 2048;
+  static constexpr int CODES_TX = 124 * 128, X_TX = 4 * 2048;
+  static constexpr int A_COL0 = 0, D_COL0 = 256;
+};
+template <>
+struct Q4Cfg<false> {
+  static constexpr int BN = 256, GS = 1, STAGES = 5, NA = 8, ND = 1, ROWS = 128;
+  static constexpr int CODES_BYTES = 4096, XBOX = 32768, X_BYTES = 32768;
+  static constexpr int CODES_TX = 4096, X_TX = 32768;
+  static constexpr int A_COL0 = 256, D_COL0 = 0;
+};
+
+struct UnitInfo {
+  int job, part, tile, ntile, tile_lin, sidx, g0, g1;
+};
+
+__device__ __forceinline__ void q4_decode_unit(const Q4Args &a, int u, UnitInfo &ui) {
+  int j = 0;
+  while (j + 1 < a.njobs && u >= a.jobs[j + 1].unit_begin) ++j;
+  const Q4Job &J = a.jobs[j];
+  const int local = u - J.unit_begin;
+  ui.job = j;
+  ui.tile_lin = local / J.splits;
+  ui.sidx = local - ui.tile_lin * J.splits;
+  ui.tile = ui.tile_lin % J.tiles;
+  ui.ntile = ui.tile_lin / J.tiles;
+  int p = 0, c = ui.sidx;
+  while (p + 1 < J.nparts && c >= a.parts[J.part0 + p].nchunk) {
+    c -= a.parts[J.part0 + p].nchunk;
+    ++p;
+  }
+  const Q4Part &P = a.parts[J.part0 + p];
+  ui.part = J.part0 + p;
+  ui.g0 = c * P.chunk_groups;
+  ui.g1 = min(P.groups, ui.g0 + P.chunk_groups);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// Eight 4-bit codes (one word, element e at bits 4e) -> four bf16x2 words of
+// the exact integers, natural element order (low half = even element).
+// 0x4300 | n is the bf16 of 128 + n; one fused multiply-add by (1, 1) and
+// (-128, -128) returns n exactly.
+__device__ __forceinline__ void codes_to_int_bf16(uint32_t w, uint32_t *o) {
+  const uint32_t a = (w & 0x000F000Fu) | 0x43004300u;          // (n0, n4)
+  const uint32_t b = ((w >> 4) & 0x000F000Fu) | 0x43004300u;   // (n1, n5)
+  const uint32_t c = ((w >> 8) & 0x000F000Fu) | 0x43004300u;   // (n2, n6)
+  const uint32_t d = ((w >> 12) & 0x000F000Fu) | 0x43004300u;  // (n3, n7)
+  const uint32_t one = 0x3F803F80u, m128 = 0xC300C300u;
+  o[0] = fma_bf16x2(prmt(a, b, 0x5410), one, m128);  // (n0, n1)
+  o[1] = fma_bf16x2(prmt(c, d, 0x5410), one, m128);  // (n2, n3)
+  o[2] = fma_bf16x2(prmt(a, b, 0x7632), one, m128);  // (n4, n5)
+  o[3] = fma_bf16x2(prmt(c, d, 0x7632), one, m128);  // (n6, n7)
+}
+
+// Eight codes -> four bf16x2 words of s*code + b (float32 math, one rounding).
+// 0x4B000000 | n is the float 2^23 + n; subtracting 2^23 gives n exactly.
+__device__ __forceinline__ void codes_to_values_bf16(uint32_t w, float s, float b, uint32_t *o) {
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const float q0 = __uint_as_float(((w >> (4 * e)) & 0xFu) | 0x4B000000u) - 8388608.0f;
+    const float q1 = __uint_as_float(((w >> (4 * e + 4)) & 0xFu) | 0x4B000000u) - 8388608.0f;
+    __nv_bfloat162 h = __floats2bfloat162_rn(fmaf(s, q0, b), fmaf(s, q1, b));
+    o[e / 2] = *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+
+__device__ __forceinline__ void q4_store(const Q4Args &a, const Q4Job &J, int t, int orow, float v) {
+  const int64_t idx = (int64_t)t * J.ldc + orow;
+  if (a.out_dt == TP_F32)
+    static_cast<float *>(J.C)[idx] = v;
+  else if (a.out_dt == TP_BF16)
+    static_cast<uint16_t *>(J.C)[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  else
+    static_cast<uint16_t *>(J.C)[idx] = __half_as_ushort(__float2half_rn(v));
+}
+
+#define Q4_WAIT_ALL(bar, par, okvar)                                                   \
+  {                                                                                    \
+    const bool _r = mbar_wait((bar), (par), lim, a.status, &abort_sh);                 \
+    if (!__all_sync(0xffffffffu, _r)) {                                                \
+      okvar = false;                                                                   \
+    }                                                                                  \
+  }
+
+template <bool DECODE>
+__global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_constant__ Q4Args a) {
+  using C = Q4Cfg<DECODE>;
+  constexpr int STAGE_BYTES = C::CODES_BYTES + C::X_BYTES;
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[C::STAGES], empty_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t afull_bar[C::NA], aempty_bar[C::NA];
+  __shared__ __align__(8) uint64_t dfull_bar[C::ND], dempty_bar[C::ND];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint64_t lim = a.wait_ns;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), 1);
+    }
+    for (int i = 0; i < C::NA; ++i) {
+      mbar_init(smem_u32(&afull_bar[i]), 8);
+      mbar_init(smem_u32(&aempty_bar[i]), 1);
+    }
+    for (int i = 0; i < C::ND; ++i) {
+      mbar_init(smem_u32(&dfull_bar[i]), 1);
+      mbar_init(smem_u32(&dempty_bar[i]), 4);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      bool used[C::STAGES];
+      uint32_t lastph[C::STAGES];
+#pragma unroll
+      for (int i = 0; i < C::STAGES; ++i) used[i] = false;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        UnitInfo ui;
+        q4_decode_unit(a, u, ui);
+        const Q4Part &P = a.parts[ui.part];
+        for (int gs = ui.g0; gs < ui.g1; gs += C::GS) {
+          if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          const uint32_t base = sbase + st * STAGE_BYTES;
+          const uint32_t fb = smem_u32(&full_bar[st]);
+          mbar_arrive_expect_tx(fb, C::CODES_TX + C::X_TX);
+          tma_load_2d(base, &a.cmaps[P.cmap], fb, gs * 8, ui.tile * C::ROWS);
+#pragma unroll
+          for (int gi = 0; gi < C::GS; ++gi)
+            tma_load_2d(base + C::CODES_BYTES + gi * C::XBOX, &a.xmaps[P.xmap], fb, (gs + gi) * 64,
+                        ui.ntile * C::BN);
+          used[st] = true;
+          lastph[st] = ph;
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok)
+        for (int i = 0; i < C::STAGES; ++i)
+          if (used[i]) mbar_wait(smem_u32(&full_bar[i]), lastph[i], lim, a.status, nullptr);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int st = 0, as = 0, ds = 0;
+      uint32_t ph = 0, aph = 0, dph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        UnitInfo ui;
+        q4_decode_unit(a, u, ui);
+        bool first = true;
+        for (int gs = ui.g0; ok && gs < ui.g1; gs += C::GS) {
+          if (!mbar_wait(smem_u32(&full_bar[st]), ph, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t base = sbase + st * STAGE_BYTES;
+          const int ng = min(C::GS, ui.g1 - gs);
+          for (int gi = 0; gi < ng; ++gi) {
+            if (!mbar_wait(smem_u32(&afull_bar[as]), aph, lim, a.status, &abort_sh)) {
+              ok = false;
+              break;
+            }
+            if (DECODE || first) {
+              if (!mbar_wait(smem_u32(&dempty_bar[ds]), dph ^ 1, lim, a.status, &abort_sh)) {
+                ok = false;
+                break;
+              }
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + C::D_COL0 + ds * C::BN;
+            const uint32_t xb = base + C::CODES_BYTES + (DECODE ? gi * C::XBOX : 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = DECODE ? (kk > 0 ? 1u : 0u) : ((first && kk == 0) ? 0u : 1u);
+              umma_f16_ts(d, tmem + C::A_COL0 + as * 32 + kk * 8,
+                          umma_desc_sw128(xb + kk * 32, 16, 1024), a.idesc, acc);
+            }
+            umma_commit(smem_u32(&aempty_bar[as]));
+            if (++as == C::NA) {
+              as = 0;
+              aph ^= 1;
+            }
+            if (DECODE) {
+              umma_commit(smem_u32(&dfull_bar[ds]));
+              if (++ds == C::ND) {
+                ds = 0;
+                dph ^= 1;
+              }
+            }
+            first = false;
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&empty_bar[st]));
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!DECODE && ok) {
+          umma_commit(smem_u32(&dfull_bar[ds]));
+          if (++ds == C::ND) {
+            ds = 0;
+            dph ^= 1;
+          }
+        }
+      }
+      umma_commit(smem_u32(&drain_bar));
+      mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
+    }
+  } else if (warp < 10) {
+    // ---------------------------------------------------------- converters
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const bool ones = DECODE && lane == 31;
+    const int srow = DECODE ? quarter * 31 + lane : quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    int st = 0, as = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+      UnitInfo ui;
+      q4_decode_unit(a, u, ui);
+      const Q4Part &P = a.parts[ui.part];
+      const Q4Job &J = a.jobs[ui.job];
+      const int orow = ui.tile * C::ROWS + srow;
+      for (int gs = ui.g0; ok && gs < ui.g1; gs += C::GS) {
+        Q4_WAIT_ALL(smem_u32(&full_bar[st]), ph, ok);
+        if (!ok) break;
+        const uint32_t base = sbase + st * STAGE_BYTES;
+        const int ng = min(C::GS, ui.g1 - gs);
+        for (int gi = 0; gi < ng; ++gi) {
+          Q4_WAIT_ALL(smem_u32(&aempty_bar[as]), aph ^ 1, ok);
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t out[16];
+          if (DECODE) {
+            if (ones) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) out[i] = 0x3F803F80u;
+            } else {
+              const int c = gi * 2 + half;
+              const uint4 w = lds128(base + srow * 128 + ((c ^ (srow & 7)) << 4));
+              codes_to_int_bf16(w.x, out + 0);
+              codes_to_int_bf16(w.y, out + 4);
+              codes_to_int_bf16(w.z, out + 8);
+              codes_to_int_bf16(w.w, out + 12);
+            }
+          } else {
+            float sc = 0.f, bq = 0.f;
+            if (orow < J.rows) {
+              const int64_t gi64 = (int64_t)orow * P.groups + gs + gi;
+              sc = h2f(__ldg(P.sc + gi64));
+              bq = h2f(__ldg(P.qb + gi64));
+            }
+            const uint4 w = lds128(base + srow * 32 + half * 16);
+            codes_to_values_bf16(w.x, sc, bq, out + 0);
+            codes_to_values_bf16(w.y, sc, bq, out + 4);
+            codes_to_values_bf16(w.z, sc, bq, out + 8);
+            codes_to_values_bf16(w.w, sc, bq, out + 12);
+          }
+          tmem_st16(tmem + lane_off + C::A_COL0 + as * 32 + half * 16, out);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&afull_bar[as]));
+          if (++as == C::NA) {
+            as = 0;
+            aph ^= 1;
+          }
+        }
+        if (++st == C::STAGES) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const bool ones = DECODE && lane == 31;
+    const int srow = DECODE ? quarter * 31 + lane : m;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    int ds = 0;
+    uint32_t dph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+      UnitInfo ui;
+      q4_decode_unit(a, u, ui);
+      const Q4Part &P = a.parts[ui.part];
+      const Q4Job &J = a.jobs[ui.job];
+      const int orow = ui.tile * C::ROWS + srow;
+      const bool valid = !ones && orow < J.rows;
+      if constexpr (DECODE) {
+        float acc[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+        for (int g = ui.g0; g < ui.g1; ++g) {
+          Q4_WAIT_ALL(smem_u32(&dfull_bar[ds]), dph, ok);
+          if (!ok) break;
+          tc_fence_after();
+          float v[16];
+          tmem_ld16(tmem + lane_off + C::D_COL0 + ds * 16, v);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[ds]));
+          if (++ds == C::ND) {
+            ds = 0;
+            dph ^= 1;
+          }
+          float sc = 0.f, bq = 0.f;
+          if (valid) {
+            const int64_t gi64 = (int64_t)orow * P.groups + g;
+            sc = h2f(__ldg(P.sc + gi64));
+            bq = h2f(__ldg(P.qb + gi64));
+          }
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float xs = __shfl_sync(0xffffffffu, v[t], 31);
+            acc[t] = fmaf(sc, v[t], fmaf(bq, xs, acc[t]));
+          }
+        }
+        if (!ok) break;
+        if (J.splits == 1) {
+          if (valid) {
+            const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              if (t < J.T) q4_store(a, J, t, orow, acc[t] + bias);
+          }
+        } else {
+          // Split tile: every warp owns its 32 rows; the warp that arrives last
+          // at its (tile, quarter) counter adds the split partials in order.
+          float *slot = a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 + m) * C::BN;
+#pragma unroll
+          for (int t = 0; t < 16; t += 4)
+            __stcg(reinterpret_cast<float4 *>(slot + t), make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]));
+          __threadfence();
+          __syncwarp();
+          int prev = 0;
+          int *cnt = a.cnt + (int64_t)(J.cnt_base + ui.tile_lin) * 4 + quarter;
+          if (lane == 0) prev = atomicAdd(cnt, 1);
+          prev = __shfl_sync(0xffffffffu, prev, 0);
+          if (prev == J.splits - 1) {
+            __threadfence();
+            float sum[16];
+            const float *s0 = a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits) * 128 + m) * C::BN;
+#pragma unroll
+            for (int t = 0; t < 16; t += 4) {
+              const float4 f = __ldcg(reinterpret_cast<const float4 *>(s0 + t));
+              sum[t] = f.x;
+              sum[t + 1] = f.y;
+              sum[t + 2] = f.z;
+              sum[t + 3] = f.w;
+            }
+            for (int j = 1; j < J.splits; ++j) {
+              const float *sj = s0 + (int64_t)j * 128 * C::BN;
+#pragma unroll
+              for (int t = 0; t < 16; t += 4) {
+                const float4 f = __ldcg(reinterpret_cast<const float4 *>(sj + t));
+                sum[t] += f.x;
+                sum[t + 1] += f.y;
+                sum[t + 2] += f.z;
+                sum[t + 3] += f.w;
+              }
+            }
+            if (valid) {
+              const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
+#pragma unroll
+              for (int t = 0; t < 16; ++t)
+                if (t < J.T) q4_store(a, J, t, orow, sum[t] + bias);
+            }
+            __syncwarp();
+            if (lane == 0) *cnt = 0;  // ready for the next call
+          }
+        }
+      } else {
+        Q4_WAIT_ALL(smem_u32(&dfull_bar[ds]), dph, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float bias = (valid && J.bias) ? __ldg(J.bias + orow) : 0.f;
+        const int t0 = ui.ntile * C::BN;
+        const bool split = J.splits > 1;
+        float *slot = split ? a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 + m) * C::BN
+                            : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < C::BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tmem + lane_off + C::D_COL0 + ds * C::BN + c * 32, v);
+          tmem_wait_ld();
+          if (split) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              __stcg(reinterpret_cast<float4 *>(slot + c * 32 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+          } else if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int t = t0 + c * 32 + i;
+              if (t < J.T) q4_store(a, J, t, orow, v[i] + bias);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[ds]));
+        if (++ds == C::ND) {
+          ds = 0;
+          dph ^= 1;
+        }
+        if (split) {
+          __threadfence();
+          __syncwarp();
+          int prev = 0;
+          int *cnt = a.cnt + (int64_t)(J.cnt_base + ui.tile_lin) * 4 + quarter;
+          if (lane == 0) prev = atomicAdd(cnt, 1);
+          prev = __shfl_sync(0xffffffffu, prev, 0);
+          if (prev == J.splits - 1) {
+            __threadfence();
+            const float *s0 = a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits) * 128 + m) * C::BN;
+#pragma unroll 1
+            for (int c = 0; c < C::BN / 32; ++c) {
+              float sum[32];
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const float4 f = __ldcg(reinterpret_cast<const float4 *>(s0 + c * 32 + i));
+                sum[i] = f.x;
+                sum[i + 1] = f.y;
+                sum[i + 2] = f.z;
+                sum[i + 3] = f.w;
+              }
+              for (int j = 1; j < J.splits; ++j) {
+                const float *sj = s0 + (int64_t)j * 128 * C::BN + c * 32;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                  const float4 f = __ldcg(reinterpret_cast<const float4 *>(sj + i));
+                  sum[i] += f.x;
+                  sum[i + 1] += f.y;
+                  sum[i + 2] += f.z;
+                  sum[i + 3] += f.w;
+                }
+              }
+              if (valid) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const int t = t0 + c * 32 + i;
+                  if (t < J.T) q4_store(a, J, t, orow, sum[i] + bias);
+                }
+              }
+            }
+            __syncwarp();
+            if (lane == 0) *cnt = 0;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+std::mutex g_q4_mu;
+
+bool al16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+template <bool DECODE>
+int q4_launch_cfg(Q4Args &args, int sms, cudaStream_t s) {
+  using C = Q4Cfg<DECODE>;
+  auto kern = q4_umma_kernel<DECODE>;
+  constexpr int smem = C::STAGES * (C::CODES_BYTES + C::X_BYTES) + 1024;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(q4)");
+    attr_done[dev & 63] = true;
+  }
+  const int grid = args.total_units < sms ? args.total_units : sms;
+  kern<<<grid, kQThreads, smem, s>>>(args);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_error(e, "q4_umma_kernel launch");
+}
+
+// Chunks per part for the decode split: minimize waves x groups per unit.
+int choose_chunks(const Problem &p, int tiles_total_parts, int groups, int sms) {
+  int best = 1;
+  double best_cost = 1e300;
+  for (int c = 1; c <= 8 && c <= groups; ++c) {
+    const int cg = ((groups + c - 1) / c + 3) / 4 * 4;
+    const int nch = (groups + cg - 1) / cg;
+    if (nch != c && c > 1) continue;
+    const long units = (long)tiles_total_parts * nch;
+    const double waves = (double)((units + sms - 1) / sms);
+    const double cost = waves * (cg + 2.0) + (nch > 1 ? 1.0 : 0.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = c;
+    }
+  }
   (void)p;
-  (void)s;
-  *handled = false;  // dequant-fused tensor-core kernels not built yet
-  return TP_OK;
+  return best;
+}
+
+}  // namespace
+
+int launch_q4(const Problem &p, cudaStream_t s, bool *handled) {
+  *handled = false;
+  if (p.in_dt != TP_BF16) return TP_OK;
+  int64_t maxT = 0;
+  for (int j = 0; j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    if (J.M > maxT) maxT = J.M;
+    if (J.N > INT32_MAX / 2 || J.M > INT32_MAX / 2) return TP_OK;
+    for (int q = 0; q < J.nparts; ++q) {
+      const Part &P = p.parts[J.part0 + q];
+      if (!al16(P.A) || (P.lda % 8) || !al16(P.B) || (P.ldb % 4) || (P.K % 64)) return TP_OK;
+    }
+  }
+  const bool decode = maxT <= 16;
+  const int ROWS = decode ? 124 : 128;
+  const int BN = decode ? 16 : 256;
+  const int GS = decode ? 4 : 1;
+
+  std::lock_guard<std::mutex> lk(g_q4_mu);
+  const int sms = sm_count();
+  static Q4Args args;
+  memset(&args, 0, sizeof(args));
+
+  // split choice (decode): the same number of chunks for every part
+  int64_t tiles_parts = 0;
+  int groups_max = 0;
+  for (int j = 0; j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    const int tiles = (int)((J.N + ROWS - 1) / ROWS);
+    tiles_parts += (int64_t)tiles * J.nparts;
+    for (int q = 0; q < J.nparts; ++q) {
+      const int g = (int)(p.parts[J.part0 + q].K / 64);
+      if (g > groups_max) groups_max = g;
+    }
+  }
+  const int c = decode ? choose_chunks(p, (int)tiles_parts, groups_max, sms) : 1;
+
+  const void *cptr[kMaxParts], *xptr[kMaxParts];
+  int ncm = 0, nxm = 0;
+  int64_t units = 0, slots = 0;
+  int counters = 0;
+  for (int j = 0; j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    Q4Job &Q = args.jobs[j];
+    Q.C = J.C;
+    Q.bias = J.bias;
+    Q.ldc = J.ldc;
+    Q.rows = (int)J.N;
+    Q.T = (int)J.M;
+    Q.part0 = J.part0;
+    Q.nparts = J.nparts;
+    Q.tiles = (Q.rows + ROWS - 1) / ROWS;
+    Q.ntiles = decode ? 1 : (Q.T + BN - 1) / BN;
+    int splits = 0;
+    for (int q = 0; q < J.nparts; ++q) {
+      const Part &P = p.parts[J.part0 + q];
+      Q4Part &QP = args.parts[J.part0 + q];
+      QP.sc = (const uint16_t *)P.scales;
+      QP.qb = (const uint16_t *)P.qbias;
+      QP.groups = (int)(P.K / 64);
+      int cg = (QP.groups + c - 1) / c;
+      cg = (cg + GS - 1) / GS * GS;
+      if (cg > QP.groups) cg = QP.groups;
+      QP.chunk_groups = cg;
+      QP.nchunk = (QP.groups + cg - 1) / cg;
+      splits += QP.nchunk;
+      int ic = -1, ix = -1;
+      for (int i = 0; i < ncm; ++i)
+        if (cptr[i] == P.B) ic = i;
+      for (int i = 0; i < nxm; ++i)
+        if (xptr[i] == P.A) ix = i;
+      int rc;
+      if (ic < 0) {
+        rc = make_tmap_2d(&args.cmaps[ncm], P.B, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (uint64_t)(P.K / 8),
+                          (uint64_t)Q.rows, (uint64_t)P.ldb, (uint32_t)(GS * 8), (uint32_t)ROWS,
+                          decode ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc) return rc;
+        cptr[ncm] = P.B;
+        ic = ncm++;
+      }
+      if (ix < 0) {
+        rc = make_tmap_2d(&args.xmaps[nxm], P.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)P.K,
+                          (uint64_t)Q.T, (uint64_t)P.lda, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc) return rc;
+        xptr[nxm] = P.A;
+        ix = nxm++;
+      }
+      QP.cmap = (int16_t)ic;
+      QP.xmap = (int16_t)ix;
+    }
+    Q.splits = splits;
+    Q.unit_begin = (int)units;
+    Q.cnt_base = counters;
+    Q.ws_base = slots;
+    const int64_t tl = (int64_t)Q.tiles * Q.ntiles;
+    units += tl * splits;
+    if (splits > 1) {
+      slots += tl * splits;
+      counters += (int)tl;
+    }
+  }
+  if (units == 0) {
+    *handled = true;
+    return TP_OK;
+  }
+  if (units > INT32_MAX) return TP_OK;
+  if (slots > 0) {
+    int rc = split_workspace(s, (size_t)slots * 128 * BN * sizeof(float), (size_t)counters * 4, &args.ws,
+                             &args.cnt);
+    if (rc) return rc;
+  }
+  args.njobs = p.njobs;
+  args.total_units = (int)units;
+  args.ncm = ncm;
+  args.nxm = nxm;
+  args.out_dt = p.out_dt;
+  args.idesc = umma_idesc_f16(1u, 0u, 128u, (uint32_t)BN);
+  args.status = p.status;
+  args.wait_ns = (uint64_t)p.wait_ns;
+  int rc = decode ? q4_launch_cfg<true>(args, sms, s) : q4_launch_cfg<false>(args, sms, s);
+  if (rc == TP_OK) *handled = true;
+  return rc;
 }
 
 }  // namespace tp

@@ -23,13 +23,11 @@
 // TP_ERR_TIMEOUT in the status word and the CTA drains its in-flight copies and
 // MMAs, frees its TMEM and returns.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <string.h>
 
 #include <mutex>
-#include <unordered_map>
 
 #include "ptx.cuh"
 #include "tp_internal.h"
@@ -346,7 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       const int colb = tb * BN + half * HALF;
       const int nep = a.chain ? 1 : J.nparts;
       for (int pe = 0; pe < nep; ++pe) {
-        if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, lim, a.status, &abort_sh)) {
+        // warp-uniform: every lane must take the same path into tcgen05.ld
+        const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, lim, a.status, &abort_sh);
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
@@ -405,65 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 // ====================================================================== host
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_mu;
 
-struct MapKey {
-  uint64_t ptr, inner, outer, stride;
-  uint32_t box0, box1, dt;
-  bool operator==(const MapKey &o) const {
-    return ptr == o.ptr && inner == o.inner && outer == o.outer && stride == o.stride &&
-           box0 == o.box0 && box1 == o.box1 && dt == o.dt;
-  }
-};
-struct MapKeyHash {
-  size_t operator()(const MapKey &k) const {
-    uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
-    h ^= k.inner + 0x7f4a7c15 + (h << 6) + (h >> 2);
-    h ^= k.outer + 0x2545F491 + (h << 6) + (h >> 2);
-    h ^= k.stride + ((uint64_t)k.box0 << 32 | k.box1) + (h << 6) + (h >> 2);
-    return (size_t)(h ^ k.dt);
-  }
-};
-std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
-int g_sms[64] = {0};
-
-int get_encoder() {
-  if (g_encode) return TP_OK;
-  void *fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                   cudaEnableDefault, &q);
-  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-    return set_error(TP_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled");
-  g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-  return TP_OK;
-}
-
-// 2-D row-major tensor map: `inner` contiguous elements per row, `outer`
-// rows, row stride `ld` elements; box (box0 inner, box1 rows), 128B swizzle.
+// 2-D bf16/f16 row-major tensor map, 128B swizzle.
 int make_map(CUtensorMap *out, const void *ptr, int dt, uint64_t inner, uint64_t outer, uint64_t ld,
              uint32_t box0, uint32_t box1) {
-  MapKey key{(uint64_t)(uintptr_t)ptr, inner, outer, ld, box0, box1, (uint32_t)dt};
-  {
-    auto it = g_maps.find(key);
-    if (it != g_maps.end()) {
-      *out = it->second;
-      return TP_OK;
-    }
-  }
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {box0, box1};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(out, dt == TP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        2, const_cast<void *>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  if (g_maps.size() > 8192) g_maps.clear();
-  g_maps.emplace(key, *out);
-  return TP_OK;
+  return make_tmap_2d(out, ptr,
+                      dt == TP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      2, inner, outer, ld, box0, box1, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int BN, bool B_MN, bool SWAP, bool PARTIALS, int STAGES, int NACC>
@@ -515,12 +464,8 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     BN = partials ? 128 : 256;
 
   std::lock_guard<std::mutex> lk(g_mu);
-  int rc = get_encoder();
-  if (rc) return rc;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!g_sms[dev & 63]) cudaDeviceGetAttribute(&g_sms[dev & 63], cudaDevAttrMultiProcessorCount, dev);
-  const int sms = g_sms[dev & 63];
+  int rc = TP_OK;
+  const int sms = sm_count();
 
   static UmmaArgs args;  // large; guarded by g_mu
   memset(&args, 0, sizeof(args));
@@ -607,8 +552,8 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
 }
 
 void umma_shutdown() {
-  std::lock_guard<std::mutex> lk(g_mu);
-  g_maps.clear();
+  tmap_cache_clear();
+  split_workspace_free();
 }
 
 }  // namespace tp

@@ -101,6 +101,7 @@ int tp_query_status(tp_stream_t stream, int *device_status) {
   if (e != cudaSuccess) return cuda_error(e, "read status word");
   e = cudaMemset(w, 0, sizeof(int));
   if (e != cudaSuccess) return cuda_error(e, "clear status word");
+  if (v != 0) split_workspace_reset();  // a kernel may have stopped mid-reduction
   *device_status = v;
   return TP_OK;
 }

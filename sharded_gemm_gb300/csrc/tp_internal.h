@@ -13,6 +13,7 @@
 // row-parallel all_sum over ranks r = 0..N-1).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -68,5 +69,18 @@ int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void 
                     void *qbias, cudaStream_t s);
 int launch_debug_wait(int64_t limit_ns, int *status, cudaStream_t s);
 void umma_shutdown();
+
+// ---- shared host helpers (tmap.cu)
+int sm_count();
+int make_tmap_2d(CUtensorMap *out, const void *ptr, CUtensorMapDataType dt, int elem_bytes,
+                 uint64_t inner, uint64_t outer, uint64_t ld_elems, uint32_t box0, uint32_t box1,
+                 CUtensorMapSwizzle swz);
+void tmap_cache_clear();
+// Per-(device, stream) workspace of the split-tile reductions: float partials and
+// int arrival counters (zero between calls).  Grows on demand.
+int split_workspace(cudaStream_t s, size_t partial_bytes, size_t ncounters, float **partials,
+                    int **counters);
+void split_workspace_reset();  // clears every counter (after a device-side error)
+void split_workspace_free();
 
 }  // namespace tp
