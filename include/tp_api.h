@@ -228,6 +228,40 @@ int tp_q4_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K,
                          tp_stream_t stream);
 
 /*
+ * tp_q4_sharded_to_all without device allocation.  The pages have no
+ * counterpart; this exists for callers that cannot call cudaMalloc, such as
+ * a serving loop being captured into a CUDA graph, an engine whose device
+ * memory belongs to its own pool allocator, or a latency-critical path where
+ * cudaMalloc's implicit device synchronization is not acceptable.
+ *
+ * Arguments, layout, result and errors are those of tp_q4_sharded_to_all.
+ * Instead of allocating a workspace it uses one fixed 8 MiB array of device
+ * memory that belongs to the library image: the driver creates it on every
+ * GPU that loads the library and it lives until the process exits.  Of it,
+ * 64 KiB hold the split counters and 8 MiB - 64.25 KiB the float32 split
+ * partials; a call whose split needs more (large T or many output rows)
+ * returns TP_ERR_UNSUPPORTED with the sizes in the message and launches
+ * nothing.  Decode-sized calls (T <= 16) of an 8192 x 28672 layer split 8
+ * ways need about 4.4 MB.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, no allocation); make that first call before any
+ *    stream capture.
+ *  - Every call, on every stream, shares the same array, and the array keeps
+ *    what the last call left in it.  Each call clears the counters it uses
+ *    (an asynchronous memset on `stream`) before its kernel.  Calls that can
+ *    overlap on the GPU (on different streams without ordering) race on the
+ *    array and give undefined results: order them.
+ *  - Device-side wait timeouts of this entry point are recorded in the
+ *    array, not in the word tp_query_status() reads; after a timeout the
+ *    output is unspecified.
+ */
+int tp_q4_sharded_to_all_noalloc(int N, const void *const *x, int64_t T, int64_t K,
+                                 const uint32_t *const *wq, const void *const *scales,
+                                 const void *const *qbias, int group_size, int64_t O,
+                                 const void *bias, void *y, int64_t ldy, tp_dtype out_dt,
+                                 tp_stream_t stream);
+
+/*
  * Fault check of the bounded waits (no counterpart on the pages): launches a
  * one-block kernel that waits on a shared-memory barrier nothing ever
  * arrives at, with the given limit (1e6 .. 6e10 ns).  The wait runs out,

@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             "tp_q4_all_to_sharded": ([i32, vp, i64, i64, vpp, vpp, vpp, i32, i64, vpp, vpp, i64, i32, vp], i32),
             "tp_q4_sharded_to_all": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
             "tp_debug_wait_timeout": ([i64, vp], i32),
+            "tp_q4_sharded_to_all_noalloc": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -330,4 +331,29 @@ def tp_q4_sharded_to_all(x, wq, scales, qbias, bias=None, out=None, out_dtype=No
     _check(lib().tp_q4_sharded_to_all(N, xp, T, Kn * N, qp, sp, bq, group_size, O,
                                       None if bias is None else bias.data_ptr(), out.data_ptr(), ldy,
                                       _dt(out), _stream(stream)))
+    return out
+
+
+def tp_q4_sharded_to_all_noalloc(x, wq, scales, qbias, bias=None, out=None, group_size: int = 64,
+                                 stream=None):
+    """a7 row-parallel without any device allocation inside the library call:
+    the split workspace is a fixed array inside libtp.so.  ``out`` must be
+    given (allocating it is the caller's business)."""
+    if out is None:
+        raise ValueError("out must be provided")
+    N = len(x)
+    for lst, nm in ((x, "x"), (wq, "wq"), (scales, "scales"), (qbias, "qbias")):
+        for i, t in enumerate(lst):
+            _contig(t, "%s[%d]" % (nm, i))
+    T, Kn = x[0].shape
+    O = wq[0].shape[0]
+    _rowmajor(out, "out")
+    xp, k1 = _ptrs(x)
+    qp, k2 = _ptrs(wq)
+    sp, k3 = _ptrs(scales)
+    bq, k4 = _ptrs(qbias)
+    ldy = out.stride(0) if T > 1 else O
+    _check(lib().tp_q4_sharded_to_all_noalloc(N, xp, T, Kn * N, qp, sp, bq, group_size, O,
+                                              None if bias is None else bias.data_ptr(),
+                                              out.data_ptr(), ldy, _dt(out), _stream(stream)))
     return out

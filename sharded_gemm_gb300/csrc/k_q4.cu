@@ -689,9 +689,10 @@ int choose_chunks(const Problem &p, int tiles_total_parts, int groups, int sms) 
   return best;
 }
 
-}  // namespace
-
-int launch_q4(const Problem &p, cudaStream_t s, bool *handled) {
+// Builds the launch of `p` and runs it.  `get_ws(bytes, ncounters, &ws, &cnt)`
+// supplies the split-reduction workspace when the launch needs one.
+template <class WsFn>
+int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws) {
   *handled = false;
   if (p.in_dt != TP_BF16) return TP_OK;
   int64_t maxT = 0;
@@ -798,8 +799,7 @@ int launch_q4(const Problem &p, cudaStream_t s, bool *handled) {
   }
   if (units > INT32_MAX) return TP_OK;
   if (slots > 0) {
-    int rc = split_workspace(s, (size_t)slots * 128 * BN * sizeof(float), (size_t)counters * 4, &args.ws,
-                             &args.cnt);
+    int rc = get_ws((size_t)slots * 128 * BN * sizeof(float), (size_t)counters * 4, &args.ws, &args.cnt);
     if (rc) return rc;
   }
   args.njobs = p.njobs;
@@ -813,6 +813,30 @@ int launch_q4(const Problem &p, cudaStream_t s, bool *handled) {
   int rc = decode ? q4_launch_cfg<true>(args, sms, s) : q4_launch_cfg<false>(args, sms, s);
   if (rc == TP_OK) *handled = true;
   return rc;
+}
+
+}  // namespace
+
+int launch_q4(const Problem &p, cudaStream_t s, bool *handled) {
+  return launch_q4_impl(p, s, handled, [s](size_t bytes, size_t ncnt, float **ws, int **cnt) -> int {
+    return split_workspace(s, bytes, ncnt, ws, cnt);
+  });
+}
+
+int launch_q4_fixed_workspace(const Problem &p, cudaStream_t s, bool *handled, float *ws,
+                              size_t ws_bytes, int *cnt, size_t ncnt_max) {
+  return launch_q4_impl(p, s, handled, [&](size_t bytes, size_t ncnt, float **w, int **c) -> int {
+    if (bytes > ws_bytes || ncnt > ncnt_max)
+      return set_error(TP_ERR_UNSUPPORTED,
+                       "this call needs %zu bytes of split scratch and %zu counters; the fixed "
+                       "buffer holds %zu bytes and %zu counters",
+                       bytes, ncnt, ws_bytes, ncnt_max);
+    cudaError_t e = cudaMemsetAsync(cnt, 0, ncnt * sizeof(int), s);
+    if (e != cudaSuccess) return cuda_error(e, "clearing the split counters");
+    *w = ws;
+    *c = cnt;
+    return TP_OK;
+  });
 }
 
 }  // namespace tp

@@ -63,6 +63,10 @@ int cuda_error(cudaError_t e, const char *what);
 int launch_simt(const Problem &p, cudaStream_t s);
 int launch_umma(const Problem &p, cudaStream_t s, bool *handled);
 int launch_q4(const Problem &p, cudaStream_t s, bool *handled);
+// launch_q4 with a caller-provided split workspace instead of the per-stream one;
+// fails with TP_ERR_UNSUPPORTED if the launch needs more than it holds.
+int launch_q4_fixed_workspace(const Problem &p, cudaStream_t s, bool *handled, float *ws,
+                              size_t ws_bytes, int *cnt, size_t ncnt_max);
 int launch_shard(const void *w, int64_t rows, int64_t cols, int elem_bytes, int axis,
                  int segments, int N, void *const *shards, cudaStream_t s);
 int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void *scales,
