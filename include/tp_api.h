@@ -77,6 +77,19 @@ int tp_set_policy(int policy);
  * Values below 1e6 or above 6e10 are rejected with TP_ERR_INVALID_ARG. */
 int tp_set_wait_limit_ns(int64_t limit_ns);
 
+/* Role timeline tracing (profiling aid; no counterpart on the pages).  With a
+ * non-NULL device buffer of `bytes` bytes (>= 256 KiB + 128 bytes, 16-byte
+ * aligned, caller owned), CTA 0 of every later tensor-core q4 decode launch
+ * writes the globaltimer value (ns) of event e at stage sequence number s
+ * (s < 1024, e < 32) into 64-bit word 16 + e*1024 + s, with plain stores.
+ * NULL switches tracing off.  Events: 1 producer issued the stage's loads;
+ * 2/3/4 the MMA thread saw the stage's data / A operand / free accumulator,
+ * 5 it committed the stage; 6/7 converter warp 2 saw the data / a free A
+ * slot, 12 finished the x reorder, 13 its tensor-memory stores completed, 8
+ * signalled the MMA; 9/10/11 epilogue warp 10 saw the accumulator, released
+ * it, finished the stage. */
+int tp_set_trace(void *device_buffer, int64_t bytes);
+
 /* Frees the per-device status words and cached descriptors. */
 int tp_shutdown(void);
 

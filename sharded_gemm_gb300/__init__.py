@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             "tp_q4_all_to_sharded": ([i32, vp, i64, i64, vpp, vpp, vpp, i32, i64, vpp, vpp, i64, i32, vp], i32),
             "tp_q4_sharded_to_all": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
             "tp_debug_wait_timeout": ([i64, vp], i32),
+            "tp_set_trace": ([vp, i64], i32),
             "tp_q4_sharded_to_all_noalloc": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
         }
         for name, (args, res) in sig.items():
@@ -156,6 +157,27 @@ def tp_set_wait_limit_ns(ns: int) -> None:
 
 def tp_shutdown() -> None:
     _check(lib().tp_shutdown())
+
+
+def tp_set_trace(buf=None) -> None:
+    """Start (buf: zeroed CUDA uint8/int64 tensor) or stop (None) role tracing."""
+    if buf is None:
+        _check(lib().tp_set_trace(None, 0))
+    else:
+        _check(lib().tp_set_trace(buf.data_ptr(), buf.numel() * buf.element_size()))
+
+
+def decode_trace(buf) -> dict:
+    """{event: {stage sequence: ns}} of a trace buffer (non-zero entries)."""
+    import numpy as np
+    w = buf.detach().cpu().numpy().view(np.uint64)
+    out = {}
+    for e in range(32):
+        row = w[16 + e * 1024:16 + (e + 1) * 1024]
+        nz = np.nonzero(row)[0]
+        if len(nz):
+            out[e] = {int(i): int(row[i]) for i in nz}
+    return out
 
 
 def tp_query_status(stream=None) -> int:

@@ -130,12 +130,21 @@ struct Q4Args {
   Q4Part parts[kMaxParts];
   int njobs, total_units, ncm, nxm;
   int out_dt;
+  int sb_vec;  // scales/biases allow 8-byte loads of 4 groups (groups % 4 == 0, 8B aligned)
   uint32_t idesc;
   float *ws;
   int *cnt;
   int *status;
   uint64_t wait_ns;
+  unsigned long long *trace;  // role timeline of CTA 0, or null
+  int64_t trace_cap;
 };
+
+// Records the time of (event, stage sequence) when tracing CTA 0.
+__device__ __forceinline__ void q4_trace(const Q4Args &a, int role, int event, int seq) {
+  (void)role;
+  if (a.trace != nullptr && blockIdx.x == 0 && seq < 1024) a.trace[16 + event * 1024 + seq] = globaltimer_ns();
+}
 
 template <bool DECODE>
 struct Q4Cfg;
@@ -189,6 +198,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 
 __device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+
 // Eight 4-bit codes (one word, element e at bits 4e) -> four bf16x2 words of
 // the exact integers, natural element order (low half = even element).
 // 0x4300 | n is the bf16 of 128 + n; one fused multiply-add by (1, 1) and
@@ -205,16 +224,33 @@ __device__ __forceinline__ void codes_to_int_bf16(uint32_t w, uint32_t *o) {
   o[3] = fma_bf16x2(prmt(c, d, 0x7632), one, m128);  // (n6, n7)
 }
 
-// Eight codes -> four bf16x2 words of s*code + b (float32 math, one rounding).
-// 0x4B000000 | n is the float 2^23 + n; subtracting 2^23 gives n exactly.
-__device__ __forceinline__ void codes_to_values_bf16(uint32_t w, float s, float b, uint32_t *o) {
-#pragma unroll
-  for (int e = 0; e < 8; e += 2) {
-    const float q0 = __uint_as_float(((w >> (4 * e)) & 0xFu) | 0x4B000000u) - 8388608.0f;
-    const float q1 = __uint_as_float(((w >> (4 * e + 4)) & 0xFu) | 0x4B000000u) - 8388608.0f;
-    __nv_bfloat162 h = __floats2bfloat162_rn(fmaf(s, q0, b), fmaf(s, q1, b));
-    o[e / 2] = *reinterpret_cast<uint32_t *>(&h);
-  }
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Eight codes of one word -> four f16x2 words of s*code + b in the blocked K
+// order (n0,n4), (n1,n5), (n2,n6), (n3,n7).  0x6400 | n is the f16 of 1024 + n;
+// subtracting 1024 gives n exactly, and one f16 fused multiply-add forms
+// s*n + b with a single rounding.  s2, b2 hold the group's f16 s and b twice.
+__device__ __forceinline__ void codes_to_values_f16_blocked(uint32_t w, uint32_t s2, uint32_t b2,
+                                                            uint32_t *o) {
+  const uint32_t m = 0x64006400u;
+  o[0] = hfma2_u32(hsub2_u32((w & 0x000F000Fu) | m, m), s2, b2);
+  o[1] = hfma2_u32(hsub2_u32(((w >> 4) & 0x000F000Fu) | m, m), s2, b2);
+  o[2] = hfma2_u32(hsub2_u32(((w >> 8) & 0x000F000Fu) | m, m), s2, b2);
+  o[3] = hfma2_u32(hsub2_u32(((w >> 12) & 0x000F000Fu) | m, m), s2, b2);
 }
 
 __device__ __forceinline__ void q4_store(const Q4Args &a, const Q4Job &J, int t, int orow, float v) {
@@ -427,17 +463,34 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
               codes_to_int_bf16(w.w, out + 12);
             }
           } else {
-            float sc = 0.f, bq = 0.f;
+            // x tile of this group (BN rows x 64): bf16 -> f16 in place, blocked
+            // K order, so both MMA operands are f16 (exact for |x| in the f16
+            // normal range).
+            const int cid = (warp - 2) * 32 + lane;
+#pragma unroll 2
+            for (int k = 0; k < C::BN * 8 / 256; ++k) {
+              const uint32_t addr = base + C::CODES_BYTES + gi * C::XBOX + ((cid + k * 256) << 4);
+              const uint4 v = lds128(addr);
+              uint4 o;
+              o.x = f32x2_to_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.z << 16));
+              o.y = f32x2_to_f16x2(__uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.z & 0xFFFF0000u));
+              o.z = f32x2_to_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.w << 16));
+              o.w = f32x2_to_f16x2(__uint_as_float(v.y & 0xFFFF0000u), __uint_as_float(v.w & 0xFFFF0000u));
+              sts128(addr, o);
+            }
+            fence_proxy_async_smem();
+            uint32_t s2 = 0, b2 = 0;
             if (orow < J.rows) {
               const int64_t gi64 = (int64_t)orow * P.groups + gs + gi;
-              sc = h2f(__ldg(P.sc + gi64));
-              bq = h2f(__ldg(P.qb + gi64));
+              const uint32_t sh = __ldg(P.sc + gi64), bh = __ldg(P.qb + gi64);
+              s2 = sh | (sh << 16);
+              b2 = bh | (bh << 16);
             }
             const uint4 w = lds128(base + srow * 32 + half * 16);
-            codes_to_values_bf16(w.x, sc, bq, out + 0);
-            codes_to_values_bf16(w.y, sc, bq, out + 4);
-            codes_to_values_bf16(w.z, sc, bq, out + 8);
-            codes_to_values_bf16(w.w, sc, bq, out + 12);
+            codes_to_values_f16_blocked(w.x, s2, b2, out + 0);
+            codes_to_values_f16_blocked(w.y, s2, b2, out + 4);
+            codes_to_values_f16_blocked(w.z, s2, b2, out + 8);
+            codes_to_values_f16_blocked(w.w, s2, b2, out + 12);
           }
           tmem_st16(tmem + lane_off + C::A_COL0 + as * 32 + half * 16, out);
           tmem_wait_st();
@@ -646,6 +699,409 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
   }
 }
 
+// ---------------------------------------------------------------- decode kernel
+// T <= 16.  Work is handed between roles one stage (4 groups of 64 codes) at a
+// time.  Inside every 8-element block of K the weights and x use the same
+// order (0,4,1,5,2,6,3,7): a packed code word then expands with one mask per
+// output register, and the converters apply the same order to the x tile in
+// shared memory (a 16-byte chunk holds one block, so the swizzle is unaffected).
+// A dot product does not depend on the order of its terms, so D is unchanged.
+struct DecCfg {
+  static constexpr int BN = 16, GS = 4, STAGES = 8, ROWS = 124;
+  static constexpr int CODES_BYTES = 16384, XBOX = 2048, X_BYTES = 4 * 2048;
+  static constexpr int STAGE_BYTES = CODES_BYTES + X_BYTES;
+  static constexpr int TX = 124 * 128 + 4 * 2048;
+  static constexpr int NA = 2, A_COLS = 128, A_COL0 = 0;  // one A slot = one stage
+  static constexpr int ND = 2, D_COLS = 64, D_COL0 = 256;  // one D slot = one stage
+};
+
+// Eight codes of one word -> four bf16x2 words of exact integers, blocked order.
+__device__ __forceinline__ void codes_to_int_bf16_blocked(uint32_t w, uint32_t *o) {
+  const uint32_t one = 0x3F803F80u, m128 = 0xC300C300u;
+  o[0] = fma_bf16x2((w & 0x000F000Fu) | 0x43004300u, one, m128);          // (n0, n4)
+  o[1] = fma_bf16x2(((w >> 4) & 0x000F000Fu) | 0x43004300u, one, m128);   // (n1, n5)
+  o[2] = fma_bf16x2(((w >> 8) & 0x000F000Fu) | 0x43004300u, one, m128);   // (n2, n6)
+  o[3] = fma_bf16x2(((w >> 12) & 0x000F000Fu) | 0x43004300u, one, m128);  // (n3, n7)
+}
+
+template <int TCAP>
+__global__ void __launch_bounds__(kQThreads, 1) q4_decode_kernel(const __grid_constant__ Q4Args a) {
+  using C = DecCfg;
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[C::STAGES], empty_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t afull_bar[C::NA], aempty_bar[C::NA];
+  __shared__ __align__(8) uint64_t dfull_bar[C::ND], dempty_bar[C::ND];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint64_t lim = a.wait_ns;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), 1);
+    }
+    for (int i = 0; i < C::NA; ++i) {
+      mbar_init(smem_u32(&afull_bar[i]), 8);
+      mbar_init(smem_u32(&aempty_bar[i]), 1);
+    }
+    for (int i = 0; i < C::ND; ++i) {
+      mbar_init(smem_u32(&dfull_bar[i]), 1);
+      mbar_init(smem_u32(&dempty_bar[i]), 4);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int st = 0, pseq = 0;
+      uint32_t ph = 0;
+      bool used[C::STAGES];
+      uint32_t lastph[C::STAGES];
+#pragma unroll
+      for (int i = 0; i < C::STAGES; ++i) used[i] = false;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        UnitInfo ui;
+        q4_decode_unit(a, u, ui);
+        const Q4Part &P = a.parts[ui.part];
+        for (int gs = ui.g0; gs < ui.g1; gs += C::GS) {
+          if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          const uint32_t base = sbase + st * C::STAGE_BYTES;
+          const uint32_t fb = smem_u32(&full_bar[st]);
+          mbar_arrive_expect_tx(fb, C::TX);
+          tma_load_2d(base, &a.cmaps[P.cmap], fb, gs * 8, ui.tile * C::ROWS);
+#pragma unroll
+          for (int gi = 0; gi < C::GS; ++gi)
+            tma_load_2d(base + C::CODES_BYTES + gi * C::XBOX, &a.xmaps[P.xmap], fb, (gs + gi) * 64, 0);
+          q4_trace(a, 1, 1, pseq++);
+          used[st] = true;
+          lastph[st] = ph;
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok)
+        for (int i = 0; i < C::STAGES; ++i)
+          if (used[i]) mbar_wait(smem_u32(&full_bar[i]), lastph[i], lim, a.status, nullptr);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int st = 0, as = 0, ds = 0, mseq = 0;
+      uint32_t ph = 0, aph = 0, dph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        UnitInfo ui;
+        q4_decode_unit(a, u, ui);
+        for (int gs = ui.g0; gs < ui.g1; gs += C::GS) {
+          if (!mbar_wait(smem_u32(&full_bar[st]), ph, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          q4_trace(a, 2, 2, mseq);
+          if (!mbar_wait(smem_u32(&afull_bar[as]), aph, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          q4_trace(a, 2, 3, mseq);
+          if (!mbar_wait(smem_u32(&dempty_bar[ds]), dph ^ 1, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          q4_trace(a, 2, 4, mseq);
+          tc_fence_after();
+          const uint32_t xb = sbase + st * C::STAGE_BYTES + C::CODES_BYTES;
+          const int ng = min(C::GS, ui.g1 - gs);
+          // k-major order: consecutive MMAs go to different groups' accumulators,
+          // so no MMA waits for the one issued just before it.
+          // Descriptors and TMEM addresses are formed once per stage; the
+          // 4-group case is fully unrolled so each MMA costs one add and the issue.
+          const uint64_t bd0 = umma_desc_sw128(xb, 16, 1024);
+          const uint32_t d0 = tmem + C::D_COL0 + ds * C::D_COLS;
+          const uint32_t a0 = tmem + C::A_COL0 + as * C::A_COLS;
+          if (ng == C::GS) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+              for (int gi = 0; gi < C::GS; ++gi)
+                umma_f16_ts(d0 + gi * 16, a0 + gi * 32 + kk * 8,
+                            bd0 + (uint64_t)((gi * C::XBOX + kk * 32) >> 4), a.idesc, kk > 0 ? 1u : 0u);
+          } else {
+            for (int kk = 0; kk < 4; ++kk)
+              for (int gi = 0; gi < ng; ++gi)
+                umma_f16_ts(d0 + gi * 16, a0 + gi * 32 + kk * 8,
+                            bd0 + (uint64_t)((gi * C::XBOX + kk * 32) >> 4), a.idesc, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&dfull_bar[ds]));
+          umma_commit(smem_u32(&aempty_bar[as]));
+          umma_commit(smem_u32(&empty_bar[st]));
+          q4_trace(a, 2, 5, mseq++);
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+          if (++as == C::NA) {
+            as = 0;
+            aph ^= 1;
+          }
+          if (++ds == C::ND) {
+            ds = 0;
+            dph ^= 1;
+          }
+        }
+      }
+      umma_commit(smem_u32(&drain_bar));
+      mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
+    }
+  } else if (warp < 10) {
+    // ---------------------------------------------------------- converters
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int cid = (warp - 2) * 32 + lane;  // 0..255, for the x reorder
+    const bool ones = lane == 31;
+    const int srow = quarter * 31 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool tr = (warp == 2 && lane == 0);
+    int st = 0, as = 0, cseq = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+      UnitInfo ui;
+      q4_decode_unit(a, u, ui);
+      for (int gs = ui.g0; gs < ui.g1; gs += C::GS) {
+        Q4_WAIT_ALL(smem_u32(&full_bar[st]), ph, ok);
+        if (!ok) break;
+        if (tr) q4_trace(a, 3, 6, cseq);
+        Q4_WAIT_ALL(smem_u32(&aempty_bar[as]), aph ^ 1, ok);
+        if (!ok) break;
+        if (tr) q4_trace(a, 3, 7, cseq);
+        tc_fence_after();
+        const uint32_t base = sbase + st * C::STAGE_BYTES;
+        // x tile (4 groups x 16 rows x 128 B = 512 chunks): blocked order in place
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t addr = base + C::CODES_BYTES + (cid + k * 256) * 16;
+          const uint4 v = lds128(addr);
+          uint4 w;
+          w.x = prmt(v.x, v.z, 0x5410);
+          w.y = prmt(v.x, v.z, 0x7632);
+          w.z = prmt(v.y, v.w, 0x5410);
+          w.w = prmt(v.y, v.w, 0x7632);
+          sts128(addr, w);
+        }
+        fence_proxy_async_smem();
+        if (tr) q4_trace(a, 3, 12, cseq);
+        const int ng = min(C::GS, ui.g1 - gs);
+        uint4 wv[C::GS];
+#pragma unroll
+        for (int gi = 0; gi < C::GS; ++gi) {
+          const int c = gi * 2 + half;
+          wv[gi] = (ones || gi >= ng) ? make_uint4(0, 0, 0, 0)
+                                      : lds128(base + srow * 128 + ((c ^ (srow & 7)) << 4));
+        }
+        uint32_t out[C::GS][16];
+#pragma unroll
+        for (int gi = 0; gi < C::GS; ++gi) {
+          if (ones) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) out[gi][i] = 0x3F803F80u;
+          } else {
+            codes_to_int_bf16_blocked(wv[gi].x, out[gi] + 0);
+            codes_to_int_bf16_blocked(wv[gi].y, out[gi] + 4);
+            codes_to_int_bf16_blocked(wv[gi].z, out[gi] + 8);
+            codes_to_int_bf16_blocked(wv[gi].w, out[gi] + 12);
+          }
+        }
+#pragma unroll
+        for (int gi = 0; gi < C::GS; ++gi)
+          if (gi < ng) tmem_st16(tmem + lane_off + C::A_COL0 + as * C::A_COLS + gi * 32 + half * 16, out[gi]);
+        tmem_wait_st();
+        if (tr) q4_trace(a, 3, 13, cseq);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&afull_bar[as]));
+        if (tr) q4_trace(a, 3, 8, cseq++);
+        if (++st == C::STAGES) {
+          st = 0;
+          ph ^= 1;
+        }
+        if (++as == C::NA) {
+          as = 0;
+          aph ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const bool ones = lane == 31;
+    const int srow = quarter * 31 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool tr = (warp == 10 && lane == 0);
+    int ds = 0, eseq = 0;
+    uint32_t dph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+      UnitInfo ui;
+      q4_decode_unit(a, u, ui);
+      const Q4Part &P = a.parts[ui.part];
+      const Q4Job &J = a.jobs[ui.job];
+      const int orow = ui.tile * C::ROWS + srow;
+      const bool valid = !ones && orow < J.rows;
+      float acc[TCAP];
+#pragma unroll
+      for (int t = 0; t < TCAP; ++t) acc[t] = 0.f;
+      for (int gs = ui.g0; gs < ui.g1; gs += C::GS) {
+        const int ng = min(C::GS, ui.g1 - gs);
+        float sc[4] = {0.f, 0.f, 0.f, 0.f}, bq[4] = {0.f, 0.f, 0.f, 0.f};
+        if (valid) {
+          const int64_t g64 = (int64_t)orow * P.groups + gs;
+          if (a.sb_vec && ng == 4) {
+            const uint2 s4 = __ldg(reinterpret_cast<const uint2 *>(P.sc + g64));
+            const uint2 b4 = __ldg(reinterpret_cast<const uint2 *>(P.qb + g64));
+            sc[0] = h2f((uint16_t)(s4.x & 0xFFFF));
+            sc[1] = h2f((uint16_t)(s4.x >> 16));
+            sc[2] = h2f((uint16_t)(s4.y & 0xFFFF));
+            sc[3] = h2f((uint16_t)(s4.y >> 16));
+            bq[0] = h2f((uint16_t)(b4.x & 0xFFFF));
+            bq[1] = h2f((uint16_t)(b4.x >> 16));
+            bq[2] = h2f((uint16_t)(b4.y & 0xFFFF));
+            bq[3] = h2f((uint16_t)(b4.y >> 16));
+          } else {
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi)
+              if (gi < ng) {
+                sc[gi] = h2f(__ldg(P.sc + g64 + gi));
+                bq[gi] = h2f(__ldg(P.qb + g64 + gi));
+              }
+          }
+        }
+        Q4_WAIT_ALL(smem_u32(&dfull_bar[ds]), dph, ok);
+        if (!ok) break;
+        if (tr) q4_trace(a, 4, 9, eseq);
+        tc_fence_after();
+        float v[64];
+        {
+          float lo[32], hi[32];
+          tmem_ld32(tmem + lane_off + C::D_COL0 + ds * C::D_COLS, lo);
+          tmem_ld32(tmem + lane_off + C::D_COL0 + ds * C::D_COLS + 32, hi);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v[i] = lo[i];
+            v[32 + i] = hi[i];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[ds]));
+        if (tr) q4_trace(a, 4, 10, eseq);
+        if (++ds == C::ND) {
+          ds = 0;
+          dph ^= 1;
+        }
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          if (gi < ng) {
+#pragma unroll
+            for (int t = 0; t < TCAP; ++t) {
+              const float xs = __shfl_sync(0xffffffffu, v[gi * 16 + t], 31);
+              acc[t] = fmaf(sc[gi], v[gi * 16 + t], fmaf(bq[gi], xs, acc[t]));
+            }
+          }
+        }
+        if (tr) q4_trace(a, 4, 11, eseq++);
+      }
+      if (!ok) break;
+      if (J.splits == 1) {
+        if (valid) {
+          const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
+#pragma unroll
+          for (int t = 0; t < TCAP; ++t)
+            if (t < J.T) q4_store(a, J, t, orow, acc[t] + bias);
+        }
+      } else {
+        float *slot = a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 + m) * 16;
+#pragma unroll
+        for (int t = 0; t < TCAP; ++t) __stcg(slot + t, acc[t]);
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        int *cnt = a.cnt + (int64_t)(J.cnt_base + ui.tile_lin) * 4 + quarter;
+        if (lane == 0) prev = atomicAdd(cnt, 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == J.splits - 1) {
+          __threadfence();
+          const float *s0 = a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits) * 128 + m) * 16;
+          float sum[TCAP];
+#pragma unroll
+          for (int t = 0; t < TCAP; ++t) sum[t] = __ldcg(s0 + t);
+          for (int j = 1; j < J.splits; ++j) {
+            const float *sj = s0 + (int64_t)j * 128 * 16;
+#pragma unroll
+            for (int t = 0; t < TCAP; ++t) sum[t] += __ldcg(sj + t);
+          }
+          if (valid) {
+            const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
+#pragma unroll
+            for (int t = 0; t < TCAP; ++t)
+              if (t < J.T) q4_store(a, J, t, orow, sum[t] + bias);
+          }
+          __syncwarp();
+          if (lane == 0) *cnt = 0;  // ready for the next call
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int TCAP>
+int q4_decode_launch(Q4Args &args, int sms, cudaStream_t s) {
+  auto kern = q4_decode_kernel<TCAP>;
+  constexpr int smem = DecCfg::STAGES * DecCfg::STAGE_BYTES + 1024;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(q4 decode)");
+    attr_done[dev & 63] = true;
+  }
+  const int grid = args.total_units < sms ? args.total_units : sms;
+  kern<<<grid, kQThreads, smem, s>>>(args);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_error(e, "q4_decode_kernel launch");
+}
+
 std::mutex g_q4_mu;
 
 bool al16(const void *p) { return ((uintptr_t)p & 15) == 0; }
@@ -807,10 +1263,27 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws)
   args.ncm = ncm;
   args.nxm = nxm;
   args.out_dt = p.out_dt;
-  args.idesc = umma_idesc_f16(1u, 0u, 128u, (uint32_t)BN);
+  // decode: exact integer codes and x in bf16; prefill: f16 values and f16 x
+  args.idesc = umma_idesc_f16(decode ? 1u : 0u, 0u, 128u, (uint32_t)BN);
   args.status = p.status;
   args.wait_ns = (uint64_t)p.wait_ns;
-  int rc = decode ? q4_launch_cfg<true>(args, sms, s) : q4_launch_cfg<false>(args, sms, s);
+  trace_buffer(&args.trace, &args.trace_cap);
+  int sbv = 1;
+  for (int j = 0; j < p.njobs; ++j)
+    for (int q = 0; q < p.jobs[j].nparts; ++q) {
+      const Q4Part &QP = args.parts[p.jobs[j].part0 + q];
+      if ((QP.groups % 4) || ((uintptr_t)QP.sc & 7) || ((uintptr_t)QP.qb & 7)) sbv = 0;
+    }
+  args.sb_vec = sbv;
+  int rc;
+  if (!decode)
+    rc = q4_launch_cfg<false>(args, sms, s);
+  else if (maxT <= 1)
+    rc = q4_decode_launch<1>(args, sms, s);
+  else if (maxT <= 4)
+    rc = q4_decode_launch<4>(args, sms, s);
+  else
+    rc = q4_decode_launch<16>(args, sms, s);
   if (rc == TP_OK) *handled = true;
   return rc;
 }

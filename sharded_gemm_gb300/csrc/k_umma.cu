@@ -150,25 +150,21 @@ __device__ __forceinline__ void store_col_chunk(const UmmaArgs &a, const UJob &J
   }
 }
 
-template <int BN, bool SWAP>
-__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[(BN / 2 < 32) ? BN / 2 : 32]) {
-  constexpr int CH = (BN / 2 < 32) ? BN / 2 : 32;
+// Epilogue chunk width: the widest of 32 / 16 / 8 columns that divides half a tile.
+template <int HALF>
+struct ChunkOf {
+  static constexpr int v = (HALF % 32 == 0) ? 32 : (HALF % 16 == 0) ? 16 : 8;
+};
+
+template <int CH>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH]) {
   if constexpr (CH == 32) {
     tmem_ld32(taddr, v);
+  } else if constexpr (CH == 16) {
+    tmem_ld16(taddr, v);
   } else {
-    static_assert(CH == 16 || CH == 8, "chunk");
-    if constexpr (CH == 16) {
-      tmem_ld16(taddr, v);
-    } else {
-      uint32_t r[8];
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-            "=r"(r[7])
-          : "r"(taddr));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-    }
+    static_assert(CH == 8, "chunk");
+    tmem_ld8(taddr, v);
   }
 }
 
@@ -184,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr int TCOLS = TmemCols<NACC * BN>::v;
   constexpr int HALF = BN / 2;
-  constexpr int CH = HALF < 32 ? HALF : 32;
+  constexpr int CH = ChunkOf<HALF>::v;
   constexpr int NCH = HALF / CH;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(NACC * BN <= 512, "TMEM capacity");
@@ -356,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
           float v[CH];
-          tmem_load_chunk<BN, SWAP>(tb_addr + c * CH, v);
+          tmem_load_chunk<CH>(tb_addr + c * CH, v);
           tmem_wait_ld();
           if constexpr (PARTIALS) {
 #pragma unroll
@@ -456,12 +452,33 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   const bool swap = !summa && maxM <= 16;
   const bool partials = !p.chain;
   int BN;
-  if (summa)
+  if (summa) {
     BN = 256;
-  else if (swap)
+  } else if (swap) {
     BN = 16;
-  else
-    BN = partials ? 128 : 256;
+  } else if (partials) {
+    BN = 128;
+  } else {
+    // Tile width: rounds of tiles over the SMs times the per-k-block cost of
+    // a 128 x BN tile, which grows like (128 + BN) (the shared-memory bytes the
+    // tile moves per k-block) once the MMA itself is not the limit.
+    const int sms0 = sm_count();
+    const int cand[3] = {256, 192, 160};
+    double best = 1e300;
+    BN = 256;
+    for (int ci = 0; ci < 3; ++ci) {
+      const int bn = cand[ci];
+      int64_t tiles = 0;
+      for (int j = 0; j < p.njobs; ++j)
+        tiles += ((p.jobs[j].M + BM - 1) / BM) * ((p.jobs[j].N + bn - 1) / bn);
+      const double rounds = (double)((tiles + sms0 - 1) / sms0);
+      const double cost = rounds * (128.0 + bn);
+      if (cost < best - 1e-9) {
+        best = cost;
+        BN = bn;
+      }
+    }
+  }
 
   std::lock_guard<std::mutex> lk(g_mu);
   int rc = TP_OK;
@@ -545,6 +562,10 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     rc = launch_config<16, false, true, false, 8, 4>(args, sms, s);
   else if (partials)
     rc = launch_config<128, false, false, true, 6, 4>(args, sms, s);
+  else if (BN == 160)
+    rc = launch_config<160, false, false, false, 6, 2>(args, sms, s);
+  else if (BN == 192)
+    rc = launch_config<192, false, false, false, 5, 2>(args, sms, s);
   else
     rc = launch_config<256, false, false, false, 4, 2>(args, sms, s);
   if (rc == TP_OK) *handled = true;

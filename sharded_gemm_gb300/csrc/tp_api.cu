@@ -15,6 +15,8 @@ namespace tp {
 static thread_local std::string t_last_error;
 static std::atomic<int> g_policy{TP_POLICY_AUTO};
 static std::atomic<int64_t> g_wait_ns{2000000000LL};
+static std::atomic<unsigned long long *> g_trace{nullptr};
+static std::atomic<int64_t> g_trace_cap{0};
 static std::mutex g_status_mu;
 static int *g_status[64] = {nullptr};
 
@@ -33,6 +35,11 @@ int cuda_error(cudaError_t e, const char *what) {
 }
 
 int64_t wait_limit_ns() { return g_wait_ns.load(); }
+
+void trace_buffer(unsigned long long **buf, int64_t *cap_records) {
+  *buf = g_trace.load();
+  *cap_records = g_trace_cap.load();
+}
 
 int *device_status_word() {
   int dev = 0;
@@ -87,6 +94,19 @@ int tp_set_wait_limit_ns(int64_t ns) {
   if (ns < 1000000LL || ns > 60000000000LL)
     return set_error(TP_ERR_INVALID_ARG, "wait limit %lld ns outside [1e6, 6e10]", (long long)ns);
   g_wait_ns.store(ns);
+  return TP_OK;
+}
+
+int tp_set_trace(void *device_buffer, int64_t bytes) {
+  if (!device_buffer) {
+    g_trace.store(nullptr);
+    g_trace_cap.store(0);
+    return TP_OK;
+  }
+  if (bytes < (int64_t)(16 + 32 * 1024) * 8 || ((uintptr_t)device_buffer & 15))
+    return set_error(TP_ERR_INVALID_ARG, "trace buffer must be >= 262272 bytes and 16-byte aligned");
+  g_trace_cap.store(bytes / 8);
+  g_trace.store((unsigned long long *)device_buffer);
   return TP_OK;
 }
 

@@ -1,0 +1,106 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+bench times (the same `workloads` objects and calls), checked against the
+fp64 oracle on sampled output rows (every row for T <= 16).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sharded_gemm_gb300 as tp
+from sharded_gemm_gb300 import build as tpbuild
+from sharded_gemm_gb300 import synth
+from sharded_gemm_gb300.workloads import MLPPair, Q4Pair, QKV, Summa, to_host
+from gpu_util import bf16, check_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    tpbuild.build()
+    tp.tp_set_policy(tp.TP_POLICY_AUTO)
+
+
+def test_full_mlp_pair():
+    cfg = synth.mlp()
+    pair = MLPPair(cfg)
+    pair.step()
+    assert tp.tp_query_status() == 0
+    rows = sample_rows(cfg["T"], 12)
+    x = bf16(cfg["x"])[rows]
+    N = cfg["N"]
+    w1 = [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, N)]
+    b1 = [p.astype(np.float64) for p in oracle.shard(cfg["b1"], 0, 1, N)]
+    ref_mid = oracle.all_to_sharded(x, w1, b1)
+    mids = [to_host(m)[rows] for m in pair.mid]
+    for r in range(N):
+        check_close(mids[r], ref_mid[r], "mid shard %d" % r)
+    w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
+    check_close(to_host(pair.y)[rows], oracle.sharded_to_all(mids, w2, cfg["b2"]), "y")
+
+
+@pytest.mark.parametrize("q", [2, 4])
+def test_full_summa(q):
+    cfg = synth.summa()
+    s = Summa(cfg, q)
+    s.step()
+    assert tp.tp_query_status() == 0
+    bm = cfg["M"] // q
+    rows = sample_rows(bm, 4, seed=q)
+    Xb = [bf16(b)[rows] for b in oracle.blocks(cfg["X"], q)]
+    Ab = [bf16(b) for b in oracle.blocks(cfg["A"], q)]
+    ref = oracle.summa(Xb, Ab, q)  # Y_ij restricted to the sampled local rows
+    for b in range(q * q):
+        check_close(to_host(s.Y[b])[rows], ref[b], "block %d" % b)
+
+
+@pytest.mark.parametrize("T", [1, 16, 2048])
+def test_full_qkv(T):
+    cfg = synth.qkv(T=T)
+    w = QKV(cfg)
+    w.step()
+    assert tp.tp_query_status() == 0
+    N, D = cfg["N"], cfg["D"]
+    rows = sample_rows(T, 8)
+    x = bf16(cfg["x"])[rows]
+    # fused QKV: shard r holds rows {s*D + r*D/N + i} of W_qkv
+    wq = oracle.shard(cfg["w_qkv"], 0, 3, N)
+    bq = oracle.shard(cfg["b_qkv"], 0, 3, N)
+    for r in (0, N - 1):
+        check_close(to_host(w.qkv[r])[rows], oracle.linear(x, bf16(wq[r]), bq[r]), "qkv shard %d" % r)
+    # W_o: row-parallel over x's column slices
+    xs = oracle.shard(cfg["x"], -1, 1, N)
+    wo = oracle.shard(cfg["w_o"], -1, 1, N)
+    ref_o = oracle.sharded_to_all([bf16(p)[rows] for p in xs], [bf16(p) for p in wo], cfg["b_o"])
+    check_close(to_host(w.attn_out)[rows], ref_o, "W_o")
+    # vocab-parallel LM head: gathered logits, sampled columns of every shard
+    V = cfg["V"]
+    cols = np.sort(np.concatenate([r * (V // N) + sample_rows(V // N, 64, seed=r) for r in range(N)]))
+    ref_l = oracle.linear(x, bf16(cfg["w_lm"][cols]))
+    check_close(to_host(w.logits)[rows][:, cols], ref_l, "LM head")
+
+
+@pytest.mark.parametrize("T", [1, 16, 256])
+def test_full_q4_pair(T):
+    cfg = synth.q4(T=T)
+    N, D, F = cfg["N"], cfg["D"], cfg["F"]
+    up = oracle.quantize_affine4(cfg["w_up"], 64)
+    down = oracle.quantize_affine4(cfg["w_down"], 64)
+    w = Q4Pair(cfg, quantized=(up, down))
+    w.step()
+    assert tp.tp_query_status() == 0
+    rows = sample_rows(T, 6)
+    x = bf16(cfg["x"])[rows]
+    # up: column-parallel, sampled output columns of shards 0 and N-1
+    for r in (0, N - 1):
+        cols = sample_rows(F // N, 96, seed=r)
+        g = [a[r * (F // N):(r + 1) * (F // N)][cols] for a in up]
+        ref = oracle.q4_all_to_sharded(x, [g[0]], [g[1]], [g[2]], 64)[0]
+        check_close(to_host(w.mid[r])[rows][:, cols], ref, "q4 up shard %d" % r)
+    # down: row-parallel over the GPU's own intermediate, sampled output columns
+    cols = sample_rows(D, 128, seed=11)
+    mids = [to_host(m)[rows] for m in w.mid]
+    dq = [oracle.shard(a[cols], -1, 1, N) for a in down]
+    ref = oracle.q4_sharded_to_all(mids, dq[0], dq[1], dq[2], 64)
+    check_close(to_host(w.y)[rows][:, cols], ref, "q4 down")
