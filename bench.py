@@ -262,6 +262,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--policy", default="auto", choices=["auto", "single_sm", "simt"],
+                    help="kernel family (diagnostics; the product default is auto)")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
@@ -282,6 +284,8 @@ def main():
             tpbuild.build()
         dist.barrier()
     peaks = load_peaks()
+    tp.tp_set_policy({"auto": tp.TP_POLICY_AUTO, "single_sm": tp.TP_POLICY_SINGLE_SM,
+                      "simt": tp.TP_POLICY_SIMT}[args.policy])
 
     w, step, info = make_workload(args.config, rank, device)
     launches = split_step(args.config, w)
@@ -387,6 +391,8 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": info["launches_per_step"] * args.steps, "clocks": clocks,
         }
+        if args.policy != "auto":
+            line["policy"] = args.policy
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

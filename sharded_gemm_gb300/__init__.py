@@ -24,7 +24,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "tp_api.h")
 TP_OK, TP_ERR_INVALID_ARG, TP_ERR_NOT_DIVISIBLE, TP_ERR_ALIGNMENT = 0, -1, -2, -3
 TP_ERR_UNSUPPORTED, TP_ERR_CUDA, TP_ERR_TIMEOUT = -4, -5, -6
 TP_F32, TP_BF16, TP_F16 = 0, 1, 2
-TP_POLICY_AUTO, TP_POLICY_SIMT = 0, 1
+TP_POLICY_AUTO, TP_POLICY_SIMT, TP_POLICY_SINGLE_SM = 0, 1, 2
 
 _lib = None
 

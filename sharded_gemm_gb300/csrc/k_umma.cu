@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -398,6 +399,216 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   }
 }
 
+// ====================================================================== CTA pairs
+// umma_pair_kernel: the chain-mode GEMM on 2-CTA clusters with the pair MMA
+// (tcgen05.mma.cta_group::2, M = 256).  Rank 0 of a pair issues the MMAs for
+// both CTAs; each CTA stages its own 128 rows of A and its half (BN/2 rows) of
+// B, so a CTA holds (128 + BN/2) x 64 operand elements per k-block instead of
+// (128 + BN) x 64 and the same shared memory covers more latency.  Every TMA
+// load of the pair completes on rank 0's stage barrier; rank 0's commits reach
+// both CTAs' barriers; both epilogues release the accumulator on rank 0's
+// barrier.  Each CTA's TMEM holds its own 128 rows of the 256 x BN tile.
+template <int BN, bool B_MN, int STAGES, int NACC>
+__global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_constant__ UmmaArgs a) {
+  constexpr int BNH = BN / 2;
+  constexpr int A_BYTES = BM * BK * 2;
+  constexpr int B_BYTES = BNH * BK * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr int TCOLS = TmemCols<NACC * BN>::v;
+  constexpr int HALF = BN / 2;
+  constexpr int CH = ChunkOf<HALF>::v;
+  constexpr int NCH = HALF / CH;
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(NACC * BN <= 512, "TMEM capacity");
+  static_assert(!B_MN || BNH % 64 == 0, "MN-major B needs 64-column boxes");
+
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[NACC], tempty_bar[NACC];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint64_t lim = a.wait_ns;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int s = 0; s < NACC; ++s) {
+      mbar_init(smem_u32(&tfull_bar[s]), 1);
+      mbar_init(smem_u32(&tempty_bar[s]), 2 * kEpiWarps);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&tmem_base_sh), TCOLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < a.nmapA && i < 8; ++i) prefetch_tmap(&a.mapA[i]);
+    for (int i = 0; i < a.nmapB && i < 8; ++i) prefetch_tmap(&a.mapB[i]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_phase[STAGES];
+      bool used[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) used[s] = false;
+      bool ok = true;
+      for (int u = pair; ok && u < a.total_units; u += npairs) {
+        const UJob &J = a.jobs[find_job(a, u)];
+        const int local = u - J.unit_begin;
+        const int ta = local % J.tilesA, tb = local / J.tilesA;
+        const int rowA0 = ta * 2 * BM + (int)rank * BM, rowB0 = tb * BN + (int)rank * BNH;
+        for (int p = 0; ok && p < J.nparts; ++p) {
+          const UPart P = a.parts[J.part0 + p];
+          for (int kb = 0; kb < P.kblocks; ++kb) {
+            if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, lim, a.status, &abort_sh)) {
+              ok = false;
+              break;
+            }
+            const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
+            const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2 * STAGE_BYTES);
+            tma_load_2d_pair(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
+            if constexpr (B_MN) {
+#pragma unroll
+              for (int c = 0; c < BNH / 64; ++c)
+                tma_load_2d_pair(sb + c * 8192, &a.mapB[P.bmap], fb, rowB0 + c * 64, kb * BK);
+            } else {
+              tma_load_2d_pair(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
+            }
+            used[stage] = true;
+            last_phase[stage] = phase;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+      }
+      if (!ok && rank == 0) {
+        for (int s = 0; s < STAGES; ++s)
+          if (used[s]) mbar_wait(smem_u32(&full_bar[s]), last_phase[s], lim, a.status, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (lane == 0 && rank == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < a.total_units; u += npairs) {
+        const UJob &J = a.jobs[find_job(a, u)];
+        for (int p = 0; ok && p < J.nparts; ++p) {
+          const UPart P = a.parts[J.part0 + p];
+          if (p == 0) {
+            if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, lim, a.status, &abort_sh)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+          for (int kb = 0; kb < P.kblocks; ++kb) {
+            if (!mbar_wait(smem_u32(&full_bar[stage]), phase, lim, a.status, &abort_sh)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = umma_desc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                       : umma_desc_sw128(sb + kk * 32, 16, 1024);
+              umma_f16_pair(d, ad, bd, a.idesc, (kb > 0 || kk > 0 || p > 0) ? 1u : 0u);
+            }
+            umma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          if (p == J.nparts - 1) {
+            umma_commit_pair(smem_u32(&tfull_bar[acc]), (uint16_t)3);
+            if (++acc == NACC) {
+              acc = 0;
+              acc_phase ^= 1;
+            }
+          }
+        }
+      }
+      umma_commit_pair(smem_u32(&drain_bar), (uint16_t)1);
+      mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int half = ew >> 2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = pair; ok && u < a.total_units; u += npairs) {
+      const UJob &J = a.jobs[find_job(a, u)];
+      const int local = u - J.unit_begin;
+      const int ta = local % J.tilesA, tb = local / J.tilesA;
+      const int row = ta * 2 * BM + (int)rank * BM + quarter * 32 + lane;
+      const int colb = tb * BN + half * HALF;
+      const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, lim, a.status, &abort_sh);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb_addr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)(half * HALF);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        float v[CH];
+        tmem_load_chunk<CH>(tb_addr + c * CH, v);
+        tmem_wait_ld();
+        store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+      if (++acc == NACC) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still use its memory
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TCOLS);
+  }
+}
+
 // ====================================================================== host
 namespace {
 
@@ -429,6 +640,38 @@ int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_gemm_kernel launch");
 }
 
+template <int BN, bool B_MN, int STAGES, int NACC>
+int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
+  auto kern = umma_pair_kernel<BN, B_MN, STAGES, NACC>;
+  constexpr int smem = STAGES * (BM * BK * 2 + (BN / 2) * BK * 2) + 1024;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(pair)");
+    attr_done[dev & 63] = true;
+  }
+  const int max_pairs = sms / 2;
+  const int pairs = args.total_units < max_pairs ? args.total_units : max_pairs;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_pair_kernel launch");
+}
+
 bool al16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
 }  // namespace
@@ -451,31 +694,37 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   const bool summa = p.b_layout == BL_MNMAJOR;
   const bool swap = !summa && maxM <= 16;
   const bool partials = !p.chain;
+  // Kernel and tile choice.  Per k-block a tile costs about
+  // max(MMA cycles, 2.2 x the operand rows one CTA stages): a CTA can keep
+  // only so many bytes in flight, so the staged rows set the pace once the
+  // MMA is fast enough.  Rounds of tiles over the SMs multiply that.
   int BN;
-  if (summa) {
-    BN = 256;
-  } else if (swap) {
+  bool pair = false;
+  if (swap) {
     BN = 16;
   } else if (partials) {
     BN = 128;
   } else {
-    // Tile width: rounds of tiles over the SMs times the per-k-block cost of
-    // a 128 x BN tile, which grows like (128 + BN) (the shared-memory bytes the
-    // tile moves per k-block) once the MMA itself is not the limit.
     const int sms0 = sm_count();
-    const int cand[3] = {256, 192, 160};
+    const bool allow_pair = pair_policy_allowed() && sms0 >= 2;
     double best = 1e300;
     BN = 256;
-    for (int ci = 0; ci < 3; ++ci) {
-      const int bn = cand[ci];
-      int64_t tiles = 0;
-      for (int j = 0; j < p.njobs; ++j)
-        tiles += ((p.jobs[j].M + BM - 1) / BM) * ((p.jobs[j].N + bn - 1) / bn);
-      const double rounds = (double)((tiles + sms0 - 1) / sms0);
-      const double cost = rounds * (128.0 + bn);
-      if (cost < best - 1e-9) {
-        best = cost;
-        BN = bn;
+    for (int pm = 0; pm < (allow_pair ? 2 : 1); ++pm) {
+      for (int bn : {256, 192, 160}) {
+        if (summa && bn != 256) continue;
+        const int64_t mrows = pm ? 2 * BM : BM;
+        int64_t tiles = 0;
+        for (int j = 0; j < p.njobs; ++j)
+          tiles += ((p.jobs[j].M + mrows - 1) / mrows) * ((p.jobs[j].N + bn - 1) / bn);
+        const int64_t slots = pm ? sms0 / 2 : sms0;
+        const double rounds = (double)((tiles + slots - 1) / slots);
+        const double per_kb = std::max(2.0 * bn, 2.2 * (128.0 + (pm ? bn / 2 : bn)));
+        const double cost = rounds * per_kb;
+        if (cost < best - 1e-9) {
+          best = cost;
+          BN = bn;
+          pair = pm == 1;
+        }
       }
     }
   }
@@ -499,7 +748,7 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     U.rowsB = (int)(swap ? J.M : J.N);
     U.part0 = J.part0;
     U.nparts = J.nparts;
-    U.tilesA = (U.rowsA + BM - 1) / BM;
+    U.tilesA = (U.rowsA + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
     U.tilesB = (U.rowsB + BN - 1) / BN;
     U.unit_begin = (int)units;
     units += (int64_t)U.tilesA * U.tilesB;
@@ -526,7 +775,8 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
         if (summa)  // B block (K, Nblk) row-major: inner = N
           rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)U.rowsB, (uint64_t)P.K, (uint64_t)ldB, 64, BK);
         else
-          rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsB, (uint64_t)ldB, BK, BN);
+          rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsB, (uint64_t)ldB, BK,
+                        (uint32_t)(pair ? BN / 2 : BN));
         if (rc) return rc;
         bptr[nB] = opB;
         ib = nB++;
@@ -550,11 +800,19 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   for (int j = 0; j < p.njobs; ++j)
     if (!al16(p.jobs[j].C) || ((p.jobs[j].ldc * oe) % 16)) vec = 0;
   args.vec_ok = vec;
-  args.idesc = umma_idesc_f16(p.in_dt == TP_BF16 ? 1u : 0u, summa ? 1u : 0u, BM, (uint32_t)BN);
+  args.idesc = umma_idesc_f16(p.in_dt == TP_BF16 ? 1u : 0u, summa ? 1u : 0u, pair ? 2 * BM : BM, (uint32_t)BN);
   args.status = p.status;
   args.wait_ns = (uint64_t)p.wait_ns;
 
-  if (summa)
+  if (pair && summa)
+    rc = launch_pair<256, true, 6, 2>(args, sms, s);
+  else if (pair && BN == 160)
+    rc = launch_pair<160, false, 8, 2>(args, sms, s);
+  else if (pair && BN == 192)
+    rc = launch_pair<192, false, 7, 2>(args, sms, s);
+  else if (pair)
+    rc = launch_pair<256, false, 6, 2>(args, sms, s);
+  else if (summa)
     rc = launch_config<256, true, false, false, 4, 2>(args, sms, s);
   else if (swap && partials)
     rc = launch_config<16, false, true, true, 8, 4>(args, sms, s);

@@ -36,6 +36,8 @@ int cuda_error(cudaError_t e, const char *what) {
 
 int64_t wait_limit_ns() { return g_wait_ns.load(); }
 
+bool pair_policy_allowed() { return g_policy.load() != TP_POLICY_SINGLE_SM; }
+
 void trace_buffer(unsigned long long **buf, int64_t *cap_records) {
   *buf = g_trace.load();
   *cap_records = g_trace_cap.load();
@@ -66,7 +68,7 @@ static int dispatch(Problem &p, cudaStream_t s) {
   if (!p.status) return set_error(TP_ERR_CUDA, "cannot allocate the device status word");
   p.wait_ns = wait_limit_ns();
   bool handled = false;
-  if (g_policy.load() == TP_POLICY_AUTO) {
+  if (g_policy.load() != TP_POLICY_SIMT) {
     int rc = p.b_layout == BL_Q4 ? launch_q4(p, s, &handled) : launch_umma(p, s, &handled);
     if (rc != TP_OK || handled) return rc;
   }
@@ -84,7 +86,7 @@ int tp_version(void) { return 100; }
 const char *tp_last_error(void) { return t_last_error.c_str(); }
 
 int tp_set_policy(int policy) {
-  if (policy != TP_POLICY_AUTO && policy != TP_POLICY_SIMT)
+  if (policy != TP_POLICY_AUTO && policy != TP_POLICY_SIMT && policy != TP_POLICY_SINGLE_SM)
     return set_error(TP_ERR_INVALID_ARG, "unknown policy %d", policy);
   g_policy.store(policy);
   return TP_OK;

@@ -31,7 +31,8 @@ def built():
     tp.tp_set_policy(tp.TP_POLICY_AUTO)
 
 
-@pytest.fixture(params=[tp.TP_POLICY_AUTO, tp.TP_POLICY_SIMT], ids=["auto", "simt"])
+@pytest.fixture(params=[tp.TP_POLICY_AUTO, tp.TP_POLICY_SINGLE_SM, tp.TP_POLICY_SIMT],
+                ids=["auto", "single_sm", "simt"])
 def policy(request):
     tp.tp_set_policy(request.param)
     yield request.param
