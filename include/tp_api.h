@@ -54,7 +54,7 @@ typedef enum { TP_F32 = 0, TP_BF16 = 1, TP_F16 = 2 } tp_dtype;
 typedef enum {
     TP_POLICY_AUTO = 0,      /* tensor-core (tcgen05) kernels where they apply  */
     TP_POLICY_SIMT = 1,      /* plain CUDA-core kernels only (slow cross-check)  */
-    TP_POLICY_SINGLE_SM = 2  /* tensor-core kernels, no 2-SM (CTA pair) MMA     */
+    TP_POLICY_SINGLE_SM = 2  /* tensor-core kernels, one CTA per output tile    */
 } tp_policy;
 
 typedef void *tp_stream_t; /* a cudaStream_t */

@@ -63,10 +63,17 @@ struct UmmaArgs {
   UPart parts[kMaxParts];
   int njobs, total_units, nmapA, nmapB;
   int chain, out_dt, vec_ok;
+  int cluster_n;  // ranks per cluster (row-parallel cluster kernel)
+  unsigned long long *trace;  // optional timeline of CTA 0 (tp_set_trace)
   uint32_t idesc;
   int *status;
   uint64_t wait_ns;
 };
+
+// Records the time of (event, k-block sequence) for CTA 0 when tracing.
+__device__ __forceinline__ void umma_trace(const UmmaArgs &a, int event, int seq) {
+  if (a.trace != nullptr && blockIdx.x == 0 && seq < 1024) a.trace[16 + event * 1024 + seq] = globaltimer_ns();
+}
 
 __device__ __forceinline__ int find_job(const UmmaArgs &a, int u) {
   int j = 0;
@@ -465,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int stage = 0;
+      int stage = 0, pseq = 0;
       uint32_t phase = 0;
       uint32_t last_phase[STAGES];
       bool used[STAGES];
@@ -495,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
             } else {
               tma_load_2d_pair(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
             }
+            umma_trace(a, 1, pseq++);
             used[stage] = true;
             last_phase[stage] = phase;
             if (++stage == STAGES) {
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
     if (lane == 0 && rank == 0) {
-      int stage = 0, acc = 0;
+      int stage = 0, acc = 0, mseq = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int u = pair; ok && u < a.total_units; u += npairs) {
@@ -532,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
               ok = false;
               break;
             }
+            umma_trace(a, 2, mseq);
             tc_fence_after();
             const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
@@ -542,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
               umma_f16_pair(d, ad, bd, a.idesc, (kb > 0 || kk > 0 || p > 0) ? 1u : 0u);
             }
             umma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)3);
+            umma_trace(a, 3, mseq++);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1;
@@ -609,6 +619,176 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
   }
 }
 
+// ====================================================================== rank clusters
+// umma_row_cluster_kernel: the row-parallel GEMM with one CTA per (output
+// tile, rank r), the N CTAs of a tile forming one cluster.  CTA r forms rank
+// r's partial x_r W_r^T of the 128 x BN tile from zero in TMEM and parks it in
+// its own shared memory; after a cluster barrier CTA r sums column slice r of
+// the tile over the N partials in ascending rank order (reading its peers'
+// shared memory), adds the bias once and stores.  The partials never leave
+// the chip.  One unit per CTA (not persistent).
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __grid_constant__ UmmaArgs a) {
+  constexpr int A_BYTES = BM * BK * 2;
+  constexpr int B_BYTES = BN * BK * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr int TCOLS = TmemCols<BN>::v;
+  constexpr int HALF = BN / 2;
+  constexpr int CH = ChunkOf<HALF>::v;
+  constexpr int NCH = HALF / CH;
+  constexpr int RED_LD = BN + 4;  // floats per row of the parked partial
+  static_assert(BM * RED_LD * 4 <= STAGES * STAGE_BYTES, "partial must fit the stage memory");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.cluster_n;
+  const uint32_t rank = cluster_ctarank();
+  const int tile = blockIdx.x / N;
+  const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint64_t lim = a.wait_ns;
+  const UJob &J = a.jobs[0];
+  const int ta = tile % J.tilesA, tbn = tile / J.tilesA;
+  const int rowA0 = ta * BM, rowB0 = tbn * BN;
+  const UPart P = a.parts[J.part0 + (int)rank];
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_u32(&tfull_bar), 1);
+    mbar_init(smem_u32(&drain_bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&a.mapA[P.amap]);
+      prefetch_tmap(&a.mapB[P.bmap]);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_phase[STAGES];
+      bool used[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) used[s] = false;
+      bool ok = true;
+      for (int kb = 0; kb < P.kblocks; ++kb) {
+        if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, lim, a.status, &abort_sh)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
+        const uint32_t fb = smem_u32(&full_bar[stage]);
+        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        tma_load_2d(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
+        tma_load_2d(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
+        used[stage] = true;
+        last_phase[stage] = phase;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < STAGES; ++s)
+          if (used[s]) mbar_wait(smem_u32(&full_bar[s]), last_phase[s], lim, a.status, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = 0; kb < P.kblocks; ++kb) {
+        if (!mbar_wait(smem_u32(&full_bar[stage]), phase, lim, a.status, &abort_sh)) break;
+        tc_fence_after();
+        const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_f16(tmem_base, umma_desc_sw128(sa + kk * 32, 16, 1024),
+                   umma_desc_sw128(sb + kk * 32, 16, 1024), a.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(smem_u32(&empty_bar[stage]));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      umma_commit(smem_u32(&tfull_bar));
+      umma_commit(smem_u32(&drain_bar));
+      mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
+    }
+  } else {
+    // park this rank's partial in shared memory (row-major, padded rows)
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    const bool got = mbar_wait(smem_u32(&tfull_bar), 0, lim, a.status, &abort_sh);
+    if (__all_sync(0xffffffffu, got)) {
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * HALF);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        float v[CH];
+        tmem_load_chunk<CH>(taddr + c * CH, v);
+        tmem_wait_ld();
+        const uint32_t dst = sbase + (uint32_t)((row * RED_LD + half * HALF + c * CH) * 4);
+#pragma unroll
+        for (int i = 0; i < CH; i += 4)
+          asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(dst + i * 4), "f"(v[i]),
+                       "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
+                       : "memory");
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // every rank's partial is parked
+
+  if (warp >= 2) {
+    // column slice `rank` of the tile: sum over ranks 0..N-1 in order, then bias
+    const int slice = BN / N;
+    const int per_row = slice / 4;
+    const int t = threadIdx.x - 64;
+    for (int idx = t; idx < BM * per_row; idx += 256) {
+      const int r = idx / per_row;
+      const int c = (int)rank * slice + (idx - r * per_row) * 4;
+      const uint32_t off = sbase + (uint32_t)((r * RED_LD + c) * 4);
+      float4 acc = ld_cluster_f4(mapa_shared(off, 0));
+      for (int q = 1; q < N; ++q) {
+        const float4 v = ld_cluster_f4(mapa_shared(off, (uint32_t)q));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      float o[4] = {acc.x, acc.y, acc.z, acc.w};
+      store_row_chunk<4>(a, J, rowA0 + r, rowB0 + c, o);
+    }
+  }
+
+  __syncthreads();
+  cluster_sync_all();  // peers stop reading this CTA's shared memory
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TCOLS);
+  }
+}
+
 // ====================================================================== host
 namespace {
 
@@ -672,6 +852,39 @@ int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_pair_kernel launch");
 }
 
+template <int BN, int STAGES>
+int launch_row_cluster(UmmaArgs &args, cudaStream_t s) {
+  auto kern = umma_row_cluster_kernel<BN, STAGES>;
+  constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(row cluster)");
+    attr_done[dev & 63] = true;
+  }
+  const int N = args.cluster_n;
+  const int64_t tiles = (int64_t)args.jobs[0].tilesA * args.jobs[0].tilesB;
+  if (tiles * N > INT32_MAX) return set_error(TP_ERR_UNSUPPORTED, "too many tiles");
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(tiles * N), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)N;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_row_cluster_kernel launch");
+}
+
 bool al16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
 }  // namespace
@@ -699,11 +912,33 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   // only so many bytes in flight, so the staged rows set the pace once the
   // MMA is fast enough.  Rounds of tiles over the SMs multiply that.
   int BN;
-  bool pair = false;
+  bool pair = false, rowclu = false;
   if (swap) {
     BN = 16;
   } else if (partials) {
     BN = 128;
+    // Rank clusters (one CTA per rank of a 128 x 256 tile) when one CTA per
+    // 128 x 128 tile would leave SMs idle; costs in cycles, measured rates.
+    const int sms0 = sm_count();
+    if (pair_policy_allowed() && p.njobs == 1) {
+      const Job &J = p.jobs[0];
+      const int N = J.nparts;
+      bool same_k = true;
+      for (int q = 1; q < N; ++q) same_k = same_k && p.parts[J.part0 + q].K == p.parts[J.part0].K;
+      const double kb = (double)((p.parts[J.part0].K + BK - 1) / BK);
+      // Measured: 4-rank clusters win on long K (MLP 2752 per rank); 8-rank
+      // clusters and short K lose to the fixed per-CTA cost of this kernel.
+      if (N >= 2 && N <= 4 && kb >= 32 && (256 % N) == 0 && same_k) {
+        const int64_t mt = (J.M + BM - 1) / BM;
+        const int64_t t128 = mt * ((J.N + 127) / 128), t256 = mt * ((J.N + 255) / 256);
+        const double single = (double)((t128 + sms0 - 1) / sms0) * N * kb * 720.0;
+        const double clu = (double)((t256 * N + sms0 - 1) / sms0) * (kb * 850.0 + 12000.0);
+        if (clu < single) {
+          rowclu = true;
+          BN = 256;
+        }
+      }
+    }
   } else {
     const int sms0 = sm_count();
     const bool allow_pair = pair_policy_allowed() && sms0 >= 2;
@@ -793,6 +1028,11 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   args.nmapA = nA;
   args.nmapB = nB;
   args.total_units = (int)units;
+  args.cluster_n = rowclu ? p.jobs[0].nparts : 1;
+  {
+    int64_t cap = 0;
+    trace_buffer(&args.trace, &cap);
+  }
   args.chain = p.chain;
   args.out_dt = p.out_dt;
   const int oe = p.out_dt == TP_F32 ? 4 : 2;
@@ -804,7 +1044,9 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   args.status = p.status;
   args.wait_ns = (uint64_t)p.wait_ns;
 
-  if (pair && summa)
+  if (rowclu)
+    rc = launch_row_cluster<256, 4>(args, s);
+  else if (pair && summa)
     rc = launch_pair<256, true, 6, 2>(args, sms, s);
   else if (pair && BN == 160)
     rc = launch_pair<160, false, 8, 2>(args, sms, s);

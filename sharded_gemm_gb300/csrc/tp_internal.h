@@ -56,7 +56,7 @@ struct Problem {
 // ---- shared host state (tp_api.cu)
 int *device_status_word();  // per current device; nullptr on failure
 int64_t wait_limit_ns();
-bool pair_policy_allowed();  // false under TP_POLICY_SINGLE_SM
+bool pair_policy_allowed();  // false under TP_POLICY_SINGLE_SM (no pairs, no rank clusters)
 void trace_buffer(unsigned long long **buf, int64_t *cap_records);
 int set_error(int code, const char *fmt, ...);
 int cuda_error(cudaError_t e, const char *what);

@@ -294,3 +294,27 @@ def test_bounded_wait_times_out_and_context_survives():
     torch.cuda.synchronize()
     assert tp.tp_query_status() == 0
     assert torch.isfinite(y[0]).all()
+
+
+def test_many_pair_tiles_bias_and_determinism():
+    # More 256 x 256 pair tiles (80) than pairs of SMs, long K, a bias: sampled
+    # rows against the oracle and bit-identical repeats.
+    tp.tp_set_policy(tp.TP_POLICY_AUTO)
+    T, K, On, N = 300, 2048, 2560, 4
+    x = rand_bf16((T, K))
+    w = rand_bf16((On * N, K), 0.03)
+    b = (RNG.standard_normal(On * N) * 0.5).astype(np.float32)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), 0, 1, N)
+    bs = tp.tp_shard_weight(to_device(b, "f32"), 0, 1, N)
+    xd = to_device(x, "bf16")
+    ys = tp.tp_all_to_sharded(xd, ws, bs, out_dtype=torch.float32)
+    _status_ok()
+    first = _digest(ys)
+    rows = sample_rows(T, 10)
+    ref = oracle.all_to_sharded(bf16(x)[rows], [bf16(p) for p in oracle.shard(w, 0, 1, N)],
+                                [p.astype(np.float64) for p in oracle.shard(b, 0, 1, N)])
+    for r in range(N):
+        check_close(to_host(ys[r])[rows], ref[r], "shard %d" % r)
+    for _ in range(3):
+        ys = tp.tp_all_to_sharded(xd, ws, bs, out_dtype=torch.float32)
+        assert _digest(ys) == first
