@@ -1161,6 +1161,16 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws)
       if (!al16(P.A) || (P.lda % 8) || !al16(P.B) || (P.ldb % 4) || (P.K % 64)) return TP_OK;
     }
   }
+  // One or two tokens: the CUDA-core GEMV (HBM-bound; the tensor-core decode
+  // below is bound by its MMA issue rate there).  TP_POLICY_SINGLE_SM keeps
+  // the tensor-core decode.
+  if (maxT <= 2 && pair_policy_allowed()) {
+    GvWorkspaceFn thunk = [](void *ctx, size_t bytes, size_t ncnt, float **ws, int **cnt) -> int {
+      return (*static_cast<WsFn *>(ctx))(bytes, ncnt, ws, cnt);
+    };
+    int rc = launch_q4_gemv(p, s, handled, thunk, &get_ws);
+    if (rc != TP_OK || *handled) return rc;
+  }
   const bool decode = maxT <= 16;
   const int ROWS = decode ? 124 : 128;
   const int BN = decode ? 16 : 256;

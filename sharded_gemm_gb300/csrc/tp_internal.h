@@ -69,6 +69,12 @@ int launch_q4(const Problem &p, cudaStream_t s, bool *handled);
 // fails with TP_ERR_UNSUPPORTED if the launch needs more than it holds.
 int launch_q4_fixed_workspace(const Problem &p, cudaStream_t s, bool *handled, float *ws,
                               size_t ws_bytes, int *cnt, size_t ncnt_max);
+// Split-reduction workspace supplier: bytes of float32 slots and a count of
+// zeroed int counters; returns TP_OK or a tp_status.
+typedef int (*GvWorkspaceFn)(void *ctx, size_t bytes, size_t ncounters, float **ws, int **cnt);
+// CUDA-core 4-bit GEMV for decode batches of one or two tokens; leaves
+// *handled false (and returns TP_OK) for problems it does not take.
+int launch_q4_gemv(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx);
 int launch_shard(const void *w, int64_t rows, int64_t cols, int elem_bytes, int axis,
                  int segments, int N, void *const *shards, cudaStream_t s);
 int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void *scales,

@@ -236,7 +236,10 @@ def _q4_host(rows, K, seed):
     return oracle.quantize_affine4(w, 64)
 
 
-@pytest.mark.parametrize("T,K,On,N", [(1, 256, 128, 2), (16, 512, 200, 4), (40, 1024, 136, 8), (256, 128, 64, 1)])
+# (2, 1088, 37, 3): two tokens, 34 items of 32 per row (a ragged second slab),
+# 37 rows (a ragged last block of 4); (1, 64, 1, 1): one group, one row.
+@pytest.mark.parametrize("T,K,On,N", [(1, 256, 128, 2), (2, 1088, 37, 3), (1, 64, 1, 1), (16, 512, 200, 4),
+                                      (40, 1024, 136, 8), (256, 128, 64, 1)])
 def test_q4_all_to_sharded(policy, T, K, On, N):
     x = rand_bf16((T, K))
     pq, ps, pb = _q4_host(On * N, K, T + K)
@@ -249,7 +252,10 @@ def test_q4_all_to_sharded(policy, T, K, On, N):
         check_close(to_host(ys[r]), ref[r], "q4 col shard %d" % r)
 
 
-@pytest.mark.parametrize("T,Kn,O,N", [(1, 128, 256, 2), (16, 64, 130, 8), (33, 256, 72, 4), (256, 192, 128, 2)])
+# (2, 192, 75, 5): two tokens, 6 items per rank, 75 rows; (1, 2112, 130, 3):
+# 66 items per rank (three slabs, ragged), 130 rows.
+@pytest.mark.parametrize("T,Kn,O,N", [(1, 128, 256, 2), (2, 192, 75, 5), (1, 2112, 130, 3), (16, 64, 130, 8),
+                                      (33, 256, 72, 4), (256, 192, 128, 2)])
 def test_q4_sharded_to_all(policy, T, Kn, O, N):
     x = rand_bf16((T, Kn * N))
     pq, ps, pb = _q4_host(O, Kn * N, O + Kn)
