@@ -258,19 +258,33 @@ __device__ __forceinline__ void store_out(void *C, int out_dt, int64_t idx, floa
     static_cast<__half *>(C)[idx] = __float2half_rn(v);
 }
 
-// Sums partial slots 0..nparts-1 of rows b*kGvRows.. of job J in part order,
-// adds the bias, stores, and resets the row block's counter (lane 0).
+// Output k (row k/TT, token k%TT) of row block b of job J: its partial slots
+// 0..nparts-1 added in part order (loads issued eight at a time, ahead of the
+// adds), plus the bias, stored.
+template <int TT>
+__device__ __forceinline__ void reduce_one(const GvJob &J, int b, int k, int out_dt, const float *ws) {
+  const float *slots = ws + J.ws_base + (int64_t)b * J.nparts * (kGvRows * TT) + k;
+  const int o = b * kGvRows + k / TT;
+  if (o >= J.rows) return;
+  float r = 0.f;
+  for (int q0 = 0; q0 < J.nparts; q0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = q0 + u < J.nparts ? ldcg_f(slots + (q0 + u) * (kGvRows * TT)) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (q0 + u < J.nparts) r = q0 + u == 0 ? v[u] : r + v[u];
+  }
+  if (J.bias) r += J.bias[o];
+  store_out(J.C, out_dt, (int64_t)(k % TT) * J.ldc + o, r);
+}
+
+// The warp reduces row block b of job J (lanes 0..kGvRows*TT-1) and resets its
+// counter.
 template <int TT>
 __device__ __forceinline__ void reduce_parts(const GvJob &J, int b, int lane, int out_dt, const float *ws,
                                              int *cnt) {
-  const float *slots = ws + J.ws_base + (int64_t)b * J.nparts * (kGvRows * TT);
-  const int o = b * kGvRows + lane / TT;
-  if (lane < kGvRows * TT && o < J.rows) {
-    float r = ldcg_f(slots + lane);
-    for (int q = 1; q < J.nparts; ++q) r += ldcg_f(slots + q * (kGvRows * TT) + lane);
-    if (J.bias) r += J.bias[o];
-    store_out(J.C, out_dt, (int64_t)(lane % TT) * J.ldc + o, r);
-  }
+  if (lane < kGvRows * TT) reduce_one<TT>(J, b, lane, out_dt, ws);
   if (lane == 0) cnt[J.cnt_base + b] = 0;
 }
 
@@ -568,10 +582,13 @@ __global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __g
   GtCur ci, cc;
   gt_set(a, R, gw, ci);
   cc = ci;
-  int ki = 0;
+  // issue and compute cursors walk the same steps; slot indices and the
+  // compute phase advance incrementally (S is a launch parameter)
+  int ki = 0, si = 0;
   // prologue: the first S-1 steps go out before x is staged
   for (; ki < S - 1 && ci.u >= 0; ++ki) {
-    if (lane == 0) gt_issue(a, ci, smem_u32(ring + (ki % S) * kGtSlot), bars + 8 * (ki % S));
+    if (lane == 0) gt_issue(a, ci, ring_s + si * kGtSlot, bars + 8 * si);
+    si = si + 1 == S ? 0 : si + 1;
     gt_next(a, R, Wr, ci);
   }
 
@@ -584,17 +601,18 @@ __global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __g
 #pragma unroll
     for (int tk = 0; tk < TT; ++tk) acc[i][tk] = 0.f;
 
-  int kc = 0;
+  int kc = 0, slot = 0;
+  uint32_t phase = 0;
   bool ok = true;
   while (cc.u >= 0) {
     // refill the slot the previous step freed
     if (ci.u >= 0) {
-      if (lane == 0) gt_issue(a, ci, smem_u32(ring + (ki % S) * kGtSlot), bars + 8 * (ki % S));
+      if (lane == 0) gt_issue(a, ci, ring_s + si * kGtSlot, bars + 8 * si);
+      si = si + 1 == S ? 0 : si + 1;
       gt_next(a, R, Wr, ci);
       ++ki;
     }
-    const int slot = kc % S;
-    ok = mbar_wait(bars + 8 * slot, (kc / S) & 1, a.wait_ns, a.status, nullptr);
+    ok = mbar_wait(bars + 8 * slot, phase, a.wait_ns, a.status, nullptr);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     const int G = a.parts[cc.q].G;
@@ -620,6 +638,10 @@ __global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __g
     __syncwarp();
     gt_next(a, R, Wr, cc);
     ++kc;
+    if (++slot == S) {
+      slot = 0;
+      phase ^= 1u;
+    }
   }
   if (!ok) {
     // a wait ran out: let the copies already issued land (bounded) before
@@ -644,11 +666,24 @@ __global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __g
     }
     unsigned m = __ballot_sync(0xffffffffu, last);
     if (m) __threadfence();
+    // up to 32/(kGvRows*TT) row blocks at a time, lanes split by (block, output)
+    constexpr int kPer = kGvRows * TT, kAtOnce = 32 / kPer;
     while (m) {
-      const int l = __ffs(m) - 1;
-      m &= m - 1;
-      const int jl = __shfl_sync(0xffffffffu, jj, l), bl = __shfl_sync(0xffffffffu, bb, l);
-      reduce_parts<TT>(a.jobs[jl], bl, lane, a.out_dt, a.ws, a.cnt);
+      int src = -1;
+      unsigned mm = m;
+      for (int t = 0; t < kAtOnce && mm; ++t) {
+        const int l = __ffs(mm) - 1;
+        mm &= mm - 1;
+        if (lane / kPer == t) src = l;
+      }
+      m = mm;
+      const int jl = __shfl_sync(0xffffffffu, jj, src < 0 ? 0 : src);
+      const int bl = __shfl_sync(0xffffffffu, bb, src < 0 ? 0 : src);
+      if (src >= 0) {
+        const GvJob &J = a.jobs[jl];
+        reduce_one<TT>(J, bl, lane % kPer, a.out_dt, a.ws);
+        if (lane % kPer == 0) a.cnt[J.cnt_base + bl] = 0;
+      }
     }
     if (!__any_sync(0xffffffffu, gw + (base + 32) * Wr < R.units)) break;
   }
