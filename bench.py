@@ -23,6 +23,7 @@ scaling); no collective touches the data path.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -48,6 +49,44 @@ def load_peaks() -> dict:
                     bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
                     source="measured")
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
+# config's kernels, from one ncu capture of `python bench.py --config C --steps 3
+# --warmup 3 --no-cpu-baseline` (the summary is in profiles/dram_traffic_by_config.md).
+# It is reported only while the kernel sources hash to TRAFFIC_SOURCES, since a
+# changed kernel needs a new capture.
+TRAFFIC_SOURCES = "0941216380804b06"
+TRAFFIC = {
+    ("mlp", "tp_all_to_sharded"): 98046464, ("mlp", "tp_sharded_to_all"): 104730624,
+    ("summa2", "tp_summa"): 1535383808, ("summa4", "tp_summa"): 1346387712,
+    ("qkv1", "tp_all_to_sharded(qkv)"): 103951872, ("qkv1", "tp_sharded_to_all(o)"): 33606400,
+    ("qkv1", "tp_all_to_sharded(lm_head)"): 412361984,
+    ("qkv16", "tp_all_to_sharded(qkv)"): 104039424, ("qkv16", "tp_sharded_to_all(o)"): 33727744,
+    ("qkv16", "tp_all_to_sharded(lm_head)"): 414381312,
+    ("qkv2048", "tp_all_to_sharded(qkv)"): 148083200, ("qkv2048", "tp_sharded_to_all(o)"): 51198976,
+    ("qkv2048", "tp_all_to_sharded(lm_head)"): 841149184,
+    ("q4_1", "tp_q4_all_to_sharded"): 135343872, ("q4_1", "tp_q4_sharded_to_all"): 132427520,
+    ("q4_16", "tp_q4_all_to_sharded"): 136604416, ("q4_16", "tp_q4_sharded_to_all"): 134206208,
+    ("q4_256", "tp_q4_all_to_sharded"): 141671936, ("q4_256", "tp_q4_sharded_to_all"): 214105856,
+}
+
+
+def kernel_sources_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "sharded_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(config: str, kernel: str):
+    if kernel_sources_hash() != TRAFFIC_SOURCES:
+        return None
+    return TRAFFIC.get((config, kernel))
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -369,7 +408,8 @@ def main():
         achieved = info["kernel_work"][k] / (per_kernel[k] * 1e-3) / 1e9
         peak_kind = "hbm_gbs"
     roofline = {"bound": info["bound"], "kernel": info["kernel_names"][k], "achieved": round(achieved, 2),
-                "peak": peak, "unit": punit, "frac": round(achieved / peak, 4), "traffic": None,
+                "peak": peak, "unit": punit, "frac": round(achieved / peak, 4),
+                "traffic": traffic_for(args.config, info["kernel_names"][k]),
                 "peak_source": "%s of %s" % (peak_kind, peaks["source"])}
 
     cpu = None

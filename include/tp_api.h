@@ -26,8 +26,13 @@
  *    makes the kernel record TP_ERR_TIMEOUT in a device status word and
  *    return.  tp_query_status() reads (and clears) that word.
  *  - The library allocates one 4-byte device status word per device on
- *    first use and caches host-side TMA descriptors; tp_shutdown() frees
- *    them.  Nothing else is allocated.
+ *    first use and caches host-side TMA descriptors.  Calls whose kernel
+ *    splits a sum across CTAs (the row-parallel 4-bit linears, and split-K
+ *    4-bit tiles) use a per-(device, stream) float32 workspace with zeroed
+ *    counters, allocated (cudaMalloc) on first need and grown when a larger
+ *    call needs more; the counters are back at zero when each kernel ends.
+ *    tp_shutdown() frees all of it.  tp_q4_sharded_to_all_noalloc never
+ *    allocates.
  */
 #ifndef TP_API_H
 #define TP_API_H
