@@ -415,18 +415,25 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 // load of the pair completes on rank 0's stage barrier; rank 0's commits reach
 // both CTAs' barriers; both epilogues release the accumulator on rank 0's
 // barrier.  Each CTA's TMEM holds its own 128 rows of the 256 x BN tile.
-template <int BN, bool B_MN, int STAGES, int NACC>
+//
+// NSUB = 2: a unit is two neighbouring 256 x BN tiles that share their A rows;
+// each k-block stages A once and both tiles' B halves, and the MMAs of the two
+// tiles go to two accumulators.  Per SM, a k-block then stages 128 + BN rows
+// for 2 x BN columns of MMA work instead of 128 + BN/2 rows for BN.
+template <int BN, bool B_MN, int STAGES, int NACC, int NSUB>
 __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_constant__ UmmaArgs a) {
+  static_assert(NSUB == 1 || !B_MN, "two-tile units are for K-major B");
   constexpr int BNH = BN / 2;
   constexpr int A_BYTES = BM * BK * 2;
-  constexpr int B_BYTES = BNH * BK * 2;
+  constexpr int B_SUB = BNH * BK * 2;  // one tile's B half, a multiple of 1024
+  constexpr int B_BYTES = NSUB * B_SUB;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr int TCOLS = TmemCols<NACC * BN>::v;
+  constexpr int TCOLS = TmemCols<NACC * NSUB * BN>::v;
   constexpr int HALF = BN / 2;
   constexpr int CH = ChunkOf<HALF>::v;
   constexpr int NCH = HALF / CH;
-  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-  static_assert(NACC * BN <= 512, "TMEM capacity");
+  static_assert(STAGE_BYTES % 1024 == 0 && B_SUB % 1024 == 0, "stage alignment");
+  static_assert(NACC * NSUB * BN <= 512, "TMEM capacity");
   static_assert(!B_MN || BNH % 64 == 0, "MN-major B needs 64-column boxes");
 
   extern __shared__ uint8_t dsmem[];
@@ -483,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
         const UJob &J = a.jobs[find_job(a, u)];
         const int local = u - J.unit_begin;
         const int ta = local % J.tilesA, tb = local / J.tilesA;
-        const int rowA0 = ta * 2 * BM + (int)rank * BM, rowB0 = tb * BN + (int)rank * BNH;
+        const int rowA0 = ta * 2 * BM + (int)rank * BM, rowB0 = tb * NSUB * BN + (int)rank * BNH;
         for (int p = 0; ok && p < J.nparts; ++p) {
           const UPart P = a.parts[J.part0 + p];
           for (int kb = 0; kb < P.kblocks; ++kb) {
@@ -500,7 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
               for (int c = 0; c < BNH / 64; ++c)
                 tma_load_2d_pair(sb + c * 8192, &a.mapB[P.bmap], fb, rowB0 + c * 64, kb * BK);
             } else {
-              tma_load_2d_pair(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
+#pragma unroll
+              for (int sub = 0; sub < NSUB; ++sub)
+                tma_load_2d_pair(sb + sub * B_SUB, &a.mapB[P.bmap], fb, kb * BK, rowB0 + sub * BN);
             }
             umma_trace(a, 1, pseq++);
             used[stage] = true;
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
             }
             tc_fence_after();
           }
-          const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+          const uint32_t d = tmem_base + (uint32_t)(acc * NSUB * BN);
           for (int kb = 0; kb < P.kblocks; ++kb) {
             if (!mbar_wait(smem_u32(&full_bar[stage]), phase, lim, a.status, &abort_sh)) {
               ok = false;
@@ -546,9 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t ad = umma_desc_sw128(sa + kk * 32, 16, 1024);
-              const uint64_t bd = B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
-                                       : umma_desc_sw128(sb + kk * 32, 16, 1024);
-              umma_f16_pair(d, ad, bd, a.idesc, (kb > 0 || kk > 0 || p > 0) ? 1u : 0u);
+#pragma unroll
+              for (int sub = 0; sub < NSUB; ++sub) {
+                const uint64_t bd = B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                         : umma_desc_sw128(sb + sub * B_SUB + kk * 32, 16, 1024);
+                umma_f16_pair(d + (uint32_t)(sub * BN), ad, bd, a.idesc, (kb > 0 || kk > 0 || p > 0) ? 1u : 0u);
+              }
             }
             umma_commit_pair(smem_u32(&empty_bar[stage]), (uint16_t)3);
             umma_trace(a, 3, mseq++);
@@ -583,21 +595,24 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
       const int local = u - J.unit_begin;
       const int ta = local % J.tilesA, tb = local / J.tilesA;
       const int row = ta * 2 * BM + (int)rank * BM + quarter * 32 + lane;
-      const int colb = tb * BN + half * HALF;
       const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, lim, a.status, &abort_sh);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t tb_addr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16) +
-                               (uint32_t)(half * HALF);
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float v[CH];
-        tmem_load_chunk<CH>(tb_addr + c * CH, v);
-        tmem_wait_ld();
-        store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+      for (int sub = 0; sub < NSUB; ++sub) {
+        const int colb = tb * NSUB * BN + sub * BN + half * HALF;
+        const uint32_t tb_addr = tmem_base + (uint32_t)((acc * NSUB + sub) * BN) + ((uint32_t)(quarter * 32) << 16) +
+                                 (uint32_t)(half * HALF);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          float v[CH];
+          tmem_load_chunk<CH>(tb_addr + c * CH, v);
+          tmem_wait_ld();
+          store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -627,12 +642,17 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
 // the tile over the N partials in ascending rank order (reading its peers'
 // shared memory), adds the bias once and stores.  The partials never leave
 // the chip.  One unit per CTA (not persistent).
-template <int BN, int STAGES>
+//
+// MSUB = 2: the tile is 256 x BN, two 128-row sub-tiles sharing each k-block's
+// B rows (two accumulators), so a k-block stages 256 + BN rows for twice the
+// MMA work; the partial is parked and reduced one sub-tile at a time.
+template <int BN, int STAGES, int MSUB>
 __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __grid_constant__ UmmaArgs a) {
-  constexpr int A_BYTES = BM * BK * 2;
+  constexpr int A_SUB = BM * BK * 2;
+  constexpr int A_BYTES = MSUB * A_SUB;
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr int TCOLS = TmemCols<BN>::v;
+  constexpr int TCOLS = TmemCols<MSUB * BN>::v;
   constexpr int HALF = BN / 2;
   constexpr int CH = ChunkOf<HALF>::v;
   constexpr int NCH = HALF / CH;
@@ -654,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
   const uint64_t lim = a.wait_ns;
   const UJob &J = a.jobs[0];
   const int ta = tile % J.tilesA, tbn = tile / J.tilesA;
-  const int rowA0 = ta * BM, rowB0 = tbn * BN;
+  const int rowA0 = ta * MSUB * BM, rowB0 = tbn * BN;
   const UPart P = a.parts[J.part0 + (int)rank];
 
   if (threadIdx.x == 0) {
@@ -695,7 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
         const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
         const uint32_t fb = smem_u32(&full_bar[stage]);
         mbar_arrive_expect_tx(fb, STAGE_BYTES);
-        tma_load_2d(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
+#pragma unroll
+        for (int m = 0; m < MSUB; ++m) tma_load_2d(sa + m * A_SUB, &a.mapA[P.amap], fb, kb * BK, rowA0 + m * BM);
         tma_load_2d(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
         used[stage] = true;
         last_phase[stage] = phase;
@@ -718,8 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
         const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          umma_f16(tmem_base, umma_desc_sw128(sa + kk * 32, 16, 1024),
-                   umma_desc_sw128(sb + kk * 32, 16, 1024), a.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int m = 0; m < MSUB; ++m)
+            umma_f16(tmem_base + (uint32_t)(m * BN), umma_desc_sw128(sa + m * A_SUB + kk * 32, 16, 1024),
+                     umma_desc_sw128(sb + kk * 32, 16, 1024), a.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
         umma_commit(smem_u32(&empty_bar[stage]));
         if (++stage == STAGES) {
           stage = 0;
@@ -730,15 +753,24 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
       umma_commit(smem_u32(&drain_bar));
       mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
     }
-  } else {
-    // park this rank's partial in shared memory (row-major, padded rows)
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int row = quarter * 32 + lane;
-    const bool got = mbar_wait(smem_u32(&tfull_bar), 0, lim, a.status, &abort_sh);
-    if (__all_sync(0xffffffffu, got)) {
+  }
+
+  // Per 128-row sub-tile: park this rank's partial in shared memory (row-major,
+  // padded rows), cluster barrier, sum column slice `rank` over the ranks in
+  // order and store, cluster barrier (peers are done reading before the next
+  // sub-tile is parked over it).
+  bool got = true;
+  if (warp >= 2) {
+    got = mbar_wait(smem_u32(&tfull_bar), 0, lim, a.status, &abort_sh);
+    got = __all_sync(0xffffffffu, got);
+  }
+  for (int m = 0; m < MSUB; ++m) {
+    if (warp >= 2 && got) {
+      const int quarter = warp & 3;
+      const int half = (warp - 2) >> 2;
+      const int row = quarter * 32 + lane;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * HALF);
+      const uint32_t taddr = tmem_base + (uint32_t)(m * BN) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * HALF);
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         float v[CH];
@@ -752,31 +784,35 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
                        : "memory");
       }
     }
-  }
 
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync_all();  // every rank's partial is parked
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // every rank's partial of sub-tile m is parked
 
-  if (warp >= 2) {
-    // column slice `rank` of the tile: sum over ranks 0..N-1 in order, then bias
-    const int slice = BN / N;
-    const int per_row = slice / 4;
-    const int t = threadIdx.x - 64;
-    for (int idx = t; idx < BM * per_row; idx += 256) {
-      const int r = idx / per_row;
-      const int c = (int)rank * slice + (idx - r * per_row) * 4;
-      const uint32_t off = sbase + (uint32_t)((r * RED_LD + c) * 4);
-      float4 acc = ld_cluster_f4(mapa_shared(off, 0));
-      for (int q = 1; q < N; ++q) {
-        const float4 v = ld_cluster_f4(mapa_shared(off, (uint32_t)q));
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+    if (warp >= 2) {
+      // column slice `rank` of the sub-tile: sum over ranks 0..N-1 in order, then bias
+      const int slice = BN / N;
+      const int per_row = slice / 4;
+      const int t = threadIdx.x - 64;
+      for (int idx = t; idx < BM * per_row; idx += 256) {
+        const int r = idx / per_row;
+        const int c = (int)rank * slice + (idx - r * per_row) * 4;
+        const uint32_t off = sbase + (uint32_t)((r * RED_LD + c) * 4);
+        float4 acc = ld_cluster_f4(mapa_shared(off, 0));
+        for (int q = 1; q < N; ++q) {
+          const float4 v = ld_cluster_f4(mapa_shared(off, (uint32_t)q));
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        float o[4] = {acc.x, acc.y, acc.z, acc.w};
+        store_row_chunk<4>(a, J, rowA0 + m * BM + r, rowB0 + c, o);
       }
-      float o[4] = {acc.x, acc.y, acc.z, acc.w};
-      store_row_chunk<4>(a, J, rowA0 + r, rowB0 + c, o);
+    }
+    if (m + 1 < MSUB) {
+      __syncthreads();
+      cluster_sync_all();  // peers are done reading sub-tile m
     }
   }
 
@@ -820,10 +856,10 @@ int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_gemm_kernel launch");
 }
 
-template <int BN, bool B_MN, int STAGES, int NACC>
+template <int BN, bool B_MN, int STAGES, int NACC, int NSUB>
 int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
-  auto kern = umma_pair_kernel<BN, B_MN, STAGES, NACC>;
-  constexpr int smem = STAGES * (BM * BK * 2 + (BN / 2) * BK * 2) + 1024;
+  auto kern = umma_pair_kernel<BN, B_MN, STAGES, NACC, NSUB>;
+  constexpr int smem = STAGES * (BM * BK * 2 + NSUB * (BN / 2) * BK * 2) + 1024;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -852,10 +888,10 @@ int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_pair_kernel launch");
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int MSUB>
 int launch_row_cluster(UmmaArgs &args, cudaStream_t s) {
-  auto kern = umma_row_cluster_kernel<BN, STAGES>;
-  constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024;
+  auto kern = umma_row_cluster_kernel<BN, STAGES, MSUB>;
+  constexpr int smem = STAGES * (MSUB * BM * BK * 2 + BN * BK * 2) + 1024;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -911,7 +947,7 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   // max(MMA cycles, 2.2 x the operand rows one CTA stages): a CTA can keep
   // only so many bytes in flight, so the staged rows set the pace once the
   // MMA is fast enough.  Rounds of tiles over the SMs multiply that.
-  int BN;
+  int BN, nsub = 1, msub = 1;
   bool pair = false, rowclu = false;
   if (swap) {
     BN = 16;
@@ -928,37 +964,59 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
       const double kb = (double)((p.parts[J.part0].K + BK - 1) / BK);
       // Measured: 4-rank clusters win on long K (MLP 2752 per rank); 8-rank
       // clusters and short K lose to the fixed per-CTA cost of this kernel.
+      // msub = 2: 256 x 256 tiles (two row sub-tiles sharing B; 64 KB
+      // k-blocks, about 4/3 the time of a 48 KB one, and two reduce rounds).
+      // Clusters of four CTAs: 144 of the 152 SMs can hold them at once.
       if (N >= 2 && N <= 4 && kb >= 32 && (256 % N) == 0 && same_k) {
-        const int64_t mt = (J.M + BM - 1) / BM;
-        const int64_t t128 = mt * ((J.N + 127) / 128), t256 = mt * ((J.N + 255) / 256);
-        const double single = (double)((t128 + sms0 - 1) / sms0) * N * kb * 720.0;
-        const double clu = (double)((t256 * N + sms0 - 1) / sms0) * (kb * 850.0 + 12000.0);
-        if (clu < single) {
+        const int64_t mt = (J.M + BM - 1) / BM, mt2 = (J.M + 2 * BM - 1) / (2 * BM);
+        const int64_t nt = (J.N + 255) / 256;
+        const int64_t resident = N == 4 ? sms0 / 152.0 * 144 : sms0;
+        const double single = (double)(((mt * ((J.N + 127) / 128)) + sms0 - 1) / sms0) * N * kb * 720.0;
+        const double clu1 = (double)((mt * nt * N + resident - 1) / resident) * (kb * 850.0 + 12000.0);
+        const double clu2 = (double)((mt2 * nt * N + resident - 1) / resident) * (kb * 1133.0 + 24000.0);
+        if (std::min(clu1, clu2) < single) {
           rowclu = true;
           BN = 256;
+          msub = clu2 < clu1 ? 2 : 1;
         }
       }
     }
   } else {
+    // Candidates: one CTA or a CTA pair per unit, a unit one tile or (pairs)
+    // two neighbouring tiles sharing A (nsub = 2, one accumulator set, so its
+    // epilogue is not hidden behind the next unit's main loop: about 5000
+    // cycles).  Cost: rounds x (k-blocks x per-k-block cost + exposed
+    // epilogue).
     const int sms0 = sm_count();
     const bool allow_pair = pair_policy_allowed() && sms0 >= 2;
+    int64_t kbw = 1;  // k-blocks of one unit (the chained parts together)
+    for (int j = 0; j < p.njobs; ++j) {
+      int64_t kb = 0;
+      for (int q = 0; q < p.jobs[j].nparts; ++q) kb += (p.parts[p.jobs[j].part0 + q].K + BK - 1) / BK;
+      if (kb > kbw) kbw = kb;
+    }
     double best = 1e300;
     BN = 256;
     for (int pm = 0; pm < (allow_pair ? 2 : 1); ++pm) {
-      for (int bn : {256, 192, 160}) {
-        if (summa && bn != 256) continue;
-        const int64_t mrows = pm ? 2 * BM : BM;
-        int64_t tiles = 0;
-        for (int j = 0; j < p.njobs; ++j)
-          tiles += ((p.jobs[j].M + mrows - 1) / mrows) * ((p.jobs[j].N + bn - 1) / bn);
-        const int64_t slots = pm ? sms0 / 2 : sms0;
-        const double rounds = (double)((tiles + slots - 1) / slots);
-        const double per_kb = std::max(2.0 * bn, 2.2 * (128.0 + (pm ? bn / 2 : bn)));
-        const double cost = rounds * per_kb;
-        if (cost < best - 1e-9) {
-          best = cost;
-          BN = bn;
-          pair = pm == 1;
+      for (int ns = 1; ns <= 2; ++ns) {
+        if (ns == 2 && (!pm || summa)) continue;
+        for (int bn : {256, 192, 160}) {
+          if (summa && bn != 256) continue;
+          const int64_t mrows = pm ? 2 * BM : BM;
+          int64_t units = 0;
+          for (int j = 0; j < p.njobs; ++j)
+            units += ((p.jobs[j].M + mrows - 1) / mrows) * ((p.jobs[j].N + ns * bn - 1) / (ns * bn));
+          const int64_t slots = pm ? sms0 / 2 : sms0;
+          const double rounds = (double)((units + slots - 1) / slots);
+          const double per_kb = std::max(2.0 * bn * ns, 2.2 * (128.0 + ns * (pm ? bn / 2 : bn)));
+          const double epi = 5000.0;
+          const double cost = rounds * (double)kbw * per_kb + (ns == 2 ? rounds * epi : epi);
+          if (cost < best - 1e-9) {
+            best = cost;
+            BN = bn;
+            pair = pm == 1;
+            nsub = ns;
+          }
         }
       }
     }
@@ -983,8 +1041,8 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     U.rowsB = (int)(swap ? J.M : J.N);
     U.part0 = J.part0;
     U.nparts = J.nparts;
-    U.tilesA = (U.rowsA + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
-    U.tilesB = (U.rowsB + BN - 1) / BN;
+    U.tilesA = (U.rowsA + (pair || msub == 2 ? 2 * BM : BM) - 1) / (pair || msub == 2 ? 2 * BM : BM);
+    U.tilesB = (U.rowsB + nsub * BN - 1) / (nsub * BN);
     U.unit_begin = (int)units;
     units += (int64_t)U.tilesA * U.tilesB;
     for (int q = 0; q < J.nparts; ++q) {
@@ -1044,16 +1102,24 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   args.status = p.status;
   args.wait_ns = (uint64_t)p.wait_ns;
 
-  if (rowclu)
-    rc = launch_row_cluster<256, 4>(args, s);
+  if (rowclu && msub == 2)
+    rc = launch_row_cluster<256, 3, 2>(args, s);
+  else if (rowclu)
+    rc = launch_row_cluster<256, 4, 1>(args, s);
   else if (pair && summa)
-    rc = launch_pair<256, true, 6, 2>(args, sms, s);
+    rc = launch_pair<256, true, 6, 2, 1>(args, sms, s);
+  else if (pair && nsub == 2 && BN == 160)
+    rc = launch_pair<160, false, 6, 1, 2>(args, sms, s);
+  else if (pair && nsub == 2 && BN == 192)
+    rc = launch_pair<192, false, 5, 1, 2>(args, sms, s);
+  else if (pair && nsub == 2)
+    rc = launch_pair<256, false, 4, 1, 2>(args, sms, s);
   else if (pair && BN == 160)
-    rc = launch_pair<160, false, 8, 2>(args, sms, s);
+    rc = launch_pair<160, false, 8, 2, 1>(args, sms, s);
   else if (pair && BN == 192)
-    rc = launch_pair<192, false, 7, 2>(args, sms, s);
+    rc = launch_pair<192, false, 7, 2, 1>(args, sms, s);
   else if (pair)
-    rc = launch_pair<256, false, 6, 2>(args, sms, s);
+    rc = launch_pair<256, false, 6, 2, 1>(args, sms, s);
   else if (summa)
     rc = launch_config<256, true, false, false, 4, 2>(args, sms, s);
   else if (swap && partials)
