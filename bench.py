@@ -56,19 +56,19 @@ def load_peaks() -> dict:
 # --warmup 3 --no-cpu-baseline` (the summary is in profiles/dram_traffic_by_config.md).
 # It is reported only while the kernel sources hash to TRAFFIC_SOURCES, since a
 # changed kernel needs a new capture.
-TRAFFIC_SOURCES = "0941216380804b06"
+TRAFFIC_SOURCES = "6879dfb0ad67fe3e"
 TRAFFIC = {
-    ("mlp", "tp_all_to_sharded"): 98046464, ("mlp", "tp_sharded_to_all"): 104730624,
-    ("summa2", "tp_summa"): 1535383808, ("summa4", "tp_summa"): 1346387712,
-    ("qkv1", "tp_all_to_sharded(qkv)"): 103951872, ("qkv1", "tp_sharded_to_all(o)"): 33606400,
-    ("qkv1", "tp_all_to_sharded(lm_head)"): 412361984,
-    ("qkv16", "tp_all_to_sharded(qkv)"): 104039424, ("qkv16", "tp_sharded_to_all(o)"): 33727744,
-    ("qkv16", "tp_all_to_sharded(lm_head)"): 414381312,
-    ("qkv2048", "tp_all_to_sharded(qkv)"): 148083200, ("qkv2048", "tp_sharded_to_all(o)"): 51198976,
-    ("qkv2048", "tp_all_to_sharded(lm_head)"): 841149184,
-    ("q4_1", "tp_q4_all_to_sharded"): 135343872, ("q4_1", "tp_q4_sharded_to_all"): 132427520,
-    ("q4_16", "tp_q4_all_to_sharded"): 136604416, ("q4_16", "tp_q4_sharded_to_all"): 134206208,
-    ("q4_256", "tp_q4_all_to_sharded"): 141671936, ("q4_256", "tp_q4_sharded_to_all"): 214105856,
+    ("mlp", "tp_all_to_sharded"): 97898240, ("mlp", "tp_sharded_to_all"): 102631424,
+    ("summa2", "tp_summa"): 1531145984, ("summa4", "tp_summa"): 1342970624,
+    ("qkv1", "tp_all_to_sharded(qkv)"): 103917568, ("qkv1", "tp_sharded_to_all(o)"): 33609984,
+    ("qkv1", "tp_all_to_sharded(lm_head)"): 412302592,
+    ("qkv16", "tp_all_to_sharded(qkv)"): 103808256, ("qkv16", "tp_sharded_to_all(o)"): 33728512,
+    ("qkv16", "tp_all_to_sharded(lm_head)"): 414408960,
+    ("qkv2048", "tp_all_to_sharded(qkv)"): 151419392, ("qkv2048", "tp_sharded_to_all(o)"): 51041280,
+    ("qkv2048", "tp_all_to_sharded(lm_head)"): 929753856,
+    ("q4_1", "tp_q4_all_to_sharded"): 135372032, ("q4_1", "tp_q4_sharded_to_all"): 132407552,
+    ("q4_16", "tp_q4_all_to_sharded"): 136930304, ("q4_16", "tp_q4_sharded_to_all"): 134341632,
+    ("q4_256", "tp_q4_all_to_sharded"): 141455872, ("q4_256", "tp_q4_sharded_to_all"): 215676672,
 }
 
 
