@@ -715,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
         const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
         const uint32_t fb = smem_u32(&full_bar[stage]);
         mbar_arrive_expect_tx(fb, STAGE_BYTES);
-#pragma unroll
-        for (int m = 0; m < MSUB; ++m) tma_load_2d(sa + m * A_SUB, &a.mapA[P.amap], fb, kb * BK, rowA0 + m * BM);
+        // A: one box of all MSUB * 128 rows (the map's box height), B: one box
+        tma_load_2d(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
         tma_load_2d(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
         used[stage] = true;
         last_phase[stage] = phase;
@@ -1058,7 +1058,9 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
         if (bptr[i] == opB) ib = i;
       if (ia < 0) {
         if (nA == kMaxMaps) return TP_OK;
-        rc = make_map(&args.mapA[nA], opA, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsA, (uint64_t)ldA, BK, BM);
+        // the rank clusters with 256-row tiles load A as one 256-row box
+        rc = make_map(&args.mapA[nA], opA, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsA, (uint64_t)ldA, BK,
+                      rowclu ? msub * BM : BM);
         if (rc) return rc;
         aptr[nA] = opA;
         ia = nA++;
