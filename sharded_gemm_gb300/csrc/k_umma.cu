@@ -416,10 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 // both CTAs' barriers; both epilogues release the accumulator on rank 0's
 // barrier.  Each CTA's TMEM holds its own 128 rows of the 256 x BN tile.
 //
-// NSUB = 2: a unit is two neighbouring 256 x BN tiles that share their A rows;
-// each k-block stages A once and both tiles' B halves, and the MMAs of the two
-// tiles go to two accumulators.  Per SM, a k-block then stages 128 + BN rows
-// for 2 x BN columns of MMA work instead of 128 + BN/2 rows for BN.
+// NSUB = 2: a unit is 256 x 2BN (two accumulators of BN columns) sharing its A
+// rows; each k-block stages A once and BN rows of B per CTA, so an SM stages
+// 128 + BN rows for 2 x BN columns of MMA work instead of 128 + BN/2 rows for
+// BN.  CTA r holds the unit's B rows [r*BN, (r+1)*BN) as one box; MMA s takes
+// rows [s*BN/2, (s+1)*BN/2) of each CTA's box, so accumulator s's columns are
+// the unit's columns s*BN/2 + [0, BN/2) (from CTA 0) and BN + s*BN/2 + [0, BN/2)
+// (from CTA 1).
 template <int BN, bool B_MN, int STAGES, int NACC, int NSUB>
 __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_constant__ UmmaArgs a) {
   static_assert(NSUB == 1 || !B_MN, "two-tile units are for K-major B");
@@ -490,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
         const UJob &J = a.jobs[find_job(a, u)];
         const int local = u - J.unit_begin;
         const int ta = local % J.tilesA, tb = local / J.tilesA;
-        const int rowA0 = ta * 2 * BM + (int)rank * BM, rowB0 = tb * NSUB * BN + (int)rank * BNH;
+        const int rowA0 = ta * 2 * BM + (int)rank * BM;
+        const int rowB0 = tb * NSUB * BN + (int)rank * (NSUB == 2 ? BN : BNH);
         for (int p = 0; ok && p < J.nparts; ++p) {
           const UPart P = a.parts[J.part0 + p];
           for (int kb = 0; kb < P.kblocks; ++kb) {
@@ -507,9 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
               for (int c = 0; c < BNH / 64; ++c)
                 tma_load_2d_pair(sb + c * 8192, &a.mapB[P.bmap], fb, rowB0 + c * 64, kb * BK);
             } else {
-#pragma unroll
-              for (int sub = 0; sub < NSUB; ++sub)
-                tma_load_2d_pair(sb + sub * B_SUB, &a.mapB[P.bmap], fb, kb * BK, rowB0 + sub * BN);
+              tma_load_2d_pair(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);  // NSUB * BN/2 rows
             }
             umma_trace(a, 1, pseq++);
             used[stage] = true;
@@ -603,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
       tc_fence_after();
 #pragma unroll
       for (int sub = 0; sub < NSUB; ++sub) {
-        const int colb = tb * NSUB * BN + sub * BN + half * HALF;
+        const int colb = NSUB == 2 ? tb * 2 * BN + half * BN + sub * BNH : tb * BN + half * HALF;
         const uint32_t tb_addr = tmem_base + (uint32_t)((acc * NSUB + sub) * BN) + ((uint32_t)(quarter * 32) << 16) +
                                  (uint32_t)(half * HALF);
 #pragma unroll
@@ -1071,7 +1073,7 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
           rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)U.rowsB, (uint64_t)P.K, (uint64_t)ldB, 64, BK);
         else
           rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsB, (uint64_t)ldB, BK,
-                        (uint32_t)(pair ? BN / 2 : BN));
+                        (uint32_t)(pair ? nsub * BN / 2 : BN));
         if (rc) return rc;
         bptr[nB] = opB;
         ib = nB++;
