@@ -8,8 +8,10 @@ logical shards, x (512, 4096) bf16, W1 (11008, 4096), W2 (4096, 11008); one
 step = the column-parallel GEMM (x @ W1_r^T for r = 0..3, bf16 intermediate
 kept sharded) followed by the row-parallel GEMM (sum of the 4 partials in rank
 order, + bias, float32 output), both through the C ABI.  Other configs
-(summa2, summa4, qkv1, qkv16, qkv2048, q4_1, q4_16, q4_256) time the other
-workloads the same way.
+(mlp_ag_rs, summa2, summa4, qkv1, qkv16, qkv2048, q4_1, q4_16, q4_256) time the other
+workloads the same way; mlp_ag_rs is the MLP pair with its input and output
+sharded along the model width (an all-gather of the input's column shards
+into W1, a reduce-scatter of W2's partial sums).
 
 Prints ONE JSON line (rank 0).  ``value`` is device-timed throughput with the
 inputs resident in HBM; ``e2e`` is the same metric with the step's input
@@ -179,7 +181,7 @@ class ClockSampler:
 def make_workload(name: str, rank: int, device: str):
     """Returns (obj, step_fn, info) for a config name."""
     from sharded_gemm_gb300 import synth
-    from sharded_gemm_gb300.workloads import MLPPair, Q4Pair, QKV, Summa
+    from sharded_gemm_gb300.workloads import MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa
     seed = synth.SEED + rank
     if name == "mlp":
         cfg = synth.mlp(seed=seed)
@@ -189,6 +191,17 @@ def make_workload(name: str, rank: int, device: str):
                     work=w.flops, bound="tensor", kernel_names=["tp_all_to_sharded", "tp_sharded_to_all"],
                     kernel_work=[2.0 * T * D * F, 2.0 * T * D * F],
                     launches_per_step=2, h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
+        return w, w.step, info
+    if name == "mlp_ag_rs":
+        cfg = synth.mlp(seed=seed)
+        w = MLPGatherScatter(cfg, device=device)
+        T, D, F = cfg["T"], cfg["D"], cfg["F"]
+        info = dict(workload="mlp_allgather_reducescatter", T=T, D=D, F=F, N=cfg["N"], unit="TFLOP/s",
+                    work=w.flops, bound="tensor",
+                    kernel_names=["tp_gathered_to_sharded", "tp_sharded_to_sharded"],
+                    kernel_work=[2.0 * T * D * F, 2.0 * T * D * F],
+                    launches_per_step=2, h2d=("x shards", w.xs), d2h=("y shards", w.ys),
+                    cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     if name in ("summa2", "summa4"):
         q = int(name[-1])
@@ -234,6 +247,9 @@ def split_step(name: str, w):
     if name == "mlp":
         return [lambda s: tp.tp_all_to_sharded(w.x, w.w1, w.b1, out=w.mid, stream=s),
                 lambda s: tp.tp_sharded_to_all(w.mid, w.w2, w.b2, out=w.y, stream=s)]
+    if name == "mlp_ag_rs":
+        return [lambda s: tp.tp_gathered_to_sharded(w.xs, w.w1, w.b1, out=w.mid, stream=s),
+                lambda s: tp.tp_sharded_to_sharded(w.mid, w.w2, w.b2, out=w.ys, stream=s)]
     if name.startswith("summa"):
         return [lambda s: w.step(stream=s)]
     if name.startswith("qkv"):
@@ -375,27 +391,32 @@ def main():
     # e2e: pinned host input -> device, the step, device -> pinned host output
     e2e = None
     if info.get("h2d"):
-        _, dev_in = info["h2d"]
-        _, dev_out = info["d2h"]
-        host_in = torch.empty(dev_in.shape, dtype=dev_in.dtype, pin_memory=True)
-        host_in.copy_(dev_in)
-        host_out = torch.empty(dev_out.shape, dtype=dev_out.dtype, pin_memory=True)
+        # one tensor, or a list of shard tensors (one copy each)
+        dev_in, dev_out = info["h2d"][1], info["d2h"][1]
+        dev_in = list(dev_in) if isinstance(dev_in, (list, tuple)) else [dev_in]
+        dev_out = list(dev_out) if isinstance(dev_out, (list, tuple)) else [dev_out]
+        host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_in]
+        for h, t in zip(host_in, dev_in):
+            h.copy_(t)
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
         e_steps = max(1, min(args.steps, 500))
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e_steps)]
         for i in range(e_steps):
             flush.fill_(float(i & 7))
             evs[i][0].record(stream)
-            dev_in.copy_(host_in, non_blocking=True)
+            for t, h in zip(dev_in, host_in):
+                t.copy_(h, non_blocking=True)
             for fn in launches:
                 fn(stream)
-            host_out.copy_(dev_out, non_blocking=True)
+            for h, t in zip(host_out, dev_out):
+                h.copy_(t, non_blocking=True)
             evs[i][1].record(stream)
         torch.cuda.synchronize()
         e_ms = sum(a.elapsed_time(b) for a, b in evs) / e_steps
         e_max, e_work = aggregate(e_ms, info["work"], world, group, device)
         e2e = {"value": round(scale(e_work, e_max, info["unit"]), 3), "unit": info["unit"],
-               "h2d_bytes_per_step": dev_in.numel() * dev_in.element_size(),
-               "d2h_bytes_per_step": dev_out.numel() * dev_out.element_size()}
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in dev_in),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in dev_out)}
 
     # roofline of the dominant kernel
     k = max(range(nk), key=lambda i: per_kernel[i])

@@ -169,6 +169,59 @@ int tp_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K, int64_t
                       void *y, int64_t ldy, tp_dtype out_dt, tp_stream_t stream);
 
 /*
+ * f1 -- row-parallel linear with a reduce-scatter, "sharded-to-sharded"
+ * ("sharded matrices" notes, case 3, second option: reduce-scatter the
+ * partial sums instead of all-reducing them, so the output stays sharded
+ * along its columns; primitive table, ReduceScatter_{X,K}).
+ *
+ * For c = 0..N-1:
+ *   y[c] = (sum over r = 0..N-1, ascending, of x[r] @ W_r[c]^T) + bias[c*O/N ..]
+ * where W_r[c] is rows c*O/N .. (c+1)*O/N - 1 of w[r].
+ *   x[r]   (T, K/N) in_dt, row stride ldx (>= K/N): shard r of the input;
+ *   w[r]   (O, K/N) in_dt contiguous: shard r of the (O, K) weight, split on
+ *          its last axis (the same shards as tp_sharded_to_all);
+ *   bias   NULL or float32 (O), the layer's replicated bias; rank c adds its
+ *          block c*O/N .. once, after the sum;
+ *   y[c]   (T, O/N) out_dt, row stride ldy (>= O/N): rank c's block of the
+ *          output.  With y[c] = base + c*(O/N) and ldy = O the blocks form
+ *          the all-reduced (T, O) output of tp_sharded_to_all.
+ * Every partial is formed in float32 from zero and the N partials of a block
+ * are added in ascending r, as in tp_sharded_to_all; partials do not go
+ * through device memory.
+ * Errors: TP_ERR_NOT_DIVISIBLE if K % N != 0 ("Cannot shard the input of
+ * size K across N devices.") or O % N != 0 ("Cannot shard the output ...");
+ * TP_ERR_UNSUPPORTED if N * N > 64; otherwise as tp_sharded_to_all, with
+ * ldy checked against O/N.  T = 0 is valid and launches nothing.
+ */
+int tp_sharded_to_sharded(int N, const void *const *x, int64_t T, int64_t K, int64_t ldx,
+                          const void *const *w, int64_t O, const void *bias, tp_dtype in_dt,
+                          void *const *y, int64_t ldy, tp_dtype out_dt, tp_stream_t stream);
+
+/*
+ * f1 -- all-gather then column-parallel linear, "gathered-to-sharded"
+ * ("sharded matrices" notes, case 2, standard route: all-gather the input's
+ * sharded contraction axis, then the local matmul; the large-batch strategy
+ * of the same notes, and the first half of their Transformer FFN with one
+ * all-gather and one reduce-scatter).
+ *
+ * For r = 0..N-1:  y[r] = concat_q(x[q]) @ w[r]^T + bias[r]
+ *   x[q]   (T, K/N) in_dt, row stride ldx (>= K/N): block q of the input's
+ *          columns (the gathered input is the N blocks side by side);
+ *   w[r]   (O/N, K) in_dt contiguous: shard r of the (O, K) weight (axis 0,
+ *          as tp_all_to_sharded);
+ *   bias   NULL, or a host array of N device pointers to float32 (O/N);
+ *   y[r]   (T, O/N) out_dt, row stride ldy (>= O/N).
+ * The gather is not materialised: rank r's product reads every block x[q]
+ * against columns q*K/N .. of w[r], accumulating in one float32 sum in
+ * block order, which is the order of the gathered contraction axis.
+ * Errors: as tp_sharded_to_sharded, with bias an array of N pointers.
+ */
+int tp_gathered_to_sharded(int N, const void *const *x, int64_t T, int64_t K, int64_t ldx,
+                           const void *const *w, int64_t O, const void *const *bias,
+                           tp_dtype in_dt, void *const *y, int64_t ldy, tp_dtype out_dt,
+                           tp_stream_t stream);
+
+/*
  * a5 -- SUMMA on a q x q grid ("ColossalAI 2D tensor parallel via SUMMA",
  * SUMMA section, equations (1) and (2); Matmul_AB_2D).
  *

@@ -17,6 +17,11 @@ Everything here is the plain definition, computed in float64:
 * the column-parallel layer (section 2.1) is the local linear of each shard
   with no communication; the row-parallel layer (section 2.2) sums the local
   partial products over all shards and adds the bias once, after the sum;
+* the reduce-scatter and all-gather variants follow "sharded matrices"
+  notes, cases 2 and 3 and the collective-primitive table: the reduce-scatter
+  adds the ranks' partial products in rank order and gives rank c column
+  block c of the sum; the all-gather joins the input's column shards in rank
+  order before the column-parallel product;
 * SUMMA follows "ColossalAI 2D tensor parallel via SUMMA", equations (1) and
   (2): block ``Y_ij`` is the sum over steps ``t = 0..q-1`` of ``X_it A_tj``,
   accumulated in step order;
@@ -29,9 +34,10 @@ The matrix products run in the naive C loops of ``oracle.c`` (pinned against
 
 Pins (see ``tests/test_oracle.py``): closed-form shard index rule, brute-force
 slicing, the sharded == unsharded invariant, the SUMMA q=2 block identity and
-the blockwise-identity special case, the dequant identity on brute-force and
-constant-code inputs, the quantizer round-trip bound, and the worked-example
-shapes from the MLX page.
+the blockwise-identity special case, the all-gather / reduce-scatter
+transpose identity, the sharded == unsharded invariant of both collective
+variants, the dequant identity on brute-force and constant-code inputs, the
+quantizer round-trip bound, and the worked-example shapes from the MLX page.
 """
 from __future__ import annotations
 
@@ -194,6 +200,51 @@ def sharded_to_all(x_shards, w_shards, b=None):
     if b is not None:
         total = total + np.asarray(b, dtype=np.float64)[None, :]
     return total
+
+
+# ---------------------------------------------------------------- collectives
+def all_gather(shards, axis: int):
+    """AllGather over the group ("sharded matrices" notes, primitive table):
+    every rank receives all N shards joined in rank order along ``axis``."""
+    return np.concatenate([np.asarray(s, dtype=np.float64) for s in shards], axis=axis)
+
+
+def reduce_scatter(partials, axis: int):
+    """ReduceScatter over the group (same table): the N partial results are
+    added in rank order 0..N-1, the sum is cut along ``axis`` into N equal
+    contiguous blocks, and rank c receives block c."""
+    n = len(partials)
+    total = None
+    for p in partials:
+        p = np.asarray(p, dtype=np.float64)
+        total = p if total is None else total + p
+    length = total.shape[axis]
+    if length % n:
+        raise ValueError("cannot scatter an axis of %d over %d ranks" % (length, n))
+    w = length // n
+    return [np.take(total, np.arange(c * w, (c + 1) * w), axis=axis) for c in range(n)]
+
+
+def sharded_to_sharded(x_shards, w_shards, b=None):
+    """Row-parallel linear whose partial products are reduce-scattered over
+    the output columns instead of all-reduced ("sharded matrices" notes, case
+    3, second option): rank c receives column block c of sum_r x_r @ W_r.T
+    and adds block c of the layer's bias once, after the sum."""
+    n = len(x_shards)
+    partials = [linear(x, w) for x, w in zip(x_shards, w_shards)]
+    ys = reduce_scatter(partials, axis=1)
+    if b is not None:
+        b = np.asarray(b, dtype=np.float64)
+        w = b.shape[0] // n
+        ys = [y + b[None, c * w:(c + 1) * w] for c, y in enumerate(ys)]
+    return ys
+
+
+def gathered_to_sharded(x_shards, w_shards, b_shards=None):
+    """Case 2 of the same notes, standard route: all-gather the input, which
+    is sharded along its contraction axis (columns), then every rank's local
+    column-parallel linear x @ W_r.T + b_r."""
+    return all_to_sharded(all_gather(x_shards, axis=1), w_shards, b_shards)
 
 
 def summa(X_blocks, A_blocks, q: int):

@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
             "tp_shard_weight": ([vp, i64, i64, i32, i32, i32, i32, vpp, vp], i32),
             "tp_all_to_sharded": ([i32, vp, i64, i64, i64, vpp, i64, vpp, i32, vpp, i64, i32, vp], i32),
             "tp_sharded_to_all": ([i32, vpp, i64, i64, i64, vpp, i64, vp, i32, vp, i64, i32, vp], i32),
+            "tp_sharded_to_sharded": ([i32, vpp, i64, i64, i64, vpp, i64, vp, i32, vpp, i64, i32, vp], i32),
+            "tp_gathered_to_sharded": ([i32, vpp, i64, i64, i64, vpp, i64, vpp, i32, vpp, i64, i32, vp], i32),
             "tp_summa": ([i32, vpp, vpp, vpp, i64, i64, i64, i32, vp], i32),
             "tp_q4_quantize": ([vp, i64, i64, i32, vp, vp, vp, vp], i32),
             "tp_q4_all_to_sharded": ([i32, vp, i64, i64, vpp, vpp, vpp, i32, i64, vpp, vpp, i64, i32, vp], i32),
@@ -271,6 +273,65 @@ def tp_sharded_to_all(x, w, bias=None, out=None, out_dtype=None, stream=None):
     _check(lib().tp_sharded_to_all(N, xp, T, Kn * N, ldx, wp, O,
                                    None if bias is None else bias.data_ptr(), _dt(x[0]),
                                    out.data_ptr(), ldy, _dt(out), _stream(stream)))
+    return out
+
+
+def tp_sharded_to_sharded(x, w, bias=None, out=None, out_dtype=None, stream=None):
+    """f1: y[c] = (sum_r x[r] @ w[r][c*O/N:(c+1)*O/N].T, ascending r) + bias[c block].
+
+    The reduce-scatter form of tp_sharded_to_all: rank c keeps only column
+    block c of the sum.  ``out`` may be views of one (T, O) buffer (column
+    offset c*O/N), which then holds the all-reduced output."""
+    torch = _torch()
+    N = len(x)
+    for i, t in enumerate(x):
+        _rowmajor(t, "x[%d]" % i)
+    for i, t in enumerate(w):
+        _contig(t, "w[%d]" % i)
+    T, Kn = x[0].shape
+    O = w[0].shape[0]
+    if out is None:
+        out = [torch.empty((T, O // N), dtype=out_dtype or torch.float32, device=x[0].device)
+               for _ in range(N)]
+    for i, t in enumerate(out):
+        _rowmajor(t, "out[%d]" % i)
+    if bias is not None:
+        _contig(bias, "bias")
+    xp, k1 = _ptrs(x)
+    wp, k2 = _ptrs(w)
+    yp, k3 = _ptrs(out)
+    _check(lib().tp_sharded_to_sharded(N, xp, T, Kn * N, _common_ld(x, "x"), wp, O,
+                                       None if bias is None else bias.data_ptr(), _dt(x[0]), yp,
+                                       _common_ld(out, "out"), _dt(out[0]), _stream(stream)))
+    return out
+
+
+def tp_gathered_to_sharded(x, w, bias=None, out=None, out_dtype=None, stream=None):
+    """f1: y[r] = cat(x, dim=1) @ w[r].T + bias[r], without materialising the
+    gathered input; x[q] is column block q of the input."""
+    torch = _torch()
+    N = len(x)
+    for i, t in enumerate(x):
+        _rowmajor(t, "x[%d]" % i)
+    for i, t in enumerate(w):
+        _contig(t, "w[%d]" % i)
+    T, Kn = x[0].shape
+    On = w[0].shape[0]
+    if out is None:
+        out = [torch.empty((T, On), dtype=out_dtype or x[0].dtype, device=x[0].device) for _ in range(N)]
+    for i, t in enumerate(out):
+        _rowmajor(t, "out[%d]" % i)
+    bp, k4 = (None, None)
+    if bias is not None:
+        for i, t in enumerate(bias):
+            _contig(t, "bias[%d]" % i)
+        bp, k4 = _ptrs(bias)
+    xp, k1 = _ptrs(x)
+    wp, k2 = _ptrs(w)
+    yp, k3 = _ptrs(out)
+    _check(lib().tp_gathered_to_sharded(N, xp, T, Kn * N, _common_ld(x, "x"), wp, On * N, bp,
+                                        _dt(x[0]), yp, _common_ld(out, "out"), _dt(out[0]),
+                                        _stream(stream)))
     return out
 
 

@@ -674,8 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
   const int tile = blockIdx.x / N;
   const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint64_t lim = a.wait_ns;
-  const UJob &J = a.jobs[0];
-  const int ta = tile % J.tilesA, tbn = tile / J.tilesA;
+  const UJob &J = a.jobs[find_job(a, tile)];
+  const int local = tile - J.unit_begin;
+  const int ta = local % J.tilesA, tbn = local / J.tilesA;
   const int rowA0 = ta * MSUB * BM, rowB0 = tbn * BN;
   const UPart P = a.parts[J.part0 + (int)rank];
 
@@ -903,7 +904,7 @@ int launch_row_cluster(UmmaArgs &args, cudaStream_t s) {
     attr_done[dev & 63] = true;
   }
   const int N = args.cluster_n;
-  const int64_t tiles = (int64_t)args.jobs[0].tilesA * args.jobs[0].tilesB;
+  const int64_t tiles = args.total_units;
   if (tiles * N > INT32_MAX) return set_error(TP_ERR_UNSUPPORTED, "too many tiles");
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
@@ -958,24 +959,33 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     // Rank clusters (one CTA per rank of a 128 x 256 tile) when one CTA per
     // 128 x 128 tile would leave SMs idle; costs in cycles, measured rates.
     const int sms0 = sm_count();
-    if (pair_policy_allowed() && p.njobs == 1) {
-      const Job &J = p.jobs[0];
-      const int N = J.nparts;
+    if (pair_policy_allowed()) {
+      // Every job (one per output block: several for a reduce-scatter) must
+      // have the same rank count and every part the same K.
+      const int N = p.jobs[0].nparts;
+      const int64_t K0 = p.parts[p.jobs[0].part0].K;
       bool same_k = true;
-      for (int q = 1; q < N; ++q) same_k = same_k && p.parts[J.part0 + q].K == p.parts[J.part0].K;
-      const double kb = (double)((p.parts[J.part0].K + BK - 1) / BK);
+      int64_t mt = 0, mt2 = 0, t128 = 0;  // 128x256, 256x256 and 128x128 tiles
+      for (int j = 0; j < p.njobs; ++j) {
+        const Job &J = p.jobs[j];
+        same_k = same_k && J.nparts == N;
+        for (int q = 0; q < J.nparts; ++q) same_k = same_k && p.parts[J.part0 + q].K == K0;
+        const int64_t m1 = (J.M + BM - 1) / BM, m2 = (J.M + 2 * BM - 1) / (2 * BM);
+        mt += m1 * ((J.N + 255) / 256);
+        mt2 += m2 * ((J.N + 255) / 256);
+        t128 += m1 * ((J.N + 127) / 128);
+      }
+      const double kb = (double)((K0 + BK - 1) / BK);
       // Measured: 4-rank clusters win on long K (MLP 2752 per rank); 8-rank
       // clusters and short K lose to the fixed per-CTA cost of this kernel.
       // msub = 2: 256 x 256 tiles (two row sub-tiles sharing B; 64 KB
       // k-blocks, about 4/3 the time of a 48 KB one, and two reduce rounds).
       // Clusters of four CTAs: 144 of the 152 SMs can hold them at once.
       if (N >= 2 && N <= 4 && kb >= 32 && (256 % N) == 0 && same_k) {
-        const int64_t mt = (J.M + BM - 1) / BM, mt2 = (J.M + 2 * BM - 1) / (2 * BM);
-        const int64_t nt = (J.N + 255) / 256;
         const int64_t resident = N == 4 ? sms0 / 152.0 * 144 : sms0;
-        const double single = (double)(((mt * ((J.N + 127) / 128)) + sms0 - 1) / sms0) * N * kb * 720.0;
-        const double clu1 = (double)((mt * nt * N + resident - 1) / resident) * (kb * 850.0 + 12000.0);
-        const double clu2 = (double)((mt2 * nt * N + resident - 1) / resident) * (kb * 1133.0 + 24000.0);
+        const double single = (double)((t128 + sms0 - 1) / sms0) * N * kb * 720.0;
+        const double clu1 = (double)((mt * N + resident - 1) / resident) * (kb * 850.0 + 12000.0);
+        const double clu2 = (double)((mt2 * N + resident - 1) / resident) * (kb * 1133.0 + 24000.0);
         if (std::min(clu1, clu2) < single) {
           rowclu = true;
           BN = 256;

@@ -237,6 +237,95 @@ int tp_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K, int64_t
   return dispatch(p, (cudaStream_t)stream);
 }
 
+int tp_sharded_to_sharded(int N, const void *const *x, int64_t T, int64_t K, int64_t ldx,
+                          const void *const *w, int64_t O, const void *bias, tp_dtype in_dt,
+                          void *const *y, int64_t ldy, tp_dtype out_dt, tp_stream_t stream) {
+  if (N < 1 || N > kMaxShards) return set_error(TP_ERR_INVALID_ARG, "N must be in 1..%d", kMaxShards);
+  if (N * N > kMaxParts)
+    return set_error(TP_ERR_UNSUPPORTED, "reduce-scatter over %d ranks: at most %d partial blocks", N,
+                     kMaxParts);
+  if (!valid_dt(in_dt) || !valid_dt(out_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
+  if (T < 0 || K < 1 || O < 1) return set_error(TP_ERR_INVALID_ARG, "need T >= 0, K >= 1, O >= 1");
+  if (K % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the input of size %lld across %d devices.",
+                     (long long)K, N);
+  if (O % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the output of size %lld across %d devices.",
+                     (long long)O, N);
+  const int64_t Kn = K / N, On = O / N;
+  if (!x || !w || !y) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (ldx < Kn) return set_error(TP_ERR_INVALID_ARG, "ldx (%lld) < K/N (%lld)", (long long)ldx, (long long)Kn);
+  if (ldy < On) return set_error(TP_ERR_INVALID_ARG, "ldy (%lld) < O/N (%lld)", (long long)ldy, (long long)On);
+  const int ie = elem_size(in_dt), oe = elem_size(out_dt);
+  if (bias && !aligned(bias, 4)) return set_error(TP_ERR_ALIGNMENT, "bias not aligned to its element size");
+  for (int r = 0; r < N; ++r) {
+    if (!x[r] || !w[r] || !y[r]) return set_error(TP_ERR_INVALID_ARG, "x[%d], w[%d] or y[%d] is NULL", r, r, r);
+    if (!aligned(x[r], ie) || !aligned(w[r], ie) || !aligned(y[r], oe))
+      return set_error(TP_ERR_ALIGNMENT, "shard %d pointer not aligned to its element size", r);
+  }
+  if (T == 0) return TP_OK;
+  // Job c is output block c; its part r is rank r's partial x[r] @ W_r[c]^T,
+  // W_r[c] being rows c*O/N.. of w[r] (a contiguous (O/N, K/N) block).
+  Problem p;
+  memset(&p, 0, sizeof(p));
+  p.njobs = N;
+  p.in_dt = in_dt;
+  p.out_dt = out_dt;
+  p.b_layout = BL_KMAJOR;
+  p.chain = 0;
+  for (int c = 0; c < N; ++c) {
+    p.jobs[c] = Job{y[c], bias ? (const float *)bias + c * On : nullptr, T, On, ldy, c * N, N};
+    for (int r = 0; r < N; ++r)
+      p.parts[c * N + r] = Part{x[r], (const char *)w[r] + (size_t)(c * On * Kn) * ie, nullptr, nullptr, Kn,
+                                ldx, Kn};
+  }
+  return dispatch(p, (cudaStream_t)stream);
+}
+
+int tp_gathered_to_sharded(int N, const void *const *x, int64_t T, int64_t K, int64_t ldx,
+                           const void *const *w, int64_t O, const void *const *bias, tp_dtype in_dt,
+                           void *const *y, int64_t ldy, tp_dtype out_dt, tp_stream_t stream) {
+  if (N < 1 || N > kMaxShards) return set_error(TP_ERR_INVALID_ARG, "N must be in 1..%d", kMaxShards);
+  if (N * N > kMaxParts)
+    return set_error(TP_ERR_UNSUPPORTED, "all-gather over %d ranks: at most %d input blocks", N, kMaxParts);
+  if (!valid_dt(in_dt) || !valid_dt(out_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
+  if (T < 0 || K < 1 || O < 1) return set_error(TP_ERR_INVALID_ARG, "need T >= 0, K >= 1, O >= 1");
+  if (K % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the input of size %lld across %d devices.",
+                     (long long)K, N);
+  if (O % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the output of size %lld across %d devices.",
+                     (long long)O, N);
+  const int64_t Kn = K / N, On = O / N;
+  if (!x || !w || !y) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (ldx < Kn) return set_error(TP_ERR_INVALID_ARG, "ldx (%lld) < K/N (%lld)", (long long)ldx, (long long)Kn);
+  if (ldy < On) return set_error(TP_ERR_INVALID_ARG, "ldy (%lld) < O/N (%lld)", (long long)ldy, (long long)On);
+  const int ie = elem_size(in_dt), oe = elem_size(out_dt);
+  for (int r = 0; r < N; ++r) {
+    if (!x[r] || !w[r] || !y[r]) return set_error(TP_ERR_INVALID_ARG, "x[%d], w[%d] or y[%d] is NULL", r, r, r);
+    if (bias && !bias[r]) return set_error(TP_ERR_INVALID_ARG, "bias[%d] is NULL", r);
+    if (!aligned(x[r], ie) || !aligned(w[r], ie) || !aligned(y[r], oe) || (bias && !aligned(bias[r], 4)))
+      return set_error(TP_ERR_ALIGNMENT, "shard %d pointer not aligned to its element size", r);
+  }
+  if (T == 0) return TP_OK;
+  // Job r is rank r's column-parallel output; its parts q = 0..N-1 chain the
+  // gathered input's column blocks x[q] against columns q*K/N.. of w[r] into
+  // one float32 accumulator, in block order (the order of the gathered K).
+  Problem p;
+  memset(&p, 0, sizeof(p));
+  p.njobs = N;
+  p.in_dt = in_dt;
+  p.out_dt = out_dt;
+  p.b_layout = BL_KMAJOR;
+  p.chain = 1;
+  for (int r = 0; r < N; ++r) {
+    p.jobs[r] = Job{y[r], bias ? (const float *)bias[r] : nullptr, T, On, ldy, r * N, N};
+    for (int q = 0; q < N; ++q)
+      p.parts[r * N + q] = Part{x[q], (const char *)w[r] + (size_t)(q * Kn) * ie, nullptr, nullptr, Kn, ldx, K};
+  }
+  return dispatch(p, (cudaStream_t)stream);
+}
+
 int tp_summa(int q, const void *const *X, const void *const *A, void *const *Y, int64_t M,
              int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream) {
   if (q < 1) return set_error(TP_ERR_NOT_DIVISIBLE, "q must be >= 1 (P = q*q processors)");

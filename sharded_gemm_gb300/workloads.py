@@ -11,8 +11,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (tp_all_to_sharded, tp_q4_all_to_sharded, tp_q4_quantize, tp_q4_sharded_to_all,
-               tp_shard_weight, tp_sharded_to_all, tp_summa)
+from . import (tp_all_to_sharded, tp_gathered_to_sharded, tp_q4_all_to_sharded, tp_q4_quantize,
+               tp_q4_sharded_to_all, tp_shard_weight, tp_sharded_to_all, tp_sharded_to_sharded, tp_summa)
 
 
 def to_device(a: np.ndarray, kind: str, device="cuda") -> torch.Tensor:
@@ -62,6 +62,40 @@ class MLPPair:
         tp_all_to_sharded(self.x if x is None else x, self.w1, self.b1, out=self.mid, stream=stream)
         tp_sharded_to_all(self.mid, self.w2, self.b2, out=self.y, stream=stream)
         return self.y
+
+
+class MLPGatherScatter:
+    """The same two weights as ``MLPPair`` with the input and the output both
+    sharded along the model width: an all-gather of the input's column
+    shards feeds the column-parallel W1, and the row-parallel W2's partial
+    sums are reduce-scattered, so rank c ends with column block c of the
+    output (one all-gather and one reduce-scatter per FFN)."""
+
+    def __init__(self, cfg: dict, device="cuda", mid_dtype=torch.bfloat16, out_dtype=torch.float32):
+        self.N = N = cfg["N"]
+        kind = cfg["dtype"]
+        x = to_device(cfg["x"], kind, device)
+        self.xs = tp_shard_weight(x, -1, 1, N)
+        del x
+        w1 = to_device(cfg["w1"], kind, device)
+        w2 = to_device(cfg["w2"], kind, device)
+        self.w1 = tp_shard_weight(w1, 0, 1, N)
+        self.b1 = tp_shard_weight(to_device(cfg["b1"], "f32", device), 0, 1, N)
+        self.w2 = tp_shard_weight(w2, -1, 1, N)
+        self.b2 = to_device(cfg["b2"], "f32", device)
+        del w1, w2
+        T = self.xs[0].shape[0]
+        if kind == "f32":
+            mid_dtype = torch.float32
+        D = cfg["w2"].shape[0]
+        self.mid = [torch.empty((T, self.w1[0].shape[0]), dtype=mid_dtype, device=device) for _ in range(N)]
+        self.ys = [torch.empty((T, D // N), dtype=out_dtype, device=device) for _ in range(N)]
+        self.flops = 2.0 * T * (cfg["w1"].shape[0] * cfg["w1"].shape[1] + cfg["w2"].shape[0] * cfg["w2"].shape[1])
+
+    def step(self, xs=None, stream=None):
+        tp_gathered_to_sharded(self.xs if xs is None else xs, self.w1, self.b1, out=self.mid, stream=stream)
+        tp_sharded_to_sharded(self.mid, self.w2, self.b2, out=self.ys, stream=stream)
+        return self.ys
 
 
 class Summa:

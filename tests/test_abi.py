@@ -68,6 +68,28 @@ def test_sharded_to_all_not_divisible(L):
     assert rc == tp.TP_ERR_NOT_DIVISIBLE
 
 
+def test_reduce_scatter_and_gather_checks(L):
+    x, k1 = _arr(4)
+    w, k2 = _arr(4)
+    y, k3 = _arr(4)
+    for fn in (L.tp_sharded_to_sharded, L.tp_gathered_to_sharded):
+        # K % N and O % N are both required
+        assert fn(4, x, 2, 10, 10, w, 8, None, tp.TP_BF16, y, 2, tp.TP_F32, None) == tp.TP_ERR_NOT_DIVISIBLE
+        assert "input of size 10 across 4" in L.tp_last_error().decode()
+        assert fn(4, x, 2, 8, 8, w, 6, None, tp.TP_BF16, y, 2, tp.TP_F32, None) == tp.TP_ERR_NOT_DIVISIBLE
+        assert "output of size 6 across 4" in L.tp_last_error().decode()
+        # ldy below O/N, ldx below K/N, null shard pointer, N*N above the part limit
+        assert fn(4, x, 2, 8, 2, w, 8, None, tp.TP_BF16, y, 1, tp.TP_F32, None) == tp.TP_ERR_INVALID_ARG
+        assert fn(4, x, 2, 8, 1, w, 8, None, tp.TP_BF16, y, 2, tp.TP_F32, None) == tp.TP_ERR_INVALID_ARG
+        yn, k4 = _arr(4)
+        k4[2] = None
+        assert fn(4, x, 2, 8, 2, w, 8, None, tp.TP_BF16, yn, 2, tp.TP_F32, None) == tp.TP_ERR_INVALID_ARG
+        x9, k5 = _arr(9)
+        assert fn(9, x9, 2, 9, 1, x9, 9, None, tp.TP_BF16, x9, 1, tp.TP_F32, None) == tp.TP_ERR_UNSUPPORTED
+        # T = 0 launches nothing and succeeds
+        assert fn(4, x, 0, 8, 2, w, 8, None, tp.TP_BF16, y, 2, tp.TP_F32, None) == tp.TP_OK
+
+
 def test_summa_checks(L):
     b, k = _arr(16)
     assert L.tp_summa(0, b, b, b, 8, 8, 8, tp.TP_BF16, None) == tp.TP_ERR_NOT_DIVISIBLE

@@ -10,7 +10,7 @@ import oracle
 import sharded_gemm_gb300 as tp
 from sharded_gemm_gb300 import build as tpbuild
 from sharded_gemm_gb300 import synth
-from sharded_gemm_gb300.workloads import MLPPair, Q4Pair, QKV, Summa, to_host
+from sharded_gemm_gb300.workloads import MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_host
 from gpu_util import bf16, check_close, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -38,6 +38,28 @@ def test_full_mlp_pair():
         check_close(mids[r], ref_mid[r], "mid shard %d" % r)
     w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
     check_close(to_host(pair.y)[rows], oracle.sharded_to_all(mids, w2, cfg["b2"]), "y")
+
+
+def test_full_mlp_gather_scatter():
+    # the MLP pair with width-sharded input and output (all-gather in,
+    # reduce-scatter out), the bench's mlp_ag_rs launches
+    cfg = synth.mlp()
+    ffn = MLPGatherScatter(cfg)
+    ffn.step()
+    assert tp.tp_query_status() == 0
+    rows = sample_rows(cfg["T"], 12)
+    N = cfg["N"]
+    xs = [bf16(p)[rows] for p in oracle.shard(cfg["x"], -1, 1, N)]
+    w1 = [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, N)]
+    b1 = [p.astype(np.float64) for p in oracle.shard(cfg["b1"], 0, 1, N)]
+    ref_mid = oracle.gathered_to_sharded(xs, w1, b1)
+    mids = [to_host(m)[rows] for m in ffn.mid]
+    for r in range(N):
+        check_close(mids[r], ref_mid[r], "mid shard %d" % r)
+    w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
+    ref_y = oracle.sharded_to_sharded(mids, w2, cfg["b2"])
+    for c in range(N):
+        check_close(to_host(ffn.ys[c])[rows], ref_y[c], "y block %d" % c)
 
 
 @pytest.mark.parametrize("q", [2, 4])

@@ -15,7 +15,8 @@ import oracle
 import sharded_gemm_gb300 as tp
 from sharded_gemm_gb300 import build as tpbuild
 from sharded_gemm_gb300 import synth
-from sharded_gemm_gb300.workloads import MLPPair, Q4Pair, QKV, Summa, to_device, to_host
+from sharded_gemm_gb300.workloads import (MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_device,
+                                          to_host)
 from gpu_util import bf16, check_close, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -188,6 +189,109 @@ def test_mlp_pair_small(policy):
     check_close(to_host(pair.y), oracle.sharded_to_all(mids, w2, cfg["b2"].astype(np.float64)), "y (layer)")
     chain = oracle.linear(oracle.linear(x, bf16(cfg["w1"]), cfg["b1"]), bf16(cfg["w2"]), cfg["b2"])
     check_close(to_host(pair.y), chain, "y (end to end)")
+
+
+# ------------------------------------------------------------------ f1 reduce-scatter / all-gather
+# (520, 2048, 512, 4): 40 tiles of 128 x 256 per rank need two rounds of
+# 4-rank clusters, so the 256-row cluster tiles are taken (ragged last row
+# tile); (300, 2752, 256, 4): one round, 128-row cluster tiles; the short-K
+# cases take the single-CTA partial kernel or (T <= 16) the swapped tiles.
+@pytest.mark.parametrize("T,Kn,On,N", [(1, 64, 128, 2), (5, 96, 40, 4), (130, 320, 75, 4),
+                                       (200, 200, 130, 3), (64, 512, 32, 8), (129, 128, 129, 1),
+                                       (300, 2752, 256, 4), (520, 2048, 512, 4)])
+def test_sharded_to_sharded(policy, T, Kn, On, N):
+    x = rand_bf16((T, Kn * N))
+    w = rand_bf16((On * N, Kn * N), 0.05)
+    b = (RNG.standard_normal(On * N) * 0.1).astype(np.float32)
+    xs = tp.tp_shard_weight(to_device(x, "bf16"), -1, 1, N)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), -1, 1, N)
+    ys = tp.tp_sharded_to_sharded(xs, ws, to_device(b, "f32"))
+    _status_ok()
+    ref = oracle.sharded_to_sharded([bf16(p) for p in oracle.shard(x, -1, 1, N)],
+                                    [bf16(p) for p in oracle.shard(w, -1, 1, N)], b.astype(np.float64))
+    for c in range(N):
+        assert tuple(ys[c].shape) == (T, On)
+        check_close(to_host(ys[c]), ref[c], "block %d" % c)
+
+
+def test_sharded_to_sharded_blocks_equal_all_reduce_bits(policy):
+    # Both options of case 3 form each partial from zero and add the partials
+    # in rank order, so rank c's block is bit for bit columns c*O/N.. of the
+    # all-reduced output.
+    T, Kn, O, N = 200, 2752, 1024, 4
+    x = rand_bf16((T, Kn * N))
+    w = rand_bf16((O, Kn * N), 0.05)
+    b = (RNG.standard_normal(O) * 0.1).astype(np.float32)
+    xs = tp.tp_shard_weight(to_device(x, "bf16"), -1, 1, N)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), -1, 1, N)
+    bd = to_device(b, "f32")
+    y = tp.tp_sharded_to_all(xs, ws, bd)
+    ys = tp.tp_sharded_to_sharded(xs, ws, bd)
+    full = torch.full((T, O), float("nan"), device="cuda")
+    views = [full[:, c * (O // N):(c + 1) * (O // N)] for c in range(N)]
+    tp.tp_sharded_to_sharded(xs, ws, bd, out=views)
+    _status_ok()
+    for c in range(N):
+        assert torch.equal(ys[c], y[:, c * (O // N):(c + 1) * (O // N)]), c
+    assert torch.equal(full, y)
+
+
+@pytest.mark.parametrize("T,Kn,On,N", [(1, 64, 128, 2), (5, 96, 40, 4), (130, 320, 600, 2),
+                                       (300, 200, 264, 3), (17, 512, 256, 8), (256, 128, 512, 1),
+                                       (70, 100, 64, 2), (260, 1024, 700, 4)])
+@pytest.mark.parametrize("out_dt", [torch.bfloat16, torch.float32])
+def test_gathered_to_sharded(policy, T, Kn, On, N, out_dt):
+    x = rand_bf16((T, Kn * N))
+    w = rand_bf16((On * N, Kn * N), 0.05)
+    b = (RNG.standard_normal(On * N) * 0.1).astype(np.float32)
+    xs = tp.tp_shard_weight(to_device(x, "bf16"), -1, 1, N)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), 0, 1, N)
+    bs = tp.tp_shard_weight(to_device(b, "f32"), 0, 1, N)
+    ys = tp.tp_gathered_to_sharded(xs, ws, bs, out_dtype=out_dt)
+    _status_ok()
+    ref = oracle.gathered_to_sharded([bf16(p) for p in oracle.shard(x, -1, 1, N)],
+                                     [bf16(p) for p in oracle.shard(w, 0, 1, N)],
+                                     [p.astype(np.float64) for p in oracle.shard(b, 0, 1, N)])
+    for r in range(N):
+        check_close(to_host(ys[r]), ref[r], "shard %d" % r)
+
+
+@pytest.mark.parametrize("T", [3, 300])
+def test_gathered_equals_column_parallel_on_gathered_bits(policy, T):
+    # With K/N a multiple of the 64-wide k-block, chaining the gathered blocks
+    # runs the same k-blocks in the same order as the column-parallel product
+    # of the materialised gathered input: the results agree bit for bit.
+    Kn, On, N = 512, 384, 4
+    x = rand_bf16((T, Kn * N))
+    w = rand_bf16((On * N, Kn * N), 0.05)
+    xd = to_device(x, "bf16")
+    xs = tp.tp_shard_weight(xd, -1, 1, N)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), 0, 1, N)
+    ys = tp.tp_gathered_to_sharded(xs, ws, None, out_dtype=torch.float32)
+    ref = tp.tp_all_to_sharded(xd, ws, None, out_dtype=torch.float32)
+    _status_ok()
+    for r in range(N):
+        assert torch.equal(ys[r], ref[r]), r
+
+
+def test_mlp_gather_scatter_small(policy):
+    cfg = synth.mlp(seed=4, T=150, D=256, F=688, N=4, bias_std=0.1)
+    ffn = MLPGatherScatter(cfg)
+    ffn.step()
+    _status_ok()
+    x = bf16(cfg["x"])
+    ref_mid = oracle.gathered_to_sharded(oracle.shard(x, -1, 1, 4),
+                                         [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, 4)],
+                                         [p.astype(np.float64) for p in oracle.shard(cfg["b1"], 0, 1, 4)])
+    mids = [to_host(m) for m in ffn.mid]
+    for r in range(4):
+        check_close(mids[r], ref_mid[r], "mid %d" % r)
+    w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, 4)]
+    ref_y = oracle.sharded_to_sharded(mids, w2, cfg["b2"].astype(np.float64))
+    for c in range(4):
+        check_close(to_host(ffn.ys[c]), ref_y[c], "y block %d (layer)" % c)
+    chain = oracle.linear(oracle.linear(x, bf16(cfg["w1"]), cfg["b1"]), bf16(cfg["w2"]), cfg["b2"])
+    check_close(np.concatenate([to_host(y) for y in ffn.ys], axis=1), chain, "y (end to end)")
 
 
 # ------------------------------------------------------------------ a5 SUMMA

@@ -209,6 +209,147 @@ def test_pair_equals_unsharded_mlp_small():
     assert np.abs(y - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
 
 
+# ------------------------------------------------------------------ collectives
+def check_all_gather_closed_form(all_gather):
+    # Joining the equal column (or row) blocks of a matrix in rank order must
+    # give the matrix back exactly.
+    x = RNG.standard_normal((6, 12))
+    for N in (1, 2, 3, 4, 6, 12):
+        w = 12 // N
+        cols = [x[:, r * w:(r + 1) * w] for r in range(N)]
+        assert np.array_equal(all_gather(cols, 1), x)
+    rows = [x[r * 2:(r + 1) * 2] for r in range(3)]
+    assert np.array_equal(all_gather(rows, 0), x)
+
+
+def check_reduce_scatter_closed_form(reduce_scatter):
+    # Partials (r + 1) * M sum to N(N+1)/2 * M; rank c must get block c.
+    # Integer entries keep every sum exact.
+    for (T, w, N) in [(2, 3, 2), (3, 2, 4), (1, 4, 8), (2, 5, 1)]:
+        M = RNG.integers(-50, 50, (T, w * N)).astype(np.float64)
+        got = reduce_scatter([(r + 1) * M for r in range(N)], 1)
+        assert len(got) == N
+        for c in range(N):
+            assert np.array_equal(got[c], N * (N + 1) // 2 * M[:, c * w:(c + 1) * w])
+
+
+def check_gather_scatter_transpose(all_gather, reduce_scatter):
+    # The notes' "AllGather and ReduceScatter are transposes of each other":
+    # for u = (u_0..u_{N-1}) and per-rank v_r,
+    #   sum_r <AG(u), v_r> == sum_c <u_c, RS(v)_c>.
+    # Integer entries make both sides exact.
+    for (T, w, N) in [(3, 2, 2), (4, 5, 4), (2, 3, 8)]:
+        u = [RNG.integers(-9, 10, (T, w)).astype(np.float64) for _ in range(N)]
+        v = [RNG.integers(-9, 10, (T, w * N)).astype(np.float64) for _ in range(N)]
+        g = all_gather(u, 1)
+        lhs = sum(float(np.sum(g * vr)) for vr in v)
+        rs = reduce_scatter(v, 1)
+        rhs = sum(float(np.sum(uc * rc)) for uc, rc in zip(u, rs))
+        assert lhs == rhs
+
+
+def check_rs_invariant(sharded_to_sharded, shard):
+    # Rank c's block of the reduce-scattered output equals columns
+    # c*O/N.. of the unsharded x @ W.T + b.
+    for (T, K, O, N) in [(5, 8, 6, 2), (3, 64, 12, 4), (9, 24, 16, 8), (2, 3, 2, 1)]:
+        x = RNG.standard_normal((T, K))
+        w = RNG.standard_normal((O, K))
+        b = RNG.standard_normal(O)
+        full = np.matmul(x, w.T) + b
+        ys = sharded_to_sharded(shard(x, -1, 1, N), shard(w, -1, 1, N), b)
+        On = O // N
+        assert len(ys) == N
+        for c in range(N):
+            ref = full[:, c * On:(c + 1) * On]
+            assert ys[c].shape == ref.shape
+            assert np.abs(ys[c] - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
+def check_rs_bias_once(sharded_to_sharded, shard):
+    # Zero input: every partial vanishes and block c must be exactly bias
+    # block c (adding it per partial would give N times the bias).
+    N = 4
+    x = np.zeros((3, 8))
+    w = RNG.standard_normal((8, 8))
+    b = RNG.standard_normal(8)
+    ys = sharded_to_sharded(shard(x, -1, 1, N), shard(w, -1, 1, N), b)
+    for c in range(N):
+        assert np.array_equal(ys[c], np.broadcast_to(b[c * 2:(c + 1) * 2], (3, 2)))
+
+
+def check_ag_invariant(gathered_to_sharded, shard):
+    # Input sharded along its contraction axis, gathered, then rank r's
+    # column-parallel product: equals columns r*O/N.. of x @ W.T + b.
+    for (T, K, O, N) in [(5, 8, 6, 2), (3, 64, 12, 4), (9, 24, 16, 8), (2, 3, 2, 1)]:
+        x = RNG.standard_normal((T, K))
+        w = RNG.standard_normal((O, K))
+        b = RNG.standard_normal(O)
+        full = np.matmul(x, w.T) + b
+        ys = gathered_to_sharded(shard(x, -1, 1, N), shard(w, 0, 1, N), shard(b, 0, 1, N))
+        On = O // N
+        for r in range(N):
+            ref = full[:, r * On:(r + 1) * On]
+            assert ys[r].shape == ref.shape
+            assert np.abs(ys[r] - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
+def test_all_gather_closed_form():
+    check_all_gather_closed_form(oracle.all_gather)
+
+
+def test_reduce_scatter_closed_form():
+    check_reduce_scatter_closed_form(oracle.reduce_scatter)
+
+
+def test_gather_scatter_transpose():
+    check_gather_scatter_transpose(oracle.all_gather, oracle.reduce_scatter)
+
+
+def test_reduce_scatter_not_divisible_raises():
+    with pytest.raises(ValueError):
+        oracle.reduce_scatter([np.zeros((2, 6))] * 4, 1)
+
+
+def test_rs_equals_unsharded():
+    check_rs_invariant(oracle.sharded_to_sharded, oracle.shard)
+
+
+def test_rs_bias_added_once_after_sum():
+    check_rs_bias_once(oracle.sharded_to_sharded, oracle.shard)
+
+
+def test_rs_blocks_join_to_all_reduce():
+    # Case 3's two options give the same numbers: the reduce-scattered blocks
+    # side by side are the all-reduced output.
+    T, K, O, N = 4, 32, 16, 4
+    x = RNG.standard_normal((T, K))
+    w = RNG.standard_normal((O, K))
+    b = RNG.standard_normal(O)
+    xs, ws = oracle.shard(x, -1, 1, N), oracle.shard(w, -1, 1, N)
+    ys = oracle.sharded_to_sharded(xs, ws, b)
+    y = oracle.sharded_to_all(xs, ws, b)
+    assert np.abs(np.concatenate(ys, axis=1) - y).max() <= 1e-12 * (1 + np.abs(y).max())
+
+
+def test_ag_equals_unsharded():
+    check_ag_invariant(oracle.gathered_to_sharded, oracle.shard)
+
+
+def test_ffn_one_gather_one_scatter():
+    # The notes' Transformer FFN with F sharded: one all-gather in, one
+    # reduce-scatter out; the output comes back sharded like the input.
+    T, D, F, N = 5, 16, 24, 4
+    x = RNG.standard_normal((T, D))
+    w_in, b_in = RNG.standard_normal((F, D)), RNG.standard_normal(F)
+    w_out, b_out = RNG.standard_normal((D, F)), RNG.standard_normal(D)
+    xs = oracle.shard(x, -1, 1, N)
+    mid = oracle.gathered_to_sharded(xs, oracle.shard(w_in, 0, 1, N), oracle.shard(b_in, 0, 1, N))
+    out = oracle.sharded_to_sharded(mid, oracle.shard(w_out, -1, 1, N), b_out)
+    ref = np.matmul(np.matmul(x, w_in.T) + b_in, w_out.T) + b_out
+    assert [o.shape for o in out] == [s.shape for s in xs]
+    assert np.abs(np.concatenate(out, axis=1) - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
 # ------------------------------------------------------------------ SUMMA
 def check_summa_q2_identity(summa):
     # Equations (1) + (2) of the SUMMA page, written out block by block.

@@ -70,3 +70,44 @@ def test_mutation_dequant_nibble_order():
         gi = np.arange(k) // g
         return s.astype(np.float64)[:, gi] * codes + b.astype(np.float64)[:, gi]
     _expect_fail(T.check_dequant_bruteforce, bad_dequant)
+
+
+def test_mutation_reduce_scatter_wrong_block():
+    def bad_rs(parts, axis):
+        got = oracle.reduce_scatter(parts, axis)
+        return got[1:] + got[:1]
+    _expect_fail(T.check_reduce_scatter_closed_form, bad_rs)
+
+
+def test_mutation_reduce_scatter_transposed_pairing():
+    # pairs rank c with the mirrored block N-1-c: a consistent AllGather
+    # in rank order no longer transposes it
+    def bad_rs(parts, axis):
+        return oracle.reduce_scatter(parts, axis)[::-1]
+    _expect_fail(T.check_gather_scatter_transpose, oracle.all_gather, bad_rs)
+
+
+def test_mutation_all_gather_reversed():
+    _expect_fail(T.check_all_gather_closed_form, lambda s, axis: oracle.all_gather(s[::-1], axis))
+
+
+def test_mutation_rs_bias_per_partial():
+    def bad_rs(xs, ws, b=None):
+        parts = [oracle.linear(x, w, b) for x, w in zip(xs, ws)]
+        return oracle.reduce_scatter(parts, 1)
+    _expect_fail(T.check_rs_bias_once, bad_rs, oracle.shard)
+
+
+def test_mutation_rs_scatter_rows():
+    # scattering the token axis instead of the output columns
+    def bad_rs(xs, ws, b=None):
+        parts = [oracle.linear(x, w, b) for x, w in zip(xs, ws)]
+        tot = sum(parts)
+        return np.array_split(tot, len(xs), axis=0)
+    _expect_fail(T.check_rs_invariant, bad_rs, oracle.shard)
+
+
+def test_mutation_ag_reversed_blocks():
+    def bad_ag(xs, ws, bs=None):
+        return oracle.all_to_sharded(np.concatenate(xs[::-1], axis=1), ws, bs)
+    _expect_fail(T.check_ag_invariant, bad_ag, oracle.shard)
