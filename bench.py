@@ -8,8 +8,10 @@ logical shards, x (512, 4096) bf16, W1 (11008, 4096), W2 (4096, 11008); one
 step = the column-parallel GEMM (x @ W1_r^T for r = 0..3, bf16 intermediate
 kept sharded) followed by the row-parallel GEMM (sum of the 4 partials in rank
 order, + bias, float32 output), both through the C ABI.  Other configs
-(mlp_ag_rs, summa2, summa4, qkv1, qkv16, qkv2048, q4_1, q4_16, q4_256) time the other
-workloads the same way; mlp_ag_rs is the MLP pair with its input and output
+(mlp_ag_rs, ffn_gated, summa2, summa4, qkv1, qkv16, qkv2048, q4_1, q4_16, q4_256)
+time the other workloads the same way; ffn_gated is the Llama FFN (gate and up
+projections in one gated column-parallel launch, then the row-parallel down
+projection); mlp_ag_rs is the MLP pair with its input and output
 sharded along the model width (an all-gather of the input's column shards
 into W1, a reduce-scatter of W2's partial sums).
 
@@ -181,7 +183,7 @@ class ClockSampler:
 def make_workload(name: str, rank: int, device: str):
     """Returns (obj, step_fn, info) for a config name."""
     from sharded_gemm_gb300 import synth
-    from sharded_gemm_gb300.workloads import MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa
+    from sharded_gemm_gb300.workloads import GatedFFN, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa
     seed = synth.SEED + rank
     if name == "mlp":
         cfg = synth.mlp(seed=seed)
@@ -191,6 +193,17 @@ def make_workload(name: str, rank: int, device: str):
                     work=w.flops, bound="tensor", kernel_names=["tp_all_to_sharded", "tp_sharded_to_all"],
                     kernel_work=[2.0 * T * D * F, 2.0 * T * D * F],
                     launches_per_step=2, h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
+        return w, w.step, info
+    if name == "ffn_gated":
+        cfg = synth.ffn(seed=seed)
+        w = GatedFFN(cfg, device=device)
+        T, D, F = cfg["T"], cfg["D"], cfg["F"]
+        info = dict(workload="llama_gated_ffn", T=T, D=D, F=F, N=cfg["N"], unit="TFLOP/s",
+                    work=w.flops, bound="tensor",
+                    kernel_names=["tp_gated_all_to_sharded", "tp_sharded_to_all"],
+                    kernel_work=[4.0 * T * D * F, 2.0 * T * D * F],
+                    launches_per_step=2, h2d=("x", w.x), d2h=("y", w.y),
+                    cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     if name == "mlp_ag_rs":
         cfg = synth.mlp(seed=seed)
@@ -247,6 +260,9 @@ def split_step(name: str, w):
     if name == "mlp":
         return [lambda s: tp.tp_all_to_sharded(w.x, w.w1, w.b1, out=w.mid, stream=s),
                 lambda s: tp.tp_sharded_to_all(w.mid, w.w2, w.b2, out=w.y, stream=s)]
+    if name == "ffn_gated":
+        return [lambda s: tp.tp_gated_all_to_sharded(w.x, w.w1, w.w3, w.b1, w.b3, out=w.h, stream=s),
+                lambda s: tp.tp_sharded_to_all(w.h, w.w2, w.b2, out=w.y, stream=s)]
     if name == "mlp_ag_rs":
         return [lambda s: tp.tp_gathered_to_sharded(w.xs, w.w1, w.b1, out=w.mid, stream=s),
                 lambda s: tp.tp_sharded_to_sharded(w.mid, w.w2, w.b2, out=w.ys, stream=s)]

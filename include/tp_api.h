@@ -149,6 +149,35 @@ int tp_all_to_sharded(int N, const void *x, int64_t T, int64_t K, int64_t ldx,
                       tp_stream_t stream);
 
 /*
+ * f2 -- gated FFN input projections, both column-parallel on the same input
+ * (MLX tensor parallelism guide, section 5.2: the FFN's gate projection w1
+ * and up projection w3 become all-to-sharded, w2 sharded-to-all; section
+ * 5.3: the elementwise product between them keeps the sharding, so it runs
+ * on each rank's shard with no communication).  The activation of the gate
+ * is SiLU, silu(a) = a / (1 + exp(-a)), as in the Llama FFN the guide shards.
+ *
+ * For r = 0..N-1:
+ *   h[r] = silu(x @ w1[r]^T + b1[r]) * (x @ w3[r]^T + b3[r])   (elementwise)
+ *   x       (T, K) in_dt, row stride ldx (>= K), replicated input;
+ *   w1[r], w3[r]  (F/N, K) in_dt contiguous: shard r of the (F, K) gate and
+ *           up weights (axis 0);
+ *   b1, b3  NULL, or host arrays of N device pointers to float32 (F/N);
+ *   h[r]    (T, F/N) out_dt, row stride ldh (>= F/N): the input of the
+ *           row-parallel w2 (tp_sharded_to_all with x[r] = h[r]).
+ * Both projections accumulate in float32; the gate, the SiLU and the product
+ * are formed in float32 from the two sums and rounded once to out_dt.  The
+ * SiLU uses the fast exponential (relative error a few units in the last
+ * float32 place for |a| below 80).
+ * Errors: TP_ERR_NOT_DIVISIBLE if F % N != 0 ("Cannot shard the output of
+ * size F across N devices."); otherwise as tp_all_to_sharded, with ldh
+ * checked against F/N.  T = 0 is valid and launches nothing.
+ */
+int tp_gated_all_to_sharded(int N, const void *x, int64_t T, int64_t K, int64_t ldx,
+                            const void *const *w1, const void *const *w3, int64_t F,
+                            const void *const *b1, const void *const *b3, tp_dtype in_dt,
+                            void *const *h, int64_t ldh, tp_dtype out_dt, tp_stream_t stream);
+
+/*
  * a3 -- row-parallel linear, "sharded-to-all" (MLX page, section 2.2
  * ShardedToAllLinear: local matmul, then all_sum over the group, then the
  * bias; the pages' Linear1D_Row; "sharded matrices" notes, case 3).

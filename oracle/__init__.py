@@ -17,6 +17,9 @@ Everything here is the plain definition, computed in float64:
 * the column-parallel layer (section 2.1) is the local linear of each shard
   with no communication; the row-parallel layer (section 2.2) sums the local
   partial products over all shards and adds the bias once, after the sum;
+* the gated FFN follows the same page, sections 5.2-5.3: gate (w1) and up
+  (w3) projections are both column-parallel, and the elementwise
+  ``silu(gate) * up`` runs on each rank's shard;
 * the reduce-scatter and all-gather variants follow "sharded matrices"
   notes, cases 2 and 3 and the collective-primitive table: the reduce-scatter
   adds the ranks' partial products in rank order and gives rank c column
@@ -34,8 +37,9 @@ The matrix products run in the naive C loops of ``oracle.c`` (pinned against
 
 Pins (see ``tests/test_oracle.py``): closed-form shard index rule, brute-force
 slicing, the sharded == unsharded invariant, the SUMMA q=2 block identity and
-the blockwise-identity special case, the all-gather / reduce-scatter
-transpose identity, the sharded == unsharded invariant of both collective
+the blockwise-identity special case, SiLU closed forms, the gated
+sharded == unsharded invariant, the all-gather / reduce-scatter transpose
+identity, the sharded == unsharded invariant of both collective
 variants, the dequant identity on brute-force and constant-code inputs, the
 quantizer round-trip bound, and the worked-example shapes from the MLX page.
 """
@@ -200,6 +204,28 @@ def sharded_to_all(x_shards, w_shards, b=None):
     if b is not None:
         total = total + np.asarray(b, dtype=np.float64)[None, :]
     return total
+
+
+# ---------------------------------------------------------------- gated FFN
+def silu(a):
+    """SiLU, a * sigmoid(a) = a / (1 + exp(-a)), in float64 (the gate of the
+    Llama FFN the MLX guide shards, sections 5.2-5.4).  For a below about -709
+    exp(-a) overflows to infinity and the quotient is -0, the limit."""
+    a = np.asarray(a, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
+
+
+def gated_all_to_sharded(x, w1_shards, w3_shards, b1_shards=None, b3_shards=None):
+    """Gate (w1) and up (w3) projections, both column-parallel on the same
+    input (MLX guide, section 5.2), combined elementwise on each rank's shard
+    (section 5.3): h_r = silu(x @ W1_r.T + b1_r) * (x @ W3_r.T + b3_r)."""
+    out = []
+    for r, (w1, w3) in enumerate(zip(w1_shards, w3_shards)):
+        g = linear(x, w1, None if b1_shards is None else b1_shards[r])
+        u = linear(x, w3, None if b3_shards is None else b3_shards[r])
+        out.append(silu(g) * u)
+    return out
 
 
 # ---------------------------------------------------------------- collectives

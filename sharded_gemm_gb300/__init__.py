@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
             "tp_shard_weight": ([vp, i64, i64, i32, i32, i32, i32, vpp, vp], i32),
             "tp_all_to_sharded": ([i32, vp, i64, i64, i64, vpp, i64, vpp, i32, vpp, i64, i32, vp], i32),
             "tp_sharded_to_all": ([i32, vpp, i64, i64, i64, vpp, i64, vp, i32, vp, i64, i32, vp], i32),
+            "tp_gated_all_to_sharded": ([i32, vp, i64, i64, i64, vpp, vpp, i64, vpp, vpp, i32, vpp, i64, i32, vp],
+                                        i32),
             "tp_sharded_to_sharded": ([i32, vpp, i64, i64, i64, vpp, i64, vp, i32, vpp, i64, i32, vp], i32),
             "tp_gathered_to_sharded": ([i32, vpp, i64, i64, i64, vpp, i64, vpp, i32, vpp, i64, i32, vp], i32),
             "tp_summa": ([i32, vpp, vpp, vpp, i64, i64, i64, i32, vp], i32),
@@ -248,6 +250,40 @@ def tp_all_to_sharded(x, w, bias=None, out=None, out_dtype=None, stream=None):
     ldx = x.stride(0) if T > 1 else K
     _check(lib().tp_all_to_sharded(N, x.data_ptr(), T, K, ldx, wp, On * N, bp, _dt(x), yp,
                                    _common_ld(out, "out"), _dt(out[0]), _stream(stream)))
+    return out
+
+
+def tp_gated_all_to_sharded(x, w1, w3, b1=None, b3=None, out=None, out_dtype=None, stream=None):
+    """f2: h[r] = silu(x @ w1[r].T + b1[r]) * (x @ w3[r].T + b3[r]); returns h list."""
+    torch = _torch()
+    _rowmajor(x, "x")
+    N = len(w1)
+    if len(w3) != N:
+        raise ValueError("w1 and w3 need the same number of shards")
+    T, K = x.shape
+    Fn = w1[0].shape[0]
+    for i, t in enumerate(list(w1) + list(w3)):
+        _contig(t, "weight shard %d" % i)
+    if out is None:
+        out = [torch.empty((T, Fn), dtype=out_dtype or x.dtype, device=x.device) for _ in range(N)]
+    for i, t in enumerate(out):
+        _rowmajor(t, "out[%d]" % i)
+    keep = []
+
+    def ptrs_or_none(ts, name):
+        if ts is None:
+            return None
+        for i, t in enumerate(ts):
+            _contig(t, "%s[%d]" % (name, i))
+        p, k = _ptrs(ts)
+        keep.append(k)
+        return p
+    w1p, w3p = ptrs_or_none(w1, "w1"), ptrs_or_none(w3, "w3")
+    b1p, b3p = ptrs_or_none(b1, "b1"), ptrs_or_none(b3, "b3")
+    yp, k_out = _ptrs(out)
+    ldx = x.stride(0) if T > 1 else K
+    _check(lib().tp_gated_all_to_sharded(N, x.data_ptr(), T, K, ldx, w1p, w3p, Fn * N, b1p, b3p, _dt(x),
+                                         yp, _common_ld(out, "out"), _dt(out[0]), _stream(stream)))
     return out
 
 

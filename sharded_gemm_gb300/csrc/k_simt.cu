@@ -5,7 +5,8 @@
 // 64 x 64 output tile per block, 256 threads, 4 x 4 outputs per thread,
 // float32 accumulation with k ascending inside each part; parts either
 // continue one accumulator (chain) or are separate partials added in part
-// order (row-parallel sum over ranks).
+// order (row-parallel sum over ranks).  Gated problems carry a second
+// accumulator for the up projection and store silu(gate) * up.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -43,19 +44,20 @@ __device__ __forceinline__ void store_out(void *C, int64_t i, float v, int dt) {
     static_cast<__half *>(C)[i] = __float2half_rn(v);
 }
 
-template <int DT, int BL>
+template <int DT, int BL, bool GATED>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ Problem P) {
   const Job &J = P.jobs[blockIdx.z];
   const int64_t m0 = (int64_t)blockIdx.y * 64, n0 = (int64_t)blockIdx.x * 64;
   if (m0 >= J.M || n0 >= J.N) return;
   __shared__ float As[16][68];
   __shared__ float Bs[16][68];
+  __shared__ float Bs2[GATED ? 16 : 1][68];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4], tot[4][4];
+  float acc[4][4], tot[4][4], acc2[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = 0.f;
+    for (int j = 0; j < 4; ++j) acc[i][j] = tot[i][j] = acc2[i][j] = 0.f;
 
   for (int pi = 0; pi < J.nparts; ++pi) {
     const Part &pt = P.parts[J.part0 + pi];
@@ -72,6 +74,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
         As[kk][mm] = (gm < J.M && gk < pt.K) ? load_elem<DT>(pt.A, gm * pt.lda + gk) : 0.f;
         const int64_t gn = n0 + mm;
         Bs[kk][mm] = (gn < J.N && gk < pt.K) ? load_b<DT, BL>(pt, gn, gk) : 0.f;
+        if constexpr (GATED)
+          Bs2[kk][mm] = (gn < J.N && gk < pt.K) ? load_elem<DT>(pt.B2, gn * pt.ldb + gk) : 0.f;
       }
       __syncthreads();
 #pragma unroll
@@ -85,6 +89,14 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        if constexpr (GATED) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) b[j] = Bs2[kk][tx * 4 + j];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc2[i][j] = fmaf(a[i], b[j], acc2[i][j]);
+        }
       }
       __syncthreads();
     }
@@ -105,6 +117,11 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
       if (gn >= J.N) continue;
       float v = P.chain ? acc[i][j] : tot[i][j];
       if (J.bias) v += J.bias[gn];
+      if constexpr (GATED) {
+        float up = acc2[i][j];
+        if (J.bias2) up += J.bias2[gn];
+        v = silu_f(v) * up;
+      }
       store_out(J.C, gm * J.ldc + gn, v, P.out_dt);
     }
   }
@@ -120,11 +137,16 @@ int launch_simt(const Problem &p, cudaStream_t s) {
   const int64_t gx = (maxN + 63) / 64, gy = (maxM + 63) / 64;
   if (gy > 65535) return set_error(TP_ERR_UNSUPPORTED, "M too large for the CUDA-core kernel");
   dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)p.njobs);
-#define TP_SIMT_CASE(DT, BL)                                  \
-  if (p.in_dt == DT && p.b_layout == BL) {                    \
-    simt_gemm_kernel<DT, BL><<<grid, 256, 0, s>>>(p);         \
-    cudaError_t e = cudaGetLastError();                       \
-    return e == cudaSuccess ? TP_OK : cuda_error(e, "simt_gemm_kernel launch"); \
+  if (p.gated && (p.b_layout != BL_KMAJOR || !p.chain))
+    return set_error(TP_ERR_UNSUPPORTED, "gated products need chained K-major weights");
+#define TP_SIMT_CASE(DT, BL)                                                      \
+  if (p.in_dt == DT && p.b_layout == BL) {                                        \
+    if (p.gated)                                                                  \
+      simt_gemm_kernel<DT, BL, BL == BL_KMAJOR><<<grid, 256, 0, s>>>(p);          \
+    else                                                                          \
+      simt_gemm_kernel<DT, BL, false><<<grid, 256, 0, s>>>(p);                    \
+    cudaError_t e = cudaGetLastError();                                           \
+    return e == cudaSuccess ? TP_OK : cuda_error(e, "simt_gemm_kernel launch");   \
   }
   TP_SIMT_CASE(TP_F32, BL_KMAJOR)
   TP_SIMT_CASE(TP_BF16, BL_KMAJOR)

@@ -49,11 +49,13 @@ struct UJob {
   int part0, nparts;
   int tilesA, tilesB;
   int unit_begin;
+  const float *bias2;  // gated: the up projection's bias (nullable)
 };
 
 struct UPart {
   int16_t amap, bmap;
   int32_t kblocks;
+  int16_t bmap2;  // gated: the up projection's weight map
 };
 
 struct UmmaArgs {
@@ -91,11 +93,11 @@ __device__ __forceinline__ uint32_t pack_f16(float x, float y) {
 }
 
 // Stores CH consecutive output values of one thread (row-major, normal mode).
-template <int CH>
+template <int CH, bool BIAS = true>
 __device__ __forceinline__ void store_row_chunk(const UmmaArgs &a, const UJob &J, int row, int col0,
                                                 float (&v)[CH]) {
   if (row >= J.rowsA) return;
-  if (J.bias) {
+  if (BIAS && J.bias) {
 #pragma unroll
     for (int i = 0; i < CH; ++i)
       if (col0 + i < J.rowsB) v[i] += __ldg(J.bias + col0 + i);
@@ -423,9 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 // rows [s*BN/2, (s+1)*BN/2) of each CTA's box, so accumulator s's columns are
 // the unit's columns s*BN/2 + [0, BN/2) (from CTA 0) and BN + s*BN/2 + [0, BN/2)
 // (from CTA 1).
-template <int BN, bool B_MN, int STAGES, int NACC, int NSUB>
+//
+// GATED (NSUB = 2): a unit is 256 x BN output columns; accumulator 0 is the
+// gate projection x W1^T and accumulator 1 the up projection x W3^T of the
+// same columns (CTA r loads BN/2 rows of each weight as two boxes), and the
+// epilogue stores silu(gate + b1) * (up + b3).
+template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false>
 __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_constant__ UmmaArgs a) {
   static_assert(NSUB == 1 || !B_MN, "two-tile units are for K-major B");
+  static_assert(!GATED || (NSUB == 2 && NACC == 1), "gated units are two accumulators of one tile");
   constexpr int BNH = BN / 2;
   constexpr int A_BYTES = BM * BK * 2;
   constexpr int B_SUB = BNH * BK * 2;  // one tile's B half, a multiple of 1024
@@ -494,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
         const int local = u - J.unit_begin;
         const int ta = local % J.tilesA, tb = local / J.tilesA;
         const int rowA0 = ta * 2 * BM + (int)rank * BM;
-        const int rowB0 = tb * NSUB * BN + (int)rank * (NSUB == 2 ? BN : BNH);
+        const int rowB0 = GATED ? tb * BN + (int)rank * BNH : tb * NSUB * BN + (int)rank * (NSUB == 2 ? BN : BNH);
         for (int p = 0; ok && p < J.nparts; ++p) {
           const UPart P = a.parts[J.part0 + p];
           for (int kb = 0; kb < P.kblocks; ++kb) {
@@ -510,6 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
 #pragma unroll
               for (int c = 0; c < BNH / 64; ++c)
                 tma_load_2d_pair(sb + c * 8192, &a.mapB[P.bmap], fb, rowB0 + c * 64, kb * BK);
+            } else if constexpr (GATED) {
+              tma_load_2d_pair(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);  // BN/2 rows of W1
+              tma_load_2d_pair(sb + B_SUB, &a.mapB[P.bmap2], fb, kb * BK, rowB0);  // and of W3
             } else {
               tma_load_2d_pair(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);  // NSUB * BN/2 rows
             }
@@ -603,8 +614,28 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
         break;
       }
       tc_fence_after();
+      if constexpr (GATED) {
+        const int colb = tb * BN + half * HALF;
+        const uint32_t g_addr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * HALF);
 #pragma unroll
-      for (int sub = 0; sub < NSUB; ++sub) {
+        for (int c = 0; c < NCH; ++c) {
+          float g[CH], v[CH];
+          tmem_load_chunk<CH>(g_addr + c * CH, g);
+          tmem_load_chunk<CH>(g_addr + BN + c * CH, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < CH; ++i) {
+            const int col = colb + c * CH + i;
+            const bool in = col < J.rowsB;
+            const float gb = (J.bias && in) ? g[i] + __ldg(J.bias + col) : g[i];
+            const float ub = (J.bias2 && in) ? v[i] + __ldg(J.bias2 + col) : v[i];
+            v[i] = silu_f(gb) * ub;
+          }
+          store_row_chunk<CH, false>(a, J, row, colb + c * CH, v);
+        }
+      }
+#pragma unroll
+      for (int sub = 0; sub < (GATED ? 0 : NSUB); ++sub) {
         const int colb = NSUB == 2 ? tb * 2 * BN + half * BN + sub * BNH : tb * BN + half * HALF;
         const uint32_t tb_addr = tmem_base + (uint32_t)((acc * NSUB + sub) * BN) + ((uint32_t)(quarter * 32) << 16) +
                                  (uint32_t)(half * HALF);
@@ -859,9 +890,9 @@ int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_gemm_kernel launch");
 }
 
-template <int BN, bool B_MN, int STAGES, int NACC, int NSUB>
+template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false>
 int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
-  auto kern = umma_pair_kernel<BN, B_MN, STAGES, NACC, NSUB>;
+  auto kern = umma_pair_kernel<BN, B_MN, STAGES, NACC, NSUB, GATED>;
   constexpr int smem = STAGES * (BM * BK * 2 + NSUB * (BN / 2) * BK * 2) + 1024;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -932,6 +963,9 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   *handled = false;
   if (p.in_dt != TP_BF16 && p.in_dt != TP_F16) return TP_OK;
   if (p.b_layout != BL_KMAJOR && p.b_layout != BL_MNMAJOR) return TP_OK;
+  // Gated products run only on the CTA-pair kernel.
+  if (p.gated && (p.b_layout != BL_KMAJOR || !p.chain || !pair_policy_allowed() || sm_count() < 2))
+    return TP_OK;
   // TMA needs 16-byte aligned bases and row strides; else the CUDA-core path.
   int64_t maxM = 0;
   for (int j = 0; j < p.njobs; ++j) {
@@ -941,10 +975,11 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     for (int q = 0; q < J.nparts; ++q) {
       const Part &P = p.parts[J.part0 + q];
       if (!al16(P.A) || !al16(P.B) || (P.lda % 8) || (P.ldb % 8)) return TP_OK;
+      if (p.gated && !al16(P.B2)) return TP_OK;
     }
   }
   const bool summa = p.b_layout == BL_MNMAJOR;
-  const bool swap = !summa && maxM <= 16;
+  const bool swap = !summa && maxM <= 16 && !p.gated;
   const bool partials = !p.chain;
   // Kernel and tile choice.  Per k-block a tile costs about
   // max(MMA cycles, 2.2 x the operand rows one CTA stages): a CTA can keep
@@ -954,6 +989,33 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   bool pair = false, rowclu = false;
   if (swap) {
     BN = 16;
+  } else if (p.gated) {
+    // Pair units of 256 x BN outputs with two accumulators (gate, up): per
+    // k-block a CTA stages 128 + BN rows for 2 x BN columns of MMA work, and
+    // the epilogue (one accumulator set) is exposed once per unit.
+    const int sms0 = sm_count();
+    int64_t kbw = 1;
+    for (int j = 0; j < p.njobs; ++j) {
+      int64_t kb = 0;
+      for (int q = 0; q < p.jobs[j].nparts; ++q) kb += (p.parts[p.jobs[j].part0 + q].K + BK - 1) / BK;
+      if (kb > kbw) kbw = kb;
+    }
+    double best = 1e300;
+    BN = 256;
+    for (int bn : {256, 192, 160}) {
+      int64_t units = 0;
+      for (int j = 0; j < p.njobs; ++j)
+        units += ((p.jobs[j].M + 2 * BM - 1) / (2 * BM)) * ((p.jobs[j].N + bn - 1) / bn);
+      const double rounds = (double)((units + sms0 / 2 - 1) / (sms0 / 2));
+      const double per_kb = std::max(4.0 * bn, 2.2 * (128.0 + bn));
+      const double cost = rounds * ((double)kbw * per_kb + 6000.0);
+      if (cost < best - 1e-9) {
+        best = cost;
+        BN = bn;
+      }
+    }
+    pair = true;
+    nsub = 2;
   } else if (partials) {
     BN = 128;
     // Rank clusters (one CTA per rank of a 128 x 256 tile) when one CTA per
@@ -1054,7 +1116,8 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     U.part0 = J.part0;
     U.nparts = J.nparts;
     U.tilesA = (U.rowsA + (pair || msub == 2 ? 2 * BM : BM) - 1) / (pair || msub == 2 ? 2 * BM : BM);
-    U.tilesB = (U.rowsB + nsub * BN - 1) / (nsub * BN);
+    U.tilesB = p.gated ? (U.rowsB + BN - 1) / BN : (U.rowsB + nsub * BN - 1) / (nsub * BN);
+    U.bias2 = J.bias2;
     U.unit_begin = (int)units;
     units += (int64_t)U.tilesA * U.tilesB;
     for (int q = 0; q < J.nparts; ++q) {
@@ -1063,11 +1126,13 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
       const void *opA = swap ? P.B : P.A;
       const void *opB = swap ? P.A : P.B;
       const int64_t ldA = swap ? P.ldb : P.lda, ldB = swap ? P.lda : P.ldb;
-      int ia = -1, ib = -1;
+      int ia = -1, ib = -1, ib2 = -1;
       for (int i = 0; i < nA; ++i)
         if (aptr[i] == opA) ia = i;
-      for (int i = 0; i < nB; ++i)
+      for (int i = 0; i < nB; ++i) {
         if (bptr[i] == opB) ib = i;
+        if (p.gated && bptr[i] == P.B2) ib2 = i;
+      }
       if (ia < 0) {
         if (nA == kMaxMaps) return TP_OK;
         // the rank clusters with 256-row tiles load A as one 256-row box
@@ -1083,12 +1148,22 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
           rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)U.rowsB, (uint64_t)P.K, (uint64_t)ldB, 64, BK);
         else
           rc = make_map(&args.mapB[nB], opB, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsB, (uint64_t)ldB, BK,
-                        (uint32_t)(pair ? nsub * BN / 2 : BN));
+                        (uint32_t)(pair ? (p.gated ? BN / 2 : nsub * BN / 2) : BN));
         if (rc) return rc;
         bptr[nB] = opB;
         ib = nB++;
+        if (p.gated && P.B2 == opB) ib2 = ib;
       }
-      args.parts[J.part0 + q] = UPart{(int16_t)ia, (int16_t)ib, (int32_t)((P.K + BK - 1) / BK)};
+      if (p.gated && ib2 < 0) {
+        if (nB == kMaxMaps) return TP_OK;
+        rc = make_map(&args.mapB[nB], P.B2, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsB, (uint64_t)ldB, BK,
+                      (uint32_t)(BN / 2));
+        if (rc) return rc;
+        bptr[nB] = P.B2;
+        ib2 = nB++;
+      }
+      args.parts[J.part0 + q] =
+          UPart{(int16_t)ia, (int16_t)ib, (int32_t)((P.K + BK - 1) / BK), (int16_t)(ib2 < 0 ? 0 : ib2)};
     }
   }
   if (units == 0) {
@@ -1116,7 +1191,13 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   args.status = p.status;
   args.wait_ns = (uint64_t)p.wait_ns;
 
-  if (rowclu && msub == 2)
+  if (p.gated && BN == 160)
+    rc = launch_pair<160, false, 6, 1, 2, true>(args, sms, s);
+  else if (p.gated && BN == 192)
+    rc = launch_pair<192, false, 5, 1, 2, true>(args, sms, s);
+  else if (p.gated)
+    rc = launch_pair<256, false, 4, 1, 2, true>(args, sms, s);
+  else if (rowclu && msub == 2)
     rc = launch_row_cluster<256, 3, 2>(args, s);
   else if (rowclu)
     rc = launch_row_cluster<256, 4, 1>(args, s);

@@ -203,6 +203,46 @@ int tp_all_to_sharded(int N, const void *x, int64_t T, int64_t K, int64_t ldx,
   return dispatch(p, (cudaStream_t)stream);
 }
 
+int tp_gated_all_to_sharded(int N, const void *x, int64_t T, int64_t K, int64_t ldx,
+                            const void *const *w1, const void *const *w3, int64_t F,
+                            const void *const *b1, const void *const *b3, tp_dtype in_dt,
+                            void *const *h, int64_t ldh, tp_dtype out_dt, tp_stream_t stream) {
+  if (N < 1 || N > kMaxShards) return set_error(TP_ERR_INVALID_ARG, "N must be in 1..%d", kMaxShards);
+  if (!valid_dt(in_dt) || !valid_dt(out_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
+  if (T < 0 || K < 1 || F < 1) return set_error(TP_ERR_INVALID_ARG, "need T >= 0, K >= 1, F >= 1");
+  if (F % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the output of size %lld across %d devices.",
+                     (long long)F, N);
+  const int64_t Fn = F / N;
+  if (!x || !w1 || !w3 || !h) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (ldx < K) return set_error(TP_ERR_INVALID_ARG, "ldx (%lld) < K (%lld)", (long long)ldx, (long long)K);
+  if (ldh < Fn) return set_error(TP_ERR_INVALID_ARG, "ldh (%lld) < F/N (%lld)", (long long)ldh, (long long)Fn);
+  const int ie = elem_size(in_dt), oe = elem_size(out_dt);
+  if (!aligned(x, ie)) return set_error(TP_ERR_ALIGNMENT, "x not aligned to its element size");
+  for (int r = 0; r < N; ++r) {
+    if (!w1[r] || !w3[r] || !h[r]) return set_error(TP_ERR_INVALID_ARG, "w1[%d], w3[%d] or h[%d] is NULL", r, r, r);
+    if ((b1 && !b1[r]) || (b3 && !b3[r])) return set_error(TP_ERR_INVALID_ARG, "b1[%d] or b3[%d] is NULL", r, r);
+    if (!aligned(w1[r], ie) || !aligned(w3[r], ie) || !aligned(h[r], oe) || (b1 && !aligned(b1[r], 4)) ||
+        (b3 && !aligned(b3[r], 4)))
+      return set_error(TP_ERR_ALIGNMENT, "shard %d pointer not aligned to its element size", r);
+  }
+  if (T == 0) return TP_OK;
+  Problem p;
+  memset(&p, 0, sizeof(p));
+  p.njobs = N;
+  p.in_dt = in_dt;
+  p.out_dt = out_dt;
+  p.b_layout = BL_KMAJOR;
+  p.chain = 1;
+  p.gated = 1;
+  for (int r = 0; r < N; ++r) {
+    p.jobs[r] = Job{h[r], b1 ? (const float *)b1[r] : nullptr, T, Fn, ldh, r, 1,
+                    b3 ? (const float *)b3[r] : nullptr};
+    p.parts[r] = Part{x, w1[r], nullptr, nullptr, K, ldx, K, w3[r]};
+  }
+  return dispatch(p, (cudaStream_t)stream);
+}
+
 int tp_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K, int64_t ldx,
                       const void *const *w, int64_t O, const void *bias, tp_dtype in_dt, void *y,
                       int64_t ldy, tp_dtype out_dt, tp_stream_t stream) {

@@ -11,6 +11,10 @@
 // order (SUMMA's q steps).  `chain` = 0: every part is a separate float32
 // partial formed from zero and the partials are added in part order (the
 // row-parallel all_sum over ranks r = 0..N-1).
+// `gated` = 1 (chain mode, BL_KMAJOR only): every part carries a second
+// weight B2 and every job a second bias, and the job's output is the gated
+// product silu(G + bias) * (U + bias2), G and U the chained sums over its
+// parts of A_p B_p^T and A_p B2_p^T (the gate / up projections of a gated FFN).
 #pragma once
 
 #include <cuda.h>
@@ -33,6 +37,7 @@ struct Part {
   const void *scales;  // BL_Q4: float16 (N, K/64)
   const void *qbias;   // BL_Q4: float16 (N, K/64)
   int64_t K, lda, ldb;
+  const void *B2;      // gated problems: the up-projection weight, same layout as B
 };
 
 struct Job {
@@ -40,6 +45,7 @@ struct Job {
   const float *bias;   // nullable, (N)
   int64_t M, N, ldc;
   int part0, nparts;
+  const float *bias2;  // gated problems: nullable up-projection bias, (N)
 };
 
 struct Problem {
@@ -49,9 +55,16 @@ struct Problem {
   int in_dt, out_dt;   // tp_dtype
   int b_layout;        // BLayout
   int chain;
+  int gated;
   int *status;         // device status word
   int64_t wait_ns;     // bound of device-side waits
 };
+
+#ifdef __CUDACC__
+// SiLU, a * sigmoid(a), of the gated FFN.  For a below about -88 the
+// exponential overflows to infinity and the quotient is -0, the limit.
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+#endif
 
 // ---- shared host state (tp_api.cu)
 int *device_status_word();  // per current device; nullptr on failure

@@ -13,7 +13,8 @@ Conventions:
   float32 draw to nearest-even.
 
 Workload shapes are the ones the pages use as stand-ins: an MLX-style
-``Linear(2, 2)`` worked example, a Llama-7B-shaped MLP (4096 -> 11008), SUMMA
+``Linear(2, 2)`` worked example, a Llama-7B-shaped MLP (4096 -> 11008) and
+gated FFN (gate / up 4096 -> 11008, down 11008 -> 4096), SUMMA
 on an 8192-square product, Llama-shaped fused-QKV / output projections with an
 OPT-sized vocabulary (50272) LM head, and a Llama-70B-shaped MLP (8192 <->
 28672) for the 4-bit quantized pair.
@@ -83,6 +84,23 @@ def mlp(seed: int = SEED, T: int = 512, D: int = 4096, F: int = 11008, N: int = 
         x=normal_bf16(gx, (T, D), 1.0),
         w1=normal_bf16(gw1, (F, D), 0.02), b1=b1,
         w2=normal_bf16(gw2, (D, F), 0.02), b2=b2,
+    )
+
+
+def ffn(seed: int = SEED, T: int = 512, D: int = 4096, F: int = 11008, N: int = 4,
+        bias_std: float = 0.0) -> dict:
+    """Gated (Llama) FFN: x (T, D) bf16 N(0,1); gate W1 (F, D), up W3 (F, D),
+    down W2 (D, F) bf16 N(0, 0.02); biases zero (or N(0, bias_std) float32)."""
+    gx, gw1, gw3, gw2, gb1, gb3, gb2 = streams(seed, 7)
+
+    def bias(g, n):
+        return normal_f32(g, (n,), bias_std) if bias_std else np.zeros((n,), np.float32)
+    return dict(
+        name="ffn", N=N, T=T, D=D, F=F, dtype="bf16",
+        x=normal_bf16(gx, (T, D), 1.0),
+        w1=normal_bf16(gw1, (F, D), 0.02), w3=normal_bf16(gw3, (F, D), 0.02),
+        w2=normal_bf16(gw2, (D, F), 0.02),
+        b1=bias(gb1, F), b3=bias(gb3, F), b2=bias(gb2, D),
     )
 
 

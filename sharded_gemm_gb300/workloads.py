@@ -11,7 +11,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (tp_all_to_sharded, tp_gathered_to_sharded, tp_q4_all_to_sharded, tp_q4_quantize,
+from . import (tp_all_to_sharded, tp_gated_all_to_sharded, tp_gathered_to_sharded, tp_q4_all_to_sharded,
+               tp_q4_quantize,
                tp_q4_sharded_to_all, tp_shard_weight, tp_sharded_to_all, tp_sharded_to_sharded, tp_summa)
 
 
@@ -61,6 +62,37 @@ class MLPPair:
     def step(self, x=None, stream=None):
         tp_all_to_sharded(self.x if x is None else x, self.w1, self.b1, out=self.mid, stream=stream)
         tp_sharded_to_all(self.mid, self.w2, self.b2, out=self.y, stream=stream)
+        return self.y
+
+
+class GatedFFN:
+    """Llama FFN: gate W1 and up W3 column-parallel on the same x (one gated
+    launch writing silu(x W1_r^T) * (x W3_r^T) per shard, bf16), then the
+    row-parallel down projection W2 (float32 output)."""
+
+    def __init__(self, cfg: dict, device="cuda", mid_dtype=torch.bfloat16, out_dtype=torch.float32):
+        self.N = N = cfg["N"]
+        kind = cfg["dtype"]
+        self.x = to_device(cfg["x"], kind, device)
+        for name, axis in (("w1", 0), ("w3", 0), ("w2", -1)):
+            full = to_device(cfg[name], kind, device)
+            setattr(self, name, tp_shard_weight(full, axis, 1, N))
+            del full
+        self.b1 = tp_shard_weight(to_device(cfg["b1"], "f32", device), 0, 1, N)
+        self.b3 = tp_shard_weight(to_device(cfg["b3"], "f32", device), 0, 1, N)
+        self.b2 = to_device(cfg["b2"], "f32", device)
+        T = self.x.shape[0]
+        if kind == "f32":
+            mid_dtype = torch.float32
+        self.h = [torch.empty((T, self.w1[0].shape[0]), dtype=mid_dtype, device=device) for _ in range(N)]
+        self.y = torch.empty((T, self.w2[0].shape[0]), dtype=out_dtype, device=device)
+        D, F = cfg["D"], cfg["F"]
+        self.flops = 2.0 * T * 3 * D * F
+
+    def step(self, x=None, stream=None):
+        tp_gated_all_to_sharded(self.x if x is None else x, self.w1, self.w3, self.b1, self.b3, out=self.h,
+                                stream=stream)
+        tp_sharded_to_all(self.h, self.w2, self.b2, out=self.y, stream=stream)
         return self.y
 
 

@@ -68,6 +68,22 @@ def test_sharded_to_all_not_divisible(L):
     assert rc == tp.TP_ERR_NOT_DIVISIBLE
 
 
+def test_gated_checks(L):
+    w, k1 = _arr(4)
+    y, k2 = _arr(4)
+    fn = L.tp_gated_all_to_sharded
+    assert fn(4, FAKE, 2, 8, 8, w, w, 10, None, None, tp.TP_BF16, y, 3, tp.TP_BF16, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert "output of size 10 across 4" in L.tp_last_error().decode()
+    # ldh below F/N, ldx below K, a null up-projection shard, a null bias entry
+    assert fn(4, FAKE, 2, 8, 8, w, w, 8, None, None, tp.TP_BF16, y, 1, tp.TP_BF16, None) == tp.TP_ERR_INVALID_ARG
+    assert fn(4, FAKE, 2, 8, 4, w, w, 8, None, None, tp.TP_BF16, y, 2, tp.TP_BF16, None) == tp.TP_ERR_INVALID_ARG
+    wn, k3 = _arr(4)
+    k3[3] = None
+    assert fn(4, FAKE, 2, 8, 8, w, wn, 8, None, None, tp.TP_BF16, y, 2, tp.TP_BF16, None) == tp.TP_ERR_INVALID_ARG
+    assert fn(4, FAKE, 2, 8, 8, w, w, 8, wn, None, tp.TP_BF16, y, 2, tp.TP_BF16, None) == tp.TP_ERR_INVALID_ARG
+    assert fn(4, FAKE, 0, 8, 8, w, w, 8, None, None, tp.TP_BF16, y, 2, tp.TP_BF16, None) == tp.TP_OK
+
+
 def test_reduce_scatter_and_gather_checks(L):
     x, k1 = _arr(4)
     w, k2 = _arr(4)

@@ -10,7 +10,7 @@ import oracle
 import sharded_gemm_gb300 as tp
 from sharded_gemm_gb300 import build as tpbuild
 from sharded_gemm_gb300 import synth
-from sharded_gemm_gb300.workloads import MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_host
+from sharded_gemm_gb300.workloads import GatedFFN, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_host
 from gpu_util import bf16, check_close, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -38,6 +38,25 @@ def test_full_mlp_pair():
         check_close(mids[r], ref_mid[r], "mid shard %d" % r)
     w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
     check_close(to_host(pair.y)[rows], oracle.sharded_to_all(mids, w2, cfg["b2"]), "y")
+
+
+def test_full_gated_ffn():
+    # Llama FFN at the bench's ffn_gated size: gated gate/up launch, then W2
+    cfg = synth.ffn()
+    ffn = GatedFFN(cfg)
+    ffn.step()
+    assert tp.tp_query_status() == 0
+    rows = sample_rows(cfg["T"], 10)
+    x = bf16(cfg["x"])[rows]
+    N = cfg["N"]
+    sh = lambda a: [bf16(p) for p in oracle.shard(cfg[a], 0, 1, N)]
+    fb = lambda a: [p.astype(np.float64) for p in oracle.shard(cfg[a], 0, 1, N)]
+    ref_h = oracle.gated_all_to_sharded(x, sh("w1"), sh("w3"), fb("b1"), fb("b3"))
+    hs = [to_host(h)[rows] for h in ffn.h]
+    for r in range(N):
+        check_close(hs[r], ref_h[r], "h shard %d" % r)
+    w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
+    check_close(to_host(ffn.y)[rows], oracle.sharded_to_all(hs, w2, cfg["b2"]), "y")
 
 
 def test_full_mlp_gather_scatter():

@@ -15,7 +15,7 @@ import oracle
 import sharded_gemm_gb300 as tp
 from sharded_gemm_gb300 import build as tpbuild
 from sharded_gemm_gb300 import synth
-from sharded_gemm_gb300.workloads import (MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_device,
+from sharded_gemm_gb300.workloads import (GatedFFN, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_device,
                                           to_host)
 from gpu_util import bf16, check_close, sample_rows
 
@@ -189,6 +189,68 @@ def test_mlp_pair_small(policy):
     check_close(to_host(pair.y), oracle.sharded_to_all(mids, w2, cfg["b2"].astype(np.float64)), "y (layer)")
     chain = oracle.linear(oracle.linear(x, bf16(cfg["w1"]), cfg["b1"]), bf16(cfg["w2"]), cfg["b2"])
     check_close(to_host(pair.y), chain, "y (end to end)")
+
+
+# ------------------------------------------------------------------ f2 gated FFN
+@pytest.mark.parametrize("T,K,Fn,N", [(1, 64, 128, 2), (5, 192, 40, 4), (130, 320, 600, 2),
+                                      (300, 200, 264, 3), (17, 512, 256, 8), (256, 128, 512, 1),
+                                      (600, 1024, 1000, 2), (70, 100, 64, 2)])
+@pytest.mark.parametrize("out_dt", [torch.bfloat16, torch.float32])
+def test_gated_all_to_sharded(policy, T, K, Fn, N, out_dt):
+    x = rand_bf16((T, K))
+    w1 = rand_bf16((Fn * N, K), 0.08)
+    w3 = rand_bf16((Fn * N, K), 0.08)
+    b1 = (RNG.standard_normal(Fn * N) * 0.5).astype(np.float32)
+    b3 = (RNG.standard_normal(Fn * N) * 0.5).astype(np.float32)
+    w1s = tp.tp_shard_weight(to_device(w1, "bf16"), 0, 1, N)
+    w3s = tp.tp_shard_weight(to_device(w3, "bf16"), 0, 1, N)
+    b1s = tp.tp_shard_weight(to_device(b1, "f32"), 0, 1, N)
+    b3s = tp.tp_shard_weight(to_device(b3, "f32"), 0, 1, N)
+    hs = tp.tp_gated_all_to_sharded(to_device(x, "bf16"), w1s, w3s, b1s, b3s, out_dtype=out_dt)
+    _status_ok()
+    sh = lambda a: [bf16(p) for p in oracle.shard(a, 0, 1, N)]
+    fb = lambda a: [p.astype(np.float64) for p in oracle.shard(a, 0, 1, N)]
+    ref = oracle.gated_all_to_sharded(bf16(x), sh(w1), sh(w3), fb(b1), fb(b3))
+    for r in range(N):
+        check_close(to_host(hs[r]), ref[r], "shard %d" % r)
+
+
+def test_gated_wide_range_and_gathered_output(policy):
+    # gate values from about -60 to 60 (SiLU saturating at both ends), no
+    # biases, output written as column views of one (T, F) buffer
+    T, K, Fn, N = 150, 256, 320, 4
+    x = rand_bf16((T, K))
+    w1 = rand_bf16((Fn * N, K), 2.0)
+    w3 = rand_bf16((Fn * N, K), 0.05)
+    w1s = tp.tp_shard_weight(to_device(w1, "bf16"), 0, 1, N)
+    w3s = tp.tp_shard_weight(to_device(w3, "bf16"), 0, 1, N)
+    full = torch.full((T, Fn * N), float("nan"), device="cuda")
+    views = [full[:, r * Fn:(r + 1) * Fn] for r in range(N)]
+    tp.tp_gated_all_to_sharded(to_device(x, "bf16"), w1s, w3s, out=views)
+    _status_ok()
+    ref = oracle.gated_all_to_sharded(bf16(x), [bf16(w1)], [bf16(w3)])[0]
+    assert np.abs(oracle.linear(bf16(x), bf16(w1))).max() > 40
+    check_close(to_host(full), ref, "gated gathered")
+
+
+def test_gated_ffn_small(policy):
+    cfg = synth.ffn(seed=6, T=150, D=256, F=688, N=4, bias_std=0.1)
+    ffn = GatedFFN(cfg)
+    ffn.step()
+    _status_ok()
+    x = bf16(cfg["x"])
+    sh = lambda a: [bf16(p) for p in oracle.shard(cfg[a], 0, 1, 4)]
+    fb = lambda a: [p.astype(np.float64) for p in oracle.shard(cfg[a], 0, 1, 4)]
+    ref_h = oracle.gated_all_to_sharded(x, sh("w1"), sh("w3"), fb("b1"), fb("b3"))
+    hs = [to_host(h) for h in ffn.h]
+    for r in range(4):
+        check_close(hs[r], ref_h[r], "h %d" % r)
+    w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, 4)]
+    check_close(to_host(ffn.y), oracle.sharded_to_all(hs, w2, cfg["b2"].astype(np.float64)), "y (layer)")
+    g = oracle.linear(x, bf16(cfg["w1"]), cfg["b1"])
+    u = oracle.linear(x, bf16(cfg["w3"]), cfg["b3"])
+    chain = oracle.linear(oracle.silu(g) * u, bf16(cfg["w2"]), cfg["b2"])
+    check_close(to_host(ffn.y), chain, "y (end to end)")
 
 
 # ------------------------------------------------------------------ f1 reduce-scatter / all-gather

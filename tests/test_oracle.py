@@ -209,6 +209,73 @@ def test_pair_equals_unsharded_mlp_small():
     assert np.abs(y - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
 
 
+# ------------------------------------------------------------------ gated FFN
+def check_silu_closed_forms(silu):
+    # sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4 in closed form.
+    l3 = math.log(3.0)
+    assert silu(np.array([0.0]))[0] == 0.0
+    assert abs(silu(np.array([l3]))[0] - 0.75 * l3) <= 1e-15
+    assert abs(silu(np.array([-l3]))[0] + 0.25 * l3) <= 1e-15
+    # silu(a) - silu(-a) = a (since sigmoid(a) + sigmoid(-a) = 1)
+    a = RNG.standard_normal(64) * 6
+    assert np.abs(silu(a) - silu(-a) - a).max() <= 1e-13
+    # against the tanh form of the logistic function, sigmoid(a) = (1 + tanh(a/2)) / 2
+    b = np.linspace(-30, 30, 121)
+    assert np.abs(silu(b) - b * 0.5 * (1 + np.tanh(b / 2))).max() <= 1e-13
+    # limits
+    assert silu(np.array([-1000.0]))[0] == 0.0
+    assert silu(np.array([1000.0]))[0] == 1000.0
+
+
+def check_gated_invariant(gated, shard):
+    # Rank r's gated output equals columns r*F/N.. of the unsharded
+    # silu(x W1^T + b1) * (x W3^T + b3), the SiLU written with tanh.
+    def silu_t(a):
+        return a * 0.5 * (1 + np.tanh(a / 2))
+    for (T, K, F, N) in [(5, 8, 12, 2), (3, 64, 24, 4), (7, 9, 16, 8), (2, 3, 2, 1)]:
+        x = RNG.standard_normal((T, K))
+        w1, w3 = RNG.standard_normal((F, K)), RNG.standard_normal((F, K))
+        b1, b3 = RNG.standard_normal(F), RNG.standard_normal(F)
+        full = silu_t(np.matmul(x, w1.T) + b1) * (np.matmul(x, w3.T) + b3)
+        hs = gated(x, shard(w1, 0, 1, N), shard(w3, 0, 1, N), shard(b1, 0, 1, N), shard(b3, 0, 1, N))
+        Fn = F // N
+        assert len(hs) == N
+        for r in range(N):
+            ref = full[:, r * Fn:(r + 1) * Fn]
+            assert hs[r].shape == ref.shape
+            assert np.abs(hs[r] - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
+def test_silu_closed_forms():
+    check_silu_closed_forms(oracle.silu)
+
+
+def test_gated_equals_unsharded():
+    check_gated_invariant(oracle.gated_all_to_sharded, oracle.shard)
+
+
+def test_gated_unit_up_gives_activation():
+    # W3 = 0 and b3 = 1: the up projection is one everywhere and the output
+    # is the activated gate alone.
+    x = RNG.standard_normal((4, 16))
+    w1 = RNG.standard_normal((8, 16))
+    hs = oracle.gated_all_to_sharded(x, oracle.shard(w1, 0, 1, 2), [np.zeros((4, 16))] * 2, None,
+                                     [np.ones(4)] * 2)
+    assert np.array_equal(np.concatenate(hs, axis=1), oracle.silu(oracle.linear(x, w1)))
+
+
+def test_gated_ffn_then_row_parallel():
+    # The guide's FFN: gate and up all-to-sharded, down (w2) sharded-to-all.
+    T, D, F, N = 5, 16, 24, 4
+    x = RNG.standard_normal((T, D))
+    w1, w3, w2 = RNG.standard_normal((F, D)), RNG.standard_normal((F, D)), RNG.standard_normal((D, F))
+    hs = oracle.gated_all_to_sharded(x, oracle.shard(w1, 0, 1, N), oracle.shard(w3, 0, 1, N))
+    y = oracle.sharded_to_all(hs, oracle.shard(w2, -1, 1, N))
+    a = np.matmul(x, w1.T)
+    ref = np.matmul(a * 0.5 * (1 + np.tanh(a / 2)) * np.matmul(x, w3.T), w2.T)
+    assert np.abs(y - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
+
+
 # ------------------------------------------------------------------ collectives
 def check_all_gather_closed_form(all_gather):
     # Joining the equal column (or row) blocks of a matrix in rank order must

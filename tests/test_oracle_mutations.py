@@ -111,3 +111,24 @@ def test_mutation_ag_reversed_blocks():
     def bad_ag(xs, ws, bs=None):
         return oracle.all_to_sharded(np.concatenate(xs[::-1], axis=1), ws, bs)
     _expect_fail(T.check_ag_invariant, bad_ag, oracle.shard)
+
+
+def test_mutation_silu_sign():
+    # a * sigmoid(-a) instead of a * sigmoid(a)
+    def bad_silu(a):
+        a = np.asarray(a, dtype=np.float64)
+        with np.errstate(over="ignore"):
+            return a / (1.0 + np.exp(a))
+    _expect_fail(T.check_silu_closed_forms, bad_silu)
+
+
+def test_mutation_gated_roles_swapped():
+    def bad(x, w1s, w3s, b1s=None, b3s=None):
+        return oracle.gated_all_to_sharded(x, w3s, w1s, b3s, b1s)
+    _expect_fail(T.check_gated_invariant, bad, oracle.shard)
+
+
+def test_mutation_gated_up_bias_dropped():
+    def bad(x, w1s, w3s, b1s=None, b3s=None):
+        return oracle.gated_all_to_sharded(x, w1s, w3s, b1s, None)
+    _expect_fail(T.check_gated_invariant, bad, oracle.shard)
