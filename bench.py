@@ -8,10 +8,11 @@ logical shards, x (512, 4096) bf16, W1 (11008, 4096), W2 (4096, 11008); one
 step = the column-parallel GEMM (x @ W1_r^T for r = 0..3, bf16 intermediate
 kept sharded) followed by the row-parallel GEMM (sum of the 4 partials in rank
 order, + bias, float32 output), both through the C ABI.  Other configs
-(mlp_ag_rs, ffn_gated, summa2, summa4, qkv1, qkv16, qkv2048, q4_1, q4_16, q4_256)
+(mlp_ag_rs, ffn_gated, mlp_bwd, summa2, summa4, qkv1, qkv16, qkv2048, q4_1, q4_16, q4_256)
 time the other workloads the same way; ffn_gated is the Llama FFN (gate and up
 projections in one gated column-parallel launch, then the row-parallel down
-projection); mlp_ag_rs is the MLP pair with its input and output
+projection); mlp_bwd is the MLP pair's backward step (input, weight and bias
+gradients of both layers); mlp_ag_rs is the MLP pair with its input and output
 sharded along the model width (an all-gather of the input's column shards
 into W1, a reduce-scatter of W2's partial sums).
 
@@ -183,7 +184,7 @@ class ClockSampler:
 def make_workload(name: str, rank: int, device: str):
     """Returns (obj, step_fn, info) for a config name."""
     from sharded_gemm_gb300 import synth
-    from sharded_gemm_gb300.workloads import GatedFFN, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa
+    from sharded_gemm_gb300.workloads import GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa
     seed = synth.SEED + rank
     if name == "mlp":
         cfg = synth.mlp(seed=seed)
@@ -193,6 +194,19 @@ def make_workload(name: str, rank: int, device: str):
                     work=w.flops, bound="tensor", kernel_names=["tp_all_to_sharded", "tp_sharded_to_all"],
                     kernel_work=[2.0 * T * D * F, 2.0 * T * D * F],
                     launches_per_step=2, h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
+        return w, w.step, info
+    if name == "mlp_bwd":
+        cfg = synth.mlp(seed=seed)
+        T, D, F = cfg["T"], cfg["D"], cfg["F"]
+        w = MLPBackward(cfg, synth.grad_output(seed=seed, T=T, D=D)["dy"], device=device)
+        g = 2.0 * T * D * F
+        info = dict(workload="mlp_col_row_pair_backward", T=T, D=D, F=F, N=cfg["N"], unit="TFLOP/s",
+                    work=w.flops, bound="tensor",
+                    kernel_names=["tp_sharded_to_all_dx", "tp_sharded_dw(w2)", "tp_bias_grad(b2)",
+                                  "tp_all_to_sharded_dx", "tp_sharded_dw(w1)", "tp_bias_grad(b1)"],
+                    kernel_work=[g, g, T * D, g, g, T * F],
+                    launches_per_step=6, h2d=("dy", w.dy), d2h=("dx", w.dx),
+                    cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     if name == "ffn_gated":
         cfg = synth.ffn(seed=seed)
@@ -260,6 +274,8 @@ def split_step(name: str, w):
     if name == "mlp":
         return [lambda s: tp.tp_all_to_sharded(w.x, w.w1, w.b1, out=w.mid, stream=s),
                 lambda s: tp.tp_sharded_to_all(w.mid, w.w2, w.b2, out=w.y, stream=s)]
+    if name == "mlp_bwd":
+        return w.launches()
     if name == "ffn_gated":
         return [lambda s: tp.tp_gated_all_to_sharded(w.x, w.w1, w.w3, w.b1, w.b3, out=w.h, stream=s),
                 lambda s: tp.tp_sharded_to_all(w.h, w.w2, w.b2, out=w.y, stream=s)]

@@ -273,6 +273,90 @@ int tp_summa(int q, const void *const *X, const void *const *A, void *const *Y, 
              int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream);
 
 /*
+ * f3 -- SUMMA with the layer's bias, and the two backward products of the 2-D
+ * layer ("ColossalAI 2D tensor parallel via SUMMA", source-level section: in
+ * backward the input gradient goes through Matmul_ABT_2D (A B^T) and the
+ * weight gradient through Matmul_ATB_2D (A^T B); Linear2D adds its bias
+ * after gathering it along the column group, add_bias_2d).
+ *
+ * All three keep tp_summa's conventions: q*q blocks indexed i*q + j, float32
+ * output blocks (M/q, Ncols/q) written, q step products chained in float32
+ * in step order t, the row / column broadcasts turned into reads of the
+ * owning block.  Errors and limits as tp_summa.
+ *
+ * tp_summa_linear: Y_ij = sum_t X_it A_tj + bias[j], bias NULL or a host
+ *   array of q device pointers to float32 (Ncols/q): column block j's bias,
+ *   the gathered piece every block of column j adds.
+ * tp_summa_abt: C = A B^T with A (M, K) and B (Ncols, K):
+ *   C_ij = sum_t A_it B_jt^T;  A blocks (M/q, K/q), B blocks (Ncols/q, K/q).
+ *   (dX = dY W^T: A = dY, B = W.)
+ * tp_summa_atb: C = A^T B with A (K, M) and B (K, Ncols):
+ *   C_ij = sum_t A_ti^T B_tj;  A blocks (K/q, M/q), B blocks (K/q, Ncols/q).
+ *   (dW = X^T dY: A = X, B = dY.)
+ */
+int tp_summa_linear(int q, const void *const *X, const void *const *A, const void *const *bias,
+                    void *const *Y, int64_t M, int64_t K, int64_t Ncols, tp_dtype in_dt,
+                    tp_stream_t stream);
+int tp_summa_abt(int q, const void *const *A, const void *const *B, void *const *C, int64_t M,
+                 int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream);
+int tp_summa_atb(int q, const void *const *A, const void *const *B, void *const *C, int64_t M,
+                 int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream);
+
+/*
+ * f3 -- backward of the 1-D sharded linears.
+ *
+ * tp_all_to_sharded_dx: the input gradient of the column-parallel layer.
+ *   Its forward wraps x in sum_gradients (MLX tensor parallelism guide,
+ *   "gradient aggregation in backward": identity forward, all_sum of the
+ *   incoming gradient in backward), so every rank's local dx_r = dy[r] @ w[r]
+ *   is all-summed:
+ *     dx = sum over r = 0..N-1, ascending, of dy[r] @ w[r]
+ *   dy[r]  (T, O/N) in_dt, row stride lddy (>= O/N): gradient of y[r];
+ *   w[r]   (O/N, K) in_dt contiguous: the forward's weight shard;
+ *   dx     (T, K) out_dt, row stride lddx (>= K).
+ *   Every partial is formed in float32 from zero and the partials are added
+ *   in ascending r, as in tp_sharded_to_all.
+ *   Errors: TP_ERR_NOT_DIVISIBLE if O % N != 0; TP_ERR_INVALID_ARG for null
+ *   pointers, T < 0, K < 1, lddy < O/N or lddx < K; T = 0 launches nothing.
+ *
+ * tp_sharded_to_all_dx: the input gradient of the row-parallel layer.  Its
+ *   incoming gradient dy is replicated (the forward ended in an all_sum), so
+ *   each rank's slice needs no communication:
+ *     dx[r] = dy @ w[r]
+ *   dy     (T, O) in_dt, row stride lddy (>= O);
+ *   w[r]   (O, K/N) in_dt contiguous; dx[r] (T, K/N) out_dt, stride lddx.
+ *   Errors: TP_ERR_NOT_DIVISIBLE if K % N != 0; otherwise as above.
+ *
+ * tp_sharded_dw: weight gradients of N shards, dw[r] = dy[r]^T @ x[r]:
+ *     dw[r][o][k] = sum over tokens t of dy[r][t][o] * x[r][t][k]
+ *   dy[r]  (T, O) in_dt, row stride lddy (>= O);
+ *   x[r]   (T, K) in_dt, row stride ldx (>= K);
+ *   dw[r]  (O, K) out_dt, row stride lddw (>= K).
+ *   Column-parallel layer: dy[r] = its output gradient shard, x[r] = x for
+ *   every r; row-parallel layer: dy[r] = dy for every r, x[r] = its input
+ *   shard.  T = 0 writes zeros (the empty sum).
+ *
+ * tp_bias_grad: bias gradients, float32 column sums in a fixed order:
+ *     db[o][c] = sum over b = 0..nin-1 of sum over rows t of dy[o*nin + b][t*ld + c]
+ *   dy     nout*nin device pointers, each (rows, cols) in_dt, row stride ld;
+ *   db[o]  float32 (cols).
+ *   Column-parallel bias: nout = N, nin = 1; row-parallel bias (added once
+ *   after the sum): nout = nin = 1; Linear2D bias of column block j: nin = q
+ *   blocks dY_0j .. dY_(q-1)j.  Requires nout <= 64, nout * nin <= 64.
+ */
+int tp_all_to_sharded_dx(int N, const void *const *dy, int64_t T, int64_t O, int64_t lddy,
+                         const void *const *w, int64_t K, tp_dtype in_dt, void *dx, int64_t lddx,
+                         tp_dtype out_dt, tp_stream_t stream);
+int tp_sharded_to_all_dx(int N, const void *dy, int64_t T, int64_t O, int64_t lddy,
+                         const void *const *w, int64_t K, tp_dtype in_dt, void *const *dx,
+                         int64_t lddx, tp_dtype out_dt, tp_stream_t stream);
+int tp_sharded_dw(int N, const void *const *dy, int64_t lddy, const void *const *x, int64_t ldx,
+                  int64_t T, int64_t O, int64_t K, tp_dtype in_dt, void *const *dw, int64_t lddw,
+                  tp_dtype out_dt, tp_stream_t stream);
+int tp_bias_grad(int nout, int nin, const void *const *dy, int64_t rows, int64_t cols, int64_t ld,
+                 tp_dtype in_dt, float *const *db, tp_stream_t stream);
+
+/*
  * a6 -- affine 4-bit quantization of a float32 weight on the device (MLX
  * page, section 2.3: group_size 64, bits 4, mode "affine").  Data
  * preparation, not part of a forward pass.

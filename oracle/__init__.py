@@ -20,6 +20,11 @@ Everything here is the plain definition, computed in float64:
 * the gated FFN follows the same page, sections 5.2-5.3: gate (w1) and up
   (w3) projections are both column-parallel, and the elementwise
   ``silu(gate) * up`` runs on each rank's shard;
+* backward: the column-parallel layer's input gradient is the all_sum of the
+  ranks' local gradients (MLX guide, sum_gradients), the row-parallel one's
+  needs none; weight gradients are dy^T x per shard; bias gradients are row
+  sums; the 2-D layer's backward products are Matmul_ABT_2D / Matmul_ATB_2D
+  of the SUMMA page and its bias is added per column block (add_bias_2d);
 * the reduce-scatter and all-gather variants follow "sharded matrices"
   notes, cases 2 and 3 and the collective-primitive table: the reduce-scatter
   adds the ranks' partial products in rank order and gives rank c column
@@ -37,7 +42,9 @@ The matrix products run in the naive C loops of ``oracle.c`` (pinned against
 
 Pins (see ``tests/test_oracle.py``): closed-form shard index rule, brute-force
 slicing, the sharded == unsharded invariant, the SUMMA q=2 block identity and
-the blockwise-identity special case, SiLU closed forms, the gated
+the blockwise-identity special case, the ABT / ATB block identities and
+numpy transposes, the adjoint identity <dy, f(x)> = <f^T(dy), x> of every
+gradient, integer bias-gradient sums, SiLU closed forms, the gated
 sharded == unsharded invariant, the all-gather / reduce-scatter transpose
 identity, the sharded == unsharded invariant of both collective
 variants, the dequant identity on brute-force and constant-code inputs, the
@@ -206,6 +213,45 @@ def sharded_to_all(x_shards, w_shards, b=None):
     return total
 
 
+# ---------------------------------------------------------------- backward
+def all_to_sharded_dx(dy_shards, w_shards):
+    """Input gradient of the column-parallel layer.  Its forward passes x
+    through sum_gradients (MLX guide, gradient aggregation in backward:
+    identity forward, all_sum of the gradient backward), so the ranks' local
+    gradients dy_r @ W_r are summed, r ascending."""
+    total = None
+    for dy, w in zip(dy_shards, w_shards):
+        p = matmul(dy, w)
+        total = p if total is None else total + p
+    return total
+
+
+def sharded_to_all_dx(dy, w_shards):
+    """Input gradient of the row-parallel layer: dy is replicated (the forward
+    ended in all_sum), so rank r's slice is dy @ W_r, no communication."""
+    return [matmul(dy, w) for w in w_shards]
+
+
+def sharded_dw(dy_list, x_list):
+    """Weight gradients: dW_r = dy_r^T @ x_r (column-parallel: x_r = x;
+    row-parallel: dy_r = dy)."""
+    return [matmul(np.ascontiguousarray(np.asarray(dy, dtype=np.float64).T), x)
+            for dy, x in zip(dy_list, x_list)]
+
+
+def bias_grad(dy_groups):
+    """Bias gradient: the bias is added to every row, so its gradient is the
+    sum over rows of the output gradient, over each group's matrices in order."""
+    out = []
+    for group in dy_groups:
+        acc = None
+        for d in group:
+            cs = np.asarray(d, dtype=np.float64).sum(axis=0)
+            acc = cs if acc is None else acc + cs
+        out.append(acc)
+    return out
+
+
 # ---------------------------------------------------------------- gated FFN
 def silu(a):
     """SiLU, a * sigmoid(a) = a / (1 + exp(-a)), in float64 (the gate of the
@@ -289,6 +335,44 @@ def summa(X_blocks, A_blocks, q: int):
                 acc = p if acc is None else acc + p
             Y.append(acc)
     return Y
+
+
+def summa_linear(X_blocks, A_blocks, b_blocks, q: int):
+    """Linear2D forward: SUMMA's Y_ij plus column block j's bias (the piece
+    add_bias_2d gathers along the column group), added after the q steps."""
+    Y = summa(X_blocks, A_blocks, q)
+    if b_blocks is None:
+        return Y
+    return [Y[i * q + j] + np.asarray(b_blocks[j], dtype=np.float64)[None, :]
+            for i in range(q) for j in range(q)]
+
+
+def summa_abt(A_blocks, B_blocks, q: int):
+    """Matmul_ABT_2D (the SUMMA page, backward): C = A B^T on the grid,
+    C_ij = sum_{t=0}^{q-1} A_it B_jt^T, t ascending."""
+    C = []
+    for i in range(q):
+        for j in range(q):
+            acc = None
+            for t in range(q):
+                p = matmul(A_blocks[i * q + t], np.ascontiguousarray(np.asarray(B_blocks[j * q + t]).T))
+                acc = p if acc is None else acc + p
+            C.append(acc)
+    return C
+
+
+def summa_atb(A_blocks, B_blocks, q: int):
+    """Matmul_ATB_2D (same page): C = A^T B on the grid,
+    C_ij = sum_{t=0}^{q-1} A_ti^T B_tj, t ascending."""
+    C = []
+    for i in range(q):
+        for j in range(q):
+            acc = None
+            for t in range(q):
+                p = matmul(np.ascontiguousarray(np.asarray(A_blocks[t * q + i]).T), B_blocks[t * q + j])
+                acc = p if acc is None else acc + p
+            C.append(acc)
+    return C
 
 
 def blocks(M: np.ndarray, q: int) -> list[np.ndarray]:

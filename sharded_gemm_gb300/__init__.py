@@ -61,6 +61,13 @@ def lib() -> ctypes.CDLL:
             "tp_sharded_to_sharded": ([i32, vpp, i64, i64, i64, vpp, i64, vp, i32, vpp, i64, i32, vp], i32),
             "tp_gathered_to_sharded": ([i32, vpp, i64, i64, i64, vpp, i64, vpp, i32, vpp, i64, i32, vp], i32),
             "tp_summa": ([i32, vpp, vpp, vpp, i64, i64, i64, i32, vp], i32),
+            "tp_summa_linear": ([i32, vpp, vpp, vpp, vpp, i64, i64, i64, i32, vp], i32),
+            "tp_summa_abt": ([i32, vpp, vpp, vpp, i64, i64, i64, i32, vp], i32),
+            "tp_summa_atb": ([i32, vpp, vpp, vpp, i64, i64, i64, i32, vp], i32),
+            "tp_all_to_sharded_dx": ([i32, vpp, i64, i64, i64, vpp, i64, i32, vp, i64, i32, vp], i32),
+            "tp_sharded_to_all_dx": ([i32, vp, i64, i64, i64, vpp, i64, i32, vpp, i64, i32, vp], i32),
+            "tp_sharded_dw": ([i32, vpp, i64, vpp, i64, i64, i64, i64, i32, vpp, i64, i32, vp], i32),
+            "tp_bias_grad": ([i32, i32, vpp, i64, i64, i64, i32, vpp, vp], i32),
             "tp_q4_quantize": ([vp, i64, i64, i32, vp, vp, vp, vp], i32),
             "tp_q4_all_to_sharded": ([i32, vp, i64, i64, vpp, vpp, vpp, i32, i64, vpp, vpp, i64, i32, vp], i32),
             "tp_q4_sharded_to_all": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
@@ -118,7 +125,7 @@ def _cuda(t, name):
 
 def _rowmajor(t, name):
     _cuda(t, name)
-    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+    if t.dim() != 2 or (t.numel() > 0 and t.shape[1] > 1 and t.stride(1) != 1):
         raise ValueError("%s must be 2-D with unit column stride" % name)
     return t
 
@@ -475,4 +482,136 @@ def tp_q4_sharded_to_all_noalloc(x, wq, scales, qbias, bias=None, out=None, grou
     _check(lib().tp_q4_sharded_to_all_noalloc(N, xp, T, Kn * N, qp, sp, bq, group_size, O,
                                               None if bias is None else bias.data_ptr(),
                                               out.data_ptr(), ldy, _dt(out), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ backward (f3)
+def _summa_blocks(Xs, name):
+    for i, t in enumerate(Xs):
+        _contig(t, "%s[%d]" % (name, i))
+    return _ptrs(Xs)
+
+
+def tp_summa_linear(q: int, X, A, bias=None, Y=None, stream=None):
+    """Y_ij = sum_t X_it A_tj + bias[j] on a q x q grid (blocks indexed i*q+j)."""
+    torch = _torch()
+    bm, bk = X[0].shape
+    bn = A[0].shape[1]
+    if Y is None:
+        Y = [torch.empty((bm, bn), dtype=torch.float32, device=X[0].device) for _ in range(q * q)]
+    xp, k1 = _summa_blocks(X, "X")
+    ap, k2 = _summa_blocks(A, "A")
+    yp, k3 = _summa_blocks(Y, "Y")
+    bp, k4 = _summa_blocks(bias, "bias") if bias is not None else (None, None)
+    _check(lib().tp_summa_linear(q, xp, ap, bp, yp, bm * q, bk * q, bn * q, _dt(X[0]), _stream(stream)))
+    return Y
+
+
+def tp_summa_abt(q: int, A, B, C=None, stream=None):
+    """C_ij = sum_t A_it B_jt^T: A blocks (M/q, K/q), B blocks (N/q, K/q)."""
+    torch = _torch()
+    bm, bk = A[0].shape
+    bn = B[0].shape[0]
+    if C is None:
+        C = [torch.empty((bm, bn), dtype=torch.float32, device=A[0].device) for _ in range(q * q)]
+    ap, k1 = _summa_blocks(A, "A")
+    bp, k2 = _summa_blocks(B, "B")
+    cp, k3 = _summa_blocks(C, "C")
+    _check(lib().tp_summa_abt(q, ap, bp, cp, bm * q, bk * q, bn * q, _dt(A[0]), _stream(stream)))
+    return C
+
+
+def tp_summa_atb(q: int, A, B, C=None, stream=None):
+    """C_ij = sum_t A_ti^T B_tj: A blocks (K/q, M/q), B blocks (K/q, N/q)."""
+    torch = _torch()
+    bk, bm = A[0].shape
+    bn = B[0].shape[1]
+    if C is None:
+        C = [torch.empty((bm, bn), dtype=torch.float32, device=A[0].device) for _ in range(q * q)]
+    ap, k1 = _summa_blocks(A, "A")
+    bp, k2 = _summa_blocks(B, "B")
+    cp, k3 = _summa_blocks(C, "C")
+    _check(lib().tp_summa_atb(q, ap, bp, cp, bm * q, bk * q, bn * q, _dt(A[0]), _stream(stream)))
+    return C
+
+
+def tp_all_to_sharded_dx(dy, w, out=None, out_dtype=None, stream=None):
+    """Input gradient of the column-parallel layer: sum_r dy[r] @ w[r] (ascending r)."""
+    torch = _torch()
+    N = len(dy)
+    for i, t in enumerate(dy):
+        _rowmajor(t, "dy[%d]" % i)
+    for i, t in enumerate(w):
+        _contig(t, "w[%d]" % i)
+    T, On = dy[0].shape
+    K = w[0].shape[1]
+    if out is None:
+        out = torch.empty((T, K), dtype=out_dtype or torch.float32, device=dy[0].device)
+    _rowmajor(out, "out")
+    dp, k1 = _ptrs(dy)
+    wp, k2 = _ptrs(w)
+    _check(lib().tp_all_to_sharded_dx(N, dp, T, On * N, _common_ld(dy, "dy"), wp, K, _dt(dy[0]),
+                                      out.data_ptr(), out.stride(0) if T > 1 else K, _dt(out), _stream(stream)))
+    return out
+
+
+def tp_sharded_to_all_dx(dy, w, out=None, out_dtype=None, stream=None):
+    """Input gradient of the row-parallel layer: dx[r] = dy @ w[r]."""
+    torch = _torch()
+    _rowmajor(dy, "dy")
+    N = len(w)
+    for i, t in enumerate(w):
+        _contig(t, "w[%d]" % i)
+    T, O = dy.shape
+    Kn = w[0].shape[1]
+    if out is None:
+        out = [torch.empty((T, Kn), dtype=out_dtype or dy.dtype, device=dy.device) for _ in range(N)]
+    for i, t in enumerate(out):
+        _rowmajor(t, "out[%d]" % i)
+    wp, k1 = _ptrs(w)
+    yp, k2 = _ptrs(out)
+    _check(lib().tp_sharded_to_all_dx(N, dy.data_ptr(), T, O, dy.stride(0) if T > 1 else O, wp, Kn * N,
+                                      _dt(dy), yp, _common_ld(out, "out"), _dt(out[0]), _stream(stream)))
+    return out
+
+
+def tp_sharded_dw(dy, x, out=None, out_dtype=None, stream=None):
+    """Weight gradients dw[r] = dy[r].T @ x[r] (lists of equal length N)."""
+    torch = _torch()
+    N = len(dy)
+    if len(x) != N:
+        raise ValueError("dy and x need the same number of shards")
+    for i, t in enumerate(list(dy) + list(x)):
+        _rowmajor(t, "operand %d" % i)
+    T, O = dy[0].shape
+    K = x[0].shape[1]
+    if out is None:
+        out = [torch.empty((O, K), dtype=out_dtype or torch.float32, device=dy[0].device) for _ in range(N)]
+    for i, t in enumerate(out):
+        _rowmajor(t, "out[%d]" % i)
+    dp, k1 = _ptrs(dy)
+    xp, k2 = _ptrs(x)
+    yp, k3 = _ptrs(out)
+    _check(lib().tp_sharded_dw(N, dp, _common_ld(dy, "dy"), xp, _common_ld(x, "x"), T, O, K, _dt(dy[0]), yp,
+                               _common_ld(out, "out"), _dt(out[0]), _stream(stream)))
+    return out
+
+
+def tp_bias_grad(dy, nin: int = 1, out=None, stream=None):
+    """Float32 column sums: out[o] = sum over dy[o*nin .. o*nin+nin-1] of their row sums."""
+    torch = _torch()
+    n = len(dy)
+    if n % nin:
+        raise ValueError("len(dy) must be a multiple of nin")
+    nout = n // nin
+    for i, t in enumerate(dy):
+        _rowmajor(t, "dy[%d]" % i)
+    rows, cols = dy[0].shape
+    if out is None:
+        out = [torch.empty((cols,), dtype=torch.float32, device=dy[0].device) for _ in range(nout)]
+    for i, t in enumerate(out):
+        _contig(t, "out[%d]" % i)
+    dp, k1 = _ptrs(dy)
+    op, k2 = _ptrs(out)
+    _check(lib().tp_bias_grad(nout, nin, dp, rows, cols, _common_ld(dy, "dy"), _dt(dy[0]), op, _stream(stream)))
     return out

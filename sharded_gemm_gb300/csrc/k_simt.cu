@@ -71,7 +71,9 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
       for (int e = threadIdx.x; e < 1024; e += 256) {
         const int mm = e >> 4, kk = e & 15;
         const int64_t gm = m0 + mm, gk = k0 + kk;
-        As[kk][mm] = (gm < J.M && gk < pt.K) ? load_elem<DT>(pt.A, gm * pt.lda + gk) : 0.f;
+        As[kk][mm] = (gm < J.M && gk < pt.K)
+                         ? load_elem<DT>(pt.A, P.a_mn ? gk * pt.lda + gm : gm * pt.lda + gk)
+                         : 0.f;
         const int64_t gn = n0 + mm;
         Bs[kk][mm] = (gn < J.N && gk < pt.K) ? load_b<DT, BL>(pt, gn, gk) : 0.f;
         if constexpr (GATED)

@@ -36,6 +36,7 @@
 namespace tp {
 
 constexpr int kMaxMaps = 64;
+constexpr int kMaxCMaps = 16;  // output maps of the TMA-store epilogue
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kEpiWarps = 8;
@@ -61,6 +62,7 @@ struct UPart {
 struct UmmaArgs {
   CUtensorMap mapA[kMaxMaps];
   CUtensorMap mapB[kMaxMaps];
+  CUtensorMap mapC[kMaxCMaps];  // float32 outputs, 32 x 32 boxes, 128-byte swizzle
   UJob jobs[kMaxJobs];
   UPart parts[kMaxParts];
   int njobs, total_units, nmapA, nmapB;
@@ -138,6 +140,44 @@ __device__ __forceinline__ void store_row_chunk(const UmmaArgs &a, const UJob &J
   }
 }
 
+// TMA-store epilogue: a warp's 32 x 32 float32 chunk (lane l holds row
+// row0 + l) goes to one of the warp's two 4 KB staging buffers in the 128-byte
+// swizzled layout of the output map (row r's 16-byte piece j at position
+// j ^ (r % 8): each group of 8 lanes covers all 32 banks), and lane 0 issues
+// the tile store.
+constexpr int kTsWarpBytes = 2 * 4096;
+__device__ __forceinline__ void tstore_chunk(const UmmaArgs &a, const UJob &J, int job, int row0, int col0,
+                                             float (&v)[32], uint32_t bufs, int &cnt, int lane) {
+  // A chunk wholly outside the output (ragged last tile) is skipped outright:
+  // it neither stores nor takes a staging buffer, so a buffer is only ever
+  // rewritten after the store issued from it two stores earlier has read it.
+  if (row0 >= J.rowsA || col0 >= J.rowsB) return;
+  if (J.bias) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < J.rowsB) v[i] += __ldg(J.bias + col0 + i);
+  }
+  if (cnt >= 2) {
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+  }
+  const uint32_t buf = bufs + (uint32_t)((cnt & 1) * 4096);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t dst = buf + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) * 16));
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "f"(v[4 * j]), "f"(v[4 * j + 1]),
+                 "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                 : "memory");
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {  // the map clips a partly outside chunk
+    tma_store_2d(&a.mapC[job], buf, col0, row0);
+    bulk_commit_group();
+  }
+  ++cnt;
+}
+
 // Swap-AB store: the thread's A row is output column `row`; its values are
 // tokens col0.. of that column.
 template <int CH>
@@ -183,8 +223,9 @@ struct TmemCols {
   static constexpr int v = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : N <= 256 ? 256 : 512;
 };
 
-template <int BN, bool B_MN, bool SWAP, bool PARTIALS, int STAGES, int NACC>
+template <int BN, bool B_MN, bool SWAP, bool PARTIALS, int STAGES, int NACC, bool A_MN = false>
 __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_constant__ UmmaArgs a) {
+  static_assert(!A_MN || !SWAP, "M-major A is not swapped");
   constexpr int A_BYTES = BM * BK * 2;
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -257,7 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
             const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
             const uint32_t fb = smem_u32(&full_bar[stage]);
             mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            tma_load_2d(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
+            if constexpr (A_MN) {  // two boxes of 64 rows of M (128 bytes) x BK
+              tma_load_2d(sa, &a.mapA[P.amap], fb, rowA0, kb * BK);
+              tma_load_2d(sa + 8192, &a.mapA[P.amap], fb, rowA0 + 64, kb * BK);
+            } else {
+              tma_load_2d(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
+            }
             if constexpr (B_MN) {
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c)
@@ -307,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
             const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = umma_desc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t ad = A_MN ? umma_desc_sw128(sa + kk * 2048, 8192, 1024)
+                                       : umma_desc_sw128(sa + kk * 32, 16, 1024);
               const uint64_t bd = B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
                                        : umma_desc_sw128(sb + kk * 32, 16, 1024);
               const uint32_t accum = (kb > 0 || kk > 0 || (a.chain && p > 0)) ? 1u : 0u;
@@ -430,8 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 // gate projection x W1^T and accumulator 1 the up projection x W3^T of the
 // same columns (CTA r loads BN/2 rows of each weight as two boxes), and the
 // epilogue stores silu(gate + b1) * (up + b3).
-template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false>
+template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false, bool A_MN = false,
+          bool TSTORE = false>
 __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_constant__ UmmaArgs a) {
+  static_assert(!A_MN || NSUB == 1, "M-major A with one-tile units");
+  static_assert(!TSTORE || (!GATED && ChunkOf<BN / 2>::v == 32), "TMA stores of 32-column float32 chunks");
   static_assert(NSUB == 1 || !B_MN, "two-tile units are for K-major B");
   static_assert(!GATED || (NSUB == 2 && NACC == 1), "gated units are two accumulators of one tile");
   constexpr int BNH = BN / 2;
@@ -513,7 +563,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
             const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
             const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
             if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2 * STAGE_BYTES);
-            tma_load_2d_pair(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
+            if constexpr (A_MN) {  // two boxes of 64 rows of M (128 bytes) x BK
+              tma_load_2d_pair(sa, &a.mapA[P.amap], fb, rowA0, kb * BK);
+              tma_load_2d_pair(sa + 8192, &a.mapA[P.amap], fb, rowA0 + 64, kb * BK);
+            } else {
+              tma_load_2d_pair(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
+            }
             if constexpr (B_MN) {
 #pragma unroll
               for (int c = 0; c < BNH / 64; ++c)
@@ -567,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
             const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = umma_desc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t ad = A_MN ? umma_desc_sw128(sa + kk * 2048, 8192, 1024)
+                                       : umma_desc_sw128(sa + kk * 32, 16, 1024);
 #pragma unroll
               for (int sub = 0; sub < NSUB; ++sub) {
                 const uint64_t bd = B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
@@ -600,7 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int half = ew >> 2;
-    int acc = 0;
+    const uint32_t ts_bufs = sbase + (uint32_t)(STAGES * STAGE_BYTES + ew * kTsWarpBytes);
+    int ts_cnt = 0;
+    int acc = 0, eseq = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int u = pair; ok && u < a.total_units; u += npairs) {
@@ -613,6 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
         ok = false;
         break;
       }
+      if (ew == 0 && lane == 0) umma_trace(a, 4, eseq);
       tc_fence_after();
       if constexpr (GATED) {
         const int colb = tb * BN + half * HALF;
@@ -644,9 +703,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
           float v[CH];
           tmem_load_chunk<CH>(tb_addr + c * CH, v);
           tmem_wait_ld();
-          store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+          if constexpr (TSTORE)
+            tstore_chunk(a, J, find_job(a, u), row - lane, colb + c * CH, v, ts_bufs, ts_cnt, lane);
+          else
+            store_row_chunk<CH>(a, J, row, colb + c * CH, v);
         }
       }
+      if (ew == 0 && lane == 0) umma_trace(a, 5, eseq);
+      ++eseq;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
@@ -654,6 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
         acc = 0;
         acc_phase ^= 1;
       }
+    }
+    if constexpr (TSTORE) {
+      if (lane == 0) bulk_wait_group_all();  // the tile stores have finished
+      __syncwarp();
     }
   }
 
@@ -872,9 +940,9 @@ int make_map(CUtensorMap *out, const void *ptr, int dt, uint64_t inner, uint64_t
                       2, inner, outer, ld, box0, box1, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int BN, bool B_MN, bool SWAP, bool PARTIALS, int STAGES, int NACC>
+template <int BN, bool B_MN, bool SWAP, bool PARTIALS, int STAGES, int NACC, bool A_MN = false>
 int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
-  auto kern = umma_gemm_kernel<BN, B_MN, SWAP, PARTIALS, STAGES, NACC>;
+  auto kern = umma_gemm_kernel<BN, B_MN, SWAP, PARTIALS, STAGES, NACC, A_MN>;
   constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -890,10 +958,12 @@ int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_gemm_kernel launch");
 }
 
-template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false>
+template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false, bool A_MN = false,
+          bool TSTORE = false>
 int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
-  auto kern = umma_pair_kernel<BN, B_MN, STAGES, NACC, NSUB, GATED>;
-  constexpr int smem = STAGES * (BM * BK * 2 + NSUB * (BN / 2) * BK * 2) + 1024;
+  auto kern = umma_pair_kernel<BN, B_MN, STAGES, NACC, NSUB, GATED, A_MN, TSTORE>;
+  constexpr int smem = STAGES * (BM * BK * 2 + NSUB * (BN / 2) * BK * 2) + 1024 +
+                       (TSTORE ? kEpiWarps * kTsWarpBytes : 0);
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -963,6 +1033,8 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   *handled = false;
   if (p.in_dt != TP_BF16 && p.in_dt != TP_F16) return TP_OK;
   if (p.b_layout != BL_KMAJOR && p.b_layout != BL_MNMAJOR) return TP_OK;
+  // M-major A only with M-major B (weight gradients, SUMMA's A^T B), chained.
+  if (p.a_mn && (p.b_layout != BL_MNMAJOR || !p.chain)) return TP_OK;
   // Gated products run only on the CTA-pair kernel.
   if (p.gated && (p.b_layout != BL_KMAJOR || !p.chain || !pair_policy_allowed() || sm_count() < 2))
     return TP_OK;
@@ -1021,7 +1093,7 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     // Rank clusters (one CTA per rank of a 128 x 256 tile) when one CTA per
     // 128 x 128 tile would leave SMs idle; costs in cycles, measured rates.
     const int sms0 = sm_count();
-    if (pair_policy_allowed()) {
+    if (pair_policy_allowed() && !summa) {
       // Every job (one per output block: several for a reduce-scatter) must
       // have the same rank count and every part the same K.
       const int N = p.jobs[0].nparts;
@@ -1136,8 +1208,11 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
       if (ia < 0) {
         if (nA == kMaxMaps) return TP_OK;
         // the rank clusters with 256-row tiles load A as one 256-row box
-        rc = make_map(&args.mapA[nA], opA, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsA, (uint64_t)ldA, BK,
-                      rowclu ? msub * BM : BM);
+        if (p.a_mn)  // A stored (K, M) row-major: inner = M, boxes of 64 x BK
+          rc = make_map(&args.mapA[nA], opA, p.in_dt, (uint64_t)U.rowsA, (uint64_t)P.K, (uint64_t)ldA, 64, BK);
+        else
+          rc = make_map(&args.mapA[nA], opA, p.in_dt, (uint64_t)P.K, (uint64_t)U.rowsA, (uint64_t)ldA, BK,
+                        rowclu ? msub * BM : BM);
         if (rc) return rc;
         aptr[nA] = opA;
         ia = nA++;
@@ -1187,7 +1262,20 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   for (int j = 0; j < p.njobs; ++j)
     if (!al16(p.jobs[j].C) || ((p.jobs[j].ldc * oe) % 16)) vec = 0;
   args.vec_ok = vec;
-  args.idesc = umma_idesc_f16(p.in_dt == TP_BF16 ? 1u : 0u, summa ? 1u : 0u, pair ? 2 * BM : BM, (uint32_t)BN);
+  // TMA-store epilogue (M-major-A pair units, whose short contraction leaves
+  // the float32 output stores as the critical path): float32 outputs with
+  // 16-byte aligned bases and rows.
+  bool tstore = pair && summa && p.a_mn && p.out_dt == TP_F32 && p.njobs <= kMaxCMaps;
+  for (int j = 0; tstore && j < p.njobs; ++j)
+    tstore = al16(p.jobs[j].C) && (p.jobs[j].ldc % 4) == 0;
+  for (int j = 0; tstore && j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    rc = make_tmap_2d(&args.mapC[j], J.C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)J.N, (uint64_t)J.M,
+                      (uint64_t)J.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
+  args.idesc = umma_idesc_f16(p.in_dt == TP_BF16 ? 1u : 0u, summa ? 1u : 0u, pair ? 2 * BM : BM, (uint32_t)BN,
+                              p.a_mn ? 1u : 0u);
   args.status = p.status;
   args.wait_ns = (uint64_t)p.wait_ns;
 
@@ -1201,6 +1289,10 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     rc = launch_row_cluster<256, 3, 2>(args, s);
   else if (rowclu)
     rc = launch_row_cluster<256, 4, 1>(args, s);
+  else if (pair && summa && p.a_mn && tstore)
+    rc = launch_pair<256, true, 5, 2, 1, false, true, true>(args, sms, s);
+  else if (pair && summa && p.a_mn)
+    rc = launch_pair<256, true, 6, 2, 1, false, true>(args, sms, s);
   else if (pair && summa)
     rc = launch_pair<256, true, 6, 2, 1>(args, sms, s);
   else if (pair && nsub == 2 && BN == 160)
@@ -1215,6 +1307,10 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     rc = launch_pair<192, false, 7, 2, 1>(args, sms, s);
   else if (pair)
     rc = launch_pair<256, false, 6, 2, 1>(args, sms, s);
+  else if (summa && partials)
+    rc = launch_config<128, true, false, true, 6, 4>(args, sms, s);
+  else if (summa && p.a_mn)
+    rc = launch_config<256, true, false, false, 4, 2, true>(args, sms, s);
   else if (summa)
     rc = launch_config<256, true, false, false, 4, 2>(args, sms, s);
   else if (swap && partials)

@@ -96,6 +96,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Tile store shared -> global through the tensor map (bulk-group completion);
+// elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N committed bulk groups still read their shared source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's shared-memory writes before later async-proxy reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -193,11 +213,11 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor, kind::f16: D f32, A/B bf16 (ab_fmt 1) or f16 (0),
 // A K-major, B K-major (b_mn = 0) or MN-major (1), shape M x N.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(uint32_t ab_fmt, uint32_t b_mn, uint32_t M,
-                                                      uint32_t N) {
+                                                      uint32_t N, uint32_t a_mn = 0) {
   return (1u << 4)              // D format: f32
          | (ab_fmt << 7)        // A format
          | (ab_fmt << 10)       // B format
-         | (0u << 15)           // A major: K
+         | (a_mn << 15)         // A major
          | (b_mn << 16)         // B major
          | ((N >> 3) << 17)     // N / 8
          | ((M >> 4) << 24);    // M / 16

@@ -366,8 +366,143 @@ int tp_gathered_to_sharded(int N, const void *const *x, int64_t T, int64_t K, in
   return dispatch(p, (cudaStream_t)stream);
 }
 
-int tp_summa(int q, const void *const *X, const void *const *A, void *const *Y, int64_t M,
-             int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream) {
+int tp_all_to_sharded_dx(int N, const void *const *dy, int64_t T, int64_t O, int64_t lddy,
+                         const void *const *w, int64_t K, tp_dtype in_dt, void *dx, int64_t lddx,
+                         tp_dtype out_dt, tp_stream_t stream) {
+  if (N < 1 || N > kMaxShards) return set_error(TP_ERR_INVALID_ARG, "N must be in 1..%d", kMaxShards);
+  if (!valid_dt(in_dt) || !valid_dt(out_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
+  if (T < 0 || K < 1 || O < 1) return set_error(TP_ERR_INVALID_ARG, "need T >= 0, K >= 1, O >= 1");
+  if (O % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the output of size %lld across %d devices.",
+                     (long long)O, N);
+  const int64_t On = O / N;
+  if (!dy || !w || !dx) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (lddy < On) return set_error(TP_ERR_INVALID_ARG, "lddy (%lld) < O/N (%lld)", (long long)lddy, (long long)On);
+  if (lddx < K) return set_error(TP_ERR_INVALID_ARG, "lddx (%lld) < K (%lld)", (long long)lddx, (long long)K);
+  const int ie = elem_size(in_dt), oe = elem_size(out_dt);
+  if (!aligned(dx, oe)) return set_error(TP_ERR_ALIGNMENT, "dx not aligned to its element size");
+  for (int r = 0; r < N; ++r) {
+    if (!dy[r] || !w[r]) return set_error(TP_ERR_INVALID_ARG, "dy[%d] or w[%d] is NULL", r, r);
+    if (!aligned(dy[r], ie) || !aligned(w[r], ie))
+      return set_error(TP_ERR_ALIGNMENT, "shard %d pointer not aligned to its element size", r);
+  }
+  if (T == 0) return TP_OK;
+  // One output, N partials dy[r] @ w[r] (w[r] is (O/N, K): K-contiguous rows
+  // of the contraction), formed from zero and added in ascending r.
+  Problem p;
+  memset(&p, 0, sizeof(p));
+  p.njobs = 1;
+  p.in_dt = in_dt;
+  p.out_dt = out_dt;
+  p.b_layout = BL_MNMAJOR;
+  p.chain = 0;
+  p.jobs[0] = Job{dx, nullptr, T, K, lddx, 0, N};
+  for (int r = 0; r < N; ++r) p.parts[r] = Part{dy[r], w[r], nullptr, nullptr, On, lddy, K};
+  return dispatch(p, (cudaStream_t)stream);
+}
+
+int tp_sharded_to_all_dx(int N, const void *dy, int64_t T, int64_t O, int64_t lddy, const void *const *w,
+                         int64_t K, tp_dtype in_dt, void *const *dx, int64_t lddx, tp_dtype out_dt,
+                         tp_stream_t stream) {
+  if (N < 1 || N > kMaxShards) return set_error(TP_ERR_INVALID_ARG, "N must be in 1..%d", kMaxShards);
+  if (!valid_dt(in_dt) || !valid_dt(out_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
+  if (T < 0 || K < 1 || O < 1) return set_error(TP_ERR_INVALID_ARG, "need T >= 0, K >= 1, O >= 1");
+  if (K % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the input of size %lld across %d devices.",
+                     (long long)K, N);
+  const int64_t Kn = K / N;
+  if (!dy || !w || !dx) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (lddy < O) return set_error(TP_ERR_INVALID_ARG, "lddy (%lld) < O (%lld)", (long long)lddy, (long long)O);
+  if (lddx < Kn) return set_error(TP_ERR_INVALID_ARG, "lddx (%lld) < K/N (%lld)", (long long)lddx, (long long)Kn);
+  const int ie = elem_size(in_dt), oe = elem_size(out_dt);
+  if (!aligned(dy, ie)) return set_error(TP_ERR_ALIGNMENT, "dy not aligned to its element size");
+  for (int r = 0; r < N; ++r) {
+    if (!w[r] || !dx[r]) return set_error(TP_ERR_INVALID_ARG, "w[%d] or dx[%d] is NULL", r, r);
+    if (!aligned(w[r], ie) || !aligned(dx[r], oe))
+      return set_error(TP_ERR_ALIGNMENT, "shard %d pointer not aligned to its element size", r);
+  }
+  if (T == 0) return TP_OK;
+  Problem p;
+  memset(&p, 0, sizeof(p));
+  p.njobs = N;
+  p.in_dt = in_dt;
+  p.out_dt = out_dt;
+  p.b_layout = BL_MNMAJOR;
+  p.chain = 1;
+  for (int r = 0; r < N; ++r) {
+    p.jobs[r] = Job{dx[r], nullptr, T, Kn, lddx, r, 1};
+    p.parts[r] = Part{dy, w[r], nullptr, nullptr, O, lddy, Kn};
+  }
+  return dispatch(p, (cudaStream_t)stream);
+}
+
+int tp_sharded_dw(int N, const void *const *dy, int64_t lddy, const void *const *x, int64_t ldx, int64_t T,
+                  int64_t O, int64_t K, tp_dtype in_dt, void *const *dw, int64_t lddw, tp_dtype out_dt,
+                  tp_stream_t stream) {
+  if (N < 1 || N > kMaxShards) return set_error(TP_ERR_INVALID_ARG, "N must be in 1..%d", kMaxShards);
+  if (!valid_dt(in_dt) || !valid_dt(out_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
+  if (T < 0 || K < 1 || O < 1) return set_error(TP_ERR_INVALID_ARG, "need T >= 0, K >= 1, O >= 1");
+  if (!dy || !x || !dw) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (lddy < O) return set_error(TP_ERR_INVALID_ARG, "lddy (%lld) < O (%lld)", (long long)lddy, (long long)O);
+  if (ldx < K) return set_error(TP_ERR_INVALID_ARG, "ldx (%lld) < K (%lld)", (long long)ldx, (long long)K);
+  if (lddw < K) return set_error(TP_ERR_INVALID_ARG, "lddw (%lld) < K (%lld)", (long long)lddw, (long long)K);
+  const int ie = elem_size(in_dt), oe = elem_size(out_dt);
+  for (int r = 0; r < N; ++r) {
+    // an empty batch (T = 0) may come with null operand pointers
+    if ((T > 0 && (!dy[r] || !x[r])) || !dw[r])
+      return set_error(TP_ERR_INVALID_ARG, "dy[%d], x[%d] or dw[%d] is NULL", r, r, r);
+    if (!aligned(dy[r], ie) || !aligned(x[r], ie) || !aligned(dw[r], oe))
+      return set_error(TP_ERR_ALIGNMENT, "shard %d pointer not aligned to its element size", r);
+  }
+  if (T == 0) {  // an empty sum over tokens: the gradient is zero
+    for (int r = 0; r < N; ++r) {
+      cudaError_t e = cudaMemset2DAsync(dw[r], (size_t)(lddw * oe), 0, (size_t)(K * oe), (size_t)O,
+                                        (cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_error(e, "cudaMemset2DAsync");
+    }
+    return TP_OK;
+  }
+  // dW_r(o, k) = sum over tokens t of dy_r[t][o] * x_r[t][k]: both operands
+  // are read token-major (M- and N-major), the contraction runs over T.
+  Problem p;
+  memset(&p, 0, sizeof(p));
+  p.njobs = N;
+  p.in_dt = in_dt;
+  p.out_dt = out_dt;
+  p.b_layout = BL_MNMAJOR;
+  p.a_mn = 1;
+  p.chain = 1;
+  for (int r = 0; r < N; ++r) {
+    p.jobs[r] = Job{dw[r], nullptr, O, K, lddw, r, 1};
+    p.parts[r] = Part{dy[r], x[r], nullptr, nullptr, T, lddy, ldx};
+  }
+  return dispatch(p, (cudaStream_t)stream);
+}
+
+int tp_bias_grad(int nout, int nin, const void *const *dy, int64_t rows, int64_t cols, int64_t ld,
+                 tp_dtype in_dt, float *const *db, tp_stream_t stream) {
+  if (nout < 1 || nout > kMaxJobs || nin < 1 || nout * nin > kMaxParts)
+    return set_error(TP_ERR_INVALID_ARG, "need 1 <= nout <= %d, nin >= 1, nout * nin <= %d", kMaxJobs,
+                     kMaxParts);
+  if (!valid_dt(in_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
+  if (rows < 0 || cols < 1) return set_error(TP_ERR_INVALID_ARG, "need rows >= 0, cols >= 1");
+  if (ld < cols) return set_error(TP_ERR_INVALID_ARG, "ld (%lld) < cols (%lld)", (long long)ld, (long long)cols);
+  if (!dy || !db) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  const int ie = elem_size(in_dt);
+  for (int i = 0; i < nout * nin; ++i)
+    if ((rows > 0 && !dy[i]) || !aligned(dy[i], ie))
+      return set_error(TP_ERR_INVALID_ARG, "dy[%d] is NULL or unaligned", i);
+  for (int o = 0; o < nout; ++o)
+    if (!db[o] || !aligned(db[o], 4)) return set_error(TP_ERR_INVALID_ARG, "db[%d] is NULL or unaligned", o);
+  return launch_colsum(nout, nin, dy, rows, cols, ld, in_dt, db, (cudaStream_t)stream);
+}
+
+// SUMMA-family lowering: q*q output blocks, each chaining q block products in
+// step order t.  kind 0: Y_ij = sum_t X_it A_tj (+ bias_j);  kind 1 (A B^T):
+// Y_ij = sum_t X_it A_jt^T;  kind 2 (A^T B): Y_ij = sum_t X_ti^T A_tj.
+static int summa_lower(int kind, int q, const void *const *X, const void *const *A,
+                       const void *const *bias, void *const *Y, int64_t M, int64_t K, int64_t Ncols,
+                       tp_dtype in_dt, tp_stream_t stream) {
   if (q < 1) return set_error(TP_ERR_NOT_DIVISIBLE, "q must be >= 1 (P = q*q processors)");
   if (q > 4) return set_error(TP_ERR_UNSUPPORTED, "q = %d: this build supports q <= 4", q);
   if (!valid_dt(in_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
@@ -382,22 +517,54 @@ int tp_summa(int q, const void *const *X, const void *const *A, void *const *Y, 
     if (!aligned(X[b], ie) || !aligned(A[b], ie) || !aligned(Y[b], 4))
       return set_error(TP_ERR_ALIGNMENT, "block %d pointer not aligned to its element size", b);
   }
+  if (bias)
+    for (int j = 0; j < q; ++j)
+      if (!bias[j] || !aligned(bias[j], 4)) return set_error(TP_ERR_INVALID_ARG, "bias[%d] is NULL or unaligned", j);
   const int64_t bm = M / q, bk = K / q, bn = Ncols / q;
   Problem p;
   memset(&p, 0, sizeof(p));
   p.njobs = q * q;
   p.in_dt = in_dt;
   p.out_dt = TP_F32;
-  p.b_layout = BL_MNMAJOR;
+  p.b_layout = kind == 1 ? BL_KMAJOR : BL_MNMAJOR;
+  p.a_mn = kind == 2;
   p.chain = 1;
   for (int i = 0; i < q; ++i)
     for (int j = 0; j < q; ++j) {
       const int jb = i * q + j;
-      p.jobs[jb] = Job{Y[jb], nullptr, bm, bn, bn, jb * q, q};
-      for (int t = 0; t < q; ++t)
-        p.parts[jb * q + t] = Part{X[i * q + t], A[t * q + j], nullptr, nullptr, bk, bk, bn};
+      p.jobs[jb] = Job{Y[jb], bias ? (const float *)bias[j] : nullptr, bm, bn, bn, jb * q, q};
+      for (int t = 0; t < q; ++t) {
+        Part &P = p.parts[jb * q + t];
+        if (kind == 0)
+          P = Part{X[i * q + t], A[t * q + j], nullptr, nullptr, bk, bk, bn};
+        else if (kind == 1)
+          P = Part{X[i * q + t], A[j * q + t], nullptr, nullptr, bk, bk, bk};
+        else
+          P = Part{X[t * q + i], A[t * q + j], nullptr, nullptr, bk, bm, bn};
+      }
     }
   return dispatch(p, (cudaStream_t)stream);
+}
+
+int tp_summa(int q, const void *const *X, const void *const *A, void *const *Y, int64_t M,
+             int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream) {
+  return summa_lower(0, q, X, A, nullptr, Y, M, K, Ncols, in_dt, stream);
+}
+
+int tp_summa_linear(int q, const void *const *X, const void *const *A, const void *const *bias,
+                    void *const *Y, int64_t M, int64_t K, int64_t Ncols, tp_dtype in_dt,
+                    tp_stream_t stream) {
+  return summa_lower(0, q, X, A, bias, Y, M, K, Ncols, in_dt, stream);
+}
+
+int tp_summa_abt(int q, const void *const *A, const void *const *B, void *const *C, int64_t M,
+                 int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream) {
+  return summa_lower(1, q, A, B, nullptr, C, M, K, Ncols, in_dt, stream);
+}
+
+int tp_summa_atb(int q, const void *const *A, const void *const *B, void *const *C, int64_t M,
+                 int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream) {
+  return summa_lower(2, q, A, B, nullptr, C, M, K, Ncols, in_dt, stream);
 }
 
 int tp_q4_quantize(const float *w, int64_t rows, int64_t K, int group_size, uint32_t *wq,

@@ -11,6 +11,8 @@
 // order (SUMMA's q steps).  `chain` = 0: every part is a separate float32
 // partial formed from zero and the partials are added in part order (the
 // row-parallel all_sum over ranks r = 0..N-1).
+// `a_mn` = 1: A_p(m, k) is A_p[k*lda + m] (the operand stored K-major by
+// rows, as a gradient's dy or x is when the contraction runs over tokens).
 // `gated` = 1 (chain mode, BL_KMAJOR only): every part carries a second
 // weight B2 and every job a second bias, and the job's output is the gated
 // product silu(G + bias) * (U + bias2), G and U the chained sums over its
@@ -56,6 +58,7 @@ struct Problem {
   int b_layout;        // BLayout
   int chain;
   int gated;
+  int a_mn;
   int *status;         // device status word
   int64_t wait_ns;     // bound of device-side waits
 };
@@ -93,6 +96,8 @@ int launch_shard(const void *w, int64_t rows, int64_t cols, int elem_bytes, int 
 int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void *scales,
                     void *qbias, cudaStream_t s);
 int launch_debug_wait(int64_t limit_ns, int *status, cudaStream_t s);
+int launch_colsum(int nout, int nin, const void *const *in, int64_t rows, int64_t cols, int64_t ld,
+                  int in_dt, float *const *out, cudaStream_t s);
 void umma_shutdown();
 
 // ---- shared host helpers (tmap.cu)

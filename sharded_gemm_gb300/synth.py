@@ -104,6 +104,13 @@ def ffn(seed: int = SEED, T: int = 512, D: int = 4096, F: int = 11008, N: int = 
     )
 
 
+def grad_output(seed: int = SEED, T: int = 512, D: int = 4096) -> dict:
+    """An incoming output gradient dy (T, D) bf16 N(0, 1) for a backward step
+    (its own seed stream, so it is independent of the forward's inputs)."""
+    (g,) = streams(seed + 1000003, 1)
+    return dict(name="grad", T=T, D=D, dy=normal_bf16(g, (T, D), 1.0))
+
+
 def summa(seed: int = SEED, M: int = 8192, K: int = 8192, Ncols: int = 8192) -> dict:
     """SUMMA Y = X A: X (M, K), A (K, Ncols) bf16 N(0, 1/sqrt(K))."""
     gx, ga = streams(seed, 2)

@@ -11,7 +11,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (tp_all_to_sharded, tp_gated_all_to_sharded, tp_gathered_to_sharded, tp_q4_all_to_sharded,
+from . import (tp_all_to_sharded, tp_all_to_sharded_dx, tp_bias_grad, tp_gated_all_to_sharded,
+               tp_sharded_dw, tp_sharded_to_all_dx, tp_gathered_to_sharded, tp_q4_all_to_sharded,
                tp_q4_quantize,
                tp_q4_sharded_to_all, tp_shard_weight, tp_sharded_to_all, tp_sharded_to_sharded, tp_summa)
 
@@ -128,6 +129,50 @@ class MLPGatherScatter:
         tp_gathered_to_sharded(self.xs if xs is None else xs, self.w1, self.b1, out=self.mid, stream=stream)
         tp_sharded_to_sharded(self.mid, self.w2, self.b2, out=self.ys, stream=stream)
         return self.ys
+
+
+class MLPBackward:
+    """Backward step of ``MLPPair`` (no activation between the layers) for an
+    incoming gradient dy of its (T, D) output:
+      dh_r  = dy @ W2_r                  (row-parallel input gradient, bf16)
+      dW2_r = dy^T @ h_r,  db2 = sum_t dy
+      dx    = sum_r dh_r @ W1_r          (column-parallel: all-summed, f32)
+      dW1_r = dh_r^T @ x,  db1_r = sum_t dh_r
+    Weight and bias gradients are float32.  ``h`` is the forward's sharded
+    intermediate, computed once at construction."""
+
+    def __init__(self, cfg: dict, dy: np.ndarray, device="cuda"):
+        self.fwd = MLPPair(cfg, device=device)
+        self.fwd.step()
+        f = self.fwd
+        self.N = N = f.N
+        self.dy = to_device(dy, "bf16", device)
+        T, D = self.dy.shape
+        Fn = f.w1[0].shape[0]
+        self.dh = [torch.empty((T, Fn), dtype=torch.bfloat16, device=device) for _ in range(N)]
+        self.dw2 = [torch.empty((D, Fn), dtype=torch.float32, device=device) for _ in range(N)]
+        self.db2 = [torch.empty((D,), dtype=torch.float32, device=device)]
+        self.dx = torch.empty((T, D), dtype=torch.float32, device=device)
+        self.dw1 = [torch.empty((Fn, D), dtype=torch.float32, device=device) for _ in range(N)]
+        self.db1 = [torch.empty((Fn,), dtype=torch.float32, device=device) for _ in range(N)]
+        self.flops = 4 * 2.0 * T * D * Fn * N
+
+    def launches(self):
+        f = self
+        p = self.fwd
+        return [
+            lambda s: tp_sharded_to_all_dx(f.dy, p.w2, out=f.dh, stream=s),
+            lambda s: tp_sharded_dw([f.dy] * f.N, p.mid, out=f.dw2, stream=s),
+            lambda s: tp_bias_grad([f.dy], out=f.db2, stream=s),
+            lambda s: tp_all_to_sharded_dx(f.dh, p.w1, out=f.dx, stream=s),
+            lambda s: tp_sharded_dw(f.dh, [p.x] * f.N, out=f.dw1, stream=s),
+            lambda s: tp_bias_grad(f.dh, out=f.db1, stream=s),
+        ]
+
+    def step(self, stream=None):
+        for fn in self.launches():
+            fn(stream)
+        return self.dx
 
 
 class Summa:

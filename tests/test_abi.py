@@ -68,6 +68,32 @@ def test_sharded_to_all_not_divisible(L):
     assert rc == tp.TP_ERR_NOT_DIVISIBLE
 
 
+def test_backward_checks(L):
+    a, k1 = _arr(4)
+    # column-parallel dx: O % N, lddy < O/N
+    assert L.tp_all_to_sharded_dx(4, a, 2, 10, 10, a, 8, tp.TP_BF16, FAKE, 8, tp.TP_F32, None) == \
+        tp.TP_ERR_NOT_DIVISIBLE
+    assert L.tp_all_to_sharded_dx(4, a, 2, 8, 1, a, 8, tp.TP_BF16, FAKE, 8, tp.TP_F32, None) == \
+        tp.TP_ERR_INVALID_ARG
+    # row-parallel dx: K % N
+    assert L.tp_sharded_to_all_dx(4, FAKE, 2, 8, 8, a, 10, tp.TP_BF16, a, 8, tp.TP_F32, None) == \
+        tp.TP_ERR_NOT_DIVISIBLE
+    # weight grads: lddw < K, null shard
+    assert L.tp_sharded_dw(4, a, 8, a, 8, 2, 8, 8, tp.TP_BF16, a, 4, tp.TP_F32, None) == tp.TP_ERR_INVALID_ARG
+    an, k2 = _arr(4)
+    k2[1] = None
+    assert L.tp_sharded_dw(4, a, 8, an, 8, 2, 8, 8, tp.TP_BF16, a, 8, tp.TP_F32, None) == tp.TP_ERR_INVALID_ARG
+    # bias grads: nout * nin above 64, ld < cols
+    b, k3 = _arr(65)
+    assert L.tp_bias_grad(5, 13, b, 2, 8, 8, tp.TP_BF16, b, None) == tp.TP_ERR_INVALID_ARG
+    assert L.tp_bias_grad(1, 1, b, 2, 8, 4, tp.TP_BF16, b, None) == tp.TP_ERR_INVALID_ARG
+    # SUMMA backward and linear: divisibility by q
+    s16, k4 = _arr(16)
+    for fn in (L.tp_summa_abt, L.tp_summa_atb):
+        assert fn(4, s16, s16, s16, 10, 8, 8, tp.TP_BF16, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert L.tp_summa_linear(4, s16, s16, None, s16, 8, 8, 10, tp.TP_BF16, None) == tp.TP_ERR_NOT_DIVISIBLE
+
+
 def test_gated_checks(L):
     w, k1 = _arr(4)
     y, k2 = _arr(4)

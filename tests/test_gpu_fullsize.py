@@ -10,7 +10,7 @@ import oracle
 import sharded_gemm_gb300 as tp
 from sharded_gemm_gb300 import build as tpbuild
 from sharded_gemm_gb300 import synth
-from sharded_gemm_gb300.workloads import GatedFFN, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_host
+from sharded_gemm_gb300.workloads import GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_host
 from gpu_util import bf16, check_close, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -57,6 +57,36 @@ def test_full_gated_ffn():
         check_close(hs[r], ref_h[r], "h shard %d" % r)
     w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
     check_close(to_host(ffn.y)[rows], oracle.sharded_to_all(hs, w2, cfg["b2"]), "y")
+
+
+def test_full_mlp_backward():
+    # the bench's mlp_bwd step: sampled token rows of dh and dx, sampled
+    # output rows of every weight gradient, all of both bias gradients
+    cfg = synth.mlp()
+    T, D, N = cfg["T"], cfg["D"], cfg["N"]
+    dy = synth.grad_output(T=T, D=D)["dy"]
+    bw = MLPBackward(cfg, dy)
+    bw.step()
+    assert tp.tp_query_status() == 0
+    rows = sample_rows(T, 8)
+    dyv = bf16(dy)
+    w1 = [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, N)]
+    w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
+    dh = [to_host(d) for d in bw.dh]
+    ref_dh = oracle.sharded_to_all_dx(dyv[rows], w2)
+    for r in range(N):
+        check_close(dh[r][rows], ref_dh[r], "dh %d" % r)
+    check_close(to_host(bw.dx)[rows], oracle.all_to_sharded_dx([d[rows] for d in dh], w1), "dx")
+    h = [to_host(m) for m in bw.fwd.mid]
+    x = bf16(cfg["x"])
+    for r in (0, N - 1):
+        o2 = sample_rows(D, 16, seed=r)
+        check_close(to_host(bw.dw2[r])[o2], oracle.sharded_dw([dyv[:, o2]], [h[r]])[0], "dW2 %d" % r)
+        o1 = sample_rows(dh[r].shape[1], 16, seed=10 + r)
+        check_close(to_host(bw.dw1[r])[o1], oracle.sharded_dw([dh[r][:, o1]], [x])[0], "dW1 %d" % r)
+    check_close(to_host(bw.db2[0]), oracle.bias_grad([[dyv]])[0], "db2")
+    for r, g in enumerate(oracle.bias_grad([[d] for d in dh])):
+        check_close(to_host(bw.db1[r]), g, "db1 %d" % r)
 
 
 def test_full_mlp_gather_scatter():

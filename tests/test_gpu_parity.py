@@ -15,7 +15,7 @@ import oracle
 import sharded_gemm_gb300 as tp
 from sharded_gemm_gb300 import build as tpbuild
 from sharded_gemm_gb300 import synth
-from sharded_gemm_gb300.workloads import (GatedFFN, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_device,
+from sharded_gemm_gb300.workloads import (GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_device,
                                           to_host)
 from gpu_util import bf16, check_close, sample_rows
 
@@ -189,6 +189,147 @@ def test_mlp_pair_small(policy):
     check_close(to_host(pair.y), oracle.sharded_to_all(mids, w2, cfg["b2"].astype(np.float64)), "y (layer)")
     chain = oracle.linear(oracle.linear(x, bf16(cfg["w1"]), cfg["b1"]), bf16(cfg["w2"]), cfg["b2"])
     check_close(to_host(pair.y), chain, "y (end to end)")
+
+
+# ------------------------------------------------------------------ f3 backward
+@pytest.mark.parametrize("T,On,K,N", [(1, 64, 128, 2), (5, 40, 192, 4), (130, 320, 600, 2),
+                                      (300, 264, 200, 3), (64, 256, 512, 8), (129, 128, 129, 1),
+                                      (200, 75, 64, 2)])
+def test_all_to_sharded_dx(policy, T, On, K, N):
+    dy = rand_bf16((T, On * N))
+    w = rand_bf16((On * N, K), 0.05)
+    dys = tp.tp_shard_weight(to_device(dy, "bf16"), -1, 1, N)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), 0, 1, N)
+    dx = tp.tp_all_to_sharded_dx(dys, ws)
+    _status_ok()
+    ref = oracle.all_to_sharded_dx([bf16(p) for p in oracle.shard(dy, -1, 1, N)],
+                                   [bf16(p) for p in oracle.shard(w, 0, 1, N)])
+    check_close(to_host(dx), ref, "dx")
+
+
+@pytest.mark.parametrize("T,O,Kn,N", [(1, 64, 128, 2), (5, 96, 40, 4), (130, 320, 300, 4),
+                                      (200, 200, 520, 3), (64, 512, 128, 8)])
+def test_sharded_to_all_dx(policy, T, O, Kn, N):
+    dy = rand_bf16((T, O))
+    w = rand_bf16((O, Kn * N), 0.05)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), -1, 1, N)
+    dxs = tp.tp_sharded_to_all_dx(to_device(dy, "bf16"), ws, out_dtype=torch.float32)
+    _status_ok()
+    ref = oracle.sharded_to_all_dx(bf16(dy), [bf16(p) for p in oracle.shard(w, -1, 1, N)])
+    for r in range(N):
+        check_close(to_host(dxs[r]), ref[r], "dx %d" % r)
+
+
+@pytest.mark.parametrize("T,O,K,N,shared", [(1, 128, 64, 2, "x"), (130, 300, 520, 2, "x"),
+                                            (512, 256, 384, 4, "dy"), (77, 136, 264, 3, "dy"),
+                                            (700, 520, 260, 1, "x"), (64, 40, 72, 8, "x")])
+@pytest.mark.parametrize("out_dt", [torch.float32, torch.bfloat16])
+def test_sharded_dw(policy, T, O, K, N, shared, out_dt):
+    # shared == "x": column-parallel form (per-shard dy, one x);
+    # shared == "dy": row-parallel form (one dy, per-shard x)
+    if shared == "x":
+        dyh = [rand_bf16((T, O)) for _ in range(N)]
+        xh = [rand_bf16((T, K))] * N
+    else:
+        dyh = [rand_bf16((T, O))] * N
+        xh = [rand_bf16((T, K)) for _ in range(N)]
+    dyd = [to_device(a, "bf16") for a in dyh]
+    xd = [to_device(a, "bf16") for a in xh]
+    dws = tp.tp_sharded_dw(dyd, xd, out_dtype=out_dt)
+    _status_ok()
+    ref = oracle.sharded_dw([bf16(a) for a in dyh], [bf16(a) for a in xh])
+    for r in range(N):
+        check_close(to_host(dws[r]), ref[r], "dW %d" % r)
+
+
+def test_sharded_dw_empty_batch_is_zero():
+    dy = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((0, 128), dtype=torch.bfloat16, device="cuda")
+    out = [torch.full((64, 128), float("nan"), device="cuda") for _ in range(2)]
+    tp.tp_sharded_dw([dy, dy], [x, x], out=out)
+    _status_ok()
+    for o in out:
+        assert torch.equal(o, torch.zeros_like(o))
+
+
+@pytest.mark.parametrize("rows,cols,nout,nin,dt", [(512, 4096, 1, 1, "bf16"), (130, 75, 3, 1, "f32"),
+                                                   (1, 33, 2, 2, "bf16"), (0, 64, 1, 1, "f32"),
+                                                   (257, 1000, 2, 4, "f16")])
+def test_bias_grad(rows, cols, nout, nin, dt):
+    hs = [RNG.standard_normal((rows, cols)).astype(np.float32) for _ in range(nout * nin)]
+    if dt == "bf16":
+        hs = [synth.f32_to_bf16_bits(h) for h in hs]
+        vals = [bf16(h) for h in hs]
+    elif dt == "f16":
+        hs = [h.astype(np.float16) for h in hs]
+        vals = [h.astype(np.float64) for h in hs]
+    else:
+        vals = [h.astype(np.float64) for h in hs]
+    db = tp.tp_bias_grad([to_device(h, dt) for h in hs], nin=nin)
+    _status_ok()
+    ref = oracle.bias_grad([vals[o * nin:(o + 1) * nin] for o in range(nout)])
+    for o in range(nout):
+        check_close(to_host(db[o]), ref[o], "db %d" % o)
+
+
+def _blocks_dev(M, q):
+    return [to_device(b, "bf16") for b in oracle.blocks(M, q)]
+
+
+@pytest.mark.parametrize("q,M,K,Nc", [(1, 128, 128, 256), (2, 272, 320, 528), (4, 512, 256, 1024),
+                                      (2, 48, 64, 48)])
+def test_summa_abt_atb_linear(policy, q, M, K, Nc):
+    A = rand_bf16((M, K))
+    B = rand_bf16((Nc, K))
+    C = tp.tp_summa_abt(q, _blocks_dev(A, q), _blocks_dev(B, q))
+    _status_ok()
+    ref = oracle.summa_abt([bf16(b) for b in oracle.blocks(A, q)], [bf16(b) for b in oracle.blocks(B, q)], q)
+    for b in range(q * q):
+        check_close(to_host(C[b]), ref[b], "abt block %d" % b)
+    P = rand_bf16((K, M))
+    Q = rand_bf16((K, Nc))
+    C = tp.tp_summa_atb(q, _blocks_dev(P, q), _blocks_dev(Q, q))
+    _status_ok()
+    ref = oracle.summa_atb([bf16(b) for b in oracle.blocks(P, q)], [bf16(b) for b in oracle.blocks(Q, q)], q)
+    for b in range(q * q):
+        check_close(to_host(C[b]), ref[b], "atb block %d" % b)
+    X = rand_bf16((M, K))
+    Am = rand_bf16((K, Nc))
+    bias = [(RNG.standard_normal(Nc // q) * 0.5).astype(np.float32) for _ in range(q)]
+    Y = tp.tp_summa_linear(q, _blocks_dev(X, q), _blocks_dev(Am, q), [to_device(b, "f32") for b in bias])
+    _status_ok()
+    ref = oracle.summa_linear([bf16(b) for b in oracle.blocks(X, q)], [bf16(b) for b in oracle.blocks(Am, q)],
+                              [b.astype(np.float64) for b in bias], q)
+    for b in range(q * q):
+        check_close(to_host(Y[b]), ref[b], "linear block %d" % b)
+
+
+def test_mlp_backward_small(policy):
+    cfg = synth.mlp(seed=8, T=150, D=256, F=688, N=4, bias_std=0.1)
+    dy = synth.grad_output(seed=8, T=150, D=256)["dy"]
+    bw = MLPBackward(cfg, dy)
+    bw.step()
+    _status_ok()
+    N = 4
+    x, dyv = bf16(cfg["x"]), bf16(dy)
+    w1 = [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, N)]
+    w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
+    h = [to_host(m) for m in bw.fwd.mid]
+    ref_dh = oracle.sharded_to_all_dx(dyv, w2)
+    dh = [to_host(d) for d in bw.dh]
+    for r in range(N):
+        check_close(dh[r], ref_dh[r], "dh %d" % r)
+    for r, g in enumerate(oracle.sharded_dw([dyv] * N, h)):
+        check_close(to_host(bw.dw2[r]), g, "dW2 %d" % r)
+    check_close(to_host(bw.db2[0]), oracle.bias_grad([[dyv]])[0], "db2")
+    check_close(to_host(bw.dx), oracle.all_to_sharded_dx(dh, w1), "dx")
+    for r, g in enumerate(oracle.sharded_dw(dh, [x] * N)):
+        check_close(to_host(bw.dw1[r]), g, "dW1 %d" % r)
+    for r, g in enumerate(oracle.bias_grad([[d] for d in dh])):
+        check_close(to_host(bw.db1[r]), g, "db1 %d" % r)
+    # end to end: the unsharded gradient of y = (x W1^T + b1) W2^T + b2
+    full_dx = dyv @ bf16(cfg["w2"]) @ bf16(cfg["w1"])
+    check_close(to_host(bw.dx), full_dx, "dx (end to end)")
 
 
 # ------------------------------------------------------------------ f2 gated FFN

@@ -209,6 +209,142 @@ def test_pair_equals_unsharded_mlp_small():
     assert np.abs(y - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
 
 
+# ------------------------------------------------------------------ backward
+def _ints(shape, lo=-4, hi=5):
+    return RNG.integers(lo, hi, shape).astype(np.float64)
+
+
+def _dot(a, b):
+    return float(np.sum(np.asarray(a) * np.asarray(b)))
+
+
+def check_col_adjoint(all_to_sharded_dx, sharded_dw, shard):
+    # The column-parallel forward y_r = x W_r^T is linear in x and in W, so
+    # its gradients are the adjoints:  sum_r <dy_r, x W_r^T> = <dx, x> =
+    # sum_r <dW_r, W_r>.  Small integers keep all three sums exact.
+    for (T, K, O, N) in [(3, 5, 8, 2), (4, 6, 12, 4), (2, 3, 8, 8), (5, 4, 3, 1)]:
+        x, w = _ints((T, K)), _ints((O, K))
+        ws = shard(w, 0, 1, N)
+        dys = [_ints((T, O // N)) for _ in range(N)]
+        lhs = sum(_dot(dy, x @ wr.T) for dy, wr in zip(dys, ws))
+        dx = all_to_sharded_dx(dys, ws)
+        assert dx.shape == (T, K)
+        assert _dot(dx, x) == lhs
+        dws = sharded_dw(dys, [x] * N)
+        assert [d.shape for d in dws] == [wr.shape for wr in ws]
+        assert sum(_dot(d, wr) for d, wr in zip(dws, ws)) == lhs
+
+
+def check_row_adjoint(sharded_to_all_dx, sharded_dw, shard):
+    # Row-parallel forward y = sum_r x_r W_r^T:
+    # <dy, y> = sum_r <dx_r, x_r> = sum_r <dW_r, W_r>.
+    for (T, K, O, N) in [(3, 8, 5, 2), (4, 12, 6, 4), (2, 8, 3, 8), (5, 3, 4, 1)]:
+        x, w = _ints((T, K)), _ints((O, K))
+        xs, ws = shard(x, -1, 1, N), shard(w, -1, 1, N)
+        dy = _ints((T, O))
+        lhs = _dot(dy, sum(xr @ wr.T for xr, wr in zip(xs, ws)))
+        dxs = sharded_to_all_dx(dy, ws)
+        assert [d.shape for d in dxs] == [xr.shape for xr in xs]
+        assert sum(_dot(d, xr) for d, xr in zip(dxs, xs)) == lhs
+        dws = sharded_dw([dy] * N, xs)
+        assert sum(_dot(d, wr) for d, wr in zip(dws, ws)) == lhs
+
+
+def check_bias_grad_closed_form(bias_grad):
+    # dy[t, c] = t + 2c: the column sums are T(T-1)/2 + 2cT; two matrices in a
+    # group add; and <dy, 1 b^T> = <db, b> for the bias's own adjoint.
+    T, C = 7, 5
+    t, c = np.meshgrid(np.arange(T), np.arange(C), indexing="ij")
+    dy = (t + 2 * c).astype(np.float64)
+    got = bias_grad([[dy], [dy, 3 * dy]])
+    expect = T * (T - 1) / 2 + 2 * np.arange(C) * T
+    assert np.array_equal(got[0], expect)
+    assert np.array_equal(got[1], 4 * expect)
+    b = _ints((C,))
+    d2 = _ints((T, C))
+    assert _dot(d2, np.broadcast_to(b, (T, C))) == _dot(bias_grad([[d2]])[0], b)
+
+
+def check_summa_backward(summa_abt, summa_atb):
+    # Block identities of Matmul_ABT_2D / Matmul_ATB_2D at q = 2, written out.
+    A = RNG.standard_normal((8, 6))
+    B = RNG.standard_normal((10, 6))
+    Ab, Bb = oracle.blocks(A, 2), oracle.blocks(B, 2)
+    A00, A01, A10, A11 = Ab
+    B00, B01, B10, B11 = Bb
+    expect = [A00 @ B00.T + A01 @ B01.T, A00 @ B10.T + A01 @ B11.T,
+              A10 @ B00.T + A11 @ B01.T, A10 @ B10.T + A11 @ B11.T]
+    for e, g in zip(expect, summa_abt(Ab, Bb, 2)):
+        assert g.shape == e.shape and np.abs(g - e).max() <= 1e-12 * (1 + np.abs(e).max())
+    P = RNG.standard_normal((6, 8))
+    Q = RNG.standard_normal((6, 10))
+    Pb, Qb = oracle.blocks(P, 2), oracle.blocks(Q, 2)
+    P00, P01, P10, P11 = Pb
+    Q00, Q01, Q10, Q11 = Qb
+    expect = [P00.T @ Q00 + P10.T @ Q10, P00.T @ Q01 + P10.T @ Q11,
+              P01.T @ Q00 + P11.T @ Q10, P01.T @ Q01 + P11.T @ Q11]
+    for e, g in zip(expect, summa_atb(Pb, Qb, 2)):
+        assert g.shape == e.shape and np.abs(g - e).max() <= 1e-12 * (1 + np.abs(e).max())
+    # q = 4 against numpy's transposed products
+    X = RNG.standard_normal((16, 12))
+    Y = RNG.standard_normal((8, 12))
+    got = oracle.unblock(summa_abt(oracle.blocks(X, 4), oracle.blocks(Y, 4), 4), 4)
+    assert np.abs(got - X @ Y.T).max() <= 1e-12 * (1 + np.abs(X @ Y.T).max())
+    Z = RNG.standard_normal((12, 8))
+    got = oracle.unblock(summa_atb(oracle.blocks(X.T.copy(), 4), oracle.blocks(Z, 4), 4), 4)
+    assert np.abs(got - X @ Z).max() <= 1e-12 * (1 + np.abs(X @ Z).max())
+
+
+def test_col_gradients_are_adjoints():
+    check_col_adjoint(oracle.all_to_sharded_dx, oracle.sharded_dw, oracle.shard)
+
+
+def test_row_gradients_are_adjoints():
+    check_row_adjoint(oracle.sharded_to_all_dx, oracle.sharded_dw, oracle.shard)
+
+
+def test_col_dx_equals_unsharded():
+    # the all-summed input gradient is the unsharded dy @ W
+    T, K, O, N = 5, 16, 12, 4
+    dy, w = RNG.standard_normal((T, O)), RNG.standard_normal((O, K))
+    dx = oracle.all_to_sharded_dx(oracle.shard(dy, -1, 1, N), oracle.shard(w, 0, 1, N))
+    assert np.abs(dx - dy @ w).max() <= 1e-12 * (1 + np.abs(dy @ w).max())
+
+
+def test_bias_grad_closed_form():
+    check_bias_grad_closed_form(oracle.bias_grad)
+
+
+def test_summa_backward_identities():
+    check_summa_backward(oracle.summa_abt, oracle.summa_atb)
+
+
+def test_summa_backward_adjoint():
+    # Y = X A on the grid: <dY, X A> = <dY A^T, X> = <X^T dY, A>, i.e.
+    # dX = ABT(dY, A) and dA = ATB(X, dY).
+    q = 2
+    X, A, dY = _ints((6, 4)), _ints((4, 8)), _ints((6, 8))
+    Xb, Ab, dYb = oracle.blocks(X, q), oracle.blocks(A, q), oracle.blocks(dY, q)
+    lhs = _dot(dY, X @ A)
+    dX = oracle.unblock(oracle.summa_abt(dYb, Ab, q), q)
+    dA = oracle.unblock(oracle.summa_atb(Xb, dYb, q), q)
+    assert _dot(dX, X) == lhs
+    assert _dot(dA, A) == lhs
+    assert oracle.unblock(oracle.summa(Xb, Ab, q), q).shape == dY.shape
+
+
+def test_summa_linear_bias_per_column_block():
+    # X = 0: every block is exactly its column block's bias
+    q = 2
+    Xb = oracle.blocks(np.zeros((4, 6)), q)
+    Ab = oracle.blocks(RNG.standard_normal((6, 8)), q)
+    b = [RNG.standard_normal(4) for _ in range(q)]
+    Y = oracle.summa_linear(Xb, Ab, b, q)
+    for i in range(q):
+        for j in range(q):
+            assert np.array_equal(Y[i * q + j], np.broadcast_to(b[j], (2, 4)))
+
+
 # ------------------------------------------------------------------ gated FFN
 def check_silu_closed_forms(silu):
     # sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4 in closed form.

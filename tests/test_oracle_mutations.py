@@ -132,3 +132,41 @@ def test_mutation_gated_up_bias_dropped():
     def bad(x, w1s, w3s, b1s=None, b3s=None):
         return oracle.gated_all_to_sharded(x, w1s, w3s, b1s, None)
     _expect_fail(T.check_gated_invariant, bad, oracle.shard)
+
+
+def test_mutation_col_dx_wrong_rank():
+    def bad(dys, ws):
+        n = len(ws)
+        return oracle.all_to_sharded_dx(dys, [ws[(r + 1) % n] for r in range(n)])
+    _expect_fail(T.check_col_adjoint, bad, oracle.sharded_dw, oracle.shard)
+
+
+def test_mutation_row_dx_transposed_weight():
+    def bad(dy, ws):
+        return [oracle.matmul(dy, np.ascontiguousarray(np.flipud(w))) for w in ws]
+    _expect_fail(T.check_row_adjoint, bad, oracle.sharded_dw, oracle.shard)
+
+
+def test_mutation_dw_reversed_k():
+    # dW_r with its K index reversed
+    def bad(dys, xs):
+        return [np.fliplr(g) for g in oracle.sharded_dw(dys, xs)]
+    _expect_fail(T.check_col_adjoint, oracle.all_to_sharded_dx, bad, oracle.shard)
+
+
+def test_mutation_bias_grad_wrong_axis():
+    def bad(groups):
+        return [sum(np.asarray(d).sum(axis=0)[::-1] for d in g) for g in groups]
+    _expect_fail(T.check_bias_grad_closed_form, bad)
+
+
+def test_mutation_abt_wrong_block():
+    def bad(Ab, Bb, q):
+        return oracle.summa_abt(Ab, [Bb[(b % q) * q + b // q] for b in range(q * q)], q)
+    _expect_fail(T.check_summa_backward, bad, oracle.summa_atb)
+
+
+def test_mutation_atb_wrong_block():
+    def bad(Ab, Bb, q):
+        return oracle.summa_atb([Ab[(b % q) * q + b // q] for b in range(q * q)], Bb, q)
+    _expect_fail(T.check_summa_backward, oracle.summa_abt, bad)
