@@ -747,8 +747,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
 // MSUB = 2: the tile is 256 x BN, two 128-row sub-tiles sharing each k-block's
 // B rows (two accumulators), so a k-block stages 256 + BN rows for twice the
 // MMA work; the partial is parked and reduced one sub-tile at a time.
-template <int BN, int STAGES, int MSUB>
+// B_MN: the weights are stored N-contiguous (K, N) and staged as BN/64 boxes
+// of 64 columns (the input gradient of the column-parallel layer, dy_r W_r).
+template <int BN, int STAGES, int MSUB, bool B_MN = false>
 __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __grid_constant__ UmmaArgs a) {
+  static_assert(!B_MN || BN % 64 == 0, "M/N-major B needs 64-column boxes");
   constexpr int A_SUB = BM * BK * 2;
   constexpr int A_BYTES = MSUB * A_SUB;
   constexpr int B_BYTES = BN * BK * 2;
@@ -818,8 +821,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
         const uint32_t fb = smem_u32(&full_bar[stage]);
         mbar_arrive_expect_tx(fb, STAGE_BYTES);
         // A: one box of all MSUB * 128 rows (the map's box height), B: one box
+        // (K-major) or BN/64 boxes of 64 columns (N-major)
         tma_load_2d(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
-        tma_load_2d(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
+        if constexpr (B_MN) {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192, &a.mapB[P.bmap], fb, rowB0 + c * 64, kb * BK);
+        } else {
+          tma_load_2d(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
+        }
         used[stage] = true;
         last_phase[stage] = phase;
         if (++stage == STAGES) {
@@ -844,7 +853,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
 #pragma unroll
           for (int m = 0; m < MSUB; ++m)
             umma_f16(tmem_base + (uint32_t)(m * BN), umma_desc_sw128(sa + m * A_SUB + kk * 32, 16, 1024),
-                     umma_desc_sw128(sb + kk * 32, 16, 1024), a.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                     B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024) : umma_desc_sw128(sb + kk * 32, 16, 1024),
+                     a.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
         umma_commit(smem_u32(&empty_bar[stage]));
         if (++stage == STAGES) {
           stage = 0;
@@ -992,9 +1002,9 @@ int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_pair_kernel launch");
 }
 
-template <int BN, int STAGES, int MSUB>
+template <int BN, int STAGES, int MSUB, bool B_MN = false>
 int launch_row_cluster(UmmaArgs &args, cudaStream_t s) {
-  auto kern = umma_row_cluster_kernel<BN, STAGES, MSUB>;
+  auto kern = umma_row_cluster_kernel<BN, STAGES, MSUB, B_MN>;
   constexpr int smem = STAGES * (MSUB * BM * BK * 2 + BN * BK * 2) + 1024;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -1093,7 +1103,7 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     // Rank clusters (one CTA per rank of a 128 x 256 tile) when one CTA per
     // 128 x 128 tile would leave SMs idle; costs in cycles, measured rates.
     const int sms0 = sm_count();
-    if (pair_policy_allowed() && !summa) {
+    if (pair_policy_allowed() && !p.a_mn) {
       // Every job (one per output block: several for a reduce-scatter) must
       // have the same rank count and every part the same K.
       const int N = p.jobs[0].nparts;
@@ -1285,6 +1295,10 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     rc = launch_pair<192, false, 5, 1, 2, true>(args, sms, s);
   else if (p.gated)
     rc = launch_pair<256, false, 4, 1, 2, true>(args, sms, s);
+  else if (rowclu && msub == 2 && summa)
+    rc = launch_row_cluster<256, 3, 2, true>(args, s);
+  else if (rowclu && summa)
+    rc = launch_row_cluster<256, 4, 1, true>(args, s);
   else if (rowclu && msub == 2)
     rc = launch_row_cluster<256, 3, 2>(args, s);
   else if (rowclu)
