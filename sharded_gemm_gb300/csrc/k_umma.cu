@@ -141,27 +141,27 @@ __device__ __forceinline__ void store_row_chunk(const UmmaArgs &a, const UJob &J
 }
 
 // TMA-store epilogue: a warp's 32 x 32 float32 chunk (lane l holds row
-// row0 + l) goes to one of the warp's two 4 KB staging buffers in the 128-byte
+// row0 + l) goes to the warp's 4 KB staging buffer in the 128-byte
 // swizzled layout of the output map (row r's 16-byte piece j at position
 // j ^ (r % 8): each group of 8 lanes covers all 32 banks), and lane 0 issues
 // the tile store.
-constexpr int kTsWarpBytes = 2 * 4096;
+constexpr int kTsWarpBytes = 4096;
 __device__ __forceinline__ void tstore_chunk(const UmmaArgs &a, const UJob &J, int job, int row0, int col0,
                                              float (&v)[32], uint32_t bufs, int &cnt, int lane) {
   // A chunk wholly outside the output (ragged last tile) is skipped outright:
-  // it neither stores nor takes a staging buffer, so a buffer is only ever
-  // rewritten after the store issued from it two stores earlier has read it.
+  // it neither stores nor writes the staging buffer, which is rewritten only
+  // after the store issued from it has read it.
   if (row0 >= J.rowsA || col0 >= J.rowsB) return;
   if (J.bias) {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (col0 + i < J.rowsB) v[i] += __ldg(J.bias + col0 + i);
   }
-  if (cnt >= 2) {
-    if (lane == 0) bulk_wait_group_read<1>();
+  if (cnt >= 1) {  // the previous store has read the buffer
+    if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
-  const uint32_t buf = bufs + (uint32_t)((cnt & 1) * 4096);
+  const uint32_t buf = bufs;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint32_t dst = buf + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) * 16));
@@ -1304,11 +1304,11 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   else if (rowclu)
     rc = launch_row_cluster<256, 4, 1>(args, s);
   else if (pair && summa && p.a_mn && tstore)
-    rc = launch_pair<256, true, 5, 2, 1, false, true, true>(args, sms, s);
+    rc = launch_pair<256, true, 6, 2, 1, false, true, true>(args, sms, s);
   else if (pair && summa && p.a_mn)
     rc = launch_pair<256, true, 6, 2, 1, false, true>(args, sms, s);
   else if (pair && summa)
-    rc = launch_pair<256, true, 6, 2, 1>(args, sms, s);
+    rc = launch_pair<256, true, 7, 2, 1>(args, sms, s);
   else if (pair && nsub == 2 && BN == 160)
     rc = launch_pair<160, false, 6, 1, 2>(args, sms, s);
   else if (pair && nsub == 2 && BN == 192)
