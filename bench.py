@@ -61,19 +61,37 @@ def load_peaks() -> dict:
 # --warmup 3 --no-cpu-baseline` (the summary is in profiles/dram_traffic_by_config.md).
 # It is reported only while the kernel sources hash to TRAFFIC_SOURCES, since a
 # changed kernel needs a new capture.
-TRAFFIC_SOURCES = "6879dfb0ad67fe3e"
+TRAFFIC_SOURCES = "2113f9c28be08f97"
 TRAFFIC = {
-    ("mlp", "tp_all_to_sharded"): 97898240, ("mlp", "tp_sharded_to_all"): 102631424,
-    ("summa2", "tp_summa"): 1531145984, ("summa4", "tp_summa"): 1342970624,
-    ("qkv1", "tp_all_to_sharded(qkv)"): 103917568, ("qkv1", "tp_sharded_to_all(o)"): 33609984,
-    ("qkv1", "tp_all_to_sharded(lm_head)"): 412302592,
-    ("qkv16", "tp_all_to_sharded(qkv)"): 103808256, ("qkv16", "tp_sharded_to_all(o)"): 33728512,
-    ("qkv16", "tp_all_to_sharded(lm_head)"): 414408960,
-    ("qkv2048", "tp_all_to_sharded(qkv)"): 151419392, ("qkv2048", "tp_sharded_to_all(o)"): 51041280,
-    ("qkv2048", "tp_all_to_sharded(lm_head)"): 929753856,
-    ("q4_1", "tp_q4_all_to_sharded"): 135372032, ("q4_1", "tp_q4_sharded_to_all"): 132407552,
-    ("q4_16", "tp_q4_all_to_sharded"): 136930304, ("q4_16", "tp_q4_sharded_to_all"): 134341632,
-    ("q4_256", "tp_q4_all_to_sharded"): 141455872, ("q4_256", "tp_q4_sharded_to_all"): 215676672,
+    ("mlp", "tp_all_to_sharded"): 97733376,
+    ("mlp", "tp_sharded_to_all"): 102651904,
+    ("mlp_ag_rs", "tp_gathered_to_sharded"): 98006528,
+    ("mlp_ag_rs", "tp_sharded_to_sharded"): 102726144,
+    ("ffn_gated", "tp_gated_all_to_sharded"): 193692416,
+    ("ffn_gated", "tp_sharded_to_all"): 102894080,
+    ("summa2", "tp_summa"): 1535408640,
+    ("summa4", "tp_summa"): 1343912448,
+    ("qkv1", "tp_all_to_sharded(qkv)"): 103909888,
+    ("qkv1", "tp_sharded_to_all(o)"): 33606912,
+    ("qkv1", "tp_all_to_sharded(lm_head)"): 412300288,
+    ("qkv16", "tp_all_to_sharded(qkv)"): 104377600,
+    ("qkv16", "tp_sharded_to_all(o)"): 33729792,
+    ("qkv16", "tp_all_to_sharded(lm_head)"): 414397440,
+    ("qkv2048", "tp_all_to_sharded(qkv)"): 151568640,
+    ("qkv2048", "tp_sharded_to_all(o)"): 51130368,
+    ("qkv2048", "tp_all_to_sharded(lm_head)"): 929835264,
+    ("q4_1", "tp_q4_all_to_sharded"): 135430912,
+    ("q4_1", "tp_q4_sharded_to_all"): 132484352,
+    ("q4_16", "tp_q4_all_to_sharded"): 136994560,
+    ("q4_16", "tp_q4_sharded_to_all"): 134219008,
+    ("q4_256", "tp_q4_all_to_sharded"): 141797120,
+    ("q4_256", "tp_q4_sharded_to_all"): 212517120,
+    ("mlp_bwd", "tp_sharded_dw(w1)"): 135343616,
+    ("mlp_bwd", "tp_bias_grad(b1)"): 11291904,
+    ("mlp_bwd", "tp_sharded_to_all_dx"): 95180288,
+    ("mlp_bwd", "tp_sharded_dw(w2)"): 131258112,
+    ("mlp_bwd", "tp_bias_grad(b2)"): 4212480,
+    ("mlp_bwd", "tp_all_to_sharded_dx"): 101732096,
 }
 
 
