@@ -35,7 +35,10 @@ Everything here is the plain definition, computed in float64:
   accumulated in step order;
 * the 4-bit affine quantized weight (same MLX page, section 2.3: group_size 64,
   bits 4, mode "affine") dequantizes to ``s[o, g] * q[o, k] + b[o, g]`` with
-  ``g = k // group_size``.
+  ``g = k // group_size``;
+* the "mxfp8" mode of the same section (no per-group biases) is the OCP
+  microscaling FP8 format: E4M3 codes, one power-of-two E8M0 scale per 32
+  consecutive elements; ``W_hat[o, k] = e4m3(q[o, k]) * 2^(s[o, k // 32] - 127)``.
 
 The matrix products run in the naive C loops of ``oracle.c`` (pinned against
 ``numpy.matmul`` by the tests); slicing and sums use numpy directly.
@@ -48,7 +51,9 @@ gradient, integer bias-gradient sums, SiLU closed forms, the gated
 sharded == unsharded invariant, the all-gather / reduce-scatter transpose
 identity, the sharded == unsharded invariant of both collective
 variants, the dequant identity on brute-force and constant-code inputs, the
-quantizer round-trip bound, and the worked-example shapes from the MLX page.
+quantizer round-trip bound, the E4M3 value table's closed forms, its rounding at every
+midpoint and the MXFP8 scale choice, error bound and exact grid, and the worked-example shapes
+from the MLX page.
 """
 from __future__ import annotations
 
@@ -464,3 +469,92 @@ def q4_sharded_to_all(x_shards, packed_shards, scale_shards, bias_q_shards, grou
     w = [dequant_affine4(p, s, bq, group_size)
          for p, s, bq in zip(packed_shards, scale_shards, bias_q_shards)]
     return sharded_to_all(x_shards, w, b)
+
+
+# ---------------------------------------------------------------- mxfp8
+# The MLX guide (section 2.3, and the distributed tests of section 4) names a
+# second quantization mode, "mxfp8", passed through sharding like the affine
+# one and with no per-group biases.  Its format is the microscaling FP8 of the
+# OCP MX specification: blocks of 32 consecutive input elements share one
+# power-of-two scale stored as an 8-bit exponent (E8M0, value 2^(s - 127)),
+# and each element is an FP8 E4M3 number (1 sign, 4 exponent bits with bias 7,
+# 3 mantissa bits; exponent field 0 is subnormal; 0x7F / 0xFF are NaN, so the
+# largest finite magnitude is 448).  The quantized matmul keeps x in its own
+# type and multiplies by the dequantized weight.
+MX_GROUP = 32
+MX_EMAX_ELEM = 8  # exponent of the largest E4M3 normal (448 = 1.75 * 2^8)
+
+
+def e4m3_value(byte: int) -> float:
+    """Value of one E4M3 code from the format's definition (NaN for 0x7F, 0xFF)."""
+    s = -1.0 if byte & 0x80 else 1.0
+    e = (byte >> 3) & 0xF
+    m = byte & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * m * 2.0 ** -9          # subnormal: m/8 * 2^(1-7)
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([e4m3_value(b) for b in range(256)], dtype=np.float64)
+
+
+def e4m3_from_f64(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest finite E4M3 code, ties to the even code (even
+    mantissa), magnitudes above 448 saturating to 448, the sign kept (a
+    negative value that rounds to zero gives -0, 0x80).  Written as a search
+    over the 127 non-negative finite codes 0x00..0x7E (their values ascend
+    with the code), so it follows the definition directly."""
+    v = np.asarray(v, dtype=np.float64)
+    mag = np.minimum(np.abs(v), 448.0)
+    pos = E4M3_TABLE[:0x7F]                                  # codes 0..126, ascending
+    hi = np.searchsorted(pos, mag, side="left")             # first code with value >= mag
+    hi = np.minimum(hi, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = mag - pos[lo]
+    d_hi = pos[hi] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    # the sign is kept, also when the magnitude rounds to zero (-0 is 0x80)
+    sign = np.signbit(v).astype(np.uint8) << 7
+    return (code | sign).astype(np.uint8)
+
+
+def quantize_mxfp8(w: np.ndarray):
+    """MXFP8 quantization of a float32 weight (rows, K), per row in blocks of
+    32 consecutive input elements (OCP MX conversion):
+      X = floor(log2(max |w| of the block)) - 8, clamped to [-127, 127]
+      (X = -127 for an all-zero block); scale byte = X + 127;
+      code = E4M3 round-to-nearest-even, saturating, of w / 2^X.
+    Returns (codes uint8 (rows, K), scales uint8 (rows, K/32))."""
+    w = np.asarray(w, dtype=np.float32)
+    rows, k = w.shape
+    if k % MX_GROUP:
+        raise ValueError("K must be a multiple of 32")
+    g = w.reshape(rows, k // MX_GROUP, MX_GROUP).astype(np.float64)
+    amax = np.abs(g).max(axis=2)
+    _, ex = np.frexp(amax)                 # amax = f * 2^ex, f in [0.5, 1)
+    X = np.where(amax > 0, ex - 1 - MX_EMAX_ELEM, -127)
+    X = np.clip(X, -127, 127)
+    codes = e4m3_from_f64(g / np.ldexp(1.0, X)[:, :, None])
+    return codes.reshape(rows, k), (X + 127).astype(np.uint8)
+
+
+def dequant_mxfp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """W_hat[o, k] = e4m3(code[o, k]) * 2^(scale[o, k // 32] - 127) in float64."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    k = codes.shape[1]
+    gi = np.arange(k) // MX_GROUP
+    return E4M3_TABLE[codes] * np.ldexp(1.0, scales.astype(np.int64) - 127)[:, gi]
+
+
+def mx_all_to_sharded(x, code_shards, scale_shards, b_shards=None):
+    """MXFP8 column-parallel linear: rank r computes x @ W_hat_r.T (+ b_r)."""
+    return all_to_sharded(x, [dequant_mxfp8(c, s) for c, s in zip(code_shards, scale_shards)], b_shards)
+
+
+def mx_sharded_to_all(x_shards, code_shards, scale_shards, b=None):
+    """MXFP8 row-parallel linear: sum_r x_r @ W_hat_r.T in rank order (+ b)."""
+    return sharded_to_all(x_shards, [dequant_mxfp8(c, s) for c, s in zip(code_shards, scale_shards)], b)

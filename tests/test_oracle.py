@@ -675,6 +675,96 @@ def test_q4_row_equals_dequant_unsharded():
     assert np.abs(y - ref).max() <= 1e-12 * (1 + np.abs(ref).max())
 
 
+# ------------------------------------------------------------------ mxfp8
+def check_e4m3_table(table):
+    # closed forms of the E4M3 definition (bias 7, 3 mantissa bits)
+    assert table[0x38] == 1.0 and table[0x7E] == 448.0
+    assert table[0x01] == 2.0 ** -9 and table[0x07] == 7 * 2.0 ** -9   # subnormals
+    assert table[0x08] == 2.0 ** -6                                       # smallest normal
+    assert table[0x3C] == 1.5 and table[0x44] == 3.0 and table[0x30] == 0.5
+    assert np.isnan(table[0x7F]) and np.isnan(table[0xFF])
+    assert table[0x00] == 0.0 and table[0x80] == 0.0 and np.signbit(table[0x80])
+    pos = table[:0x7F]
+    assert np.all(np.diff(pos) > 0)                                       # ascending, distinct
+    assert np.array_equal(table[0x80:0xFF], -pos)                         # sign mirror
+
+
+def check_e4m3_rounding(conv, table):
+    pos = table[:0x7F]
+    codes = np.arange(0x7F)
+    assert np.array_equal(conv(pos), codes)                 # representable values are exact
+    assert np.array_equal(conv(-pos[1:]), codes[1:] | 0x80)
+    mid = (pos[:-1] + pos[1:]) / 2                           # ties go to the even code
+    even = np.where(codes[:-1] % 2 == 0, codes[:-1], codes[1:])
+    assert np.array_equal(conv(mid), even)
+    eps = (pos[1:] - pos[:-1]) / 1024
+    assert np.array_equal(conv(mid - eps), codes[:-1])
+    assert np.array_equal(conv(mid + eps), codes[1:])
+    assert list(conv(np.array([449.0, 1e9, -500.0]))) == [0x7E, 0x7E, 0xFE]  # saturation
+    assert list(conv(np.array([2.0 ** -11, -2.0 ** -11]))) == [0x00, 0x80]    # to zero, sign kept
+
+
+def check_mx_quantize(quantize, dequant):
+    rng = np.random.default_rng(7)
+    w = (rng.standard_normal((6, 128)) * np.array([1e-3, 0.02, 1.0, 30.0, 5e3, 1e-30])[:, None]).astype(np.float32)
+    w[0, :32] = 0.0                                          # all-zero block
+    codes, scales = quantize(w)
+    assert codes.shape == (6, 128) and scales.shape == (6, 4)
+    assert scales[0, 0] == 0 and not codes[0, :32].any()
+    X = scales.astype(np.int64) - 127
+    amax = np.abs(w.astype(np.float64)).reshape(6, 4, 32).max(axis=2)
+    nz = (amax > 0) & (X > -127)
+    # the block maximum lands in E4M3's top binade: 2^(X+8) <= amax < 2^(X+9)
+    assert np.all(np.ldexp(1.0, X + 8)[nz] <= amax[nz]) and np.all(amax[nz] < np.ldexp(1.0, X + 9)[nz])
+    wh = dequant(codes, scales)
+    err = np.abs(wh - w.astype(np.float64))
+    bound = np.maximum(np.abs(w) * 2.0 ** -4, np.ldexp(1.0, X - 10).repeat(32, axis=1))
+    assert np.all(err <= bound)
+    # exact grid: values that are E4M3 numbers times 2^X come back unchanged
+    grid = (rng.integers(0, 0x7F, (2, 64)) | (rng.integers(0, 2, (2, 64)) << 7)).astype(np.uint8)
+    grid[:, ::32] = 0x78                                     # 256 = 2^8 sets X = 0 in each block
+    g = oracle.E4M3_TABLE[grid].astype(np.float32) * np.float32(2.0 ** -5)
+    c2, s2 = quantize(g)
+    assert np.all(s2 == 127 - 5)
+    assert np.array_equal(dequant(c2, s2), g.astype(np.float64))
+
+
+def test_e4m3_table():
+    check_e4m3_table(oracle.E4M3_TABLE)
+
+
+def test_e4m3_rounding():
+    check_e4m3_rounding(oracle.e4m3_from_f64, oracle.E4M3_TABLE)
+
+
+def test_mx_quantize():
+    check_mx_quantize(oracle.quantize_mxfp8, oracle.dequant_mxfp8)
+
+
+def test_mx_dequant_bruteforce():
+    codes = np.array([[0x38, 0xB8, 0x01, 0x7E] * 8], dtype=np.uint8)
+    scales = np.array([[127 + 3]], dtype=np.uint8)
+    expect = np.array([[8.0, -8.0, 2.0 ** -6, 448.0 * 8] * 8])
+    assert np.array_equal(oracle.dequant_mxfp8(codes, scales), expect)
+
+
+def test_mx_layers_equal_unsharded():
+    rng = np.random.default_rng(11)
+    T, K, O, N = 3, 256, 16, 4
+    x = rng.standard_normal((T, K))
+    w = (rng.standard_normal((O, K)) * 0.02).astype(np.float32)
+    codes, scales = oracle.quantize_mxfp8(w)
+    wh = oracle.dequant_mxfp8(codes, scales)
+    b = rng.standard_normal(O)
+    ys = oracle.mx_all_to_sharded(x, oracle.shard(codes, 0, 1, N), oracle.shard(scales, 0, 1, N),
+                                  oracle.shard(b, 0, 1, N))
+    full = np.matmul(x, wh.T) + b
+    assert np.abs(np.concatenate(ys, axis=1) - full).max() <= 1e-12 * (1 + np.abs(full).max())
+    y = oracle.mx_sharded_to_all(oracle.shard(x, -1, 1, N), oracle.shard(codes, -1, 1, N),
+                                 oracle.shard(scales, -1, 1, N), b)
+    assert np.abs(y - full).max() <= 1e-12 * (1 + np.abs(full).max())
+
+
 def test_bf16_widen_exact():
     bits = np.array([0x3F80, 0xBF80, 0x4049, 0x0000, 0x7F7F], dtype=np.uint16)
     want = [1.0, -1.0, 3.140625, 0.0, 3.3895313892515355e38]

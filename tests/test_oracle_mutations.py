@@ -170,3 +170,39 @@ def test_mutation_atb_wrong_block():
     def bad(Ab, Bb, q):
         return oracle.summa_atb([Ab[(b % q) * q + b // q] for b in range(q * q)], Bb, q)
     _expect_fail(T.check_summa_backward, oracle.summa_abt, bad)
+
+
+def test_mutation_e4m3_wrong_bias():
+    bad = np.array([oracle.e4m3_value(b) * 0.5 for b in range(256)])
+    _expect_fail(T.check_e4m3_table, bad)
+
+
+def test_mutation_e4m3_ties_away():
+    def bad(v):
+        v = np.asarray(v, dtype=np.float64)
+        out = oracle.e4m3_from_f64(v)
+        pos = oracle.E4M3_TABLE[:0x7F]
+        mid = (pos[:-1] + pos[1:]) / 2
+        hit = np.isin(np.abs(v), mid)
+        return np.where(hit, np.searchsorted(pos, np.abs(v)) | (np.signbit(v) << 7), out).astype(np.uint8)
+    _expect_fail(T.check_e4m3_rounding, bad, oracle.E4M3_TABLE)
+
+
+def test_mutation_mx_scale_off_by_one():
+    # X = floor(log2 amax) - 7: the block maximum lands one binade low
+    def bad(w):
+        w = np.asarray(w, dtype=np.float32)
+        _, s = oracle.quantize_mxfp8(w)
+        s = np.where(s > 0, s + 1, s).astype(np.uint8)
+        X = s.astype(np.int64) - 127
+        g = w.astype(np.float64) / np.ldexp(1.0, X).repeat(32, axis=1)
+        return oracle.e4m3_from_f64(g), s
+    _expect_fail(T.check_mx_quantize, bad, oracle.dequant_mxfp8)
+
+
+def test_mutation_mx_dequant_group_64():
+    def bad(codes, scales):
+        k = codes.shape[1]
+        gi = np.arange(k) // 64
+        return oracle.E4M3_TABLE[codes] * np.ldexp(1.0, scales.astype(np.int64) - 127)[:, gi]
+    _expect_fail(T.check_mx_quantize, oracle.quantize_mxfp8, bad)
