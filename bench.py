@@ -8,11 +8,12 @@ logical shards, x (512, 4096) bf16, W1 (11008, 4096), W2 (4096, 11008); one
 step = the column-parallel GEMM (x @ W1_r^T for r = 0..3, bf16 intermediate
 kept sharded) followed by the row-parallel GEMM (sum of the 4 partials in rank
 order, + bias, float32 output), both through the C ABI.  Other configs
-(mlp_ag_rs, ffn_gated, mlp_bwd, summa2, summa4, qkv1, qkv16, qkv2048, q4_1, q4_16, q4_256)
+(mlp_ag_rs, ffn_gated, mlp_bwd, mx_1, summa2, summa4, qkv1, qkv16, qkv2048, q4_1, q4_16, q4_256)
 time the other workloads the same way; ffn_gated is the Llama FFN (gate and up
 projections in one gated column-parallel launch, then the row-parallel down
 projection); mlp_bwd is the MLP pair's backward step (input, weight and bias
-gradients of both layers); mlp_ag_rs is the MLP pair with its input and output
+gradients of both layers); mx_T is the 4-bit pair's shapes with MXFP8 weights (E4M3 codes,
+a power-of-two scale per 32 weights); mlp_ag_rs is the MLP pair with its input and output
 sharded along the model width (an all-gather of the input's column shards
 into W1, a reduce-scatter of W2's partial sums).
 
@@ -202,7 +203,8 @@ class ClockSampler:
 def make_workload(name: str, rank: int, device: str):
     """Returns (obj, step_fn, info) for a config name."""
     from sharded_gemm_gb300 import synth
-    from sharded_gemm_gb300.workloads import GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa
+    from sharded_gemm_gb300.workloads import (GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, MXPair, Q4Pair,
+                                              QKV, Summa)
     seed = synth.SEED + rank
     if name == "mlp":
         cfg = synth.mlp(seed=seed)
@@ -283,6 +285,19 @@ def make_workload(name: str, rank: int, device: str):
                     kernel_work=[per, per] if decode else [2.0 * T * D * F] * 2, launches_per_step=2,
                     h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
+    if name.startswith("mx_"):
+        T = int(name[3:])
+        cfg = synth.q4(seed=seed, T=T)
+        w = MXPair(cfg, device=device)
+        D, F = cfg["D"], cfg["F"]
+        decode = T <= 16
+        per = D * F * (1.0 + 1.0 / 32)
+        info = dict(workload="mxfp8_pair_T%d" % T, unit="GB/s" if decode else "TFLOP/s",
+                    work=(w.weight_bytes if decode else w.flops), bound="hbm" if decode else "tensor",
+                    kernel_names=["tp_mx_all_to_sharded", "tp_mx_sharded_to_all"],
+                    kernel_work=[per, per] if decode else [2.0 * T * D * F] * 2, launches_per_step=2,
+                    h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
+        return w, w.step, info
     raise SystemExit("unknown config %s" % name)
 
 
@@ -309,6 +324,9 @@ def split_step(name: str, w):
     if name.startswith("q4_"):
         return [lambda s: tp.tp_q4_all_to_sharded(w.x, *w.up, out=w.mid, stream=s),
                 lambda s: tp.tp_q4_sharded_to_all(w.mid, *w.down, out=w.y, stream=s)]
+    if name.startswith("mx_"):
+        return [lambda s: tp.tp_mx_all_to_sharded(w.x, *w.up, out=w.mid, stream=s),
+                lambda s: tp.tp_mx_sharded_to_all(w.mid, *w.down, out=w.y, stream=s)]
     raise SystemExit(name)
 
 

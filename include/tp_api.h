@@ -273,6 +273,41 @@ int tp_summa(int q, const void *const *X, const void *const *A, void *const *Y, 
              int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream);
 
 /*
+ * f4 -- the "mxfp8" quantization mode of the sharded linears (MLX tensor
+ * parallelism guide, section 2.3: mode "mxfp8" is passed through sharding
+ * like "affine" and has no per-group biases; section 4's tests check that
+ * it propagates).  Format (OCP microscaling FP8): E4M3 codes, one byte per
+ * weight (1 sign, 4 exponent bits with bias 7, 3 mantissa bits), and one
+ * E8M0 scale byte per 32 consecutive weights of a row, value 2^(s - 127):
+ *   W_hat[o][k] = e4m3(codes[o][k]) * 2^(scales[o][k / 32] - 127).
+ *
+ * tp_mx_quantize: w (rows, K) float32 -> codes uint8 (rows, K) and scales
+ *   uint8 (rows, K/32).  Per block: X = floor(log2(max |w|)) - 8 clamped to
+ *   [-127, 127] (-127 for an all-zero block), scale byte X + 127, code = E4M3
+ *   of w * 2^-X rounded to nearest even, saturated to +-448, sign kept.
+ *   Errors: TP_ERR_NOT_DIVISIBLE if K % 32 != 0.
+ * tp_mx_all_to_sharded: y[r] = x @ W_hat_r^T + bias[r]; x (T, K) bf16
+ *   contiguous; codes[r] (O/N, K), scales[r] (O/N, K/32) (the rows of shard
+ *   r); bias NULL or N float32 (O/N); y[r] (T, O/N) out_dt, row stride ldy.
+ * tp_mx_sharded_to_all: y = sum over r ascending of x[r] @ W_hat_r^T, then
+ *   bias once; x[r] (T, K/N) bf16 contiguous; codes[r] (O, K/N), scales[r]
+ *   (O, K/(32 N)) (split on the last axis, whole blocks per shard); y (T, O).
+ * x is used as given (bf16); every product x * e4m3 is exact in float32 and
+ * the sums are float32.  Errors as the 4-bit linears: TP_ERR_NOT_DIVISIBLE
+ * if O % N (all-to-sharded), K % N or (K/N) % 32 (sharded-to-all) or K % 32
+ * is not zero.  T = 0 launches nothing.
+ */
+int tp_mx_quantize(const float *w, int64_t rows, int64_t K, uint8_t *codes, uint8_t *scales,
+                   tp_stream_t stream);
+int tp_mx_all_to_sharded(int N, const void *x, int64_t T, int64_t K, const uint8_t *const *codes,
+                         const uint8_t *const *scales, int64_t O, const void *const *bias,
+                         void *const *y, int64_t ldy, tp_dtype out_dt, tp_stream_t stream);
+int tp_mx_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K,
+                         const uint8_t *const *codes, const uint8_t *const *scales, int64_t O,
+                         const void *bias, void *y, int64_t ldy, tp_dtype out_dt,
+                         tp_stream_t stream);
+
+/*
  * f3 -- SUMMA with the layer's bias, and the two backward products of the 2-D
  * layer ("ColossalAI 2D tensor parallel via SUMMA", source-level section: in
  * backward the input gradient goes through Matmul_ABT_2D (A B^T) and the

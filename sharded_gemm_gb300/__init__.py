@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
             "tp_sharded_to_all_dx": ([i32, vp, i64, i64, i64, vpp, i64, i32, vpp, i64, i32, vp], i32),
             "tp_sharded_dw": ([i32, vpp, i64, vpp, i64, i64, i64, i64, i32, vpp, i64, i32, vp], i32),
             "tp_bias_grad": ([i32, i32, vpp, i64, i64, i64, i32, vpp, vp], i32),
+            "tp_mx_quantize": ([vp, i64, i64, vp, vp, vp], i32),
+            "tp_mx_all_to_sharded": ([i32, vp, i64, i64, vpp, vpp, i64, vpp, vpp, i64, i32, vp], i32),
+            "tp_mx_sharded_to_all": ([i32, vpp, i64, i64, vpp, vpp, i64, vp, vp, i64, i32, vp], i32),
             "tp_q4_quantize": ([vp, i64, i64, i32, vp, vp, vp, vp], i32),
             "tp_q4_all_to_sharded": ([i32, vp, i64, i64, vpp, vpp, vpp, i32, i64, vpp, vpp, i64, i32, vp], i32),
             "tp_q4_sharded_to_all": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
@@ -614,4 +617,66 @@ def tp_bias_grad(dy, nin: int = 1, out=None, stream=None):
     dp, k1 = _ptrs(dy)
     op, k2 = _ptrs(out)
     _check(lib().tp_bias_grad(nout, nin, dp, rows, cols, _common_ld(dy, "dy"), _dt(dy[0]), op, _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ mxfp8 (f4)
+def tp_mx_quantize(w, stream=None):
+    """MXFP8-quantize a float32 (rows, K) CUDA tensor: returns (codes uint8
+    (rows, K), scales uint8 (rows, K/32))."""
+    torch = _torch()
+    _contig(w, "w")
+    if w.dtype != torch.float32:
+        raise TypeError("w must be float32")
+    rows, K = w.shape
+    codes = torch.empty((rows, K), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((rows, K // 32), dtype=torch.uint8, device=w.device)
+    _check(lib().tp_mx_quantize(w.data_ptr(), rows, K, codes.data_ptr(), scales.data_ptr(), _stream(stream)))
+    return codes, scales
+
+
+def tp_mx_all_to_sharded(x, codes, scales, bias=None, out=None, out_dtype=None, stream=None):
+    """y[r] = x @ W_hat_r.T (+ bias[r]) with MXFP8 weight shards; returns y list."""
+    torch = _torch()
+    _contig(x, "x")
+    N = len(codes)
+    T, K = x.shape
+    On = codes[0].shape[0]
+    for i, t in enumerate(list(codes) + list(scales)):
+        _contig(t, "weight %d" % i)
+    if out is None:
+        out = [torch.empty((T, On), dtype=out_dtype or x.dtype, device=x.device) for _ in range(N)]
+    for i, t in enumerate(out):
+        _rowmajor(t, "out[%d]" % i)
+    cp, k1 = _ptrs(codes)
+    sp, k2 = _ptrs(scales)
+    yp, k3 = _ptrs(out)
+    bp, k4 = (None, None)
+    if bias is not None:
+        for i, t in enumerate(bias):
+            _contig(t, "bias[%d]" % i)
+        bp, k4 = _ptrs(bias)
+    _check(lib().tp_mx_all_to_sharded(N, x.data_ptr(), T, K, cp, sp, On * N, bp, yp, _common_ld(out, "out"),
+                                      _dt(out[0]), _stream(stream)))
+    return out
+
+
+def tp_mx_sharded_to_all(x, codes, scales, bias=None, out=None, out_dtype=None, stream=None):
+    """y = sum_r x[r] @ W_hat_r.T (ascending r) (+ bias) with MXFP8 weight shards."""
+    torch = _torch()
+    N = len(x)
+    for i, t in enumerate(list(x) + list(codes) + list(scales)):
+        _contig(t, "operand %d" % i)
+    T, Kn = x[0].shape
+    O = codes[0].shape[0]
+    if out is None:
+        out = torch.empty((T, O), dtype=out_dtype or torch.float32, device=x[0].device)
+    _rowmajor(out, "out")
+    if bias is not None:
+        _contig(bias, "bias")
+    xp, k1 = _ptrs(x)
+    cp, k2 = _ptrs(codes)
+    sp, k3 = _ptrs(scales)
+    _check(lib().tp_mx_sharded_to_all(N, xp, T, Kn * N, cp, sp, O, None if bias is None else bias.data_ptr(),
+                                      out.data_ptr(), out.stride(0) if T > 1 else O, _dt(out), _stream(stream)))
     return out

@@ -9,6 +9,7 @@
 // accumulator for the up projection and store silu(gate) * up.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "tp_internal.h"
 
@@ -26,6 +27,12 @@ template <int DT, int BL>
 __device__ __forceinline__ float load_b(const Part &pt, int64_t n, int64_t k) {
   if (BL == BL_KMAJOR) return load_elem<DT>(pt.B, n * pt.ldb + k);
   if (BL == BL_MNMAJOR) return load_elem<DT>(pt.B, k * pt.ldb + n);
+  if (BL == BL_MX) {  // E4M3 code times the block's power-of-two scale, both exact
+    const uint8_t code = static_cast<const uint8_t *>(pt.B)[n * pt.ldb + k];
+    const uint32_t sb = static_cast<const uint8_t *>(pt.scales)[n * (pt.K >> 5) + (k >> 5)];
+    const float c = __half2float(__half(__nv_cvt_fp8_to_halfraw(code, __NV_E4M3)));
+    return c * (sb ? __uint_as_float(sb << 23) : __uint_as_float(0x00400000u));
+  }
   // BL_Q4: ldb = words per row; scales / qbias have K/64 entries per row.
   const uint32_t word = static_cast<const uint32_t *>(pt.B)[n * pt.ldb + (k >> 3)];
   const float code = (float)((word >> (4 * (k & 7))) & 15u);
@@ -157,6 +164,7 @@ int launch_simt(const Problem &p, cudaStream_t s) {
   TP_SIMT_CASE(TP_BF16, BL_MNMAJOR)
   TP_SIMT_CASE(TP_F16, BL_MNMAJOR)
   TP_SIMT_CASE(TP_BF16, BL_Q4)
+  TP_SIMT_CASE(TP_BF16, BL_MX)
 #undef TP_SIMT_CASE
   return set_error(TP_ERR_UNSUPPORTED, "no CUDA-core kernel for dtype %d / layout %d", p.in_dt,
                    p.b_layout);

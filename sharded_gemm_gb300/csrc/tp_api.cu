@@ -69,7 +69,9 @@ static int dispatch(Problem &p, cudaStream_t s) {
   p.wait_ns = wait_limit_ns();
   bool handled = false;
   if (g_policy.load() != TP_POLICY_SIMT) {
-    int rc = p.b_layout == BL_Q4 ? launch_q4(p, s, &handled) : launch_umma(p, s, &handled);
+    int rc = p.b_layout == BL_Q4   ? launch_q4(p, s, &handled)
+             : p.b_layout == BL_MX ? launch_mx(p, s, &handled)
+                                   : launch_umma(p, s, &handled);
     if (rc != TP_OK || handled) return rc;
   }
   return launch_simt(p, s);
@@ -565,6 +567,90 @@ int tp_summa_abt(int q, const void *const *A, const void *const *B, void *const 
 int tp_summa_atb(int q, const void *const *A, const void *const *B, void *const *C, int64_t M,
                  int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream) {
   return summa_lower(2, q, A, B, nullptr, C, M, K, Ncols, in_dt, stream);
+}
+
+static int mx_check_common(int64_t T, int64_t K, int64_t O, tp_dtype out_dt) {
+  if (!valid_dt(out_dt)) return set_error(TP_ERR_INVALID_ARG, "bad dtype");
+  if (T < 0 || K < 1 || O < 1) return set_error(TP_ERR_INVALID_ARG, "need T >= 0, K >= 1, O >= 1");
+  return TP_OK;
+}
+
+int tp_mx_quantize(const float *w, int64_t rows, int64_t K, uint8_t *codes, uint8_t *scales,
+                   tp_stream_t stream) {
+  if (!w || !codes || !scales) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (rows < 1 || K < 1) return set_error(TP_ERR_INVALID_ARG, "rows and K must be >= 1");
+  if (K % 32) return set_error(TP_ERR_NOT_DIVISIBLE, "K (%lld) not a multiple of 32", (long long)K);
+  if (!aligned(w, 4)) return set_error(TP_ERR_ALIGNMENT, "w not aligned to its element size");
+  return launch_mx_quantize(w, rows, K, codes, scales, (cudaStream_t)stream);
+}
+
+int tp_mx_all_to_sharded(int N, const void *x, int64_t T, int64_t K, const uint8_t *const *codes,
+                         const uint8_t *const *scales, int64_t O, const void *const *bias, void *const *y,
+                         int64_t ldy, tp_dtype out_dt, tp_stream_t stream) {
+  if (N < 1 || N > kMaxShards) return set_error(TP_ERR_INVALID_ARG, "N must be in 1..%d", kMaxShards);
+  int rc = mx_check_common(T, K, O, out_dt);
+  if (rc) return rc;
+  if (O % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the output of size %lld across %d devices.",
+                     (long long)O, N);
+  if (K % 32) return set_error(TP_ERR_NOT_DIVISIBLE, "K (%lld) not a multiple of 32", (long long)K);
+  const int64_t On = O / N;
+  if (!x || !codes || !scales || !y) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (ldy < On) return set_error(TP_ERR_INVALID_ARG, "ldy < O/N");
+  const int oe = elem_size(out_dt);
+  if (!aligned(x, 2)) return set_error(TP_ERR_ALIGNMENT, "x not aligned");
+  for (int r = 0; r < N; ++r) {
+    if (!codes[r] || !scales[r] || !y[r] || (bias && !bias[r]))
+      return set_error(TP_ERR_INVALID_ARG, "shard %d pointer is NULL", r);
+    if (!aligned(y[r], oe) || (bias && !aligned(bias[r], 4)))
+      return set_error(TP_ERR_ALIGNMENT, "shard %d pointer not aligned to its element size", r);
+  }
+  if (T == 0) return TP_OK;
+  Problem p;
+  memset(&p, 0, sizeof(p));
+  p.njobs = N;
+  p.in_dt = TP_BF16;
+  p.out_dt = out_dt;
+  p.b_layout = BL_MX;
+  p.chain = 1;
+  for (int r = 0; r < N; ++r) {
+    p.jobs[r] = Job{y[r], bias ? (const float *)bias[r] : nullptr, T, On, ldy, r, 1};
+    p.parts[r] = Part{x, codes[r], scales[r], nullptr, K, K, K};
+  }
+  return dispatch(p, (cudaStream_t)stream);
+}
+
+int tp_mx_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K, const uint8_t *const *codes,
+                         const uint8_t *const *scales, int64_t O, const void *bias, void *y, int64_t ldy,
+                         tp_dtype out_dt, tp_stream_t stream) {
+  if (N < 1 || N > kMaxShards) return set_error(TP_ERR_INVALID_ARG, "N must be in 1..%d", kMaxShards);
+  int rc = mx_check_common(T, K, O, out_dt);
+  if (rc) return rc;
+  if (K % N != 0)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "Cannot shard the input of size %lld across %d devices.",
+                     (long long)K, N);
+  const int64_t Kn = K / N;
+  if (Kn % 32)
+    return set_error(TP_ERR_NOT_DIVISIBLE, "K/N (%lld) must hold whole blocks of 32", (long long)Kn);
+  if (!x || !codes || !scales || !y) return set_error(TP_ERR_INVALID_ARG, "null pointer");
+  if (ldy < O) return set_error(TP_ERR_INVALID_ARG, "ldy < O");
+  const int oe = elem_size(out_dt);
+  if (!aligned(y, oe) || (bias && !aligned(bias, 4))) return set_error(TP_ERR_ALIGNMENT, "y or bias not aligned");
+  for (int r = 0; r < N; ++r) {
+    if (!x[r] || !codes[r] || !scales[r]) return set_error(TP_ERR_INVALID_ARG, "shard %d pointer is NULL", r);
+    if (!aligned(x[r], 2)) return set_error(TP_ERR_ALIGNMENT, "shard %d pointer not aligned", r);
+  }
+  if (T == 0) return TP_OK;
+  Problem p;
+  memset(&p, 0, sizeof(p));
+  p.njobs = 1;
+  p.in_dt = TP_BF16;
+  p.out_dt = out_dt;
+  p.b_layout = BL_MX;
+  p.chain = 0;
+  p.jobs[0] = Job{y, (const float *)bias, T, O, ldy, 0, N};
+  for (int r = 0; r < N; ++r) p.parts[r] = Part{x[r], codes[r], scales[r], nullptr, Kn, Kn, Kn};
+  return dispatch(p, (cudaStream_t)stream);
 }
 
 int tp_q4_quantize(const float *w, int64_t rows, int64_t K, int group_size, uint32_t *wq,

@@ -31,7 +31,9 @@ constexpr int kMaxShards = 64;
 constexpr int kMaxJobs = 64;
 constexpr int kMaxParts = 64;
 
-enum BLayout { BL_KMAJOR = 0, BL_MNMAJOR = 1, BL_Q4 = 2 };
+// BL_MX: MXFP8 weights: B = E4M3 codes uint8 (N, K) (ldb = bytes per row),
+// scales = E8M0 uint8 (N, K/32); W(n, k) = e4m3(B[n][k]) * 2^(scales[n][k/32] - 127).
+enum BLayout { BL_KMAJOR = 0, BL_MNMAJOR = 1, BL_Q4 = 2, BL_MX = 3 };
 
 struct Part {
   const void *A;       // (M, K) row-major, row stride lda
@@ -96,6 +98,9 @@ int launch_shard(const void *w, int64_t rows, int64_t cols, int elem_bytes, int 
 int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void *scales,
                     void *qbias, cudaStream_t s);
 int launch_debug_wait(int64_t limit_ns, int *status, cudaStream_t s);
+int launch_mx(const Problem &p, cudaStream_t s, bool *handled);
+int launch_mx_quantize(const float *w, int64_t rows, int64_t K, uint8_t *codes, uint8_t *scales,
+                       cudaStream_t s);
 int launch_colsum(int nout, int nin, const void *const *in, int64_t rows, int64_t cols, int64_t ld,
                   int in_dt, float *const *out, cudaStream_t s);
 void umma_shutdown();

@@ -12,6 +12,7 @@ import numpy as np
 import torch
 
 from . import (tp_all_to_sharded, tp_all_to_sharded_dx, tp_bias_grad, tp_gated_all_to_sharded,
+               tp_mx_all_to_sharded, tp_mx_quantize, tp_mx_sharded_to_all,
                tp_sharded_dw, tp_sharded_to_all_dx, tp_gathered_to_sharded, tp_q4_all_to_sharded,
                tp_q4_quantize,
                tp_q4_sharded_to_all, tp_shard_weight, tp_sharded_to_all, tp_sharded_to_sharded, tp_summa)
@@ -259,4 +260,39 @@ class Q4Pair:
     def step(self, x=None, stream=None):
         tp_q4_all_to_sharded(self.x if x is None else x, *self.up, out=self.mid, stream=stream)
         tp_q4_sharded_to_all(self.mid, *self.down, out=self.y, stream=stream)
+        return self.y
+
+
+class MXPair:
+    """MXFP8 up (column-parallel) / down (row-parallel) pair on the 4-bit pair's
+    shapes: the float32 source weights are quantized on the device (or
+    ``quantized`` holds host (codes, scales) for both), then sliced into the N
+    shards (codes and scales on the same axis)."""
+
+    def __init__(self, cfg: dict, device="cuda", quantized=None):
+        self.N = N = cfg["N"]
+        self.x = to_device(cfg["x"], "bf16", device)
+        T, D, F = self.x.shape[0], cfg["D"], cfg["F"]
+        if quantized is None:
+            wu = to_device(cfg["w_up"], "f32", device)
+            up = tp_mx_quantize(wu)
+            del wu
+            wd = to_device(cfg["w_down"], "f32", device)
+            down = tp_mx_quantize(wd)
+            del wd
+        else:
+            (uc, us), (dc, ds) = quantized
+            up = tuple(torch.from_numpy(a).to(device) for a in (uc, us))
+            down = tuple(torch.from_numpy(a).to(device) for a in (dc, ds))
+        self.up = [tp_shard_weight(a, 0, 1, N) for a in up]
+        self.down = [tp_shard_weight(a, -1, 1, N) for a in down]
+        del up, down
+        self.mid = [torch.empty((T, F // N), dtype=torch.bfloat16, device=device) for _ in range(N)]
+        self.y = torch.empty((T, D), dtype=torch.float32, device=device)
+        self.flops = 2.0 * T * 2 * D * F
+        self.weight_bytes = 2 * D * F * (1.0 + 1.0 / 32)
+
+    def step(self, x=None, stream=None):
+        tp_mx_all_to_sharded(self.x if x is None else x, *self.up, out=self.mid, stream=stream)
+        tp_mx_sharded_to_all(self.mid, *self.down, out=self.y, stream=stream)
         return self.y

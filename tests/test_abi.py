@@ -68,6 +68,20 @@ def test_sharded_to_all_not_divisible(L):
     assert rc == tp.TP_ERR_NOT_DIVISIBLE
 
 
+def test_mx_checks(L):
+    a, k1 = _arr(4)
+    assert L.tp_mx_quantize(FAKE, 4, 48, FAKE, FAKE, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert L.tp_mx_quantize(None, 4, 64, FAKE, FAKE, None) == tp.TP_ERR_INVALID_ARG
+    # column-parallel: O % N, K % 32
+    assert L.tp_mx_all_to_sharded(4, FAKE, 2, 64, a, a, 10, None, a, 4, tp.TP_F32, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert L.tp_mx_all_to_sharded(4, FAKE, 2, 48, a, a, 8, None, a, 4, tp.TP_F32, None) == tp.TP_ERR_NOT_DIVISIBLE
+    # row-parallel: K % N, whole blocks per shard
+    assert L.tp_mx_sharded_to_all(4, a, 2, 66, a, a, 8, None, FAKE, 8, tp.TP_F32, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert L.tp_mx_sharded_to_all(4, a, 2, 64, a, a, 8, None, FAKE, 8, tp.TP_F32, None) == tp.TP_ERR_NOT_DIVISIBLE
+    assert "whole blocks" in L.tp_last_error().decode()
+    assert L.tp_mx_sharded_to_all(4, a, 0, 128, a, a, 8, None, FAKE, 8, tp.TP_F32, None) == tp.TP_OK
+
+
 def test_backward_checks(L):
     a, k1 = _arr(4)
     # column-parallel dx: O % N, lddy < O/N

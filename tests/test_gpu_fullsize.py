@@ -10,7 +10,7 @@ import oracle
 import sharded_gemm_gb300 as tp
 from sharded_gemm_gb300 import build as tpbuild
 from sharded_gemm_gb300 import synth
-from sharded_gemm_gb300.workloads import GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_host
+from sharded_gemm_gb300.workloads import GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, MXPair, Q4Pair, QKV, Summa, to_host
 from gpu_util import bf16, check_close, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -175,3 +175,26 @@ def test_full_q4_pair(T):
     dq = [oracle.shard(a[cols], -1, 1, N) for a in down]
     ref = oracle.q4_sharded_to_all(mids, dq[0], dq[1], dq[2], 64)
     check_close(to_host(w.y)[rows][:, cols], ref, "q4 down")
+
+
+@pytest.mark.parametrize("T", [1])
+def test_full_mx_pair(T):
+    cfg = synth.q4(T=T)
+    N, D, F = cfg["N"], cfg["D"], cfg["F"]
+    up = oracle.quantize_mxfp8(cfg["w_up"])
+    down = oracle.quantize_mxfp8(cfg["w_down"])
+    w = MXPair(cfg, quantized=(up, down))
+    w.step()
+    assert tp.tp_query_status() == 0
+    rows = sample_rows(T, 6)
+    x = bf16(cfg["x"])[rows]
+    for r in (0, N - 1):
+        cols = sample_rows(F // N, 96, seed=r)
+        sl = slice(r * (F // N), (r + 1) * (F // N))
+        ref = oracle.mx_all_to_sharded(x, [up[0][sl][cols]], [up[1][sl][cols]])[0]
+        check_close(to_host(w.mid[r])[rows][:, cols], ref, "mx up shard %d" % r)
+    cols = sample_rows(D, 128, seed=11)
+    mids = [to_host(m)[rows] for m in w.mid]
+    dq = [oracle.shard(a[cols], -1, 1, N) for a in down]
+    ref = oracle.mx_sharded_to_all(mids, dq[0], dq[1])
+    check_close(to_host(w.y)[rows][:, cols], ref, "mx down")

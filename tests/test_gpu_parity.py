@@ -15,7 +15,7 @@ import oracle
 import sharded_gemm_gb300 as tp
 from sharded_gemm_gb300 import build as tpbuild
 from sharded_gemm_gb300 import synth
-from sharded_gemm_gb300.workloads import (GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, Q4Pair, QKV, Summa, to_device,
+from sharded_gemm_gb300.workloads import (GatedFFN, MLPBackward, MLPGatherScatter, MLPPair, MXPair, Q4Pair, QKV, Summa, to_device,
                                           to_host)
 from gpu_util import bf16, check_close, sample_rows
 
@@ -189,6 +189,80 @@ def test_mlp_pair_small(policy):
     check_close(to_host(pair.y), oracle.sharded_to_all(mids, w2, cfg["b2"].astype(np.float64)), "y (layer)")
     chain = oracle.linear(oracle.linear(x, bf16(cfg["w1"]), cfg["b1"]), bf16(cfg["w2"]), cfg["b2"])
     check_close(to_host(pair.y), chain, "y (end to end)")
+
+
+# ------------------------------------------------------------------ f4 mxfp8
+@pytest.mark.parametrize("rows,K", [(1, 32), (37, 512), (256, 1024)])
+def test_mx_quantize_bitexact(rows, K):
+    w = (RNG.standard_normal((rows, K)) * 0.02).astype(np.float32)
+    w[0, :32] = 0.0                                    # all-zero block
+    if K >= 128:
+        w[0, 32:64] = -0.0                             # negative zeros
+        w[0, 64:96] *= np.float32(1e30)                # large block
+        w[0, 96:128] = np.float32(1e-40) * np.arange(32, dtype=np.float32)  # subnormal block
+    if rows > 1:
+        w[1, :] = np.where(np.arange(K) % 7 == 0, np.float32(3.0), np.float32(-1e-7))  # tiny next to large
+    codes, scales = tp.tp_mx_quantize(torch.from_numpy(w).cuda())
+    rc, rs = oracle.quantize_mxfp8(w)
+    assert scales.cpu().numpy().tobytes() == rs.tobytes()
+    assert codes.cpu().numpy().tobytes() == rc.tobytes()
+
+
+def _mx_host(rows, K, seed):
+    w = (np.random.default_rng(seed).standard_normal((rows, K)) * 0.02).astype(np.float32)
+    return oracle.quantize_mxfp8(w)
+
+
+@pytest.mark.parametrize("T,K,On,N", [(1, 512, 40, 4), (3, 1024, 130, 2), (4, 96, 7, 1), (2, 2048, 64, 8),
+                                      (20, 256, 96, 2)])
+@pytest.mark.parametrize("out_dt", [torch.bfloat16, torch.float32])
+def test_mx_all_to_sharded(policy, T, K, On, N, out_dt):
+    codes, scales = _mx_host(On * N, K, T + K)
+    x = rand_bf16((T, K))
+    cs = tp.tp_shard_weight(torch.from_numpy(codes).cuda(), 0, 1, N)
+    ss = tp.tp_shard_weight(torch.from_numpy(scales).cuda(), 0, 1, N)
+    b = (RNG.standard_normal(On * N) * 0.1).astype(np.float32)
+    bs = tp.tp_shard_weight(to_device(b, "f32"), 0, 1, N)
+    ys = tp.tp_mx_all_to_sharded(to_device(x, "bf16"), cs, ss, bs, out_dtype=out_dt)
+    _status_ok()
+    ref = oracle.mx_all_to_sharded(bf16(x), oracle.shard(codes, 0, 1, N), oracle.shard(scales, 0, 1, N),
+                                   [p.astype(np.float64) for p in oracle.shard(b, 0, 1, N)])
+    for r in range(N):
+        check_close(to_host(ys[r]), ref[r], "shard %d" % r)
+
+
+@pytest.mark.parametrize("T,Kn,O,N", [(1, 512, 40, 4), (2, 64, 130, 3), (4, 256, 64, 8), (1, 3584, 33, 2),
+                                      (17, 128, 48, 2)])
+def test_mx_sharded_to_all(policy, T, Kn, O, N):
+    codes, scales = _mx_host(O, Kn * N, T + Kn)
+    x = rand_bf16((T, Kn * N))
+    xs = tp.tp_shard_weight(to_device(x, "bf16"), -1, 1, N)
+    cs = tp.tp_shard_weight(torch.from_numpy(codes).cuda(), -1, 1, N)
+    ss = tp.tp_shard_weight(torch.from_numpy(scales).cuda(), -1, 1, N)
+    b = (RNG.standard_normal(O) * 0.1).astype(np.float32)
+    y = tp.tp_mx_sharded_to_all(xs, cs, ss, to_device(b, "f32"))
+    _status_ok()
+    ref = oracle.mx_sharded_to_all([bf16(p) for p in oracle.shard(x, -1, 1, N)], oracle.shard(codes, -1, 1, N),
+                                   oracle.shard(scales, -1, 1, N), b.astype(np.float64))
+    check_close(to_host(y), ref, "mx row")
+
+
+def test_mx_pair_small_repeatable():
+    cfg = synth.q4(seed=9, T=1, D=1024, F=2048, N=4)
+    up = oracle.quantize_mxfp8(cfg["w_up"])
+    down = oracle.quantize_mxfp8(cfg["w_down"])
+    w = MXPair(cfg, quantized=(up, down))
+    y1 = w.step().clone()
+    y2 = w.step().clone()
+    _status_ok()
+    assert torch.equal(y1, y2)
+    x = bf16(cfg["x"])
+    mid = oracle.mx_all_to_sharded(x, oracle.shard(up[0], 0, 1, 4), oracle.shard(up[1], 0, 1, 4))
+    mids = [to_host(m) for m in w.mid]
+    for r in range(4):
+        check_close(mids[r], mid[r], "up %d" % r)
+    ref = oracle.mx_sharded_to_all(mids, oracle.shard(down[0], -1, 1, 4), oracle.shard(down[1], -1, 1, 4))
+    check_close(to_host(w.y), ref, "down")
 
 
 # ------------------------------------------------------------------ f3 backward
