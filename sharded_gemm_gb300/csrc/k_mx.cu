@@ -95,7 +95,7 @@ struct MxArgs {
   MxPart parts[kMaxParts];
   const uint16_t *x[kMaxParts];
   int64_t xK[kMaxParts], xld[kMaxParts], xoff[kMaxParts];
-  int njobs, nx, T, ntasks, chain, out_dt;
+  int njobs, nx, T, ntasks, chain, out_dt, xvec;
 };
 
 __device__ __forceinline__ void mx_expand16(const uint4 q, float (&c)[16]) {
@@ -121,9 +121,22 @@ __global__ void __launch_bounds__(kMxWarps * 32, 1) mx_gemv_kernel(const __grid_
     const int64_t K = a.xK[d], ld = a.xld[d];
     const uint16_t *src = a.x[d];
     float *dst = xs + a.xoff[d];
-    for (int64_t i = threadIdx.x; i < (int64_t)TT * K; i += blockDim.x) {
-      const int64_t t = i / K, k = i - t * K;
-      dst[i] = __uint_as_float((uint32_t)__ldg(src + t * ld + k) << 16);
+    if (a.xvec) {  // 16-byte loads of 8 bf16 (rows and bases 16-byte aligned)
+      const int64_t K8 = K >> 3;
+      for (int64_t i = threadIdx.x; i < (int64_t)TT * K8; i += blockDim.x) {
+        const int64_t t = i / K8, k = (i - t * K8) << 3;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * ld + k));
+        float4 *o = reinterpret_cast<float4 *>(dst + t * K + k);
+        o[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+        o[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                           __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < (int64_t)TT * K; i += blockDim.x) {
+        const int64_t t = i / K, k = i - t * K;
+        dst[i] = __uint_as_float((uint32_t)__ldg(src + t * ld + k) << 16);
+      }
     }
   }
   __syncthreads();
@@ -148,14 +161,40 @@ __global__ void __launch_bounds__(kMxWarps * 32, 1) mx_gemv_kernel(const __grid_
 #pragma unroll
         for (int r = 0; r < kMxRows; ++r) acc[t][r] = 0.f;
       const int64_t G = P.K >> 5;
-      for (int64_t k0 = (int64_t)lane * 16; k0 < P.K; k0 += 512) {
+      // The codes and scales of the next 512-code step are loaded before the
+      // current step is computed, so one step's loads are always in flight.
+      const uint8_t *crow[kMxRows];
+      const uint8_t *srow[kMxRows];
+#pragma unroll
+      for (int r = 0; r < kMxRows; ++r) {
+        const int row = row0 + r < J.rows ? row0 + r : J.rows - 1;  // ragged tail: a valid row, result unused
+        crow[r] = P.codes + (int64_t)row * P.ldb;
+        srow[r] = P.scales + (int64_t)row * G;
+      }
+      uint4 qn[kMxRows];
+      uint32_t sn[kMxRows];
+      int64_t k0 = (int64_t)lane * 16;
+      if (k0 < P.K) {
+#pragma unroll
+        for (int r = 0; r < kMxRows; ++r) {
+          qn[r] = __ldcs(reinterpret_cast<const uint4 *>(crow[r] + k0));
+          sn[r] = __ldg(srow[r] + (k0 >> 5));
+        }
+      }
+      for (; k0 < P.K; k0 += 512) {
         uint4 q[kMxRows];
         float sc[kMxRows];
 #pragma unroll
         for (int r = 0; r < kMxRows; ++r) {
-          const int row = row0 + r < J.rows ? row0 + r : J.rows - 1;  // ragged tail: a valid row, result unused
-          q[r] = __ldcs(reinterpret_cast<const uint4 *>(P.codes + (int64_t)row * P.ldb + k0));
-          sc[r] = e8m0_value(__ldg(P.scales + (int64_t)row * G + (k0 >> 5)));
+          q[r] = qn[r];
+          sc[r] = e8m0_value(sn[r]);
+        }
+        if (k0 + 512 < P.K) {
+#pragma unroll
+          for (int r = 0; r < kMxRows; ++r) {
+            qn[r] = __ldcs(reinterpret_cast<const uint4 *>(crow[r] + k0 + 512));
+            sn[r] = __ldg(srow[r] + ((k0 + 512) >> 5));
+          }
         }
 #pragma unroll
         for (int r = 0; r < kMxRows; ++r) {
@@ -251,6 +290,9 @@ int launch_mx(const Problem &p, cudaStream_t s, bool *handled) {
   if (smem > 200 * 1024) return TP_OK;  // inputs too large to stage: the CUDA-core GEMM takes it
   args.njobs = p.njobs;
   args.T = (int)maxT;
+  args.xvec = 1;
+  for (int d = 0; d < args.nx; ++d)
+    if (((uintptr_t)args.x[d] & 15) || (args.xld[d] % 8) || (args.xK[d] % 8)) args.xvec = 0;
   args.ntasks = ntasks;
   args.chain = p.chain;
   args.out_dt = p.out_dt;
