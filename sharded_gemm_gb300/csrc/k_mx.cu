@@ -1,6 +1,7 @@
 // k_mx.cu -- MXFP8 weights ("mxfp8" quantization mode of the MLX tensor
-// parallelism guide, section 2.3): the device quantizer and the CUDA-core
-// decode GEMV of the sharded linears.
+// parallelism guide, section 2.3): the device quantizer, the CUDA-core
+// decode GEMV (T <= 4) and the tensor-core kernel (T > 4) of the sharded
+// linears.
 //
 // Format (OCP microscaling FP8): E4M3 codes, one byte per weight, row-major
 // (rows, K); one E8M0 scale byte per 32 consecutive weights of a row, (rows,
@@ -14,6 +15,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "ptx.cuh"
 #include "tp_internal.h"
 
 namespace tp {
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kMxWarps * 32, 1) mx_gemv_kernel(const __grid_
   }
 }
 
-int launch_mx(const Problem &p, cudaStream_t s, bool *handled) {
+static int launch_mx_gemv(const Problem &p, cudaStream_t s, bool *handled) {
   *handled = false;
   if (p.in_dt != TP_BF16) return TP_OK;
   int64_t maxT = 0;
@@ -312,6 +314,617 @@ int launch_mx(const Problem &p, cudaStream_t s, bool *handled) {
   if (e != cudaSuccess) return cuda_error(e, "mx_gemv_kernel launch");
   *handled = true;
   return TP_OK;
+}
+
+// ------------------------------------------------------------------ tensor cores
+// T > 4 tokens (and any shape the GEMV does not take).  Swap-AB tiles: 128
+// weight rows fill M, BN tokens fill N.  Per 64-element k-block, TMA brings the
+// 128 x 64 code bytes (64-byte swizzle) and the BN x 64 x tile (bf16, 128-byte
+// swizzle); 8 converter warps turn the codes into the exact bf16 values
+// e4m3 * 2^(s-127) (one row and one 32-element block per thread) and write
+// them as the MMA's A operand (K-major, 128-byte swizzle) into the same stage;
+// one thread issues tcgen05.mma kind::f16 (bf16 x bf16, float32 in TMEM).
+// A unit is (job, 128-row tile, token tile, split); a split is a run of
+// k-blocks of one part (rank); the float32 partials of split tiles go to
+// workspace slots (column-major, so a warp's 32 rows of one column are one
+// 128-byte line) and a second launch adds each tile's slots in split (rank)
+// order, then the bias.
+namespace {
+
+constexpr int kMtThreads = 14 * 32;  // producer, MMA, 8 converter warps, 4 epilogue warps
+
+struct MtPart {
+  const uint8_t *sc;  // scales (rows, G)
+  int G;              // K / 32
+  int kblocks;        // ceil(K / 64)
+  int16_t cmap, xmap;
+  int nchunk, chunk_kb;
+};
+struct MtJob {
+  void *C;
+  const float *bias;
+  int64_t ldc;
+  int rows, T;
+  int part0, nparts;
+  int tiles, ntiles, splits;
+  int unit_begin;
+  int64_t ws_base;
+};
+struct MtArgs {
+  CUtensorMap cmaps[kMaxParts];
+  CUtensorMap xmaps[kMaxParts];
+  MtJob jobs[kMaxJobs];
+  MtPart parts[kMaxParts];
+  int njobs, total_units, out_dt;
+  uint32_t idesc;
+  float *ws;
+  int *status;
+  uint64_t wait_ns;
+};
+
+struct MtUnit {
+  int job, part, tile, ntile, tile_lin, sidx, kb0, kb1;
+};
+
+__device__ __forceinline__ void mt_unit(const MtArgs &a, int u, MtUnit &ui) {
+  int j = 0;
+  while (j + 1 < a.njobs && u >= a.jobs[j + 1].unit_begin) ++j;
+  const MtJob &J = a.jobs[j];
+  const int local = u - J.unit_begin;
+  ui.job = j;
+  ui.tile_lin = local / J.splits;
+  ui.sidx = local - ui.tile_lin * J.splits;
+  ui.tile = ui.tile_lin % J.tiles;
+  ui.ntile = ui.tile_lin / J.tiles;
+  int p = 0, c = ui.sidx;
+  while (p + 1 < J.nparts && c >= a.parts[J.part0 + p].nchunk) {
+    c -= a.parts[J.part0 + p].nchunk;
+    ++p;
+  }
+  const MtPart &P = a.parts[J.part0 + p];
+  ui.part = J.part0 + p;
+  ui.kb0 = c * P.chunk_kb;
+  ui.kb1 = min(P.kblocks, ui.kb0 + P.chunk_kb);
+}
+
+// Eight E4M3 codes (two 32-bit words) times 2^(s-127) -> eight bf16 (one
+// 16-byte chunk, natural order).  The conversions to f16 and float32 are
+// exact, so is the power-of-two product, and the values (4 significant bits)
+// are exact in bf16.
+__device__ __forceinline__ uint32_t mx_pair_bf16(uint32_t pair, float scale) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair, __NV_E4M3);
+  const float2 f = __half22float2(__half2(h));
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(f.y * scale), "f"(f.x * scale));
+  return d;
+}
+__device__ __forceinline__ uint4 mx_chunk_bf16(uint32_t w0, uint32_t w1, float scale) {
+  return make_uint4(mx_pair_bf16(w0 & 0xffffu, scale), mx_pair_bf16(w0 >> 16, scale),
+                    mx_pair_bf16(w1 & 0xffffu, scale), mx_pair_bf16(w1 >> 16, scale));
+}
+
+// The two scale bytes of k-block kb (blocks 2kb, 2kb+1) of a row; a block
+// past the row's end reads as 0.
+__device__ __forceinline__ uint32_t mt_scale_pair(const uint8_t *row, int kb, int G) {
+  const int b = 2 * kb;
+  if (b + 1 < G && ((uintptr_t)(row + b) & 1) == 0) return __ldg(reinterpret_cast<const uint16_t *>(row + b));
+  uint32_t v = __ldg(row + b);
+  if (b + 1 < G) v |= (uint32_t)__ldg(row + b + 1) << 8;
+  return v;
+}
+
+__device__ __forceinline__ void mt_store(const MtArgs &a, const MtJob &J, int t, int orow, float v) {
+  const int64_t idx = (int64_t)t * J.ldc + orow;
+  if (a.out_dt == TP_F32)
+    static_cast<float *>(J.C)[idx] = v;
+  else if (a.out_dt == TP_BF16)
+    static_cast<__nv_bfloat16 *>(J.C)[idx] = __float2bfloat16_rn(v);
+  else
+    static_cast<__half *>(J.C)[idx] = __float2half_rn(v);
+}
+
+#define MT_WAIT_ALL(bar, par, okvar)                                   \
+  {                                                                    \
+    const bool _r = mbar_wait((bar), (par), lim, a.status, &abort_sh); \
+    if (!__all_sync(0xffffffffu, _r)) okvar = false;                   \
+  }
+
+__device__ __forceinline__ uint4 mt_lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void mt_sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+template <int BN>
+struct MtCfg {
+  static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 bf16
+  static constexpr int X_BYTES = BN * 128;   // BN tokens x 64 bf16
+  static constexpr int C_BYTES = 128 * 64;   // 128 rows x 64 codes
+  static constexpr int STAGE = A_BYTES + X_BYTES + C_BYTES;
+  static constexpr int ND = (512 / BN) < 4 ? (512 / BN) : 4;  // accumulator slots
+  static constexpr int COLS = ND * BN <= 32 ? 32 : ND * BN <= 64 ? 64 : ND * BN <= 128 ? 128 : ND * BN <= 256 ? 256 : 512;
+  static constexpr int CHK = BN >= 32 ? 32 : 16;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_constant__ MtArgs a) {
+  using C = MtCfg<BN>;
+  static_assert(STAGES == 1 || STAGES == 2 || STAGES == 4 || STAGES == 8, "8 converter warps share the slots");
+  static_assert(C::STAGE % 1024 == 0, "stage alignment");
+  constexpr int ND = C::ND;
+
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], afull_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t dfull_bar[ND], dempty_bar[ND];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint64_t lim = a.wait_ns;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&afull_bar[i]), 8 / STAGES);
+      mbar_init(smem_u32(&empty_bar[i]), 1);
+    }
+    for (int i = 0; i < ND; ++i) {
+      mbar_init(smem_u32(&dfull_bar[i]), 1);
+      mbar_init(smem_u32(&dempty_bar[i]), 4);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_sh), C::COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_sh;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      bool used[STAGES];
+      uint32_t lastph[STAGES];
+#pragma unroll
+      for (int i = 0; i < STAGES; ++i) used[i] = false;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        MtUnit ui;
+        mt_unit(a, u, ui);
+        const MtPart &P = a.parts[ui.part];
+        for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          const uint32_t base = sbase + st * C::STAGE;
+          const uint32_t fb = smem_u32(&full_bar[st]);
+          mbar_arrive_expect_tx(fb, C::X_BYTES + C::C_BYTES);
+          tma_load_2d(base + C::A_BYTES, &a.xmaps[P.xmap], fb, kb * 64, ui.ntile * BN);
+          tma_load_2d(base + C::A_BYTES + C::X_BYTES, &a.cmaps[P.cmap], fb, kb * 64, ui.tile * 128);
+          used[st] = true;
+          lastph[st] = ph;
+          if (++st == STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok)
+        for (int i = 0; i < STAGES; ++i)
+          if (used[i]) mbar_wait(smem_u32(&full_bar[i]), lastph[i], lim, a.status, nullptr);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int st = 0, ds = 0;
+      uint32_t ph = 0, dph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        MtUnit ui;
+        mt_unit(a, u, ui);
+        bool first = true;
+        for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+          // the x tile has landed and the converters have written A
+          if (!mbar_wait(smem_u32(&full_bar[st]), ph, lim, a.status, &abort_sh) ||
+              !mbar_wait(smem_u32(&afull_bar[st]), ph, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          if (first && !mbar_wait(smem_u32(&dempty_bar[ds]), dph ^ 1, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t base = sbase + st * C::STAGE;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16(tmem + ds * BN, umma_desc_sw128(base + kk * 32, 16, 1024),
+                     umma_desc_sw128(base + C::A_BYTES + kk * 32, 16, 1024), a.idesc,
+                     (first && kk == 0) ? 0u : 1u);
+          umma_commit(smem_u32(&empty_bar[st]));
+          if (++st == STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+          first = false;
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&dfull_bar[ds]));
+        if (++ds == ND) {
+          ds = 0;
+          dph ^= 1;
+        }
+      }
+      umma_commit(smem_u32(&drain_bar));
+      mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
+    }
+  } else if (warp < 10) {
+    // ---------------------------------------------------------- converters
+    // Converter warp cw owns ring slots s with s % STAGES == cw % STAGES; the
+    // 8 / STAGES warps of a slot split its 128 rows (lane l takes rows
+    // r0 + l + 32 i).  Each converts whole stages, so up to 8 stages are in
+    // conversion at once.  A row's two scale bytes of a k-block are loaded one
+    // round of the ring ahead.
+    constexpr int WPS = 8 / STAGES;          // warps per slot
+    constexpr int RPL = 128 / (32 * WPS);    // rows per lane
+    const int cw = warp - 2;
+    const int myslot = cw % STAGES;
+    const int rbase = (cw / STAGES) * (128 / WPS);
+    int n = 0;  // stage sequence number over all units of this CTA
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+      MtUnit ui;
+      mt_unit(a, u, ui);
+      const MtPart &P = a.parts[ui.part];
+      const MtJob &J = a.jobs[ui.job];
+      // first k-block of this unit that is this warp's
+      int kb = ui.kb0 + ((myslot - n % STAGES) + STAGES) % STAGES;
+      n += ui.kb1 - ui.kb0;
+      uint32_t snext[RPL];
+      const uint8_t *srow[RPL];
+      bool rv[RPL];
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) {
+        const int orow = ui.tile * 128 + rbase + lane + 32 * i;
+        rv[i] = orow < J.rows;
+        srow[i] = P.sc + (int64_t)(rv[i] ? orow : 0) * P.G;
+        snext[i] = (rv[i] && kb < ui.kb1) ? mt_scale_pair(srow[i], kb, P.G) : 0u;
+      }
+      for (; ok && kb < ui.kb1; kb += STAGES) {
+        const int seq = n - (ui.kb1 - ui.kb0) + (kb - ui.kb0);  // stage sequence number of kb
+        const uint32_t ph = (uint32_t)((seq / STAGES) & 1);
+        uint32_t scur[RPL];
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+          scur[i] = snext[i];
+          const int kn = kb + STAGES;
+          snext[i] = (rv[i] && kn < ui.kb1) ? mt_scale_pair(srow[i], kn, P.G) : 0u;
+        }
+        MT_WAIT_ALL(smem_u32(&full_bar[myslot]), ph, ok);
+        if (!ok) break;
+        const uint32_t base = sbase + myslot * C::STAGE;
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+          const int r = rbase + lane + 32 * i;
+          const float s0 = rv[i] ? e8m0_value(scur[i] & 0xffu) : 0.f;
+          const float s1 = (rv[i] && 2 * kb + 1 < P.G) ? e8m0_value(scur[i] >> 8) : 0.f;
+          const uint32_t crow = base + C::A_BYTES + C::X_BYTES + r * 64;  // 64-byte swizzled code row
+          const uint32_t arow = base + r * 128;                           // 128-byte swizzled A row
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = mt_lds128(crow + ((c ^ ((r >> 1) & 3)) << 4));
+            const float sc = c < 2 ? s0 : s1;
+            mt_sts128(arow + (((2 * c) ^ (r & 7)) << 4), mx_chunk_bf16(v.x, v.y, sc));
+            mt_sts128(arow + (((2 * c + 1) ^ (r & 7)) << 4), mx_chunk_bf16(v.z, v.w, sc));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&afull_bar[myslot]));
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    int ds = 0;
+    uint32_t dph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+      MtUnit ui;
+      mt_unit(a, u, ui);
+      const MtJob &J = a.jobs[ui.job];
+      const int orow = ui.tile * 128 + m;
+      const bool valid = orow < J.rows;
+      MT_WAIT_ALL(smem_u32(&dfull_bar[ds]), dph, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float bias = (valid && J.bias) ? __ldg(J.bias + orow) : 0.f;
+      const int t0 = ui.ntile * BN;
+      const bool split = J.splits > 1;
+      float *slot = split ? a.ws + (J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 * BN + m : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < BN / C::CHK; ++c) {
+        float v[C::CHK];
+        if constexpr (C::CHK == 32)
+          tmem_ld32(tmem + lane_off + ds * BN + c * 32, v);
+        else
+          tmem_ld16(tmem + lane_off + ds * BN + c * 16, v);
+        tmem_wait_ld();
+        if (split) {
+#pragma unroll
+          for (int i = 0; i < C::CHK; ++i) __stcg(slot + (c * C::CHK + i) * 128, v[i]);
+        } else if (valid) {
+#pragma unroll
+          for (int i = 0; i < C::CHK; ++i) {
+            const int t = t0 + c * C::CHK + i;
+            if (t < J.T) mt_store(a, J, t, orow, v[i] + bias);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[ds]));
+      if (++ds == ND) {
+        ds = 0;
+        dph ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::COLS);
+  }
+}
+
+}  // namespace
+
+namespace {
+
+// Ordered sum of the split slots: block (tile, group of CG token columns),
+// thread m = tile row; out[t][row] = (slot_0 + slot_1 + ... in split order)
+// + bias.
+struct MrJob {
+  void *C;
+  const float *bias;
+  int64_t ldc, ws_base;
+  int rows, T, tiles, splits, block0;
+};
+struct MrArgs {
+  MrJob jobs[kMaxJobs];
+  const float *ws;
+  int njobs, nblocks, BN, CG, out_dt;
+};
+
+__global__ void __launch_bounds__(256) mx_reduce_kernel(const __grid_constant__ MrArgs a) {
+  // item = (block index b over the split tiles' column groups, column c of
+  // the group, row m); consecutive threads take consecutive rows
+  const int64_t per_block = (int64_t)a.CG * 128;
+  const int64_t total = (int64_t)a.nblocks * per_block;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total; it += (int64_t)gridDim.x * blockDim.x) {
+    const int b = (int)(it / per_block);
+    const int rem = (int)(it - (int64_t)b * per_block);
+    const int cl = rem >> 7, m = rem & 127;
+    int j = 0;
+    while (j + 1 < a.njobs && b >= a.jobs[j + 1].block0) ++j;
+    const MrJob &J = a.jobs[j];
+    const int gpt = a.BN / a.CG;  // column groups per tile
+    const int local = b - J.block0;
+    const int tile_lin = local / gpt, cg = local - tile_lin * gpt;
+    const int tile = tile_lin % J.tiles, ntile = tile_lin / J.tiles;
+    const int c = cg * a.CG + cl;
+    const int orow = tile * 128 + m;
+    const int t = ntile * a.BN + c;
+    const float *s0 = a.ws + (J.ws_base + (int64_t)tile_lin * J.splits) * 128 * a.BN + (int64_t)c * 128 + m;
+    float v = __ldcg(s0);
+#pragma unroll 8
+    for (int sp = 1; sp < J.splits; ++sp) v += __ldcg(s0 + (int64_t)sp * 128 * a.BN);
+    if (orow < J.rows && t < J.T) {
+      if (J.bias) v += __ldg(J.bias + orow);
+      const int64_t idx = (int64_t)t * J.ldc + orow;
+      if (a.out_dt == TP_F32)
+        static_cast<float *>(J.C)[idx] = v;
+      else if (a.out_dt == TP_BF16)
+        static_cast<__nv_bfloat16 *>(J.C)[idx] = __float2bfloat16_rn(v);
+      else
+        static_cast<__half *>(J.C)[idx] = __float2half_rn(v);
+    }
+  }
+}
+
+std::mutex g_mt_mu;
+
+template <int BN, int STAGES>
+int mt_launch(MtArgs &args, int sms, cudaStream_t s) {
+  auto kern = mx_umma_kernel<BN, STAGES>;
+  constexpr int smem = STAGES * MtCfg<BN>::STAGE + 1024;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(mx)");
+    attr_done[dev & 63] = true;
+  }
+  const int grid = args.total_units < sms ? args.total_units : sms;
+  kern<<<grid, kMtThreads, smem, s>>>(args);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_error(e, "mx_umma_kernel launch");
+}
+
+// Tensor-core launch of `p` (bf16 x, 16-byte aligned codes and x rows).
+int launch_mx_tc(const Problem &p, cudaStream_t s, bool *handled) {
+  *handled = false;
+  int64_t maxT = 0;
+  for (int j = 0; j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    if (J.M > maxT) maxT = J.M;
+    if (J.N > INT32_MAX / 2 || J.M > INT32_MAX / 2) return TP_OK;
+    for (int q = 0; q < J.nparts; ++q) {
+      const Part &P = p.parts[J.part0 + q];
+      if (((uintptr_t)P.A & 15) || (P.lda % 8) || ((uintptr_t)P.B & 15) || (P.ldb % 16) || (P.K % 32)) return TP_OK;
+    }
+  }
+  const int BN = maxT <= 16 ? 16 : maxT <= 32 ? 32 : maxT <= 64 ? 64 : maxT <= 128 ? 128 : 256;
+  std::lock_guard<std::mutex> lk(g_mt_mu);
+  const int sms = sm_count();
+  static MtArgs args;
+  memset(&args, 0, sizeof(args));
+  // k-block chunks per part: the same count for every part, chosen to fill
+  // the SMs with the fewest k-blocks per unit (plus a small cost per split)
+  int64_t tiles_parts = 0;
+  int kb_max = 0;
+  for (int j = 0; j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    tiles_parts += ((J.N + 127) / 128) * ((J.M + BN - 1) / BN) * J.nparts;
+    for (int q = 0; q < J.nparts; ++q) kb_max = std::max(kb_max, (int)((p.parts[J.part0 + q].K + 63) / 64));
+  }
+  int chunks = 1;
+  double best = 1e300;
+  for (int c = 1; c <= 16 && c <= kb_max; ++c) {
+    const int ck = (kb_max + c - 1) / c;
+    const int64_t units = tiles_parts * ((kb_max + ck - 1) / ck);
+    const double cost = (double)((units + sms - 1) / sms) * (ck + 4.0) + (c > 1 ? 2.0 : 0.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      chunks = c;
+    }
+  }
+  const void *cptr[kMaxParts], *xptr[kMaxParts];
+  int ncm = 0, nxm = 0;
+  int64_t units = 0, slots = 0;
+  for (int j = 0; j < p.njobs; ++j) {
+    const Job &J = p.jobs[j];
+    MtJob &Q = args.jobs[j];
+    Q.C = J.C;
+    Q.bias = J.bias;
+    Q.ldc = J.ldc;
+    Q.rows = (int)J.N;
+    Q.T = (int)J.M;
+    Q.part0 = J.part0;
+    Q.nparts = J.nparts;
+    Q.tiles = (Q.rows + 127) / 128;
+    Q.ntiles = (Q.T + BN - 1) / BN;
+    int splits = 0;
+    for (int q = 0; q < J.nparts; ++q) {
+      const Part &P = p.parts[J.part0 + q];
+      MtPart &QP = args.parts[J.part0 + q];
+      QP.sc = static_cast<const uint8_t *>(P.scales);
+      QP.G = (int)(P.K / 32);
+      QP.kblocks = (int)((P.K + 63) / 64);
+      QP.chunk_kb = (QP.kblocks + chunks - 1) / chunks;
+      QP.nchunk = (QP.kblocks + QP.chunk_kb - 1) / QP.chunk_kb;
+      splits += QP.nchunk;
+      int ic = -1, ix = -1;
+      for (int i = 0; i < ncm; ++i)
+        if (cptr[i] == P.B) ic = i;
+      for (int i = 0; i < nxm; ++i)
+        if (xptr[i] == P.A) ix = i;
+      int rc;
+      if (ic < 0) {
+        rc = make_tmap_2d(&args.cmaps[ncm], P.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)P.K, (uint64_t)Q.rows,
+                          (uint64_t)P.ldb, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (rc) return rc;
+        cptr[ncm] = P.B;
+        ic = ncm++;
+      }
+      if (ix < 0) {
+        rc = make_tmap_2d(&args.xmaps[nxm], P.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)P.K, (uint64_t)Q.T,
+                          (uint64_t)P.lda, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc) return rc;
+        xptr[nxm] = P.A;
+        ix = nxm++;
+      }
+      QP.cmap = (int16_t)ic;
+      QP.xmap = (int16_t)ix;
+    }
+    Q.splits = splits;
+    Q.unit_begin = (int)units;
+    Q.ws_base = slots;
+    const int64_t tl = (int64_t)Q.tiles * Q.ntiles;
+    units += tl * splits;
+    if (splits > 1) slots += tl * splits;
+  }
+  if (units == 0) {
+    *handled = true;
+    return TP_OK;
+  }
+  if (units > INT32_MAX) return TP_OK;
+  if (slots > 0) {
+    int *unused_cnt = nullptr;
+    int rc = split_workspace(s, (size_t)slots * 128 * BN * sizeof(float), 0, &args.ws, &unused_cnt);
+    if (rc) return rc;
+  }
+  args.njobs = p.njobs;
+  args.total_units = (int)units;
+  args.out_dt = p.out_dt;
+  args.idesc = umma_idesc_f16(1u, 0u, 128u, (uint32_t)BN);
+  args.status = p.status;
+  args.wait_ns = (uint64_t)p.wait_ns;
+  int rc;
+  if (BN == 16)
+    rc = mt_launch<16, 8>(args, sms, s);
+  else if (BN == 32)
+    rc = mt_launch<32, 8>(args, sms, s);
+  else if (BN == 64)
+    rc = mt_launch<64, 4>(args, sms, s);
+  else if (BN == 128)
+    rc = mt_launch<128, 4>(args, sms, s);
+  else
+    rc = mt_launch<256, 4>(args, sms, s);
+  if (rc != TP_OK) return rc;
+  *handled = true;
+  if (slots > 0) {  // ordered sums of the split tiles
+    static MrArgs ra;
+    memset(&ra, 0, sizeof(ra));
+    int nb = 0;
+    for (int j = 0; j < p.njobs; ++j) {
+      const MtJob &Q = args.jobs[j];
+      ra.jobs[j] = MrJob{Q.C, Q.bias, Q.ldc, Q.ws_base, Q.rows, Q.T, Q.tiles, Q.splits, nb};
+      if (Q.splits > 1) nb += Q.tiles * Q.ntiles * (BN / std::min(BN, 32));
+    }
+    ra.ws = args.ws;
+    ra.CG = std::min(BN, 32);
+    ra.njobs = p.njobs;
+    ra.nblocks = nb;
+    ra.BN = BN;
+    ra.out_dt = p.out_dt;
+    const int64_t items = (int64_t)nb * ra.CG * 128;
+    const int grid = (int)std::min<int64_t>((items + 255) / 256, (int64_t)sms * 16);
+    mx_reduce_kernel<<<grid, 256, 0, s>>>(ra);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error(e, "mx_reduce_kernel launch");
+  }
+  return TP_OK;
+}
+
+}  // namespace
+
+int launch_mx(const Problem &p, cudaStream_t s, bool *handled) {
+  *handled = false;
+  if (p.in_dt != TP_BF16) return TP_OK;
+  int rc = launch_mx_gemv(p, s, handled);
+  if (rc != TP_OK || *handled) return rc;
+  return launch_mx_tc(p, s, handled);
 }
 
 }  // namespace tp

@@ -177,7 +177,7 @@ def test_full_q4_pair(T):
     check_close(to_host(w.y)[rows][:, cols], ref, "q4 down")
 
 
-@pytest.mark.parametrize("T", [1])
+@pytest.mark.parametrize("T", [1, 16, 256])
 def test_full_mx_pair(T):
     cfg = synth.q4(T=T)
     N, D, F = cfg["N"], cfg["D"], cfg["F"]

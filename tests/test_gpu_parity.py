@@ -213,8 +213,11 @@ def _mx_host(rows, K, seed):
     return oracle.quantize_mxfp8(w)
 
 
+# T <= 4: the CUDA-core GEMV; larger T: the tensor-core kernel (token tiles of
+# 16, 32, 64, 128 and 256, split-K with the ordered fixup, a 32-code tail).
 @pytest.mark.parametrize("T,K,On,N", [(1, 512, 40, 4), (3, 1024, 130, 2), (4, 96, 7, 1), (2, 2048, 64, 8),
-                                      (20, 256, 96, 2)])
+                                      (20, 256, 96, 2), (16, 4096, 130, 2), (5, 96, 128, 1),
+                                      (256, 1024, 256, 2), (300, 512, 200, 1), (64, 2048, 384, 4)])
 @pytest.mark.parametrize("out_dt", [torch.bfloat16, torch.float32])
 def test_mx_all_to_sharded(policy, T, K, On, N, out_dt):
     codes, scales = _mx_host(On * N, K, T + K)
@@ -232,7 +235,8 @@ def test_mx_all_to_sharded(policy, T, K, On, N, out_dt):
 
 
 @pytest.mark.parametrize("T,Kn,O,N", [(1, 512, 40, 4), (2, 64, 130, 3), (4, 256, 64, 8), (1, 3584, 33, 2),
-                                      (17, 128, 48, 2)])
+                                      (17, 128, 48, 2), (16, 3584, 260, 8), (256, 1024, 128, 2),
+                                      (100, 96, 129, 3)])
 def test_mx_sharded_to_all(policy, T, Kn, O, N):
     codes, scales = _mx_host(O, Kn * N, T + Kn)
     x = rand_bf16((T, Kn * N))
