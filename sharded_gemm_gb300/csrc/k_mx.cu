@@ -617,19 +617,28 @@ __global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_con
         MT_WAIT_ALL(smem_u32(&full_bar[myslot]), ph, ok);
         if (!ok) break;
         const uint32_t base = sbase + myslot * C::STAGE;
+        // all of the stage's code loads first (plain shared-memory reads, so
+        // they are issued together), then the conversions and A stores
+        uint8_t *gbase = dsmem + (base - smem_u32(dsmem));
+        uint4 cv[RPL][4];
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+          const int r = rbase + lane + 32 * i;
+          const uint8_t *crow = gbase + C::A_BYTES + C::X_BYTES + r * 64;  // 64-byte swizzled code row
+#pragma unroll
+          for (int c = 0; c < 4; ++c) cv[i][c] = *reinterpret_cast<const uint4 *>(crow + ((c ^ ((r >> 1) & 3)) << 4));
+        }
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
           const int r = rbase + lane + 32 * i;
           const float s0 = rv[i] ? e8m0_value(scur[i] & 0xffu) : 0.f;
           const float s1 = (rv[i] && 2 * kb + 1 < P.G) ? e8m0_value(scur[i] >> 8) : 0.f;
-          const uint32_t crow = base + C::A_BYTES + C::X_BYTES + r * 64;  // 64-byte swizzled code row
-          const uint32_t arow = base + r * 128;                           // 128-byte swizzled A row
+          uint4 *arow = reinterpret_cast<uint4 *>(gbase + r * 128);  // 128-byte swizzled A row
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 v = mt_lds128(crow + ((c ^ ((r >> 1) & 3)) << 4));
             const float sc = c < 2 ? s0 : s1;
-            mt_sts128(arow + (((2 * c) ^ (r & 7)) << 4), mx_chunk_bf16(v.x, v.y, sc));
-            mt_sts128(arow + (((2 * c + 1) ^ (r & 7)) << 4), mx_chunk_bf16(v.z, v.w, sc));
+            arow[(2 * c) ^ (r & 7)] = mx_chunk_bf16(cv[i][c].x, cv[i][c].y, sc);
+            arow[(2 * c + 1) ^ (r & 7)] = mx_chunk_bf16(cv[i][c].z, cv[i][c].w, sc);
           }
         }
         fence_proxy_async_smem();
