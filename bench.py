@@ -60,9 +60,9 @@ def load_peaks() -> dict:
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
 # config's kernels, from one ncu capture of `python bench.py --config C --steps 3
 # --warmup 3 --no-cpu-baseline` (the summary is in profiles/dram_traffic_by_config.md).
-# It is reported only while the kernel sources hash to TRAFFIC_SOURCES, since a
-# changed kernel needs a new capture.
-TRAFFIC_SOURCES = "2113f9c28be08f97"
+# An entry is reported only while its kernel family's sources hash to the value
+# in TRAFFIC_SOURCES, since a changed kernel needs a new capture.
+TRAFFIC_SOURCES = {}  # family -> source hash the TRAFFIC entries were measured with
 TRAFFIC = {
     ("mlp", "tp_all_to_sharded"): 97733376,
     ("mlp", "tp_sharded_to_all"): 102651904,
@@ -96,19 +96,30 @@ TRAFFIC = {
 }
 
 
-def kernel_sources_hash() -> str:
+# The sources each family of kernels is built from (the shared host code and
+# headers belong to every family).
+COMMON_SOURCES = ["tp_api.cu", "tp_internal.h", "ptx.cuh", "tmap.cu"]
+FAMILY_SOURCES = {"umma": ["k_umma.cu", "k_colsum.cu", "k_simt.cu"], "q4": ["k_q4.cu", "k_q4gemv.cu"],
+                  "mx": ["k_mx.cu"]}
+
+
+def config_family(config: str) -> str:
+    return "q4" if config.startswith("q4_") else "mx" if config.startswith("mx_") else "umma"
+
+
+def kernel_sources_hash(family: str) -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "sharded_gemm_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in COMMON_SOURCES + FAMILY_SOURCES[family]:
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def traffic_for(config: str, kernel: str):
-    if kernel_sources_hash() != TRAFFIC_SOURCES:
+    fam = config_family(config)
+    if kernel_sources_hash(fam) != TRAFFIC_SOURCES.get(fam):
         return None
     return TRAFFIC.get((config, kernel))
 
