@@ -709,57 +709,6 @@ __global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_con
 
 namespace {
 
-// Ordered sum of the split slots: block (tile, group of CG token columns),
-// thread m = tile row; out[t][row] = (slot_0 + slot_1 + ... in split order)
-// + bias.
-struct MrJob {
-  void *C;
-  const float *bias;
-  int64_t ldc, ws_base;
-  int rows, T, tiles, splits, block0;
-};
-struct MrArgs {
-  MrJob jobs[kMaxJobs];
-  const float *ws;
-  int njobs, nblocks, BN, CG, out_dt;
-};
-
-__global__ void __launch_bounds__(256) mx_reduce_kernel(const __grid_constant__ MrArgs a) {
-  // item = (block index b over the split tiles' column groups, column c of
-  // the group, row m); consecutive threads take consecutive rows
-  const int64_t per_block = (int64_t)a.CG * 128;
-  const int64_t total = (int64_t)a.nblocks * per_block;
-  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total; it += (int64_t)gridDim.x * blockDim.x) {
-    const int b = (int)(it / per_block);
-    const int rem = (int)(it - (int64_t)b * per_block);
-    const int cl = rem >> 7, m = rem & 127;
-    int j = 0;
-    while (j + 1 < a.njobs && b >= a.jobs[j + 1].block0) ++j;
-    const MrJob &J = a.jobs[j];
-    const int gpt = a.BN / a.CG;  // column groups per tile
-    const int local = b - J.block0;
-    const int tile_lin = local / gpt, cg = local - tile_lin * gpt;
-    const int tile = tile_lin % J.tiles, ntile = tile_lin / J.tiles;
-    const int c = cg * a.CG + cl;
-    const int orow = tile * 128 + m;
-    const int t = ntile * a.BN + c;
-    const float *s0 = a.ws + (J.ws_base + (int64_t)tile_lin * J.splits) * 128 * a.BN + (int64_t)c * 128 + m;
-    float v = __ldcg(s0);
-#pragma unroll 8
-    for (int sp = 1; sp < J.splits; ++sp) v += __ldcg(s0 + (int64_t)sp * 128 * a.BN);
-    if (orow < J.rows && t < J.T) {
-      if (J.bias) v += __ldg(J.bias + orow);
-      const int64_t idx = (int64_t)t * J.ldc + orow;
-      if (a.out_dt == TP_F32)
-        static_cast<float *>(J.C)[idx] = v;
-      else if (a.out_dt == TP_BF16)
-        static_cast<__nv_bfloat16 *>(J.C)[idx] = __float2bfloat16_rn(v);
-      else
-        static_cast<__half *>(J.C)[idx] = __float2half_rn(v);
-    }
-  }
-}
-
 std::mutex g_mt_mu;
 
 template <int BN, int STAGES>
@@ -903,25 +852,12 @@ int launch_mx_tc(const Problem &p, cudaStream_t s, bool *handled) {
   if (rc != TP_OK) return rc;
   *handled = true;
   if (slots > 0) {  // ordered sums of the split tiles
-    static MrArgs ra;
-    memset(&ra, 0, sizeof(ra));
-    int nb = 0;
+    SplitJob sj[kMaxJobs];
     for (int j = 0; j < p.njobs; ++j) {
       const MtJob &Q = args.jobs[j];
-      ra.jobs[j] = MrJob{Q.C, Q.bias, Q.ldc, Q.ws_base, Q.rows, Q.T, Q.tiles, Q.splits, nb};
-      if (Q.splits > 1) nb += Q.tiles * Q.ntiles * (BN / std::min(BN, 32));
+      sj[j] = SplitJob{Q.C, Q.bias, Q.ldc, Q.ws_base, Q.rows, Q.T, Q.tiles, Q.ntiles, Q.splits};
     }
-    ra.ws = args.ws;
-    ra.CG = std::min(BN, 32);
-    ra.njobs = p.njobs;
-    ra.nblocks = nb;
-    ra.BN = BN;
-    ra.out_dt = p.out_dt;
-    const int64_t items = (int64_t)nb * ra.CG * 128;
-    const int grid = (int)std::min<int64_t>((items + 255) / 256, (int64_t)sms * 16);
-    mx_reduce_kernel<<<grid, 256, 0, s>>>(ra);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "mx_reduce_kernel launch");
+    return launch_split_reduce(sj, p.njobs, args.ws, BN, p.out_dt, s);
   }
   return TP_OK;
 }

@@ -17,10 +17,11 @@
 // Prefill (T > 16): the converter writes the dequantized values
 // s*q + b (float32, rounded once to bf16) and the groups accumulate in one
 // TMEM accumulator.
-// Small-T tiles are split over CTAs by K (rank by rank for the row-parallel
-// layer); each split's float32 partial goes to a workspace slot and the CTA
+// Tiles are split over CTAs by K (rank by rank for the row-parallel layer);
+// each split's float32 partial goes to a workspace slot.  Decode: the warp
 // that arrives last at the tile's counter adds the slots in split order (rank
-// order), then the bias once.  No CTA ever waits for another.
+// order), then the bias once; no CTA ever waits for another.  Prefill: a
+// second launch adds each tile's column-major slots in split order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <string.h>
@@ -615,8 +616,11 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
         tc_fence_after();
         const float bias = (valid && J.bias) ? __ldg(J.bias + orow) : 0.f;
         const int t0 = ui.ntile * C::BN;
+        // split tiles: float32 partials to column-major workspace slots (a
+        // warp's 32 rows of one column are one 128-byte line); a second launch
+        // adds each tile's slots in split (rank) order, then the bias
         const bool split = J.splits > 1;
-        float *slot = split ? a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 + m) * C::BN
+        float *slot = split ? a.ws + (J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 * C::BN + m
                             : nullptr;
 #pragma unroll 1
         for (int c = 0; c < C::BN / 32; ++c) {
@@ -625,8 +629,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
           tmem_wait_ld();
           if (split) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              __stcg(reinterpret_cast<float4 *>(slot + c * 32 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+            for (int i = 0; i < 32; ++i) __stcg(slot + (c * 32 + i) * 128, v[i]);
           } else if (valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -641,50 +644,6 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
         if (++ds == C::ND) {
           ds = 0;
           dph ^= 1;
-        }
-        if (split) {
-          __threadfence();
-          __syncwarp();
-          int prev = 0;
-          int *cnt = a.cnt + (int64_t)(J.cnt_base + ui.tile_lin) * 4 + quarter;
-          if (lane == 0) prev = atomicAdd(cnt, 1);
-          prev = __shfl_sync(0xffffffffu, prev, 0);
-          if (prev == J.splits - 1) {
-            __threadfence();
-            const float *s0 = a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits) * 128 + m) * C::BN;
-#pragma unroll 1
-            for (int c = 0; c < C::BN / 32; ++c) {
-              float sum[32];
-#pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                const float4 f = __ldcg(reinterpret_cast<const float4 *>(s0 + c * 32 + i));
-                sum[i] = f.x;
-                sum[i + 1] = f.y;
-                sum[i + 2] = f.z;
-                sum[i + 3] = f.w;
-              }
-              for (int j = 1; j < J.splits; ++j) {
-                const float *sj = s0 + (int64_t)j * 128 * C::BN + c * 32;
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                  const float4 f = __ldcg(reinterpret_cast<const float4 *>(sj + i));
-                  sum[i] += f.x;
-                  sum[i + 1] += f.y;
-                  sum[i + 2] += f.z;
-                  sum[i + 3] += f.w;
-                }
-              }
-              if (valid) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const int t = t0 + c * 32 + i;
-                  if (t < J.T) q4_store(a, J, t, orow, sum[i] + bias);
-                }
-              }
-            }
-            __syncwarp();
-            if (lane == 0) *cnt = 0;
-          }
         }
       }
     }
@@ -1286,8 +1245,17 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws)
     }
   args.sb_vec = sbv;
   int rc;
-  if (!decode)
+  if (!decode) {
     rc = q4_launch_cfg<false>(args, sms, s);
+    if (rc == TP_OK && slots > 0) {  // ordered sums of the split tiles
+      SplitJob sj[kMaxJobs];
+      for (int j = 0; j < p.njobs; ++j) {
+        const Q4Job &Q = args.jobs[j];
+        sj[j] = SplitJob{Q.C, Q.bias, Q.ldc, Q.ws_base, Q.rows, Q.T, Q.tiles, Q.ntiles, Q.splits};
+      }
+      rc = launch_split_reduce(sj, p.njobs, args.ws, BN, p.out_dt, s);
+    }
+  }
   else if (maxT <= 1)
     rc = q4_decode_launch<1>(args, sms, s);
   else if (maxT <= 4)

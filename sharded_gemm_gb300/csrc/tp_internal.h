@@ -99,6 +99,15 @@ int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void 
                     void *qbias, cudaStream_t s);
 int launch_debug_wait(int64_t limit_ns, int *status, cudaStream_t s);
 int launch_mx(const Problem &p, cudaStream_t s, bool *handled);
+// Ordered sum of split-K partial tiles (k_split.cu): tiles of 128 rows x BN
+// token columns, `splits` float32 slots each, column-major, from ws_base.
+struct SplitJob {
+  void *C;
+  const float *bias;
+  int64_t ldc, ws_base;
+  int rows, T, tiles, ntiles, splits;
+};
+int launch_split_reduce(const SplitJob *jobs, int njobs, const float *ws, int BN, int out_dt, cudaStream_t s);
 int launch_mx_quantize(const float *w, int64_t rows, int64_t K, uint8_t *codes, uint8_t *scales,
                        cudaStream_t s);
 int launch_colsum(int nout, int nin, const void *const *in, int64_t rows, int64_t cols, int64_t ld,
