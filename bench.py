@@ -224,7 +224,7 @@ def make_workload(name: str, rank: int, device: str):
         info = dict(workload="mlp_col_row_pair", T=T, D=D, F=F, N=cfg["N"], unit="TFLOP/s",
                     work=w.flops, bound="tensor", kernel_names=["tp_all_to_sharded", "tp_sharded_to_all"],
                     kernel_work=[2.0 * T * D * F, 2.0 * T * D * F],
-                    launches_per_step=2, h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
+                    h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     if name == "mlp_bwd":
         cfg = synth.mlp(seed=seed)
@@ -236,7 +236,7 @@ def make_workload(name: str, rank: int, device: str):
                     kernel_names=["tp_sharded_to_all_dx", "tp_sharded_dw(w2)", "tp_bias_grad(b2)",
                                   "tp_all_to_sharded_dx", "tp_sharded_dw(w1)", "tp_bias_grad(b1)"],
                     kernel_work=[g, g, T * D, g, g, T * F],
-                    launches_per_step=6, h2d=("dy", w.dy), d2h=("dx", w.dx),
+                    h2d=("dy", w.dy), d2h=("dx", w.dx),
                     cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     if name == "ffn_gated":
@@ -247,7 +247,7 @@ def make_workload(name: str, rank: int, device: str):
                     work=w.flops, bound="tensor",
                     kernel_names=["tp_gated_all_to_sharded", "tp_sharded_to_all"],
                     kernel_work=[4.0 * T * D * F, 2.0 * T * D * F],
-                    launches_per_step=2, h2d=("x", w.x), d2h=("y", w.y),
+                    h2d=("x", w.x), d2h=("y", w.y),
                     cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     if name == "mlp_ag_rs":
@@ -258,7 +258,7 @@ def make_workload(name: str, rank: int, device: str):
                     work=w.flops, bound="tensor",
                     kernel_names=["tp_gathered_to_sharded", "tp_sharded_to_sharded"],
                     kernel_work=[2.0 * T * D * F, 2.0 * T * D * F],
-                    launches_per_step=2, h2d=("x shards", w.xs), d2h=("y shards", w.ys),
+                    h2d=("x shards", w.xs), d2h=("y shards", w.ys),
                     cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     if name in ("summa2", "summa4"):
@@ -266,8 +266,7 @@ def make_workload(name: str, rank: int, device: str):
         cfg = synth.summa(seed=seed)
         w = Summa(cfg, q)
         info = dict(workload="summa_%dx%d" % (q, q), unit="TFLOP/s", work=w.flops, bound="tensor",
-                    kernel_names=["tp_summa"], kernel_work=[w.flops], launches_per_step=1,
-                    h2d=None, d2h=None, cfg_keys=dict(M=8192, K=8192, N=8192, q=q))
+                    kernel_names=["tp_summa"], kernel_work=[w.flops], h2d=None, d2h=None, cfg_keys=dict(M=8192, K=8192, N=8192, q=q))
         return w, w.step, info
     if name.startswith("qkv"):
         T = int(name[3:])
@@ -280,7 +279,7 @@ def make_workload(name: str, rank: int, device: str):
         info = dict(workload="qkv_o_lmhead_T%d" % T, unit="GB/s" if decode else "TFLOP/s",
                     work=(w.weight_bytes if decode else w.flops), bound="hbm" if decode else "tensor",
                     kernel_names=["tp_all_to_sharded(qkv)", "tp_sharded_to_all(o)", "tp_all_to_sharded(lm_head)"],
-                    kernel_work=kb if decode else kw, launches_per_step=3, h2d=("x", w.x), d2h=("logits", w.logits),
+                    kernel_work=kb if decode else kw, h2d=("x", w.x), d2h=("logits", w.logits),
                     cfg_keys=dict(T=T, D=D, V=V, N=cfg["N"]))
         return w, w.step, info
     if name.startswith("q4_"):
@@ -293,8 +292,7 @@ def make_workload(name: str, rank: int, device: str):
         info = dict(workload="q4_pair_T%d" % T, unit="GB/s" if decode else "TFLOP/s",
                     work=(w.weight_bytes if decode else w.flops), bound="hbm" if decode else "tensor",
                     kernel_names=["tp_q4_all_to_sharded", "tp_q4_sharded_to_all"],
-                    kernel_work=[per, per] if decode else [2.0 * T * D * F] * 2, launches_per_step=2,
-                    h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
+                    kernel_work=[per, per] if decode else [2.0 * T * D * F] * 2, h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     if name.startswith("mx_"):
         T = int(name[3:])
@@ -306,8 +304,7 @@ def make_workload(name: str, rank: int, device: str):
         info = dict(workload="mxfp8_pair_T%d" % T, unit="GB/s" if decode else "TFLOP/s",
                     work=(w.weight_bytes if decode else w.flops), bound="hbm" if decode else "tensor",
                     kernel_names=["tp_mx_all_to_sharded", "tp_mx_sharded_to_all"],
-                    kernel_work=[per, per] if decode else [2.0 * T * D * F] * 2, launches_per_step=2,
-                    h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
+                    kernel_work=[per, per] if decode else [2.0 * T * D * F] * 2, h2d=("x", w.x), d2h=("y", w.y), cfg_keys=dict(T=T, D=D, F=F, N=cfg["N"]))
         return w, w.step, info
     raise SystemExit("unknown config %s" % name)
 
@@ -427,8 +424,10 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
     for _ in range(max(args.warmup, 3)):
+        n0 = tp.tp_launch_count()
         for fn in launches:
             fn(stream)
+        launches_per_step = tp.tp_launch_count() - n0  # the library's own kernels in one step
     torch.cuda.synchronize()
     if tp.tp_query_status() != 0:
         raise SystemExit("device status error during warm-up")
@@ -529,7 +528,7 @@ def main():
                            parallelism="1 GPU per rank; N logical shards as separate HBM buffers"),
             "kernels_ms": {n: round(t, 5) for n, t in zip(info["kernel_names"], per_kernel)},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": info["launches_per_step"] * args.steps, "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         }
         if args.policy != "auto":
             line["policy"] = args.policy

@@ -70,6 +70,11 @@ int tp_version(void);
 /* Message describing the last error returned to the calling thread ("" if none). */
 const char *tp_last_error(void);
 
+/* Number of kernels this library has launched from the calling thread so far
+ * (monotonic; a call may launch several, e.g. a GEMM and its ordered split
+ * reduction).  Never fails. */
+int64_t tp_launch_count(void);
+
 /* Synchronizes `stream`, copies the current device's status word into
  * *device_status (0 = no error, else a tp_status such as TP_ERR_TIMEOUT)
  * and resets the word to 0.  Returns TP_OK or TP_ERR_CUDA. */

@@ -49,6 +49,7 @@ def lib() -> ctypes.CDLL:
         sig = {
             "tp_version": ([], i32),
             "tp_last_error": ([], ctypes.c_char_p),
+            "tp_launch_count": ([], i64),
             "tp_query_status": ([vp, ctypes.POINTER(ctypes.c_int)], i32),
             "tp_set_policy": ([i32], i32),
             "tp_set_wait_limit_ns": ([i64], i32),
@@ -155,6 +156,11 @@ def _common_ld(ts, name):
 # ------------------------------------------------------------------ API
 def tp_version() -> int:
     return lib().tp_version()
+
+
+def tp_launch_count() -> int:
+    """Kernels launched by the library from this thread so far (monotonic)."""
+    return lib().tp_launch_count()
 
 
 def tp_last_error() -> str:

@@ -157,6 +157,7 @@ static int launch_colsum_cluster(const ColSumArgs &a, int nout, cudaStream_t s) 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, colsum_cluster_kernel<DT>, a);
+  note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "colsum_cluster_kernel launch");
 }
@@ -188,6 +189,7 @@ int launch_colsum(int nout, int nin, const void *const *in, int64_t rows, int64_
     colsum_kernel<TP_BF16><<<grid, 256, 0, s>>>(a);
   else
     colsum_kernel<TP_F16><<<grid, 256, 0, s>>>(a);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "colsum_kernel launch");
 }

@@ -24,6 +24,7 @@ __global__ void debug_wait_kernel(int64_t limit_ns, int *status) {
 
 int launch_debug_wait(int64_t limit_ns, int *status, cudaStream_t s) {
   debug_wait_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "debug_wait_kernel launch");
 }

@@ -64,6 +64,7 @@ int launch_mx_quantize(const float *w, int64_t rows, int64_t K, uint8_t *codes, 
   if (total == 0) return TP_OK;
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, 65535);
   quantize_mx_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, rows, K, codes, scales);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "quantize_mx_kernel launch");
 }
@@ -310,6 +311,7 @@ static int launch_mx_gemv(const Problem &p, cudaStream_t s, bool *handled) {
   TP_MX_CASE(3)
   TP_MX_CASE(4)
 #undef TP_MX_CASE
+  note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "mx_gemv_kernel launch");
   *handled = true;
@@ -725,6 +727,7 @@ int mt_launch(MtArgs &args, int sms, cudaStream_t s) {
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
   kern<<<grid, kMtThreads, smem, s>>>(args);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "mx_umma_kernel launch");
 }

@@ -96,6 +96,7 @@ int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void 
   if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
   quantize_affine4_kernel<<<(unsigned)blocks, 128, 0, s>>>(w, rows, K, wq, (__half *)scales,
                                                            (__half *)qbias);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "quantize kernel launch");
 }
@@ -1057,6 +1058,7 @@ int q4_decode_launch(Q4Args &args, int sms, cudaStream_t s) {
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
   kern<<<grid, kQThreads, smem, s>>>(args);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "q4_decode_kernel launch");
 }
@@ -1080,6 +1082,7 @@ int q4_launch_cfg(Q4Args &args, int sms, cudaStream_t s) {
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
   kern<<<grid, kQThreads, smem, s>>>(args);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "q4_umma_kernel launch");
 }

@@ -714,6 +714,7 @@ int launch_one(K kern, const A &args, int grid, int threads, size_t smem, int sm
     attr_done[dev & 63] = true;
   }
   kern<<<grid, threads, smem, s>>>(args);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, what);
 }

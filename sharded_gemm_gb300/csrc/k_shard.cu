@@ -96,6 +96,7 @@ int launch_shard(const void *w, int64_t rows, int64_t cols, int eb, int axis, in
     case 2: shard_kernel<uint16_t><<<(unsigned)blocks, 256, 0, s>>>(a); break;
     default: shard_kernel<uint8_t><<<(unsigned)blocks, 256, 0, s>>>(a); break;
   }
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "shard_kernel launch");
 }

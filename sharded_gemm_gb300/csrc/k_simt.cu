@@ -154,6 +154,7 @@ int launch_simt(const Problem &p, cudaStream_t s) {
       simt_gemm_kernel<DT, BL, BL == BL_KMAJOR><<<grid, 256, 0, s>>>(p);          \
     else                                                                          \
       simt_gemm_kernel<DT, BL, false><<<grid, 256, 0, s>>>(p);                    \
+    note_launch();                                                                \
     cudaError_t e = cudaGetLastError();                                           \
     return e == cudaSuccess ? TP_OK : cuda_error(e, "simt_gemm_kernel launch");   \
   }

@@ -78,6 +78,7 @@ int launch_split_reduce(const SplitJob *jobs, int njobs, const float *ws, int BN
   a.nitems = items;
   const int grid = (int)std::min<int64_t>((items + 255) / 256, (int64_t)sm_count() * 16);
   split_reduce_kernel<<<grid, 256, 0, s>>>(a);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "split_reduce_kernel launch");
 }

@@ -964,6 +964,7 @@ int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
   kern<<<grid, kThreads, smem, s>>>(args);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_gemm_kernel launch");
 }
@@ -998,6 +999,7 @@ int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
+  note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_pair_kernel launch");
 }
@@ -1031,6 +1033,7 @@ int launch_row_cluster(UmmaArgs &args, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
+  note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_row_cluster_kernel launch");
 }

@@ -13,6 +13,9 @@
 namespace tp {
 
 static thread_local std::string t_last_error;
+static thread_local int64_t t_launches = 0;
+
+void note_launch() { ++t_launches; }
 static std::atomic<int> g_policy{TP_POLICY_AUTO};
 static std::atomic<int64_t> g_wait_ns{2000000000LL};
 static std::atomic<unsigned long long *> g_trace{nullptr};
@@ -80,6 +83,8 @@ static int dispatch(Problem &p, cudaStream_t s) {
 }  // namespace tp
 
 using namespace tp;
+
+int64_t tp_launch_count(void) { return t_launches; }
 
 extern "C" {
 

@@ -77,6 +77,7 @@ int64_t wait_limit_ns();
 bool pair_policy_allowed();  // false under TP_POLICY_SINGLE_SM (no pairs, no rank clusters)
 void trace_buffer(unsigned long long **buf, int64_t *cap_records);
 int set_error(int code, const char *fmt, ...);
+void note_launch();  // counts one kernel launch of the calling thread (tp_launch_count)
 int cuda_error(cudaError_t e, const char *what);
 
 // ---- launchers (each returns TP_OK or a tp_status, error message set)

@@ -29,6 +29,11 @@ def test_exports_every_declared_symbol(L):
         assert hasattr(L, n), n
 
 
+def test_launch_count_needs_no_gpu(L):
+    n = L.tp_launch_count()
+    assert n >= 0 and L.tp_launch_count() == n
+
+
 def test_version(L):
     assert L.tp_version() >= 100
 
