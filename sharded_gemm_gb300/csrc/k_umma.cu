@@ -482,7 +482,6 @@ template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false,
 __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_constant__ UmmaArgs a) {
   static_assert(!A_MN || NSUB == 1, "M-major A with one-tile units");
   static_assert(!TSTORE || (!GATED && ChunkOf<BN / 2>::v == 32), "TMA stores of 32-column float32 chunks");
-  static_assert(NSUB == 1 || !B_MN, "two-tile units are for K-major B");
   static_assert(!GATED || (NSUB == 2 && NACC == 1), "gated units are two accumulators of one tile");
   constexpr int BNH = BN / 2;
   constexpr int A_BYTES = BM * BK * 2;
@@ -569,10 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
             } else {
               tma_load_2d_pair(sa, &a.mapA[P.amap], fb, kb * BK, rowA0);
             }
-            if constexpr (B_MN) {
+            if constexpr (B_MN) {  // per sub-tile: BN/2 columns as 64-column boxes
 #pragma unroll
-              for (int c = 0; c < BNH / 64; ++c)
-                tma_load_2d_pair(sb + c * 8192, &a.mapB[P.bmap], fb, rowB0 + c * 64, kb * BK);
+              for (int sub = 0; sub < NSUB; ++sub)
+#pragma unroll
+                for (int c = 0; c < BNH / 64; ++c)
+                  tma_load_2d_pair(sb + sub * B_SUB + c * 8192, &a.mapB[P.bmap], fb, rowB0 + sub * BNH + c * 64,
+                                   kb * BK);
             } else if constexpr (GATED) {
               tma_load_2d_pair(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);  // BN/2 rows of W1
               tma_load_2d_pair(sb + B_SUB, &a.mapB[P.bmap2], fb, kb * BK, rowB0);  // and of W3
@@ -626,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
                                        : umma_desc_sw128(sa + kk * 32, 16, 1024);
 #pragma unroll
               for (int sub = 0; sub < NSUB; ++sub) {
-                const uint64_t bd = B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
+                const uint64_t bd = B_MN ? umma_desc_sw128(sb + sub * B_SUB + kk * 2048, 8192, 1024)
                                          : umma_desc_sw128(sb + sub * B_SUB + kk * 32, 16, 1024);
                 umma_f16_pair(d + (uint32_t)(sub * BN), ad, bd, a.idesc, (kb > 0 || kk > 0 || p > 0) ? 1u : 0u);
               }
@@ -1158,7 +1160,7 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     BN = 256;
     for (int pm = 0; pm < (allow_pair ? 2 : 1); ++pm) {
       for (int ns = 1; ns <= 2; ++ns) {
-        if (ns == 2 && (!pm || summa)) continue;
+        if (ns == 2 && (!pm || p.a_mn)) continue;
         for (int bn : {256, 192, 160}) {
           if (summa && bn != 256) continue;
           const int64_t mrows = pm ? 2 * BM : BM;
@@ -1310,6 +1312,8 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     rc = launch_pair<256, true, 6, 2, 1, false, true, true>(args, sms, s);
   else if (pair && summa && p.a_mn)
     rc = launch_pair<256, true, 6, 2, 1, false, true>(args, sms, s);
+  else if (pair && summa && nsub == 2)
+    rc = launch_pair<256, true, 4, 1, 2>(args, sms, s);
   else if (pair && summa)
     rc = launch_pair<256, true, 7, 2, 1>(args, sms, s);
   else if (pair && nsub == 2 && BN == 160)
