@@ -452,6 +452,61 @@ struct MtCfg {
   static constexpr int CHK = BN >= 32 ? 32 : 16;
 };
 
+// Epilogue role (4 warps): per unit, the 128 x BN float32 tile from TMEM slot
+// ds to the output (token t, row) with the bias, or to the unit's split slot.
+template <int BN, int ND>
+__device__ __forceinline__ void mt_epilogue(const MtArgs &a, uint32_t tmem, uint64_t *dfull_bar,
+                                            uint64_t *dempty_bar, int &abort_sh, int warp, int lane) {
+  using C = MtCfg<BN>;
+  const uint64_t lim = a.wait_ns;
+  const int q = warp & 3;
+  const int m = q * 32 + lane;
+  const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+  int ds = 0;
+  uint32_t dph = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+    MtUnit ui;
+    mt_unit(a, u, ui);
+    const MtJob &J = a.jobs[ui.job];
+    const int orow = ui.tile * 128 + m;
+    const bool valid = orow < J.rows;
+    MT_WAIT_ALL(smem_u32(&dfull_bar[ds]), dph, ok);
+    if (!ok) break;
+    tc_fence_after();
+    const float bias = (valid && J.bias) ? __ldg(J.bias + orow) : 0.f;
+    const int t0 = ui.ntile * BN;
+    const bool split = J.splits > 1;
+    float *slot = split ? a.ws + (J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 * BN + m : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < BN / C::CHK; ++c) {
+      float v[C::CHK];
+      if constexpr (C::CHK == 32)
+        tmem_ld32(tmem + lane_off + ds * BN + c * 32, v);
+      else
+        tmem_ld16(tmem + lane_off + ds * BN + c * 16, v);
+      tmem_wait_ld();
+      if (split) {
+#pragma unroll
+        for (int i = 0; i < C::CHK; ++i) __stcg(slot + (c * C::CHK + i) * 128, v[i]);
+      } else if (valid) {
+#pragma unroll
+        for (int i = 0; i < C::CHK; ++i) {
+          const int t = t0 + c * C::CHK + i;
+          if (t < J.T) mt_store(a, J, t, orow, v[i] + bias);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[ds]));
+    if (++ds == ND) {
+      ds = 0;
+      dph ^= 1;
+    }
+  }
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_constant__ MtArgs a) {
   using C = MtCfg<BN>;
@@ -649,53 +704,206 @@ __global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_con
       }
     }
   } else {
-    // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;
-    const int m = q * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    int ds = 0;
-    uint32_t dph = 0;
+    mt_epilogue<BN, ND>(a, tmem, dfull_bar, dempty_bar, abort_sh, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::COLS);
+  }
+}
+
+// Decode form (BN <= 32).  The TMA ring holds only a stage's x tile and
+// codes (10-12 KB, so about 15 stages of codes are in flight); stage n is
+// converted by converter group n % 2 (4 warps, 32 rows each) into A buffer
+// n % NA (bf16 weights + a copy of the x tile), and its ring slot is released
+// as soon as it has been read.  The MMA reads only the A buffer.
+template <int BN, int STAGES, int NA>
+__global__ void __launch_bounds__(kMtThreads, 1) mx_dec_kernel(const __grid_constant__ MtArgs a) {
+  using C = MtCfg<BN>;
+  constexpr int X_BYTES = BN * 128;
+  constexpr int C_BYTES = 128 * 64;
+  constexpr int RING = X_BYTES + C_BYTES;  // x (128-byte swizzle) then codes (64-byte swizzle)
+  constexpr int A_BYTES = 128 * 128;
+  constexpr int ABUF = A_BYTES + X_BYTES;  // bf16 weights then the x copy
+  constexpr int ND = C::ND;
+  static_assert(RING % 1024 == 0 && ABUF % 1024 == 0, "alignment");
+
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t afull_bar[NA], aempty_bar[NA];
+  __shared__ __align__(8) uint64_t dfull_bar[ND], dempty_bar[ND];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint32_t abase = sbase + STAGES * RING;
+  const uint64_t lim = a.wait_ns;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), 4);
+    }
+    for (int i = 0; i < NA; ++i) {
+      mbar_init(smem_u32(&afull_bar[i]), 4);
+      mbar_init(smem_u32(&aempty_bar[i]), 1);
+    }
+    for (int i = 0; i < ND; ++i) {
+      mbar_init(smem_u32(&dfull_bar[i]), 1);
+      mbar_init(smem_u32(&dempty_bar[i]), 4);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_sh), C::COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_sh;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      bool used[STAGES];
+      uint32_t lastph[STAGES];
+#pragma unroll
+      for (int i = 0; i < STAGES; ++i) used[i] = false;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        MtUnit ui;
+        mt_unit(a, u, ui);
+        const MtPart &P = a.parts[ui.part];
+        for (int kb = ui.kb0; kb < ui.kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&empty_bar[st]), ph ^ 1, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          const uint32_t base = sbase + st * RING;
+          const uint32_t fb = smem_u32(&full_bar[st]);
+          mbar_arrive_expect_tx(fb, RING);
+          tma_load_2d(base, &a.xmaps[P.xmap], fb, kb * 64, ui.ntile * BN);
+          tma_load_2d(base + X_BYTES, &a.cmaps[P.cmap], fb, kb * 64, ui.tile * 128);
+          used[st] = true;
+          lastph[st] = ph;
+          if (++st == STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok)
+        for (int i = 0; i < STAGES; ++i)
+          if (used[i]) mbar_wait(smem_u32(&full_bar[i]), lastph[i], lim, a.status, nullptr);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int n = 0, ds = 0;
+      uint32_t dph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
+        MtUnit ui;
+        mt_unit(a, u, ui);
+        bool first = true;
+        for (int kb = ui.kb0; kb < ui.kb1; ++kb, ++n) {
+          const int ab = n % NA;
+          if (!mbar_wait(smem_u32(&afull_bar[ab]), (uint32_t)((n / NA) & 1), lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          if (first && !mbar_wait(smem_u32(&dempty_bar[ds]), dph ^ 1, lim, a.status, &abort_sh)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ba = abase + ab * ABUF;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16(tmem + ds * BN, umma_desc_sw128(ba + kk * 32, 16, 1024),
+                     umma_desc_sw128(ba + A_BYTES + kk * 32, 16, 1024), a.idesc, (first && kk == 0) ? 0u : 1u);
+          umma_commit(smem_u32(&aempty_bar[ab]));
+          first = false;
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&dfull_bar[ds]));
+        if (++ds == ND) {
+          ds = 0;
+          dph ^= 1;
+        }
+      }
+      umma_commit(smem_u32(&drain_bar));
+      mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
+    }
+  } else if (warp < 10) {
+    // ---------------------------------------------------------- converters
+    const int g = (warp - 2) >> 2, q = (warp - 2) & 3;
+    const int r = q * 32 + lane;  // weight row of the tile
+    const int tg = q * 32 + lane; // thread index in the group (x copy)
+    int n = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
       MtUnit ui;
       mt_unit(a, u, ui);
+      const MtPart &P = a.parts[ui.part];
       const MtJob &J = a.jobs[ui.job];
-      const int orow = ui.tile * 128 + m;
-      const bool valid = orow < J.rows;
-      MT_WAIT_ALL(smem_u32(&dfull_bar[ds]), dph, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const float bias = (valid && J.bias) ? __ldg(J.bias + orow) : 0.f;
-      const int t0 = ui.ntile * BN;
-      const bool split = J.splits > 1;
-      float *slot = split ? a.ws + (J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 * BN + m : nullptr;
-#pragma unroll 1
-      for (int c = 0; c < BN / C::CHK; ++c) {
-        float v[C::CHK];
-        if constexpr (C::CHK == 32)
-          tmem_ld32(tmem + lane_off + ds * BN + c * 32, v);
-        else
-          tmem_ld16(tmem + lane_off + ds * BN + c * 16, v);
-        tmem_wait_ld();
-        if (split) {
+      const int n0 = n;
+      n += ui.kb1 - ui.kb0;
+      const int orow = ui.tile * 128 + r;
+      const bool rv = orow < J.rows;
+      const uint8_t *srow = P.sc + (int64_t)(rv ? orow : 0) * P.G;
+      int kb = ui.kb0 + (((g - n0) % 2) + 2) % 2;  // this group's first k-block of the unit
+      uint32_t snext = (rv && kb < ui.kb1) ? mt_scale_pair(srow, kb, P.G) : 0u;
+      for (; ok && kb < ui.kb1; kb += 2) {
+        const int seq = n0 + (kb - ui.kb0);
+        const int cs = seq % STAGES, ab = seq % NA;
+        const uint32_t scur = snext;
+        snext = (rv && kb + 2 < ui.kb1) ? mt_scale_pair(srow, kb + 2, P.G) : 0u;
+        MT_WAIT_ALL(smem_u32(&full_bar[cs]), (uint32_t)((seq / STAGES) & 1), ok);
+        if (!ok) break;
+        MT_WAIT_ALL(smem_u32(&aempty_bar[ab]), (uint32_t)(((seq / NA) & 1) ^ 1), ok);
+        if (!ok) break;
+        uint8_t *ring = dsmem + (sbase + cs * RING - smem_u32(dsmem));
+        uint8_t *abuf = dsmem + (abase + ab * ABUF - smem_u32(dsmem));
+        uint4 cv[4];
+        const uint8_t *crow = ring + X_BYTES + r * 64;  // 64-byte swizzled code row
 #pragma unroll
-          for (int i = 0; i < C::CHK; ++i) __stcg(slot + (c * C::CHK + i) * 128, v[i]);
-        } else if (valid) {
+        for (int c = 0; c < 4; ++c) cv[c] = *reinterpret_cast<const uint4 *>(crow + ((c ^ ((r >> 1) & 3)) << 4));
+        uint4 xv[X_BYTES / 16 / 128];
 #pragma unroll
-          for (int i = 0; i < C::CHK; ++i) {
-            const int t = t0 + c * C::CHK + i;
-            if (t < J.T) mt_store(a, J, t, orow, v[i] + bias);
-          }
+        for (int i = 0; i < X_BYTES / 16 / 128; ++i) xv[i] = reinterpret_cast<const uint4 *>(ring)[tg + 128 * i];
+        const float s0 = rv ? e8m0_value(scur & 0xffu) : 0.f;
+        const float s1 = (rv && 2 * kb + 1 < P.G) ? e8m0_value(scur >> 8) : 0.f;
+        uint4 *arow = reinterpret_cast<uint4 *>(abuf + r * 128);  // 128-byte swizzled A row
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float sc = c < 2 ? s0 : s1;
+          arow[(2 * c) ^ (r & 7)] = mx_chunk_bf16(cv[c].x, cv[c].y, sc);
+          arow[(2 * c + 1) ^ (r & 7)] = mx_chunk_bf16(cv[c].z, cv[c].w, sc);
+        }
+#pragma unroll
+        for (int i = 0; i < X_BYTES / 16 / 128; ++i) reinterpret_cast<uint4 *>(abuf + A_BYTES)[tg + 128 * i] = xv[i];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&empty_bar[cs]));  // the ring slot has been read
+          mbar_arrive(smem_u32(&afull_bar[ab]));
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[ds]));
-      if (++ds == ND) {
-        ds = 0;
-        dph ^= 1;
-      }
     }
+  } else {
+    mt_epilogue<BN, ND>(a, tmem, dfull_bar, dempty_bar, abort_sh, warp, lane);
   }
 
   tc_fence_before();
@@ -712,6 +920,25 @@ __global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_con
 namespace {
 
 std::mutex g_mt_mu;
+
+template <int BN, int STAGES, int NA>
+int mt_dec_launch(MtArgs &args, int sms, cudaStream_t s) {
+  auto kern = mx_dec_kernel<BN, STAGES, NA>;
+  constexpr int smem = STAGES * (BN * 128 + 128 * 64) + NA * (128 * 128 + BN * 128) + 1024;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(mx decode)");
+    attr_done[dev & 63] = true;
+  }
+  const int grid = args.total_units < sms ? args.total_units : sms;
+  kern<<<grid, kMtThreads, smem, s>>>(args);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_error(e, "mx_dec_kernel launch");
+}
 
 template <int BN, int STAGES>
 int mt_launch(MtArgs &args, int sms, cudaStream_t s) {
@@ -843,9 +1070,9 @@ int launch_mx_tc(const Problem &p, cudaStream_t s, bool *handled) {
   args.wait_ns = (uint64_t)p.wait_ns;
   int rc;
   if (BN == 16)
-    rc = mt_launch<16, 8>(args, sms, s);
+    rc = mt_dec_launch<16, 15, 4>(args, sms, s);
   else if (BN == 32)
-    rc = mt_launch<32, 8>(args, sms, s);
+    rc = mt_dec_launch<32, 12, 4>(args, sms, s);
   else if (BN == 64)
     rc = mt_launch<64, 4>(args, sms, s);
   else if (BN == 128)
