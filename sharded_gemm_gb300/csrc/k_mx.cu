@@ -164,8 +164,10 @@ __global__ void __launch_bounds__(kMxWarps * 32, 1) mx_gemv_kernel(const __grid_
 #pragma unroll
         for (int r = 0; r < kMxRows; ++r) acc[t][r] = 0.f;
       const int64_t G = P.K >> 5;
-      // The codes and scales of the next 512-code step are loaded before the
-      // current step is computed, so one step's loads are always in flight.
+      // The codes and scales of the next PD 512-code steps are loaded before
+      // the current step is computed (PD = 2 for one or two tokens), so PD
+      // steps' loads are always in flight.
+      constexpr int PD = TT <= 2 ? 2 : 1;
       const uint8_t *crow[kMxRows];
       const uint8_t *srow[kMxRows];
 #pragma unroll
@@ -174,14 +176,16 @@ __global__ void __launch_bounds__(kMxWarps * 32, 1) mx_gemv_kernel(const __grid_
         crow[r] = P.codes + (int64_t)row * P.ldb;
         srow[r] = P.scales + (int64_t)row * G;
       }
-      uint4 qn[kMxRows];
-      uint32_t sn[kMxRows];
+      uint4 qn[PD][kMxRows];
+      uint32_t sn[PD][kMxRows];
       int64_t k0 = (int64_t)lane * 16;
-      if (k0 < P.K) {
+#pragma unroll
+      for (int d = 0; d < PD; ++d) {
+        const int64_t k = k0 + 512 * d;
 #pragma unroll
         for (int r = 0; r < kMxRows; ++r) {
-          qn[r] = __ldcs(reinterpret_cast<const uint4 *>(crow[r] + k0));
-          sn[r] = __ldg(srow[r] + (k0 >> 5));
+          qn[d][r] = k < P.K ? __ldcs(reinterpret_cast<const uint4 *>(crow[r] + k)) : make_uint4(0u, 0u, 0u, 0u);
+          sn[d][r] = k < P.K ? (uint32_t)__ldg(srow[r] + (k >> 5)) : 0u;
         }
       }
       for (; k0 < P.K; k0 += 512) {
@@ -189,14 +193,22 @@ __global__ void __launch_bounds__(kMxWarps * 32, 1) mx_gemv_kernel(const __grid_
         float sc[kMxRows];
 #pragma unroll
         for (int r = 0; r < kMxRows; ++r) {
-          q[r] = qn[r];
-          sc[r] = e8m0_value(sn[r]);
+          q[r] = qn[0][r];
+          sc[r] = e8m0_value(sn[0][r]);
         }
-        if (k0 + 512 < P.K) {
+#pragma unroll
+        for (int d = 0; d + 1 < PD; ++d)
 #pragma unroll
           for (int r = 0; r < kMxRows; ++r) {
-            qn[r] = __ldcs(reinterpret_cast<const uint4 *>(crow[r] + k0 + 512));
-            sn[r] = __ldg(srow[r] + ((k0 + 512) >> 5));
+            qn[d][r] = qn[d + 1][r];
+            sn[d][r] = sn[d + 1][r];
+          }
+        const int64_t kn = k0 + 512 * PD;
+        if (kn < P.K) {
+#pragma unroll
+          for (int r = 0; r < kMxRows; ++r) {
+            qn[PD - 1][r] = __ldcs(reinterpret_cast<const uint4 *>(crow[r] + kn));
+            sn[PD - 1][r] = __ldg(srow[r] + (kn >> 5));
           }
         }
 #pragma unroll
