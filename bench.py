@@ -62,43 +62,43 @@ def load_peaks() -> dict:
 # --warmup 3 --no-cpu-baseline` (the summary is in profiles/dram_traffic_by_config.md).
 # An entry is reported only while its kernel family's sources hash to the value
 # in TRAFFIC_SOURCES, since a changed kernel needs a new capture.
-TRAFFIC_SOURCES = {"umma": "7179c6806aef9739", "q4": "e613963860c235ea", "mx": "d9052ddd3858cad7"}
+TRAFFIC_SOURCES = {"umma": "7e3ccca1243b6c95", "q4": "e613963860c235ea", "mx": "d2effa9d4a222cea"}
 TRAFFIC = {
-    ("mlp", "tp_all_to_sharded"): 97850880,
-    ("mlp", "tp_sharded_to_all"): 103018752,
-    ("mlp_ag_rs", "tp_gathered_to_sharded"): 97697536,
-    ("mlp_ag_rs", "tp_sharded_to_sharded"): 102856448,
-    ("ffn_gated", "tp_gated_all_to_sharded"): 193791488,
-    ("ffn_gated", "tp_sharded_to_all"): 102857728,
-    ("summa2", "tp_summa"): 1535297536,
-    ("summa4", "tp_summa"): 1345086464,
-    ("qkv1", "tp_all_to_sharded(qkv)"): 103625216,
-    ("qkv1", "tp_sharded_to_all(o)"): 33605120,
-    ("qkv1", "tp_all_to_sharded(lm_head)"): 412300544,
-    ("qkv16", "tp_all_to_sharded(qkv)"): 104062976,
-    ("qkv16", "tp_sharded_to_all(o)"): 33729280,
-    ("qkv16", "tp_all_to_sharded(lm_head)"): 414420992,
-    ("qkv2048", "tp_all_to_sharded(qkv)"): 151711488,
-    ("qkv2048", "tp_sharded_to_all(o)"): 51153152,
-    ("qkv2048", "tp_all_to_sharded(lm_head)"): 931579136,
+    ("mlp", "tp_all_to_sharded"): 97645312,
+    ("mlp", "tp_sharded_to_all"): 102804992,
+    ("mlp_ag_rs", "tp_gathered_to_sharded"): 97691392,
+    ("mlp_ag_rs", "tp_sharded_to_sharded"): 102706176,
+    ("ffn_gated", "tp_gated_all_to_sharded"): 195541760,
+    ("ffn_gated", "tp_sharded_to_all"): 102808320,
+    ("summa2", "tp_summa"): 1088062976,
+    ("summa4", "tp_summa"): 1122454528,
+    ("qkv1", "tp_all_to_sharded(qkv)"): 103882240,
+    ("qkv1", "tp_sharded_to_all(o)"): 33604864,
+    ("qkv1", "tp_all_to_sharded(lm_head)"): 412291584,
+    ("qkv16", "tp_all_to_sharded(qkv)"): 104019456,
+    ("qkv16", "tp_sharded_to_all(o)"): 33731584,
+    ("qkv16", "tp_all_to_sharded(lm_head)"): 414411264,
+    ("qkv2048", "tp_all_to_sharded(qkv)"): 152962560,
+    ("qkv2048", "tp_sharded_to_all(o)"): 51380992,
+    ("qkv2048", "tp_all_to_sharded(lm_head)"): 935369728,
     ("q4_1", "tp_q4_all_to_sharded"): 135351552,
     ("q4_1", "tp_q4_sharded_to_all"): 132415744,
     ("q4_16", "tp_q4_all_to_sharded"): 136939520,
     ("q4_16", "tp_q4_sharded_to_all"): 134592768,
-    ("mx_1", "tp_mx_all_to_sharded"): 245039872,
-    ("mx_1", "tp_mx_sharded_to_all"): 242433280,
+    ("mx_1", "tp_mx_all_to_sharded"): 245032960,
+    ("mx_1", "tp_mx_sharded_to_all"): 242556928,
     ("q4_256", "tp_q4_all_to_sharded"): 141668096,
     ("q4_256", "tp_q4_sharded_to_all"): 259927552,
-    ("mx_16", "tp_mx_all_to_sharded"): 259424768,
-    ("mx_16", "tp_mx_sharded_to_all"): 248201216,
-    ("mx_256", "tp_mx_all_to_sharded"): 509751296,
-    ("mx_256", "tp_mx_sharded_to_all"): 348545024,
-    ("mlp_bwd", "tp_sharded_dw(w1)"): 135443968,
-    ("mlp_bwd", "tp_bias_grad(b1)"): 11291136,
-    ("mlp_bwd", "tp_sharded_to_all_dx"): 95092480,
-    ("mlp_bwd", "tp_sharded_dw(w2)"): 131315200,
+    ("mx_16", "tp_mx_all_to_sharded"): 259133440,
+    ("mx_16", "tp_mx_sharded_to_all"): 247998464,
+    ("mx_256", "tp_mx_all_to_sharded"): 509805312,
+    ("mx_256", "tp_mx_sharded_to_all"): 348383488,
+    ("mlp_bwd", "tp_sharded_dw(w1)"): 135404544,
+    ("mlp_bwd", "tp_bias_grad(b1)"): 11293440,
+    ("mlp_bwd", "tp_sharded_to_all_dx"): 94907648,
+    ("mlp_bwd", "tp_sharded_dw(w2)"): 130958080,
     ("mlp_bwd", "tp_bias_grad(b2)"): 4212736,
-    ("mlp_bwd", "tp_all_to_sharded_dx"): 101656576,
+    ("mlp_bwd", "tp_all_to_sharded_dx"): 101740288,
 }
 
 
