@@ -20,8 +20,14 @@ into W1, a reduce-scatter of W2's partial sums).
 Prints ONE JSON line (rank 0).  ``value`` is device-timed throughput with the
 inputs resident in HBM; ``e2e`` is the same metric with the step's input
 copied from pinned host memory and its output read back inside the timed
-region.  L2 is flushed (a 256 MiB write) between timed steps, outside the
-per-step CUDA-event intervals.  ``--impl reference`` times the fp64 CPU oracle
+region.  Between timed steps, outside the per-step CUDA-event intervals, L2
+is flushed: a 256 MiB buffer is written (evicting every line of the step
+before) and then read back, so each step starts with none of its operands in
+L2 and without the flush's own dirty lines still being written back to HBM
+while it runs.  ``value`` comes from events at the step boundaries only
+(an event between two kernels would stop the second from starting early);
+the per-kernel times behind ``roofline`` come from a second loop of the same
+steps with an event after every call.  ``--impl reference`` times the fp64 CPU oracle
 on a bounded sample of the same workload instead.
 Under torchrun (N > 1) every rank runs its own independent problem (weak
 scaling); no collective touches the data path.
@@ -104,7 +110,7 @@ TRAFFIC = {
 
 # The sources each family of kernels is built from (the shared host code and
 # headers belong to every family).
-COMMON_SOURCES = ["tp_api.cu", "tp_internal.h", "ptx.cuh", "tmap.cu"]
+COMMON_SOURCES = ["tp_api.cu", "tp_internal.h", "ptx.cuh", "tmap.cu", "k_split.cu"]
 FAMILY_SOURCES = {"umma": ["k_umma.cu", "k_colsum.cu", "k_simt.cu"], "q4": ["k_q4.cu", "k_q4gemv.cu"],
                   "mx": ["k_mx.cu"]}
 
@@ -428,6 +434,11 @@ def main():
     launches = split_step(args.config, w)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush_sum = torch.empty((), dtype=torch.float32, device=device)
+
+    def l2_flush(i):
+        flush.fill_(float(i & 7))  # every line of the previous step is evicted
+        torch.sum(flush, dim=0, out=flush_sum)  # the flush's dirty lines are written back here
 
     for _ in range(max(args.warmup, 3)):
         n0 = tp.tp_launch_count()
@@ -439,7 +450,9 @@ def main():
         raise SystemExit("device status error during warm-up")
 
     nk = len(launches)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    k_steps = max(1, min(args.steps, 500))
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(k_steps)]
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
@@ -447,28 +460,34 @@ def main():
     torch.cuda.synchronize()
     sampler.mark("begin")
     for i in range(args.steps):
-        flush.fill_(float(i & 7))
+        l2_flush(i)
         ev[i][0].record(stream)
-        for k, fn in enumerate(launches):
+        for fn in launches:
             fn(stream)
-            ev[i][k + 1].record(stream)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
-    sampler.mark("end")
     if world > 1:
         torch.distributed.barrier()
+    # per-kernel breakdown: the same steps with an event after every call
+    for i in range(k_steps):
+        l2_flush(i)
+        kev[i][0].record(stream)
+        for k, fn in enumerate(launches):
+            fn(stream)
+            kev[i][k + 1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("end")
     clocks = sampler.stop()
     status = tp.tp_query_status()
     if status != 0:
         raise SystemExit("device status error %d in the timed region" % status)
 
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     per_kernel = [0.0] * nk
-    step_ms = 0.0
-    for i in range(args.steps):
-        step_ms += ev[i][0].elapsed_time(ev[i][nk])
+    for i in range(k_steps):
         for k in range(nk):
-            per_kernel[k] += ev[i][k].elapsed_time(ev[i][k + 1])
-    step_ms /= args.steps
-    per_kernel = [x / args.steps for x in per_kernel]
+            per_kernel[k] += kev[i][k].elapsed_time(kev[i][k + 1])
+    per_kernel = [x / k_steps for x in per_kernel]
     max_ms, total_work = aggregate(step_ms, info["work"], world, group, device)
     value = scale(total_work, max_ms, info["unit"])
 
@@ -486,7 +505,7 @@ def main():
         e_steps = max(1, min(args.steps, 500))
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e_steps)]
         for i in range(e_steps):
-            flush.fill_(float(i & 7))
+            l2_flush(i)
             evs[i][0].record(stream)
             for t, h in zip(dev_in, host_in):
                 t.copy_(h, non_blocking=True)
@@ -530,7 +549,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded PCG64, shapes of the pages' Llama/OPT stand-ins)",
             "config": dict(workload=info["workload"], **info["cfg_keys"],
-                           l2="flushed between timed steps (256 MiB write, outside the step events)",
+                           l2="flushed between timed steps (256 MiB write, then read back; outside the step events)",
+                           kernel_times="second loop of %d steps with an event after every call" % k_steps,
                            parallelism="1 GPU per rank; N logical shards as separate HBM buffers"),
             "kernels_ms": {n: round(t, 5) for n, t in zip(info["kernel_names"], per_kernel)},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

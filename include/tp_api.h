@@ -27,12 +27,18 @@
  *    return.  tp_query_status() reads (and clears) that word.
  *  - The library allocates one 4-byte device status word per device on
  *    first use and caches host-side TMA descriptors.  Calls whose kernel
- *    splits a sum across CTAs (the row-parallel 4-bit linears, and split-K
- *    4-bit tiles) use a per-(device, stream) float32 workspace with zeroed
- *    counters, allocated (cudaMalloc) on first need and grown when a larger
- *    call needs more; the counters are back at zero when each kernel ends.
- *    tp_shutdown() frees all of it.  tp_q4_sharded_to_all_noalloc never
- *    allocates.
+ *    splits a sum across CTAs (the row-parallel 4-bit linears, split-K 4-bit
+ *    and MXFP8 tiles, and 16-bit linears of at most 16 tokens whose output
+ *    has fewer 128-row tiles than the GPU has SMs) use a per-(device, stream)
+ *    float32 workspace with zeroed counters, allocated (cudaMalloc) on first
+ *    need and grown when a larger call needs more; the counters are back at
+ *    zero when each kernel ends.  tp_shutdown() frees all of it.
+ *    tp_q4_sharded_to_all_noalloc never allocates.  A call may therefore be
+ *    captured into a CUDA graph once the same call has run on the capturing
+ *    stream outside the capture.
+ *  - Kernels may be launched with programmatic stream serialization: their
+ *    set-up can overlap the end of the previous kernel on the stream, but
+ *    they read and write no global memory before it has completed.
  */
 #ifndef TP_API_H
 #define TP_API_H

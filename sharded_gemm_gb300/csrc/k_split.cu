@@ -1,5 +1,5 @@
 // k_split.cu -- ordered sum of split-K partial tiles, shared by the
-// quantized tensor-core kernels.
+// quantized tensor-core kernels and the small-batch 16-bit kernel.
 //
 // A split tile is 128 output rows x BN token columns; each of its `splits`
 // partials is a float32 slot stored column-major (slot[c][m], so a warp's 32
@@ -42,11 +42,11 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const __grid_constant
     const int tile = (int)(tile_lin % J.tiles), ntile = (int)(tile_lin / J.tiles);
     const int orow = tile * 128 + m;
     const int t = ntile * a.BN + c;
-    const float *s0 = a.ws + (J.ws_base + tile_lin * J.splits) * per_tile + (int64_t)c * 128 + m;
-    float v = __ldcg(s0);
+    if (orow < J.rows && t < J.T) {  // slots past the tokens or rows may be unwritten
+      const float *s0 = a.ws + (J.ws_base + tile_lin * J.splits) * per_tile + (int64_t)c * 128 + m;
+      float v = __ldcg(s0);
 #pragma unroll 8
-    for (int sp = 1; sp < J.splits; ++sp) v += __ldcg(s0 + (int64_t)sp * per_tile);
-    if (orow < J.rows && t < J.T) {
+      for (int sp = 1; sp < J.splits; ++sp) v += __ldcg(s0 + (int64_t)sp * per_tile);
       if (J.bias) v += __ldg(J.bias + orow);
       const int64_t idx = (int64_t)t * J.ldc + orow;
       if (a.out_dt == TP_F32)

@@ -28,6 +28,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -50,7 +51,11 @@ struct UJob {
   int part0, nparts;
   int tilesA, tilesB;
   int unit_begin;
+  int splits;          // > 1: units are (tile, k-block range) pieces (swap mode)
   const float *bias2;  // gated: the up projection's bias (nullable)
+  int64_t ws_base;     // split mode: first float32 slot of this job
+  int kb_total;        // split mode: k-blocks of all parts together
+  int cnt_base;        // split mode: first tile counter (kEpiWarps per tile)
 };
 
 struct UPart {
@@ -72,6 +77,8 @@ struct UmmaArgs {
   uint32_t idesc;
   int *status;
   uint64_t wait_ns;
+  float *ws;  // split mode: float32 slots, 128 x BN per (tile, split), column-major
+  int *cnt;   // split mode: arrival counters, zero between calls
 };
 
 // Records the time of (event, k-block sequence) for CTA 0 when tracing.
@@ -83,6 +90,29 @@ __device__ __forceinline__ int find_job(const UmmaArgs &a, int u) {
   int j = 0;
   while (j + 1 < a.njobs && u >= a.jobs[j + 1].unit_begin) ++j;
   return j;
+}
+
+// Position of a unit within its job: the output tile (ta, tb) and, when the
+// job is split, the k-block range [k0, k1) of the concatenated parts and the
+// split index sp; else the whole contraction.
+struct UnitPos {
+  int ta, tb, sp, k0, k1;
+};
+__device__ __forceinline__ UnitPos unit_pos(const UJob &J, int local) {
+  UnitPos q;
+  q.ta = local % J.tilesA;
+  int rest = local / J.tilesA;
+  q.sp = 0;
+  q.k0 = 0;
+  q.k1 = INT_MAX;
+  if (J.splits > 1) {
+    q.sp = rest % J.splits;
+    rest /= J.splits;
+    q.k0 = (int)((int64_t)q.sp * J.kb_total / J.splits);
+    q.k1 = (int)((int64_t)(q.sp + 1) * J.kb_total / J.splits);
+  }
+  q.tb = rest;
+  return q;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
@@ -200,6 +230,55 @@ __device__ __forceinline__ void store_col_chunk(const UmmaArgs &a, const UJob &J
   }
 }
 
+// Split-mode store (swap): CH token columns cl0.. of output row m of the
+// unit's float32 slot (column-major, 128 rows per column); no bias, which the
+// ordered reduction adds.  Columns past the token count are not written.
+template <int CH, int BN>
+__device__ __forceinline__ void store_slot_chunk(const UmmaArgs &a, const UJob &J, const UnitPos &q, int m,
+                                                 int cl0, const float (&v)[CH]) {
+  const int64_t slot = J.ws_base + ((int64_t)q.tb * J.tilesA + q.ta) * J.splits + q.sp;
+  float *s = a.ws + slot * (BN * 128) + m;
+  const int t0 = q.tb * BN + cl0;
+#pragma unroll
+  for (int i = 0; i < CH; ++i) {
+    if (t0 + i >= J.rowsB) break;
+    __stcg(s + (cl0 + i) * 128, v[i]);
+  }
+}
+
+// Split mode, after a warp has stored its slot values: the warp that arrives
+// last at its (tile, warp) counter adds the tile's split slots in split order
+// for its 32 rows x HALF token columns (so the sum does not depend on which
+// unit finishes last), adds the bias, stores the output and re-arms the counter.
+template <int BN, int HALF>
+__device__ __forceinline__ void split_finish(const UmmaArgs &a, const UJob &J, const UnitPos &q, int ew, int row,
+                                             int m, int half, int lane) {
+  __threadfence();
+  __syncwarp();
+  const int64_t tile = (int64_t)q.tb * J.tilesA + q.ta;
+  int *cnt = a.cnt + (J.cnt_base + tile) * kEpiWarps + ew;
+  int prev = 0;
+  if (lane == 0) prev = atomicAdd(cnt, 1);
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  if (prev != J.splits - 1) return;
+  __threadfence();
+  const int cl0 = half * HALF;
+  const int ncol = J.rowsB - q.tb * BN - cl0;  // token columns of this warp that exist
+  const float *s0 = a.ws + (J.ws_base + tile * J.splits) * (BN * 128) + m;
+  float v[HALF];
+#pragma unroll
+  for (int i = 0; i < HALF; ++i) v[i] = i < ncol ? __ldcg(s0 + (cl0 + i) * 128) : 0.f;
+  for (int sp = 1; sp < J.splits; ++sp) {
+    const float *sj = s0 + (int64_t)sp * (BN * 128);
+#pragma unroll
+    for (int i = 0; i < HALF; ++i)
+      if (i < ncol) v[i] += __ldcg(sj + (cl0 + i) * 128);
+  }
+  store_col_chunk<HALF>(a, J, row, q.tb * BN + cl0, v);
+  __syncwarp();
+  if (lane == 0) *cnt = 0;
+}
+
 // Epilogue chunk width: the widest of 32 / 16 / 8 columns that divides half a tile.
 template <int HALF>
 struct ChunkOf {
@@ -272,6 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  // The set-up above overlaps the previous kernel's tail (programmatic
+  // launch); global memory is touched only after it has completed.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -285,12 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       bool ok = true;
       for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
         const UJob &J = a.jobs[find_job(a, u)];
-        const int local = u - J.unit_begin;
-        const int ta = local % J.tilesA, tb = local / J.tilesA;
-        const int rowA0 = ta * BM, rowB0 = tb * BN;
+        const UnitPos q = unit_pos(J, u - J.unit_begin);
+        const int rowA0 = q.ta * BM, rowB0 = q.tb * BN;
+        int off = 0;
         for (int p = 0; ok && p < J.nparts; ++p) {
           const UPart P = a.parts[J.part0 + p];
-          for (int kb = 0; kb < P.kblocks; ++kb) {
+          const int lo = max(0, q.k0 - off), hi = min(P.kblocks, q.k1 - off);
+          off += P.kblocks;
+          for (int kb = lo; kb < hi; ++kb) {
             if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, lim, a.status, &abort_sh)) {
               ok = false;
               break;
@@ -334,17 +419,29 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       bool ok = true;
       for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
         const UJob &J = a.jobs[find_job(a, u)];
+        const UnitPos q = unit_pos(J, u - J.unit_begin);
+        // one accumulator per unit (chained parts, or a split's k-block
+        // range), else one per part
+        const bool uchain = a.chain || J.splits > 1;
+        bool held = false;  // an accumulator is acquired and not yet committed
+        uint32_t accum = 0;
+        int off = 0;
         for (int p = 0; ok && p < J.nparts; ++p) {
           const UPart P = a.parts[J.part0 + p];
-          if (p == 0 || !a.chain) {
+          const int lo = max(0, q.k0 - off), hi = min(P.kblocks, q.k1 - off);
+          off += P.kblocks;
+          if (lo >= hi) continue;
+          if (!held) {
             if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, lim, a.status, &abort_sh)) {
               ok = false;
               break;
             }
             tc_fence_after();
+            held = true;
+            accum = 0;
           }
           const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-          for (int kb = 0; kb < P.kblocks; ++kb) {
+          for (int kb = lo; kb < hi; ++kb) {
             if (!mbar_wait(smem_u32(&full_bar[stage]), phase, lim, a.status, &abort_sh)) {
               ok = false;
               break;
@@ -357,8 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
                                        : umma_desc_sw128(sa + kk * 32, 16, 1024);
               const uint64_t bd = B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024)
                                        : umma_desc_sw128(sb + kk * 32, 16, 1024);
-              const uint32_t accum = (kb > 0 || kk > 0 || (a.chain && p > 0)) ? 1u : 0u;
               umma_f16(d, ad, bd, a.idesc, accum);
+              accum = 1u;
             }
             umma_commit(smem_u32(&empty_bar[stage]));
             if (++stage == STAGES) {
@@ -367,12 +464,20 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
             }
           }
           if (!ok) break;
-          if (p == J.nparts - 1 || !a.chain) {
+          if (!uchain) {
             umma_commit(smem_u32(&tfull_bar[acc]));
+            held = false;
             if (++acc == NACC) {
               acc = 0;
               acc_phase ^= 1;
             }
+          }
+        }
+        if (ok && held) {
+          umma_commit(smem_u32(&tfull_bar[acc]));
+          if (++acc == NACC) {
+            acc = 0;
+            acc_phase ^= 1;
           }
         }
       }
@@ -391,11 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     float sum[PARTIALS ? HALF : 1];
     for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
       const UJob &J = a.jobs[find_job(a, u)];
-      const int local = u - J.unit_begin;
-      const int ta = local % J.tilesA, tb = local / J.tilesA;
-      const int row = ta * BM + quarter * 32 + lane;
-      const int colb = tb * BN + half * HALF;
-      const int nep = a.chain ? 1 : J.nparts;
+      const UnitPos q = unit_pos(J, u - J.unit_begin);
+      const int row = q.ta * BM + quarter * 32 + lane;
+      const int colb = q.tb * BN + half * HALF;
+      const bool split = SWAP && J.splits > 1;
+      const int nep = (a.chain || split) ? 1 : J.nparts;
       for (int pe = 0; pe < nep; ++pe) {
         // warp-uniform: every lane must take the same path into tcgen05.ld
         const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, lim, a.status, &abort_sh);
@@ -415,10 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 #pragma unroll
             for (int i = 0; i < CH; ++i) sum[c * CH + i] = (pe == 0) ? v[i] : sum[c * CH + i] + v[i];
           } else {
-            if constexpr (SWAP)
-              store_col_chunk<CH>(a, J, row, colb + c * CH, v);
-            else
+            if constexpr (SWAP) {
+              if (split)
+                store_slot_chunk<CH, BN>(a, J, q, quarter * 32 + lane, half * HALF + c * CH, v);
+              else
+                store_col_chunk<CH>(a, J, row, colb + c * CH, v);
+            } else {
               store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+            }
           }
         }
         tc_fence_before();
@@ -436,12 +545,19 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
             float v[CH];
 #pragma unroll
             for (int i = 0; i < CH; ++i) v[i] = sum[c * CH + i];
-            if constexpr (SWAP)
-              store_col_chunk<CH>(a, J, row, colb + c * CH, v);
-            else
+            if constexpr (SWAP) {
+              if (split)
+                store_slot_chunk<CH, BN>(a, J, q, quarter * 32 + lane, half * HALF + c * CH, v);
+              else
+                store_col_chunk<CH>(a, J, row, colb + c * CH, v);
+            } else {
               store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+            }
           }
         }
+      }
+      if constexpr (SWAP) {
+        if (split && ok) split_finish<BN, HALF>(a, J, q, ew, row, quarter * 32 + lane, half, lane);
       }
     }
   }
@@ -965,9 +1081,20 @@ int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
     attr_done[dev & 63] = true;
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
-  kern<<<grid, kThreads, smem, s>>>(args);
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_gemm_kernel launch");
 }
 
@@ -1072,10 +1199,36 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   // max(MMA cycles, 2.2 x the operand rows one CTA stages): a CTA can keep
   // only so many bytes in flight, so the staged rows set the pace once the
   // MMA is fast enough.  Rounds of tiles over the SMs multiply that.
-  int BN, nsub = 1, msub = 1;
+  int BN, nsub = 1, msub = 1, splits = 1;
   bool pair = false, rowclu = false;
   if (swap) {
     BN = 16;
+    // Small batches: a unit streams a 128-row weight tile through one SM at
+    // about 38 GB/s (0.48 us per 64-column k-block), so with fewer tiles than
+    // SMs most of HBM sits idle.  Split each tile's contraction into S
+    // k-block ranges (float32 slots that the last-arriving unit of the tile
+    // adds in order, about 2.5 us plus the slot traffic) when that shortens
+    // the longest SM's queue.
+    const int sms0 = sm_count();
+    int64_t tiles = 0, kbw = 1;
+    for (int j = 0; j < p.njobs; ++j) {
+      int64_t kb = 0;
+      for (int q = 0; q < p.jobs[j].nparts; ++q) kb += (p.parts[p.jobs[j].part0 + q].K + BK - 1) / BK;
+      kbw = std::max(kbw, kb);
+      tiles += ((p.jobs[j].N + BM - 1) / BM) * ((p.jobs[j].M + BN - 1) / BN);
+    }
+    if (tiles < sms0 && kbw >= 2) {
+      double best = 1e300;
+      for (int sp = 1; sp <= 16 && sp <= kbw; ++sp) {
+        const double rounds = (double)((tiles * sp + sms0 - 1) / sms0);
+        const double slot_us = sp > 1 ? 2.0 * (double)(tiles * sp * BN * BM * 4) / 6.0e6 : 0.0;
+        const double cost = rounds * (double)((kbw + sp - 1) / sp) * 0.48 + (sp > 1 ? 2.5 + slot_us : 0.0);
+        if (cost < best - 1e-9) {
+          best = cost;
+          splits = sp;
+        }
+      }
+    }
   } else if (p.gated) {
     // Pair units of 256 x BN outputs with two accumulators (gate, up): per
     // k-block a CTA stages 128 + BN rows for 2 x BN columns of MMA work, and
@@ -1191,7 +1344,7 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   memset(&args, 0, sizeof(args));
   int nA = 0, nB = 0;
   const void *aptr[kMaxMaps], *bptr[kMaxMaps];
-  int64_t units = 0;
+  int64_t units = 0, tiles_so_far = 0;
   for (int j = 0; j < p.njobs; ++j) {
     const Job &J = p.jobs[j];
     UJob &U = args.jobs[j];
@@ -1206,7 +1359,13 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
     U.tilesB = p.gated ? (U.rowsB + BN - 1) / BN : (U.rowsB + nsub * BN - 1) / (nsub * BN);
     U.bias2 = J.bias2;
     U.unit_begin = (int)units;
-    units += (int64_t)U.tilesA * U.tilesB;
+    U.splits = splits;
+    U.kb_total = 0;
+    for (int q = 0; q < J.nparts; ++q) U.kb_total += (int)((p.parts[J.part0 + q].K + BK - 1) / BK);
+    U.ws_base = U.unit_begin;  // split mode: one slot per unit
+    U.cnt_base = (int)tiles_so_far;
+    tiles_so_far += (int64_t)U.tilesA * U.tilesB;
+    units += (int64_t)U.tilesA * U.tilesB * splits;
     for (int q = 0; q < J.nparts; ++q) {
       const Part &P = p.parts[J.part0 + q];
       // operand roles: normal A = activations (M rows), B = weights / SUMMA block
@@ -1293,6 +1452,11 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
                               p.a_mn ? 1u : 0u);
   args.status = p.status;
   args.wait_ns = (uint64_t)p.wait_ns;
+  if (splits > 1) {
+    rc = split_workspace(s, (size_t)units * BM * BN * sizeof(float), (size_t)tiles_so_far * kEpiWarps, &args.ws,
+                         &args.cnt);
+    if (rc) return rc;
+  }
 
   if (p.gated && BN == 160)
     rc = launch_pair<160, false, 6, 1, 2, true>(args, sms, s);

@@ -275,6 +275,19 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
   return d;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream is still
+// running; griddep_wait() blocks the calling thread until that kernel has
+// completed and its memory operations are visible, so every thread calls it
+// before its first global-memory access.  griddep_launch_dependents() lets
+// the next such kernel of the stream start early (it still waits for this
+// one to complete before touching memory).  Both are no-ops in a kernel
+// launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Barrier among `count` threads of the CTA on hardware barrier `id` (1..15).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -161,6 +161,43 @@ def test_sharded_to_all(policy, T, Kn, O, N):
     check_close(to_host(y), ref, "row")
 
 
+# Small batches (T <= 16) with fewer output tiles than SMs split each tile's
+# contraction into k-block ranges summed by an ordered reduction: ranges that
+# cross rank boundaries (22 k-blocks per rank), ragged k-blocks and tokens,
+# and a column-parallel split inside one rank's contraction.
+@pytest.mark.parametrize("T,Kn,O,N", [(1, 1376, 4096, 8), (16, 1376, 1000, 8), (9, 100, 333, 3),
+                                      (16, 512, 4096, 8)])
+def test_sharded_to_all_small_batch_split(T, Kn, O, N):
+    x = rand_bf16((T, Kn * N))
+    w = rand_bf16((O, Kn * N), 0.05)
+    b = (RNG.standard_normal(O) * 0.1).astype(np.float32)
+    xs = tp.tp_shard_weight(to_device(x, "bf16"), -1, 1, N)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), -1, 1, N)
+    bd = to_device(b, "f32")
+    y = tp.tp_sharded_to_all(xs, ws, bd)
+    y2 = tp.tp_sharded_to_all(xs, ws, bd)
+    _status_ok()
+    assert torch.equal(y, y2)
+    ref = oracle.sharded_to_all([bf16(p) for p in oracle.shard(x, -1, 1, N)],
+                                [bf16(p) for p in oracle.shard(w, -1, 1, N)], b.astype(np.float64))
+    check_close(to_host(y), ref, "row split")
+
+
+@pytest.mark.parametrize("T,K,On,N", [(1, 4096, 1536, 8), (16, 4096, 1536, 8), (7, 1000, 200, 2)])
+def test_all_to_sharded_small_batch_split(T, K, On, N):
+    x = rand_bf16((T, K))
+    w = rand_bf16((On * N, K), 0.05)
+    b = (RNG.standard_normal(On * N) * 0.1).astype(np.float32)
+    ws = tp.tp_shard_weight(to_device(w, "bf16"), 0, 1, N)
+    bs = tp.tp_shard_weight(to_device(b, "f32"), 0, 1, N)
+    ys = tp.tp_all_to_sharded(to_device(x, "bf16"), ws, bs)
+    _status_ok()
+    ref = oracle.all_to_sharded(bf16(x), [bf16(p) for p in oracle.shard(w, 0, 1, N)],
+                                [p.astype(np.float64) for p in oracle.shard(b, 0, 1, N)])
+    for r in range(N):
+        check_close(to_host(ys[r]), ref[r], "split shard %d" % r)
+
+
 def test_sharded_to_all_strided_input_columns(policy):
     # W_o style: x split by columns as strided views of one (T, K) buffer
     T, K, O, N = 48, 512, 192, 8
