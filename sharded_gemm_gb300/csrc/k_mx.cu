@@ -118,6 +118,8 @@ __device__ __forceinline__ void mx_expand16(const uint4 q, float (&c)[16]) {
 
 template <int TT>
 __global__ void __launch_bounds__(kMxWarps * 32, 1) mx_gemv_kernel(const __grid_constant__ MxArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   extern __shared__ float xs[];
   // stage every distinct input as float32
   for (int d = 0; d < a.nx; ++d) {
@@ -316,7 +318,7 @@ static int launch_mx_gemv(const Problem &p, cudaStream_t s, bool *handled) {
 #define TP_MX_CASE(TTV)                                                                                   \
   if (maxT == TTV) {                                                                                      \
     e = cudaFuncSetAttribute(mx_gemv_kernel<TTV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-    if (e == cudaSuccess) mx_gemv_kernel<TTV><<<grid, kMxWarps * 32, smem, s>>>(args);                   \
+    if (e == cudaSuccess) e = launch_pdl(mx_gemv_kernel<TTV>, dim3(grid), dim3(kMxWarps * 32), smem, s, args); \
   }
   TP_MX_CASE(1)
   TP_MX_CASE(2)
@@ -521,6 +523,8 @@ __device__ __forceinline__ void mt_epilogue(const MtArgs &a, uint32_t tmem, uint
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_constant__ MtArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   using C = MtCfg<BN>;
   static_assert(STAGES == 1 || STAGES == 2 || STAGES == 4 || STAGES == 8, "8 converter warps share the slots");
   static_assert(C::STAGE % 1024 == 0, "stage alignment");
@@ -735,6 +739,8 @@ __global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_con
 // as soon as it has been read.  The MMA reads only the A buffer.
 template <int BN, int STAGES, int NA>
 __global__ void __launch_bounds__(kMtThreads, 1) mx_dec_kernel(const __grid_constant__ MtArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   using C = MtCfg<BN>;
   constexpr int X_BYTES = BN * 128;
   constexpr int C_BYTES = 128 * 64;
@@ -946,9 +952,9 @@ int mt_dec_launch(MtArgs &args, int sms, cudaStream_t s) {
     attr_done[dev & 63] = true;
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
-  kern<<<grid, kMtThreads, smem, s>>>(args);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kMtThreads), smem, s, args);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "mx_dec_kernel launch");
 }
 
@@ -965,9 +971,9 @@ int mt_launch(MtArgs &args, int sms, cudaStream_t s) {
     attr_done[dev & 63] = true;
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
-  kern<<<grid, kMtThreads, smem, s>>>(args);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kMtThreads), smem, s, args);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "mx_umma_kernel launch");
 }
 

@@ -275,6 +275,8 @@ __device__ __forceinline__ void q4_store(const Q4Args &a, const Q4Job &J, int t,
 
 template <bool DECODE>
 __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_constant__ Q4Args a) {
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   using C = Q4Cfg<DECODE>;
   constexpr int STAGE_BYTES = C::CODES_BYTES + C::X_BYTES;
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -686,6 +688,8 @@ __device__ __forceinline__ void codes_to_int_bf16_blocked(uint32_t w, uint32_t *
 
 template <int TCAP>
 __global__ void __launch_bounds__(kQThreads, 1) q4_decode_kernel(const __grid_constant__ Q4Args a) {
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   using C = DecCfg;
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES], empty_bar[C::STAGES];
@@ -1057,9 +1061,9 @@ int q4_decode_launch(Q4Args &args, int sms, cudaStream_t s) {
     attr_done[dev & 63] = true;
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
-  kern<<<grid, kQThreads, smem, s>>>(args);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kQThreads), smem, s, args);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "q4_decode_kernel launch");
 }
 
@@ -1081,9 +1085,9 @@ int q4_launch_cfg(Q4Args &args, int sms, cudaStream_t s) {
     attr_done[dev & 63] = true;
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
-  kern<<<grid, kQThreads, smem, s>>>(args);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kQThreads), smem, s, args);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "q4_umma_kernel launch");
 }
 

@@ -446,6 +446,8 @@ __device__ __forceinline__ void advance(const GvArgs &a, const Task &cur, int v,
 
 template <int TT>
 __global__ void __launch_bounds__(kGvWarps * 32, 1) q4_gemv_kernel(const __grid_constant__ GvArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   extern __shared__ __align__(16) float xsm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int W = gridDim.x * kGvWarps;
@@ -558,6 +560,8 @@ __device__ __forceinline__ void gt_issue(const GtArgs &a, const GtCur &c, uint32
 
 template <int TT>
 __global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __grid_constant__ GtArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   extern __shared__ __align__(1024) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int S = a.stages;
@@ -713,9 +717,9 @@ int launch_one(K kern, const A &args, int grid, int threads, size_t smem, int sm
     if (e != cudaSuccess) return cuda_error(e, what);
     attr_done[dev & 63] = true;
   }
-  kern<<<grid, threads, smem, s>>>(args);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(threads), smem, s, args);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, what);
 }
 

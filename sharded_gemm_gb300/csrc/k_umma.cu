@@ -651,6 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
   cluster_sync_all();  // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -918,6 +920,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  griddep_launch_dependents();
+  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1081,18 +1085,7 @@ int launch_config(UmmaArgs &args, int sms, cudaStream_t s) {
     attr_done[dev & 63] = true;
   }
   const int grid = args.total_units < sms ? args.total_units : sms;
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, args);
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_error(e, "umma_gemm_kernel launch");
@@ -1120,13 +1113,15 @@ int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -1154,13 +1149,15 @@ int launch_row_cluster(UmmaArgs &args, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)N;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();

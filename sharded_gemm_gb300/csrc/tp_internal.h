@@ -22,6 +22,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "../../include/tp_api.h"
 
@@ -79,6 +80,26 @@ void trace_buffer(unsigned long long **buf, int64_t *cap_records);
 int set_error(int code, const char *fmt, ...);
 void note_launch();  // counts one kernel launch of the calling thread (tp_launch_count)
 int cuda_error(cudaError_t e, const char *what);
+
+// Launches `kern` with programmatic stream serialization: it may be scheduled
+// while the previous kernel of the stream finishes, so it must call
+// griddep_wait() before its first global-memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
 
 // ---- launchers (each returns TP_OK or a tp_status, error message set)
 int launch_simt(const Problem &p, cudaStream_t s);

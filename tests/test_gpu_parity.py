@@ -198,6 +198,41 @@ def test_all_to_sharded_small_batch_split(T, K, On, N):
         check_close(to_host(ys[r]), ref[r], "split shard %d" % r)
 
 
+def test_small_batch_calls_replay_in_a_cuda_graph():
+    # The split small-batch path (workspace, arrival counters) and the
+    # programmatic launches run unchanged inside a captured CUDA graph once
+    # the same calls have run on the capturing stream.
+    T, K, O, N = 1, 4096, 4096, 8
+    x = to_device(rand_bf16((T, K)), "bf16")
+    w = tp.tp_shard_weight(to_device(rand_bf16((O, K), 0.05), "bf16"), -1, 1, N)
+    xs = [x[:, r * (K // N):(r + 1) * (K // N)] for r in range(N)]
+    wc = tp.tp_shard_weight(to_device(rand_bf16((O, K), 0.05), "bf16"), 0, 1, N)
+    y = torch.empty((T, O), dtype=torch.bfloat16, device="cuda")
+    yc = [torch.empty((T, O // N), dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            tp.tp_sharded_to_all(xs, w, None, out=y, stream=s)
+            tp.tp_all_to_sharded(x, wc, None, out=yc, stream=s)
+    s.synchronize()
+    ref = [y.clone()] + [t.clone() for t in yc]
+    y.zero_()
+    for t in yc:
+        t.zero_()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tp.tp_sharded_to_all(xs, w, None, out=y, stream=s)
+        tp.tp_all_to_sharded(x, wc, None, out=yc, stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    _status_ok()
+    for a, b in zip([y] + yc, ref):
+        assert torch.equal(a, b)
+
+
 def test_sharded_to_all_strided_input_columns(policy):
     # W_o style: x split by columns as strided views of one (T, K) buffer
     T, K, O, N = 48, 512, 192, 8
