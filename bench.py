@@ -63,48 +63,48 @@ def load_peaks() -> dict:
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
-# config's kernels, from one ncu capture of `python bench.py --config C --steps 3
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per call (summed over
+# the kernels the call launches), from one ncu capture of `python bench.py --config C --steps 3
 # --warmup 3 --no-cpu-baseline` (the summary is in profiles/dram_traffic_by_config.md).
 # An entry is reported only while its kernel family's sources hash to the value
 # in TRAFFIC_SOURCES, since a changed kernel needs a new capture.
-TRAFFIC_SOURCES = {"umma": "7e3ccca1243b6c95", "q4": "e613963860c235ea", "mx": "d2effa9d4a222cea"}
+TRAFFIC_SOURCES = {"umma": "9c27d02d45748809", "q4": "9039129272703cf4", "mx": "4fb19b28baf2f4e4"}
 TRAFFIC = {
-    ("mlp", "tp_all_to_sharded"): 97645312,
-    ("mlp", "tp_sharded_to_all"): 102804992,
-    ("mlp_ag_rs", "tp_gathered_to_sharded"): 97691392,
-    ("mlp_ag_rs", "tp_sharded_to_sharded"): 102706176,
-    ("ffn_gated", "tp_gated_all_to_sharded"): 195541760,
-    ("ffn_gated", "tp_sharded_to_all"): 102808320,
-    ("summa2", "tp_summa"): 1088062976,
-    ("summa4", "tp_summa"): 1122454528,
-    ("qkv1", "tp_all_to_sharded(qkv)"): 103882240,
-    ("qkv1", "tp_sharded_to_all(o)"): 33604864,
-    ("qkv1", "tp_all_to_sharded(lm_head)"): 412291584,
-    ("qkv16", "tp_all_to_sharded(qkv)"): 104019456,
-    ("qkv16", "tp_sharded_to_all(o)"): 33731584,
-    ("qkv16", "tp_all_to_sharded(lm_head)"): 414411264,
-    ("qkv2048", "tp_all_to_sharded(qkv)"): 152962560,
-    ("qkv2048", "tp_sharded_to_all(o)"): 51380992,
-    ("qkv2048", "tp_all_to_sharded(lm_head)"): 935369728,
-    ("q4_1", "tp_q4_all_to_sharded"): 135351552,
-    ("q4_1", "tp_q4_sharded_to_all"): 132415744,
-    ("q4_16", "tp_q4_all_to_sharded"): 136939520,
-    ("q4_16", "tp_q4_sharded_to_all"): 134592768,
-    ("mx_1", "tp_mx_all_to_sharded"): 245032960,
-    ("mx_1", "tp_mx_sharded_to_all"): 242556928,
-    ("q4_256", "tp_q4_all_to_sharded"): 141668096,
-    ("q4_256", "tp_q4_sharded_to_all"): 259927552,
-    ("mx_16", "tp_mx_all_to_sharded"): 259133440,
-    ("mx_16", "tp_mx_sharded_to_all"): 247998464,
-    ("mx_256", "tp_mx_all_to_sharded"): 509805312,
-    ("mx_256", "tp_mx_sharded_to_all"): 348383488,
-    ("mlp_bwd", "tp_sharded_dw(w1)"): 135404544,
-    ("mlp_bwd", "tp_bias_grad(b1)"): 11293440,
-    ("mlp_bwd", "tp_sharded_to_all_dx"): 94907648,
-    ("mlp_bwd", "tp_sharded_dw(w2)"): 130958080,
-    ("mlp_bwd", "tp_bias_grad(b2)"): 4212736,
-    ("mlp_bwd", "tp_all_to_sharded_dx"): 101740288,
+    ("mlp", "tp_all_to_sharded"): 97284096,
+    ("mlp", "tp_sharded_to_all"): 102735104,
+    ("mlp_ag_rs", "tp_gathered_to_sharded"): 97700864,
+    ("mlp_ag_rs", "tp_sharded_to_sharded"): 102843136,
+    ("ffn_gated", "tp_gated_all_to_sharded"): 196570880,
+    ("ffn_gated", "tp_sharded_to_all"): 102977024,
+    ("summa2", "tp_summa"): 1088304640,
+    ("summa4", "tp_summa"): 1122663936,
+    ("qkv1", "tp_all_to_sharded(qkv)"): 103928832,
+    ("qkv1", "tp_sharded_to_all(o)"): 33627904,
+    ("qkv1", "tp_all_to_sharded(lm_head)"): 412323072,
+    ("qkv16", "tp_all_to_sharded(qkv)"): 104060160,
+    ("qkv16", "tp_sharded_to_all(o)"): 33751296,
+    ("qkv16", "tp_all_to_sharded(lm_head)"): 414397440,
+    ("qkv2048", "tp_all_to_sharded(qkv)"): 152982272,
+    ("qkv2048", "tp_sharded_to_all(o)"): 51164160,
+    ("qkv2048", "tp_all_to_sharded(lm_head)"): 938591488,
+    ("q4_1", "tp_q4_all_to_sharded"): 135356928,
+    ("q4_1", "tp_q4_sharded_to_all"): 132429312,
+    ("q4_16", "tp_q4_all_to_sharded"): 136966656,
+    ("q4_16", "tp_q4_sharded_to_all"): 134494464,
+    ("q4_256", "tp_q4_all_to_sharded"): 141629952,
+    ("q4_256", "tp_q4_sharded_to_all"): 261504512,
+    ("mx_1", "tp_mx_all_to_sharded"): 245041920,
+    ("mx_1", "tp_mx_sharded_to_all"): 242436352,
+    ("mx_16", "tp_mx_all_to_sharded"): 259156480,
+    ("mx_16", "tp_mx_sharded_to_all"): 248046848,
+    ("mx_256", "tp_mx_all_to_sharded"): 508315904,
+    ("mx_256", "tp_mx_sharded_to_all"): 347982080,
+    ("mlp_bwd", "tp_sharded_dw(w1)"): 135337472,
+    ("mlp_bwd", "tp_bias_grad(b1)"): 11290880,
+    ("mlp_bwd", "tp_sharded_to_all_dx"): 94629376,
+    ("mlp_bwd", "tp_sharded_dw(w2)"): 131244800,
+    ("mlp_bwd", "tp_bias_grad(b2)"): 4213248,
+    ("mlp_bwd", "tp_all_to_sharded_dx"): 102053376,
 }
 
 
@@ -381,18 +381,29 @@ class OracleMLP:
         self.oracle.sharded_to_all(mid, self.w2, self.b2)
         return time.time() - t
 
+    def seconds_per_row(self) -> float:
+        # a 64-row pass: one row alone would charge every row the fixed cost of a call
+        if not hasattr(self, "_spr"):
+            probe = min(64, self.total_rows)
+            self._spr = max(self.run(probe), 1e-4) / probe
+        return self._spr
+
     def rows_for(self, budget_s: float) -> int:
-        one = max(self.run(1), 1e-4)
-        return int(max(1, min(self.total_rows, budget_s / one)))
+        return int(max(1, min(self.total_rows, budget_s / self.seconds_per_row())))
 
 
 def oracle_sample(budget_s: float):
-    """(TFLOP/s, seconds, sample description, threads) of one bounded sample."""
+    """(TFLOP/s, seconds, sample description, threads) of one bounded sample:
+    whole passes of up to the full batch, about ``budget_s`` of CPU work."""
     o = OracleMLP()
     rows = o.rows_for(budget_s)
-    dt = o.run(rows)
-    return (o.per_row * rows / dt / 1e12, dt,
-            "%d of %d %s" % (rows, o.total_rows, o.desc), o.oracle.num_threads())
+    passes = max(1, int(budget_s / (o.seconds_per_row() * rows)))
+    t = time.time()
+    for _ in range(passes):
+        o.run(rows)
+    dt = time.time() - t
+    return (o.per_row * rows * passes / dt / 1e12, dt,
+            "%d pass(es) of %d of %d %s" % (passes, rows, o.total_rows, o.desc), o.oracle.num_threads())
 
 
 # ------------------------------------------------------------------ main

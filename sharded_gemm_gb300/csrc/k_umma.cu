@@ -92,6 +92,15 @@ __device__ __forceinline__ int find_job(const UmmaArgs &a, int u) {
   return j;
 }
 
+// Pulls a tile into L2 only (no shared memory, no barrier); parts of the tile
+// outside the tensor are skipped.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Position of a unit within its job: the output tile (ta, tb) and, when the
 // job is split, the k-block range [k0, k1) of the concatenated parts and the
 // split index sp; else the whole contraction.
@@ -268,6 +277,7 @@ __device__ __forceinline__ void split_finish(const UmmaArgs &a, const UJob &J, c
   float v[HALF];
 #pragma unroll
   for (int i = 0; i < HALF; ++i) v[i] = i < ncol ? __ldcg(s0 + (cl0 + i) * 128) : 0.f;
+#pragma unroll 4
   for (int sp = 1; sp < J.splits; ++sp) {
     const float *sj = s0 + (int64_t)sp * (BN * 128);
 #pragma unroll
@@ -352,8 +362,25 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
   // The set-up above overlaps the previous kernel's tail (programmatic
-  // launch); global memory is touched only after it has completed.
+  // launch); global memory is read and written only after it has completed.
   griddep_launch_dependents();
+  if constexpr (SWAP) {
+    // The swapped A operand is the weight matrix: start pulling this CTA's
+    // first k-blocks into L2 meanwhile.  L2 is the point of coherence, so a
+    // line the previous kernel writes after the prefetch is still what the
+    // tensor loads (issued after the wait) see.
+    if (warp == 0 && lane == 0 && (int)blockIdx.x < a.total_units) {
+      const UJob &J = a.jobs[find_job(a, blockIdx.x)];
+      const UnitPos q = unit_pos(J, blockIdx.x - J.unit_begin);
+      int off = 0, n = 0;
+      for (int p = 0; p < J.nparts && n < STAGES; ++p) {
+        const UPart P = a.parts[J.part0 + p];
+        const int lo = max(0, q.k0 - off), hi = min(P.kblocks, q.k1 - off);
+        off += P.kblocks;
+        for (int kb = lo; kb < hi && n < STAGES; ++kb, ++n) tma_prefetch_l2_2d(&a.mapA[P.amap], kb * BK, q.ta * BM);
+      }
+    }
+  }
   griddep_wait();
 
   if (warp == 0) {
@@ -1201,11 +1228,13 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
   if (swap) {
     BN = 16;
     // Small batches: a unit streams a 128-row weight tile through one SM at
-    // about 38 GB/s (0.48 us per 64-column k-block), so with fewer tiles than
-    // SMs most of HBM sits idle.  Split each tile's contraction into S
-    // k-block ranges (float32 slots that the last-arriving unit of the tile
-    // adds in order, about 2.5 us plus the slot traffic) when that shortens
-    // the longest SM's queue.
+    // about 38 GB/s (0.48 us per 64-column k-block, plus about 1.5 us per
+    // unit, measured), so with fewer tiles than SMs most of HBM sits idle,
+    // and a last round of tiles that covers only part of the SMs leaves the
+    // rest idle.
+    // Split each tile's contraction into S k-block ranges (float32 slots
+    // that the last-arriving unit of the tile adds in order: about 1 us plus
+    // the slot traffic) when that shortens the longest SM's queue.
     const int sms0 = sm_count();
     int64_t tiles = 0, kbw = 1;
     for (int j = 0; j < p.njobs; ++j) {
@@ -1214,12 +1243,15 @@ int launch_umma(const Problem &p, cudaStream_t s, bool *handled) {
       kbw = std::max(kbw, kb);
       tiles += ((p.jobs[j].N + BM - 1) / BM) * ((p.jobs[j].M + BN - 1) / BN);
     }
-    if (tiles < sms0 && kbw >= 2) {
+    int64_t maxT = 1;
+    for (int j = 0; j < p.njobs; ++j) maxT = std::max<int64_t>(maxT, std::min<int64_t>(p.jobs[j].M, BN));
+    if (kbw >= 2) {
       double best = 1e300;
       for (int sp = 1; sp <= 16 && sp <= kbw; ++sp) {
         const double rounds = (double)((tiles * sp + sms0 - 1) / sms0);
-        const double slot_us = sp > 1 ? 2.0 * (double)(tiles * sp * BN * BM * 4) / 6.0e6 : 0.0;
-        const double cost = rounds * (double)((kbw + sp - 1) / sp) * 0.48 + (sp > 1 ? 2.5 + slot_us : 0.0);
+        const double slot_us = sp > 1 ? 2.0 * (double)(tiles * sp * maxT * BM * 4) / 6.0e6 : 0.0;
+        const double cost =
+            rounds * ((double)((kbw + sp - 1) / sp) * 0.48 + 1.5) + (sp > 1 ? 1.0 + slot_us : 0.0);
         if (cost < best - 1e-9) {
           best = cost;
           splits = sp;
