@@ -241,7 +241,8 @@ __device__ __forceinline__ void store_col_chunk(const UmmaArgs &a, const UJob &J
 
 // Split-mode store (swap): CH token columns cl0.. of output row m of the
 // unit's float32 slot (column-major, 128 rows per column); no bias, which the
-// ordered reduction adds.  Columns past the token count are not written.
+// tile's ordered finish (split_finish) adds.  Columns past the token count are
+// not written.
 template <int CH, int BN>
 __device__ __forceinline__ void store_slot_chunk(const UmmaArgs &a, const UJob &J, const UnitPos &q, int m,
                                                  int cl0, const float (&v)[CH]) {

@@ -55,3 +55,23 @@ def test_oracle_sample_fills_its_budget_with_whole_passes(monkeypatch):
     assert calls[1:] == [512] * 10
     assert sample.startswith("10 pass(es) of 512 of 512")
     assert cores == 4 and secs > 0 and value > 0
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    import shutil
+    src = bench.os.path.join(bench.ROOT, "sharded_gemm_gb300", "csrc")
+    dst = tmp_path / "sharded_gemm_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_sources_hash("umma")
+    f = dst / "k_umma.cu"
+    text = f.read_text()
+    f.write_text(text + "\n// a note\n/* and a\n   block note */\n")
+    assert bench.kernel_sources_hash("umma") == h0
+    f.write_text(text + "\nstatic int unused_probe_value;\n")
+    assert bench.kernel_sources_hash("umma") != h0
+    # the shared split sum belongs to every family
+    f.write_text(text)
+    g = dst / "k_split.cu"
+    g.write_text(g.read_text() + "\nstatic int unused_probe_value;\n")
+    assert bench.kernel_sources_hash("umma") != h0
