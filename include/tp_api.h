@@ -202,6 +202,12 @@ int tp_gated_all_to_sharded(int N, const void *x, int64_t T, int64_t K, int64_t 
  * Every partial x[r] @ w[r]^T is formed in float32 from zero and the
  * partials are added in ascending r, so the result does not depend on how
  * the GPU schedules the work.  Partials do not go through device memory.
+ * Exception, T <= 16 with fewer 128-row output tiles than the GPU has SMs:
+ * the contraction over r = 0..N-1 laid end to end is cut into consecutive
+ * k-block ranges.  Each range is summed in float32 from zero, across rank
+ * boundaries too, and the range sums are added in range order through the
+ * float32 workspace.  The order is still ascending r, and it is fixed by the
+ * shapes alone.
  * Errors: TP_ERR_NOT_DIVISIBLE if K % N != 0; otherwise as tp_all_to_sharded.
  */
 int tp_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K, int64_t ldx,
@@ -227,7 +233,7 @@ int tp_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K, int64_t
  *          the all-reduced (T, O) output of tp_sharded_to_all.
  * Every partial is formed in float32 from zero and the N partials of a block
  * are added in ascending r, as in tp_sharded_to_all; partials do not go
- * through device memory.
+ * through device memory (with the same small-batch exception).
  * Errors: TP_ERR_NOT_DIVISIBLE if K % N != 0 ("Cannot shard the input of
  * size K across N devices.") or O % N != 0 ("Cannot shard the output ...");
  * TP_ERR_UNSUPPORTED if N * N > 64; otherwise as tp_sharded_to_all, with
