@@ -151,8 +151,11 @@ int tp_shard_weight(const void *w, int64_t rows, int64_t cols, int elem_bytes, i
  * Errors: TP_ERR_NOT_DIVISIBLE if O % N != 0, with the message
  * "Cannot shard the output of size O across N devices."; TP_ERR_INVALID_ARG
  * for null pointers, T < 0, K < 1, N < 1 or N > 64, ldx < K, ldy < O/N;
- * TP_ERR_ALIGNMENT if a bf16/f16 x or w[r] is not 16-byte aligned or ldx
- * is not a multiple of 8.  T = 0 is valid and launches nothing.
+ * TP_ERR_ALIGNMENT if x, w[r] or y[r] is not aligned to its element size or
+ * bias[r] to 4 bytes.  Operands the tensor copies cannot take (a base not
+ * 16-byte aligned, a row stride not a multiple of 16 bytes) run on the
+ * CUDA-core kernel instead, with the same result.  T = 0 is valid and
+ * launches nothing.
  */
 int tp_all_to_sharded(int N, const void *x, int64_t T, int64_t K, int64_t ldx,
                       const void *const *w, int64_t O, const void *const *bias,
@@ -282,9 +285,12 @@ int tp_gathered_to_sharded(int N, const void *const *x, int64_t T, int64_t K, in
  * in_dt: TP_BF16, TP_F16 or TP_F32.
  * Errors: TP_ERR_NOT_DIVISIBLE if q < 1 or M, K or Ncols is not a multiple of
  * q (the page's grid requires P = q*q processors and block dimensions that
- * divide evenly); TP_ERR_ALIGNMENT if (for bf16/f16) K/q or Ncols/q is not a
- * multiple of 8 or a block pointer is not 16-byte aligned; TP_ERR_INVALID_ARG
- * for null pointers or q > 8.
+ * divide evenly); TP_ERR_UNSUPPORTED if q > 4 (this build holds at most 16
+ * logical processors); TP_ERR_ALIGNMENT if an X or A block is not aligned
+ * to its element size or a Y block to 4 bytes; TP_ERR_INVALID_ARG for null
+ * pointers, sizes below 1 or a bad dtype.  Blocks the tensor copies cannot
+ * take (a base not 16-byte aligned, a block row not a multiple of 16 bytes)
+ * run on the CUDA-core kernel instead, with the same result.
  */
 int tp_summa(int q, const void *const *X, const void *const *A, void *const *Y, int64_t M,
              int64_t K, int64_t Ncols, tp_dtype in_dt, tp_stream_t stream);
