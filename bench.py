@@ -27,8 +27,14 @@ L2 and without the flush's own dirty lines still being written back to HBM
 while it runs.  ``value`` comes from events at the step boundaries only
 (an event between two kernels would stop the second from starting early);
 the per-kernel times behind ``roofline`` come from a second loop of the same
-steps with an event after every call.  ``--impl reference`` times the fp64 CPU oracle
-on a bounded sample of the same workload instead.
+steps with an event after every call.  Each call is checked and marshalled
+once (``tp.prepare``) and replayed through the C ABI every step, so the host
+stays ahead of the GPU.  The default line also carries ``q4_decode``: the
+4-bit pair (8192 x 28672, N = 8) at T = 1 and T = 16 timed the same way, with
+its own roofline against the copy bandwidth.  ``cpu_baseline`` is the fp64
+oracle on a bounded sample of the config's step (every product keeps its
+token rows and a fraction of its output features).  ``--impl reference``
+times that oracle as the reference arm instead.
 Under torchrun (N > 1) every rank runs its own independent problem (weak
 scaling); no collective touches the data path.
 """
@@ -366,58 +372,288 @@ def scale(work: float, ms: float, unit: str) -> float:
 
 
 # ------------------------------------------------------------------ CPU oracle legs
-class OracleMLP:
-    """The fp64 oracle on the MLP pair: weights drawn and widened once; each
-    ``run(rows)`` pushes the first ``rows`` token rows through both layers."""
+DECODE_T = 16  # token counts up to this are weight-streaming (GB/s) configs
 
-    def __init__(self, seed: int = 0):
+
+class OracleLeg:
+    """The fp64 oracle (the test suite's CPU reference, used as it stands) on
+    one bench config's step, over a bounded sample.
+
+    Sample: every product of the step keeps all of its token rows and the
+    first ceil(f * n) of its n output features (rows of a linear's weight,
+    per shard for a column-parallel layer; columns for the backward's and
+    SUMMA's products), so the work is f of a full step's (FLOPs, or weight
+    bytes for the decode configs).  A layer that consumes an earlier layer's
+    output takes a seeded stand-in of the right shape (the sampled earlier
+    layer does not produce all of it); values do not change the oracle's
+    time.  The oracle splits each product's output rows (the tokens) across
+    its OpenMP threads, so a decode step runs on min(T, threads) cores."""
+
+    def __init__(self, config: str, seed: int = 0):
         import numpy as np
         import oracle
         from sharded_gemm_gb300 import synth
-        self.oracle = oracle
-        cfg = synth.mlp(seed=seed)
-        N = cfg["N"]
-        self.w1 = [oracle.bf16_to_f64(p) for p in oracle.shard(cfg["w1"], 0, 1, N)]
-        self.b1 = [p.astype(np.float64) for p in oracle.shard(cfg["b1"], 0, 1, N)]
-        self.w2 = [oracle.bf16_to_f64(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
-        self.b2 = cfg["b2"].astype(np.float64)
-        self.x = oracle.bf16_to_f64(cfg["x"])
-        self.total_rows = cfg["T"]
-        self.per_row = 2.0 * 2 * cfg["D"] * cfg["F"]
-        self.desc = "token rows of the (512, 4096) batch through both layers (full W1, W2)"
+        self.np, self.oracle, self.synth = np, oracle, synth
+        self.config = config
+        self.seed = seed
+        self.cfg = self._draw()
+        self.f = None
 
-    def run(self, rows: int) -> float:
+    # -- inputs
+    def _draw(self):
+        s, c = self.synth, self.config
+        if c in ("mlp", "mlp_ag_rs", "mlp_bwd"):
+            cfg = s.mlp(seed=self.seed)
+            if c == "mlp_bwd":
+                cfg["dy"] = s.grad_output(seed=self.seed, T=cfg["T"], D=cfg["D"])["dy"]
+            return cfg
+        if c == "ffn_gated":
+            return s.ffn(seed=self.seed)
+        if c in ("summa2", "summa4"):
+            return s.summa(seed=self.seed)
+        if c.startswith("qkv"):
+            return s.qkv(seed=self.seed, T=int(c[3:]))
+        if c.startswith("q4_") or c.startswith("mx_"):
+            return s.q4(seed=self.seed, T=int(c[3:]))
+        raise SystemExit("no oracle leg for config %s" % c)
+
+    def _standin(self, shape, k):
+        g = self.synth.streams(self.seed + 7919 * (k + 1), 1)[0]
+        return self.oracle.bf16_to_f64(self.synth.normal_bf16(g, shape, 1.0))
+
+    @staticmethod
+    def _take(n, f):
+        return max(1, min(n, int(-(-n * f // 1))))
+
+    # -- one sample
+    def prepare(self, f: float):
+        """Widens the sampled operands to float64 (not timed) for fraction f."""
+        np, o, cfg, c = self.np, self.oracle, self.cfg, self.config
+        f = min(1.0, f)
+        self.f = f
+        b16 = o.bf16_to_f64
+        take = self._take
+        work = 0.0
+        self.ops = []
+        if c in ("mlp", "mlp_ag_rs", "ffn_gated"):
+            N, T, D, F = cfg["N"], cfg["T"], cfg["D"], cfg["F"]
+            m1, m2 = take(F // N, f), take(D // N, f) * N if c == "mlp_ag_rs" else take(D, f)
+            x = b16(cfg["x"])
+            w1 = [b16(p[:m1]) for p in o.shard(cfg["w1"], 0, 1, N)]
+            b1 = [p[:m1].astype(np.float64) for p in o.shard(cfg["b1"], 0, 1, N)]
+            w2 = [b16(p[:m2]) for p in o.shard(cfg["w2"], -1, 1, N)]
+            b2 = cfg["b2"][:m2].astype(np.float64)
+            mid = [self._standin((T, F // N), r) for r in range(N)]
+            if c == "mlp":
+                self.ops = [lambda: o.all_to_sharded(x, w1, b1), lambda: o.sharded_to_all(mid, w2, b2)]
+                work = 2.0 * T * D * m1 * N + 2.0 * T * F * m2
+            elif c == "mlp_ag_rs":
+                xs = o.shard(x, -1, 1, N)
+                self.ops = [lambda: o.gathered_to_sharded(xs, w1, b1), lambda: o.sharded_to_sharded(mid, w2, b2)]
+                work = 2.0 * T * D * m1 * N + 2.0 * T * F * m2
+            else:
+                w3 = [b16(p[:m1]) for p in o.shard(cfg["w3"], 0, 1, N)]
+                b3 = [p[:m1].astype(np.float64) for p in o.shard(cfg["b3"], 0, 1, N)]
+                self.ops = [lambda: o.gated_all_to_sharded(x, w1, w3, b1, b3), lambda: o.sharded_to_all(mid, w2, b2)]
+                work = 2.0 * 2 * T * D * m1 * N + 2.0 * T * F * m2
+            self.rows = T
+        elif c == "mlp_bwd":
+            N, T, D, F = cfg["N"], cfg["T"], cfg["D"], cfg["F"]
+            Fn = F // N
+            mf, md = take(Fn, f), take(D, f)
+            dy = b16(cfg["dy"])
+            x = b16(cfg["x"])
+            w2 = [np.ascontiguousarray(b16(p)[:, :mf]) for p in o.shard(cfg["w2"], -1, 1, N)]  # (D, Fn)
+            w1 = [np.ascontiguousarray(b16(p)[:, :md]) for p in o.shard(cfg["w1"], 0, 1, N)]  # (Fn, D)
+            h = [self._standin((T, Fn), r)[:, :mf].copy() for r in range(N)]
+            dh = [self._standin((T, Fn), N + r) for r in range(N)]
+            dys, xs = np.ascontiguousarray(dy[:, :md]), np.ascontiguousarray(x[:, :md])
+            self.ops = [lambda: o.sharded_to_all_dx(dy, w2), lambda: o.sharded_dw([dy] * N, h),
+                        lambda: o.bias_grad([[dys]]), lambda: o.all_to_sharded_dx(dh, w1),
+                        lambda: o.sharded_dw(dh, [xs] * N), lambda: o.bias_grad([[p[:, :mf]] for p in dh])]
+            work = 2.0 * T * D * mf * N * 2 + 2.0 * T * Fn * md * N * 2
+            self.rows = T
+        elif c in ("summa2", "summa4"):
+            q = int(c[-1])
+            M, K, Nc = cfg["M"], cfg["K"], cfg["Ncols"]
+            mb = take(Nc // q, f)
+            X = o.blocks(b16(cfg["X"]), q)
+            A = [np.ascontiguousarray(a[:, :mb]) for a in o.blocks(b16(cfg["A"]), q)]
+            self.ops = [lambda: o.summa(X, A, q)]
+            work = 2.0 * M * K * mb * q
+            self.rows = M // q
+        elif c.startswith("qkv"):
+            N, T, D, V = cfg["N"], cfg["T"], cfg["D"], cfg["V"]
+            mq, mo, ml = take(3 * D // N, f), take(D, f), take(V // N, f)
+            x = b16(cfg["x"])
+            wq = [b16(p[:mq]) for p in o.shard(cfg["w_qkv"], 0, 3, N)]
+            bq = [p[:mq].astype(np.float64) for p in o.shard(cfg["b_qkv"], 0, 3, N)]
+            wo = [b16(p[:mo]) for p in o.shard(cfg["w_o"], -1, 1, N)]
+            bo = cfg["b_o"][:mo].astype(np.float64)
+            wl = [b16(p[:ml]) for p in o.shard(cfg["w_lm"], 0, 1, N)]
+            xc = o.shard(x, -1, 1, N)
+            self.ops = [lambda: o.all_to_sharded(x, wq, bq), lambda: o.sharded_to_all(xc, wo, bo),
+                        lambda: o.all_to_sharded(x, wl)]
+            per = mq * N * D + mo * D + ml * N * D  # weights touched (W_o: mo rows of D/N per rank)
+            work = 2.0 * per if T <= DECODE_T else 2.0 * T * per
+            self.rows = T
+        else:  # q4_T, mx_T
+            N, T, D, F = cfg["N"], cfg["T"], cfg["D"], cfg["F"]
+            mu, md = take(F // N, f), take(D, f)
+            x = b16(cfg["x"])
+            mid = [self._standin((T, F // N), r) for r in range(N)]
+            up_rows = np.concatenate([np.arange(r * (F // N), r * (F // N) + mu) for r in range(N)])
+            wu, wd = cfg["w_up"][up_rows], cfg["w_down"][:md]
+            if c.startswith("q4_"):
+                qu, qd = o.quantize_affine4(wu, 64), o.quantize_affine4(wd, 64)
+                ups = [[a[r * mu:(r + 1) * mu] for r in range(N)] for a in qu]
+                dns = [o.shard(a, -1, 1, N) for a in qd]
+                self.ops = [lambda: o.q4_all_to_sharded(x, *ups, 64), lambda: o.q4_sharded_to_all(mid, *dns, 64)]
+                bpw = 0.5 + 4.0 / 64
+            else:
+                qu, qd = o.quantize_mxfp8(wu), o.quantize_mxfp8(wd)
+                ups = [[a[r * mu:(r + 1) * mu] for r in range(N)] for a in qu]
+                dns = [o.shard(a, -1, 1, N) for a in qd]
+                self.ops = [lambda: o.mx_all_to_sharded(x, *ups), lambda: o.mx_sharded_to_all(mid, *dns)]
+                bpw = 1.0 + 1.0 / 32
+            weights = mu * N * D + md * F
+            work = weights * bpw if T <= DECODE_T else 2.0 * T * weights
+            self.rows = T
+        self.work = work
+        self.full = self._full_work()
+
+    def _full_work(self):
+        cfg, c = self.cfg, self.config
+        if c in ("mlp", "mlp_ag_rs"):
+            return 2.0 * 2 * cfg["T"] * cfg["D"] * cfg["F"]
+        if c == "ffn_gated":
+            return 2.0 * 3 * cfg["T"] * cfg["D"] * cfg["F"]
+        if c == "mlp_bwd":
+            return 2.0 * 4 * cfg["T"] * cfg["D"] * cfg["F"]
+        if c.startswith("summa"):
+            return 2.0 * cfg["M"] * cfg["K"] * cfg["Ncols"]
+        if c.startswith("qkv"):
+            D, V, T = cfg["D"], cfg["V"], cfg["T"]
+            w = D * (3 * D + D + V)
+            return 2.0 * w if T <= DECODE_T else 2.0 * T * w
+        D, F, T = cfg["D"], cfg["F"], cfg["T"]
+        bpw = 0.5 + 4.0 / 64 if c.startswith("q4_") else 1.0 + 1.0 / 32
+        return 2 * D * F * bpw if T <= DECODE_T else 2.0 * T * 2 * D * F
+
+    def unit(self):
+        c, T = self.config, self.cfg.get("T", 1 << 30)
+        decode = (c.startswith("qkv") or c.startswith("q4_") or c.startswith("mx_")) and T <= DECODE_T
+        return "GB/s" if decode else "TFLOP/s"
+
+    def cores(self):
+        return min(self.oracle.num_threads(), self.rows)
+
+    def run(self) -> float:
         t = time.time()
-        mid = self.oracle.all_to_sharded(self.x[:rows], self.w1, self.b1)
-        self.oracle.sharded_to_all(mid, self.w2, self.b2)
+        for op in self.ops:
+            op()
         return time.time() - t
 
-    def seconds_per_row(self) -> float:
-        # a 64-row pass: one row alone would charge every row the fixed cost of a call
-        if not hasattr(self, "_spr"):
-            probe = min(64, self.total_rows)
-            self._spr = max(self.run(probe), 1e-4) / probe
-        return self._spr
+    def describe(self):
+        return ("first %.4g of the output features of every product of one %s step (all token rows; "
+                "%.4g of the step's work)" % (self.f, self.config, self.work / self.full))
 
-    def rows_for(self, budget_s: float) -> int:
-        return int(max(1, min(self.total_rows, budget_s / self.seconds_per_row())))
+    def value(self, seconds: float) -> float:
+        return self.work / seconds / (1e9 if self.unit() == "GB/s" else 1e12)
+
+    def size_for(self, budget_s: float) -> float:
+        """Fraction f whose sample takes about budget_s (from a probe at f = 1/64)."""
+        self.prepare(1.0 / 64)
+        self.run()  # first call loads the C loops
+        t = max(self.run(), 1e-4)
+        return min(1.0, (1.0 / 64) * budget_s / t)
 
 
-def oracle_sample(budget_s: float):
-    """(TFLOP/s, seconds, sample description, threads) of one bounded sample:
-    whole passes of up to the full batch, about ``budget_s`` of CPU work."""
-    o = OracleMLP()
-    rows = o.rows_for(budget_s)
-    passes = max(1, int(budget_s / (o.seconds_per_row() * rows)))
+def oracle_sample(config: str, budget_s: float):
+    """(value, seconds, sample description, cores) of one bounded sample of
+    about ``budget_s`` of CPU work: whole passes of the sized sample."""
+    leg = OracleLeg(config)
+    f = leg.size_for(budget_s / 2)
+    leg.prepare(f)
+    first = leg.run()
+    passes = max(1, int((budget_s / 2) / max(first, 1e-4)))
     t = time.time()
     for _ in range(passes):
-        o.run(rows)
+        leg.run()
     dt = time.time() - t
-    return (o.per_row * rows * passes / dt / 1e12, dt,
-            "%d pass(es) of %d of %d %s" % (passes, rows, o.total_rows, o.desc), o.oracle.num_threads())
+    return (leg.value(dt / passes), dt, "%d pass(es) of the %s" % (passes, leg.describe()), leg.cores())
 
 
 # ------------------------------------------------------------------ main
+def timed_loops(launches, stream, steps, k_steps, l2_flush, tp):
+    """Device-timed steps: ``steps`` with events at the step boundaries only,
+    then ``k_steps`` with an event after every call (per-kernel times).
+    Returns (ms per step, [ms per call])."""
+    import torch
+    nk = len(launches)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(k_steps)]
+    for i in range(steps):
+        l2_flush(i)
+        ev[i][0].record(stream)
+        for fn in launches:
+            fn(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    for i in range(k_steps):
+        l2_flush(i)
+        kev[i][0].record(stream)
+        for k, fn in enumerate(launches):
+            fn(stream)
+            kev[i][k + 1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    per_kernel = [sum(kev[i][k].elapsed_time(kev[i][k + 1]) for i in range(k_steps)) / k_steps for k in range(nk)]
+    return step_ms, per_kernel
+
+
+def roofline_of(info, per_kernel, peaks, config):
+    """Roofline of the dominant call.  Every call is timed on its own (events
+    on both sides, a fraction of a millisecond), so a contraction is held to
+    the burst bf16 peak; a weight stream to the measured copy bandwidth."""
+    k = max(range(len(per_kernel)), key=lambda i: per_kernel[i])
+    if info["bound"] == "tensor":
+        peak, punit, kind = peaks["bf16_tflops"], "TFLOP/s", "bf16_tflops (burst: each call timed alone)"
+        achieved = info["kernel_work"][k] / (per_kernel[k] * 1e-3) / 1e12
+    else:
+        peak, punit, kind = peaks["hbm_gbs"], "GB/s", "hbm_gbs"
+        achieved = info["kernel_work"][k] / (per_kernel[k] * 1e-3) / 1e9
+    return {"bound": info["bound"], "kernel": info["kernel_names"][k], "achieved": round(achieved, 2),
+            "peak": peak, "unit": punit, "frac": round(achieved / peak, 4),
+            "traffic": traffic_for(config, info["kernel_names"][k]),
+            "peak_source": "%s of %s" % (kind, peaks["source"])}
+
+
+def q4_decode_workloads(device: str, seed: int):
+    """The 4-bit pair (D 8192, F 28672, N 8) at T = 1 and T = 16, one copy of the
+    weights: the T = 1 input is the first row of the T = 16 draw, which is
+    the T = 1 config's own input (the same seeded stream)."""
+    import torch
+    import sharded_gemm_gb300 as tp
+    from sharded_gemm_gb300 import synth
+    from sharded_gemm_gb300.workloads import Q4Pair
+    cfg = synth.q4(seed=seed, T=16)
+    w = Q4Pair(cfg, device=device)
+    out = {}
+    D, F, N = cfg["D"], cfg["F"], cfg["N"]
+    per = D * F * (0.5 + 4.0 / 64)
+    for T in (1, 16):
+        x = w.x[:T]
+        mid = [torch.empty((T, F // N), dtype=torch.bfloat16, device=device) for _ in range(N)]
+        y = torch.empty((T, D), dtype=torch.float32, device=device)
+        launches = [lambda s, x=x, mid=mid: tp.tp_q4_all_to_sharded(x, *w.up, out=mid, stream=s),
+                    lambda s, mid=mid, y=y: tp.tp_q4_sharded_to_all(mid, *w.down, out=y, stream=s)]
+        info = dict(bound="hbm", unit="GB/s", work=w.weight_bytes, kernel_work=[per, per],
+                    kernel_names=["tp_q4_all_to_sharded", "tp_q4_sharded_to_all"])
+        out[T] = (launches, info)
+    return w, out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,6 +662,8 @@ def main():
     ap.add_argument("--config", default="mlp")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-q4-decode", action="store_true",
+                    help="skip the q4 decode sub-record of the default (mlp) line")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--policy", default="auto", choices=["auto", "single_sm", "simt"],
                     help="kernel family (diagnostics; the product default is auto)")
@@ -453,7 +691,13 @@ def main():
                       "simt": tp.TP_POLICY_SIMT}[args.policy])
 
     w, step, info = make_workload(args.config, rank, device)
-    launches = split_step(args.config, w)
+    # every call checked and marshalled once (tp.prepare), replayed each step
+    # through the C ABI: the host stays ahead of the GPU even on decode steps
+    launches = [tp.prepare(fn, None) for fn in split_step(args.config, w)]
+    q4dec = None
+    if args.config == "mlp" and not args.no_q4_decode:
+        q4w, q4dec = q4_decode_workloads(device, 0 + rank)
+        q4dec = {T: ([tp.prepare(fn, None) for fn in lst], qi) for T, (lst, qi) in q4dec.items()}
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     flush_sum = torch.empty((), dtype=torch.float32, device=device)
@@ -462,54 +706,40 @@ def main():
         flush.fill_(float(i & 7))  # every line of the previous step is evicted
         torch.sum(flush, dim=0, out=flush_sum)  # the flush's dirty lines are written back here
 
-    for _ in range(max(args.warmup, 3)):
-        n0 = tp.tp_launch_count()
-        for fn in launches:
-            fn(stream)
-        launches_per_step = tp.tp_launch_count() - n0  # the library's own kernels in one step
+    def warm(lst):
+        n = 0
+        for _ in range(max(args.warmup, 3)):
+            n0 = tp.tp_launch_count()
+            for fn in lst:
+                fn(stream)
+            n = tp.tp_launch_count() - n0  # the library's own kernels in one step
+        return n
+
+    launches_per_step = warm(launches)
+    q4_lps = {T: warm(l) for T, (l, _) in q4dec.items()} if q4dec else {}
     torch.cuda.synchronize()
     if tp.tp_query_status() != 0:
         raise SystemExit("device status error during warm-up")
 
-    nk = len(launches)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     k_steps = max(1, min(args.steps, 500))
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(k_steps)]
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.mark("begin")
-    for i in range(args.steps):
-        l2_flush(i)
-        ev[i][0].record(stream)
-        for fn in launches:
-            fn(stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms, per_kernel = timed_loops(launches, stream, args.steps, k_steps, l2_flush, tp)
+    q4res = {}
+    for T, (lst, qi) in (q4dec or {}).items():
+        q4res[T] = timed_loops(lst, stream, args.steps, k_steps, l2_flush, tp)
     if world > 1:
         torch.distributed.barrier()
-    # per-kernel breakdown: the same steps with an event after every call
-    for i in range(k_steps):
-        l2_flush(i)
-        kev[i][0].record(stream)
-        for k, fn in enumerate(launches):
-            fn(stream)
-            kev[i][k + 1].record(stream)
-    torch.cuda.synchronize()
     sampler.mark("end")
     clocks = sampler.stop()
     status = tp.tp_query_status()
     if status != 0:
         raise SystemExit("device status error %d in the timed region" % status)
 
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    per_kernel = [0.0] * nk
-    for i in range(k_steps):
-        for k in range(nk):
-            per_kernel[k] += kev[i][k].elapsed_time(kev[i][k + 1])
-    per_kernel = [x / k_steps for x in per_kernel]
     max_ms, total_work = aggregate(step_ms, info["work"], world, group, device)
     value = scale(total_work, max_ms, info["unit"])
 
@@ -543,24 +773,24 @@ def main():
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in dev_in),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in dev_out)}
 
-    # roofline of the dominant kernel
-    k = max(range(nk), key=lambda i: per_kernel[i])
-    if info["bound"] == "tensor":
-        peak, punit = peaks["bf16_tflops_sustained"], "TFLOP/s"
-        achieved = info["kernel_work"][k] / (per_kernel[k] * 1e-3) / 1e12
-        peak_kind = "bf16_tflops_sustained (long back-to-back timed loop)"
-    else:
-        peak, punit = peaks["hbm_gbs"], "GB/s"
-        achieved = info["kernel_work"][k] / (per_kernel[k] * 1e-3) / 1e9
-        peak_kind = "hbm_gbs"
-    roofline = {"bound": info["bound"], "kernel": info["kernel_names"][k], "achieved": round(achieved, 2),
-                "peak": peak, "unit": punit, "frac": round(achieved / peak, 4),
-                "traffic": traffic_for(args.config, info["kernel_names"][k]),
-                "peak_source": "%s of %s" % (peak_kind, peaks["source"])}
+    roofline = roofline_of(info, per_kernel, peaks, args.config)
+
+    q4_decode = None
+    if q4res:
+        q4_decode = {}
+        for T, (ms, pk) in q4res.items():
+            qi = q4dec[T][1]
+            m, wk = aggregate(ms, qi["work"], world, group, device)
+            q4_decode["T%d" % T] = {
+                "value": round(scale(wk, m, "GB/s"), 1), "unit": "GB/s", "ms_per_step": round(m, 5),
+                "kernels_ms": {n: round(t, 5) for n, t in zip(qi["kernel_names"], pk)},
+                "roofline": roofline_of(qi, pk, peaks, "q4_%d" % T),
+                "gpu_launches": q4_lps[T] * args.steps,
+                "config": {"workload": "q4_pair_T%d" % T, "T": T, "D": 8192, "F": 28672, "N": 8}}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.config == "mlp":
-        v, secs, sample, cores = oracle_sample(args.cpu_budget)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, secs, sample, cores = oracle_sample(args.config, args.cpu_budget)
         cpu = {"value": round(v, 6), "unit": info["unit"], "cores": cores, "kind": "oracle",
                "sample": sample, "seconds": round(secs, 2)}
 
@@ -578,6 +808,9 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         }
+        if q4_decode is not None:
+            line["q4_decode"] = q4_decode
+            line["gpu_launches"] += sum(v["gpu_launches"] for v in q4_decode.values())
         if args.policy != "auto":
             line["policy"] = args.policy
         print(json.dumps(line), flush=True)
@@ -589,30 +822,40 @@ def main_reference(args, world, rank):
     """The oracle as the reference arm: a bounded sample per step, CPU cores."""
     if rank != 0:
         return
-    if args.config != "mlp":
-        print(json.dumps({"impl": "reference", "unavailable": "oracle arm implemented for the mlp config"}))
-        return
-    o = OracleMLP()
+    leg = OracleLeg(args.config)
     steps = args.steps + args.warmup
-    rows = o.rows_for(max(0.02, 120.0 / max(steps, 1)))
+    f = leg.size_for(max(0.02, 120.0 / max(steps, 1)))
+    leg.prepare(f)
     vals = []
     t_all = time.time()
     for i in range(steps):
-        dt = o.run(rows)
+        dt = leg.run()
         if i >= args.warmup:
             vals.append(dt)
         if time.time() - t_all > 240:
             break
     secs = statistics.median(vals) if vals else float("nan")
-    v = o.per_row * rows / secs / 1e12 if vals else 0.0
-    sample = "%d of %d %s" % (rows, o.total_rows, o.desc)
-    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
+    v = leg.value(secs) if vals else 0.0
+    unit = leg.unit()
+    cfg, c = leg.cfg, args.config
+    if c.startswith("summa"):
+        q = int(c[-1])
+        meta = dict(workload="summa_%dx%d" % (q, q), M=cfg["M"], K=cfg["K"], N=cfg["Ncols"], q=q)
+    elif c.startswith("qkv"):
+        meta = dict(workload="qkv_o_lmhead_T%d" % cfg["T"], T=cfg["T"], D=cfg["D"], V=cfg["V"], N=cfg["N"])
+    else:
+        name = {"mlp": "mlp_col_row_pair", "mlp_bwd": "mlp_col_row_pair_backward", "ffn_gated": "llama_gated_ffn",
+                "mlp_ag_rs": "mlp_allgather_reducescatter"}.get(c)
+        if name is None:
+            name = ("q4_pair_T%d" if c.startswith("q4_") else "mxfp8_pair_T%d") % cfg["T"]
+        meta = dict(workload=name, T=cfg["T"], D=cfg["D"], F=cfg["F"], N=cfg["N"])
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit, "n_gpus": world,
             "steps": len(vals), "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": "mlp_col_row_pair", "T": 512, "D": 4096, "F": 11008, "N": 4},
-            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "kind": "oracle",
-                             "cores": o.oracle.num_threads(), "sample": sample},
-            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "data": "synthetic", "config": meta,
+            "cpu_baseline": {"value": round(v, 6), "unit": unit, "kind": "oracle", "cores": leg.cores(),
+                             "sample": "per step, the " + leg.describe()},
+            "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 

@@ -16,6 +16,7 @@ from __future__ import annotations
 import ctypes
 import os
 import re
+import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libtp.so")
@@ -36,8 +37,37 @@ class TPError(RuntimeError):
         self.msg = msg
 
 
+_rec = threading.local()  # set while prepare() marshals a call
+
+
+class _Recording:
+    """Stands in for the library while prepare() runs an entry point: the one
+    call the entry point makes is recorded instead of executed."""
+
+    def __init__(self, real):
+        self.real = real
+        self.calls = []
+
+    def __getattr__(self, name):
+        if not name.startswith("tp_") or name in ("tp_last_error",):
+            return getattr(self.real, name)
+        fn = getattr(self.real, name)
+
+        def record(*args):
+            self.calls.append((fn, args))
+            return TP_OK
+        return record
+
+
 def lib() -> ctypes.CDLL:
     """The loaded libtp.so (raises RuntimeError if it has not been built)."""
+    r = getattr(_rec, "active", None)
+    if r is not None:
+        return r
+    return _load()
+
+
+def _load() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
@@ -85,6 +115,47 @@ def lib() -> ctypes.CDLL:
             fn.restype = res
         _lib = L
     return _lib
+
+
+class Prepared:
+    """One entry-point call, checked and marshalled once, replayed by
+    ``__call__(stream)`` through the C ABI with the same arguments.
+
+    It holds the device pointers of the tensors it was prepared with (and a
+    reference to each, so they stay allocated); the caller must not resize or
+    reallocate them.  Replaying costs one ctypes call, about what the C ABI
+    itself costs, instead of the per-call argument checks and array building
+    of the eager functions.  ``result`` is what the eager call returned (the
+    output tensors)."""
+
+    def __init__(self, fn, args, keep, result):
+        self.fn = fn
+        self.args = list(args)
+        self.keep = keep
+        self.result = result
+
+    def __call__(self, stream=None):
+        self.args[-1] = _stream(stream)
+        _check(self.fn(*self.args))
+        return self.result
+
+
+def prepare(entry, *args, **kwargs) -> Prepared:
+    """Prepares ``entry(*args, **kwargs)`` (one of this module's entry points
+    that takes a ``stream`` argument) for replay; nothing is launched here."""
+    if getattr(_rec, "active", None) is not None:
+        raise RuntimeError("prepare() calls do not nest")
+    rec = _Recording(_load())
+    _rec.active = rec
+    try:
+        result = entry(*args, **kwargs)
+    finally:
+        _rec.active = None
+    if len(rec.calls) != 1:
+        raise ValueError("%s made %d library calls; prepare() takes entry points that make one"
+                         % (getattr(entry, "__name__", entry), len(rec.calls)))
+    fn, cargs = rec.calls[0]
+    return Prepared(fn, cargs, (args, kwargs), result)
 
 
 def declared_functions() -> list[str]:

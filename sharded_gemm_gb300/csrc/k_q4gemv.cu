@@ -15,20 +15,25 @@
 // the path is bound by HBM (0.5625 bytes per weight: the 4-bit code plus the
 // float16 scale and bias of its group).  A 128-row tensor-core MMA takes
 // about as long for 16 tokens as for one, and at one token its issue rate,
-// not HBM, sets the pace; here the per-weight work is one ALU mask and half a
-// packed FMA, under the SM's issue rate at full HBM bandwidth.
+// not HBM, sets the pace; here the per-weight work is a quarter of a logic
+// operation and half an integer dot-product instruction per token, well under
+// the SM's issue rate at full HBM bandwidth.
 //
-// Exact decode.  Element k of a 32-bit code word sits at bits 4(k%8).  Two
-// neighbouring words form one 64-bit pair; for j = 0..3, (pair & 0xF<<4j in
-// each half), read as a float32 pair, is the subnormal code*16^j * 2^-149,
-// exact (the pair shifted right by 16 gives elements 4..7 the same way).  x
-// is staged in shared memory as float32 scaled by 2^(A-4j), with A = 125 -
-// (exponent of the largest |x| of the 64-element group), so one packed f32x2
-// FMA adds code * x * 2^(A-149), exactly formed (4 + 8 significant bits, a
-// normal float unless x is over 2^100 below the group's largest element), to a
-// float32 sum; two exact power-of-two multiplies undo the 2^(A-149) in the
-// epilogue.  Sums run in a fixed order and no atomics touch the values, so
-// repeated runs are bit-identical.
+// Integer decode.  Element k of a 32-bit code word sits at bits 4(k%8).  One
+// AND with 0x0F0F0F0F leaves the even elements (0, 2, 4, 6) as four bytes,
+// one AND with 0xF0F0F0F0 the odd ones (1, 3, 5, 7) times 16, so a word
+// costs two logic operations and no shifts.  x is staged once per CTA as
+// 16-bit integers: each 64-element group is scaled by 2^(14-emax) (emax =
+// exponent of the group's largest |x|) and rounded to the nearest integer,
+// so |x_int| < 2^15 and every element within 2^7 of the group's largest keeps
+// all eight bits of its bfloat16 significand (smaller ones lose at most half
+// a unit of 2^(emax-14)).  Four two-way integer dot products (dp2a: two
+// 16-bit x times two code bytes, added to a 32-bit sum) take a word's eight
+// products; the even and the odd sums of a group are exact integers, joined
+// as 16*even + odd = 16 * sum(code * x_int) (|.| < 2^29), and the group's
+// epilogue adds s * that * 2^(emax-18) + b * sum(x) to a float32 sum.  All
+// sums run in a fixed order and no atomics touch the values, so repeated runs
+// are bit-identical.
 //
 // Work split.  A warp task is kGvRows output rows of one part; in a step lane
 // l takes group 32v+l of those rows (32 bytes of codes per row, a warp
@@ -61,8 +66,6 @@ namespace {
 
 constexpr int kGvRows = 4;  // output rows per warp task
 
-typedef unsigned long long u64;
-
 struct GvJob {
   void *C;
   const float *bias;
@@ -72,8 +75,6 @@ struct GvJob {
 };
 
 // ------------------------------------------------------------------ helpers
-__device__ __forceinline__ float lo_f(u64 v) { return __uint_as_float((uint32_t)v); }
-__device__ __forceinline__ float hi_f(u64 v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -93,13 +94,25 @@ __device__ __forceinline__ float ldcg_f(const float *p) {
 }
 __device__ __forceinline__ float bf16_to_f(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
 __device__ __forceinline__ float f16_to_f(uint16_t v) { return __half2float(__ushort_as_half(v)); }
-__device__ __forceinline__ u64 pair_of(uint32_t lo, uint32_t hi) {
-  u64 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
+__device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
-__device__ __forceinline__ void lds_pairs(uint32_t addr, u64 &a, u64 &b) {
-  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+// the same at base + OFF (an immediate offset: no address arithmetic)
+template <int OFF>
+__device__ __forceinline__ uint4 lds_u4_at(uint32_t base) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(base), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint16_t lds_u16_at(uint32_t base) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1+%2];" : "=h"(v) : "r"(base), "n"(OFF));
+  return v;
 }
 __device__ __forceinline__ float lds_f(uint32_t addr) {
   float v;
@@ -114,50 +127,50 @@ __device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
 // 2^e as a float, for -126 <= e <= 127
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
-// One nibble position of a word pair v (64 bits: two code words): f = v &
-// (M in each half) read as a float pair (subnormal code*16^j*2^-149 each),
-// times the x pair, added to d.
-#define GV_NIB(V, MASK, X)                \
-  "and.b64 f, " V ", " MASK ";\n\t"       \
-  "fma.rn.f32x2 %0, f, " X ", %0;\n\t"
-
-// d += sum over the 16 elements of the word pair v of code * x'' * 2^-149,
-// with xp[e] the staged x pairs of nibble e (e = 0..3: low 16 bits of each
-// word, 4..7: high 16 bits).
-__device__ __forceinline__ void pair_dot(u64 &d, u64 v, const u64 (&xp)[8]) {
-  asm("{\n\t.reg .b64 f, h;\n\t"
-      GV_NIB("%1", "0x0000000F0000000F", "%2")
-      GV_NIB("%1", "0x000000F0000000F0", "%3")
-      GV_NIB("%1", "0x00000F0000000F00", "%4")
-      GV_NIB("%1", "0x0000F0000000F000", "%5")
-      "shr.b64 h, %1, 16;\n\t"
-      GV_NIB("h", "0x0000000F0000000F", "%6")
-      GV_NIB("h", "0x000000F0000000F0", "%7")
-      GV_NIB("h", "0x00000F0000000F00", "%8")
-      GV_NIB("h", "0x0000F0000000F000", "%9")
-      "}"
-      : "+l"(d)
-      : "l"(v), "l"(xp[0]), "l"(xp[1]), "l"(xp[2]), "l"(xp[3]), "l"(xp[4]), "l"(xp[5]), "l"(xp[6]), "l"(xp[7]));
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
-#undef GV_NIB
 
-// Staged x layout.  Per token, a block of 64*Gp floats (Gp = groups rounded
-// up to 32): group g's 16 chunks of 4 floats sit at ((g>>5)*16 + c)*128 +
-// (g&31)*4, interleaved across the 32 groups of a 2048-element slab so a warp
-// reading chunk c of 32 consecutive groups reads 512 contiguous bytes.
-// Chunk 4p+m pairs the elements that nibbles e = 2m, e+1 of word pair p
-// decode: (16p+e, 16p+8+e, 16p+e+1, 16p+9+e), the first two scaled by
-// 2^(A-4(e%4)), the last two by 2^(A-4((e+1)%4)).  Then, per token, three
-// arrays of Gp floats: the group's plain sum over its 64 elements in
-// ascending order, and ra, rb with ra*rb = 2^(149-A) = 2^(24+emax), each in
-// float range (emax = floor(log2 of the group's largest |x|)).
-__device__ __forceinline__ int chunk_off(int g, int c) { return ((g >> 5) * 16 + c) * 128 + (g & 31) * 4; }
+// Two-way dot products: c + a.lo16 * b.byte[0] + a.hi16 * b.byte[1] (LO) or
+// with bytes 2 and 3 (HI); a holds two signed 16-bit x, b four unsigned code
+// bytes.
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Staged x layout.  Per token, a block of 32*Gp 32-bit words (Gp = groups
+// rounded up to 32; 128 bytes a group): word m = 0..7 of group g (elements
+// 8m..8m+7) is one 16-byte chunk at byte ((g>>5)*8 + m)*512 + (g&31)*16, so
+// the 32 lanes of a warp reading chunk m of 32 consecutive groups read 512
+// contiguous bytes.  A chunk holds the integer x as four pairs of 16-bit
+// halves, (x0, x2), (x4, x6), (x1, x3), (x5, x7) (x_j = element 8m+j): the
+// even pairs meet the code bytes of (word & 0x0F0F0F0F), the odd pairs those
+// of (word & 0xF0F0F0F0).  Then, per token, three arrays of Gp floats: the
+// group's plain sum over its 64 bfloat16 elements in ascending order, and
+// ra, rb with ra*rb = 2^(emax-18), each in float range.
+__device__ __forceinline__ uint32_t chunk_byte(int g, int m) {
+  return (uint32_t)((((g >> 5) * 8 + m) * 32 + (g & 31)) * 16);
+}
+__device__ __forceinline__ uint32_t pack16(int lo, int hi) {
+  return ((uint32_t)lo & 0xFFFFu) | ((uint32_t)hi << 16);
+}
 
 // The whole CTA stages x: bfloat16 (T, 64*G), row stride lda.  Four
-// threads share a group (one word pair, 16 elements, each); the group's sum
-// adds the four quarter sums in order.  Scaling by 2^(A-4j) takes two exact
-// multiplies by powers of two (the exponent reaches 252).
-__device__ __forceinline__ void stage_x(const uint16_t *x, int64_t lda, int G, int T, float *xdst, int xstride,
+// threads share a group (two words, 16 elements, each); the group's sum adds
+// the four quarter sums in order.  Scaling by 2^(14-emax) takes two exact
+// multiplies by powers of two (the exponent reaches 147).
+// xdst, sums: per-token strides xstride, sstride in 32-bit words.
+__device__ __forceinline__ void stage_x(const uint16_t *x, int64_t lda, int G, int T, uint32_t *xdst, int xstride,
                                         float *sums, int sstride) {
   const int n = 4 * G * T;
   const int n_up = (n + 31) & ~31;  // whole warps take part in the shuffles
@@ -192,59 +205,72 @@ __device__ __forceinline__ void stage_x(const uint16_t *x, int64_t lda, int G, i
     if (!live) continue;
     // emax = floor(log2(mx)) for a normal mx (-127 bounds a subnormal one)
     const int emax = mx == 0.f ? 0 : (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
-    const int A = 125 - emax, e24 = 24 + emax;
-    float *dst = xdst + tk * xstride;
+    const int t = 14 - emax;  // in [-113, 141]
+    const float sa = pow2f(t < 127 ? t : 127), sb = pow2f(t < 127 ? 0 : t - 127);
+    int xi[16];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int e2 = 2 * m;
-      const int t0 = A - 4 * (e2 & 3), t1 = A - 4 * ((e2 + 1) & 3);  // in [-14, 252]
-      const float a0 = pow2f(t0 < 127 ? t0 : 127), b0 = pow2f(t0 < 127 ? 0 : t0 - 127);
-      const float a1 = pow2f(t1 < 127 ? t1 : 127), b1 = pow2f(t1 < 127 ? 0 : t1 - 127);
-      *reinterpret_cast<float4 *>(dst + chunk_off(g, 4 * qd + m)) =
-          make_float4(v[e2] * a0 * b0, v[8 + e2] * a0 * b0, v[e2 + 1] * a1 * b1, v[9 + e2] * a1 * b1);
+    for (int m = 0; m < 16; ++m) xi[m] = __float2int_rn(v[m] * sa * sb);
+    uint32_t *dst = xdst + tk * xstride;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int *q = xi + 8 * c;
+      *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(dst) + chunk_byte(g, 2 * qd + c)) =
+          make_uint4(pack16(q[0], q[2]), pack16(q[4], q[6]), pack16(q[1], q[3]), pack16(q[5], q[7]));
     }
     if (qd == 0) {
-      float *sb = sums + tk * 3 * sstride;
-      sb[g] = ((sum + s1) + s2) + s3;
-      sb[sstride + g] = pow2f(e24 >> 1);
-      sb[2 * sstride + g] = pow2f(e24 - (e24 >> 1));
+      const int e18 = emax - 18;  // in [-145, 109]
+      float *sbk = sums + tk * 3 * sstride;
+      sbk[g] = ((sum + s1) + s2) + s3;
+      sbk[sstride + g] = pow2f(e18 >> 1);
+      sbk[2 * sstride + g] = pow2f(e18 - (e18 >> 1));
     }
   }
 }
 
-// acc[i][t] += this lane's group g of rows i (code word pairs cw[i][0..3],
-// scale and bias s[i], b[i]) against token t's staged x.
-// xs, sums: shared-memory addresses of the staged block; strides in floats.
+// acc[i][t] += this lane's group g of rows i (code words cw[i][0..1], eight
+// words as two uint4; scale and bias s[i], b[i]) against token t's staged x.
+// xs, sums: shared-memory addresses of the staged block; strides in 32-bit
+// words.
 template <int TT>
-__device__ __forceinline__ void group_dot(const u64 (&cw)[kGvRows][4], const float (&s)[kGvRows],
+__device__ __forceinline__ void group_dot(const uint4 (&cw)[kGvRows][2], const float (&s)[kGvRows],
                                           const float (&b)[kGvRows], int g, uint32_t xs, int xstride,
                                           uint32_t sums, int sstride, float (&acc)[kGvRows][TT]) {
-  const uint32_t xg = xs + 4u * chunk_off(g, 0);
-  u64 d[kGvRows][TT][2];
-#pragma unroll
-  for (int i = 0; i < kGvRows; ++i)
-#pragma unroll
-    for (int tk = 0; tk < TT; ++tk) d[i][tk][0] = d[i][tk][1] = 0ull;
-#pragma unroll
-  for (int pp = 0; pp < 4; ++pp) {
-#pragma unroll
-    for (int tk = 0; tk < TT; ++tk) {
-      u64 xp[8];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) lds_pairs(xg + 4u * (tk * xstride + (4 * pp + m) * 128), xp[2 * m], xp[2 * m + 1]);
-#pragma unroll
-      for (int i = 0; i < kGvRows; ++i) pair_dot(d[i][tk][pp & 1], cw[i][pp], xp);
-    }
-  }
+  const uint32_t xg = xs + chunk_byte(g, 0);  // chunk m of group g is at xg + 512 m
 #pragma unroll
   for (int tk = 0; tk < TT; ++tk) {
+    const uint32_t xt = xg + 4u * tk * xstride;
+    int ev[kGvRows], od[kGvRows];
+#pragma unroll
+    for (int i = 0; i < kGvRows; ++i) ev[i] = od[i] = 0;
+    uint4 X[8];
+    X[0] = lds_u4_at<0 * 512>(xt);
+    X[1] = lds_u4_at<1 * 512>(xt);
+    X[2] = lds_u4_at<2 * 512>(xt);
+    X[3] = lds_u4_at<3 * 512>(xt);
+    X[4] = lds_u4_at<4 * 512>(xt);
+    X[5] = lds_u4_at<5 * 512>(xt);
+    X[6] = lds_u4_at<6 * 512>(xt);
+    X[7] = lds_u4_at<7 * 512>(xt);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+#pragma unroll
+      for (int i = 0; i < kGvRows; ++i) {
+        const uint4 &c4 = cw[i][m >> 2];
+        const uint32_t w = (m & 3) == 0 ? c4.x : (m & 3) == 1 ? c4.y : (m & 3) == 2 ? c4.z : c4.w;
+        const uint32_t e = w & 0x0F0F0F0Fu, o = w & 0xF0F0F0F0u;
+        ev[i] = dp2a_lo(X[m].x, e, ev[i]);
+        ev[i] = dp2a_hi(X[m].y, e, ev[i]);
+        od[i] = dp2a_lo(X[m].z, o, od[i]);
+        od[i] = dp2a_hi(X[m].w, o, od[i]);
+      }
+    }
     const uint32_t sb = sums + 4u * (tk * 3 * sstride + g);
-    const float X = lds_f(sb), ra = lds_f(sb + 4u * sstride), rb = lds_f(sb + 8u * sstride);
+    const float Xs = lds_f(sb), ra = lds_f(sb + 4u * sstride), rb = lds_f(sb + 8u * sstride);
 #pragma unroll
     for (int i = 0; i < kGvRows; ++i) {
-      const float D = (lo_f(d[i][tk][0]) + hi_f(d[i][tk][0])) + (lo_f(d[i][tk][1]) + hi_f(d[i][tk][1]));
+      const float D = (float)(16 * ev[i] + od[i]);  // 16 * sum(code * x_int), exact below 2^24
       acc[i][tk] = fmaf(s[i] * ra, D * rb, acc[i][tk]);
-      acc[i][tk] = fmaf(b[i], X, acc[i][tk]);
+      acc[i][tk] = fmaf(b[i], Xs, acc[i][tk]);
     }
   }
 }
@@ -420,18 +446,13 @@ __device__ __forceinline__ void compute_step(const GvArgs &a, const Task &t, int
   const GvPart &P = a.parts[t.q];
   const int g = v * 32 + lane;
   if (g >= P.G) return;
-  u64 cw[kGvRows][4];
   float s[kGvRows], b[kGvRows];
 #pragma unroll
   for (int i = 0; i < kGvRows; ++i) {
-    cw[i][0] = pair_of(B.c[i][0].x, B.c[i][0].y);
-    cw[i][1] = pair_of(B.c[i][0].z, B.c[i][0].w);
-    cw[i][2] = pair_of(B.c[i][1].x, B.c[i][1].y);
-    cw[i][3] = pair_of(B.c[i][1].z, B.c[i][1].w);
     s[i] = f16_to_f(B.s[i]);
     b[i] = f16_to_f(B.b[i]);
   }
-  group_dot<TT>(cw, s, b, g, smem_u32(xsm + P.xoff), P.xstride, smem_u32(xsm + P.soff), P.sstride, acc);
+  group_dot<TT>(B.c, s, b, g, smem_u32(xsm + P.xoff), P.xstride, smem_u32(xsm + P.soff), P.sstride, acc);
 }
 
 __device__ __forceinline__ void advance(const GvArgs &a, const Task &cur, int v, int W, Task &nt, int &nv) {
@@ -460,7 +481,7 @@ __global__ void __launch_bounds__(kGvWarps * 32, 1) q4_gemv_kernel(const __grid_
   if (tA.u >= 0) load_step(a, tA, 0, lane, bA);
   for (int xi = 0; xi < a.nx; ++xi) {
     const GvX &X = a.xs[xi];
-    stage_x(X.x, X.lda, X.G, a.T, xsm + X.xoff, X.xstride, xsm + X.soff, X.sstride);
+    stage_x(X.x, X.lda, X.G, a.T, reinterpret_cast<uint32_t *>(xsm + X.xoff), X.xstride, xsm + X.soff, X.sstride);
   }
   __syncthreads();
 
@@ -500,6 +521,7 @@ constexpr int kGtGroups = 32;                           // groups per step
 constexpr int kGtCodeBytes = kGvRows * kGtGroups * 32;  // 4096
 constexpr int kGtSbBytes = kGvRows * kGtGroups * 2;     // 256 (scales; again biases)
 constexpr int kGtSlot = kGtCodeBytes + 2 * kGtSbBytes;  // 4608, a multiple of 128
+static_assert(kGvRows == 4 && kGtGroups == 32, "the slot reads below are written out for 4 rows x 32 groups");
 constexpr int kGtMaxParts = 32;
 constexpr int kGtSmemMax = 227 * 1024;
 
@@ -512,16 +534,20 @@ struct GtRPart {  // a part served by a region
 struct GtRegion {
   const uint16_t *x;
   int64_t lda;
-  int G, xstride, sstride;  // x block: groups, per-token strides (floats)
+  int G, xstride, sstride;  // x block: groups, per-token strides (32-bit words)
   int rp_begin, rp_count, units;
   int cta_begin, cta_count;
 };
+// MP: the largest part, job and region count the launch holds (8 or 32); the
+// kernel's parameter block grows with it (128 bytes of tensor maps per part and
+// operand), and a smaller block starts sooner.
+template <int MP>
 struct GtArgs {
-  CUtensorMap maps[3 * kGtMaxParts];  // per part: codes, scales, biases
-  GvJob jobs[kGtMaxParts];
-  GtPart parts[kGtMaxParts];
-  GtRPart rparts[kGtMaxParts];
-  GtRegion regions[kGtMaxParts];
+  CUtensorMap maps[3 * MP];  // per part: codes, scales, biases
+  GvJob jobs[MP];
+  GtPart parts[MP];
+  GtRPart rparts[MP];
+  GtRegion regions[MP];
   int nregions, out_dt, T, stages;
   float *ws;
   int *cnt;
@@ -533,7 +559,8 @@ struct GtCur {
   int u, v, ns, q, b;
 };
 
-__device__ __forceinline__ void gt_set(const GtArgs &a, const GtRegion &R, int u, GtCur &c) {
+template <int MP>
+__device__ __forceinline__ void gt_set(const GtArgs<MP> &a, const GtRegion &R, int u, GtCur &c) {
   c.u = u < R.units ? u : -1;
   c.v = 0;
   if (c.u < 0) return;
@@ -544,13 +571,15 @@ __device__ __forceinline__ void gt_set(const GtArgs &a, const GtRegion &R, int u
   c.ns = (a.parts[c.q].G + kGtGroups - 1) / kGtGroups;
 }
 
-__device__ __forceinline__ void gt_next(const GtArgs &a, const GtRegion &R, int Wr, GtCur &c) {
+template <int MP>
+__device__ __forceinline__ void gt_next(const GtArgs<MP> &a, const GtRegion &R, int Wr, GtCur &c) {
   if (++c.v < c.ns) return;
   gt_set(a, R, c.u + Wr, c);
 }
 
 // lane 0: the three tensor copies of step c into slot `dst` (barrier `bar`)
-__device__ __forceinline__ void gt_issue(const GtArgs &a, const GtCur &c, uint32_t dst, uint32_t bar) {
+template <int MP>
+__device__ __forceinline__ void gt_issue(const GtArgs<MP> &a, const GtCur &c, uint32_t dst, uint32_t bar) {
   mbar_arrive_expect_tx(bar, kGtSlot);
   const int y = c.b * kGvRows;
   tma_load_2d(dst, &a.maps[3 * c.q], bar, c.v * kGtGroups * 8, y);
@@ -558,10 +587,18 @@ __device__ __forceinline__ void gt_issue(const GtArgs &a, const GtCur &c, uint32
   tma_load_2d(dst + kGtCodeBytes + kGtSbBytes, &a.maps[3 * c.q + 2], bar, c.v * kGtGroups, y);
 }
 
-template <int TT>
-__global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __grid_constant__ GtArgs a) {
+// L2 prefetch of step c's three tiles (no shared memory, no barrier)
+template <int MP>
+__device__ __forceinline__ void gt_prefetch(const GtArgs<MP> &a, const GtCur &c) {
+  const int y = c.b * kGvRows;
+  tma_prefetch_l2_2d(&a.maps[3 * c.q], c.v * kGtGroups * 8, y);
+  tma_prefetch_l2_2d(&a.maps[3 * c.q + 1], c.v * kGtGroups, y);
+  tma_prefetch_l2_2d(&a.maps[3 * c.q + 2], c.v * kGtGroups, y);
+}
+
+template <int TT, int MP>
+__global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __grid_constant__ GtArgs<MP> a) {
   griddep_launch_dependents();
-  griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   extern __shared__ __align__(1024) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int S = a.stages;
@@ -570,6 +607,19 @@ __global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __g
   const GtRegion &R = a.regions[ri];
   const int Wr = R.cta_count * kGtWarps;
   const int gw = ((int)blockIdx.x - R.cta_begin) * kGtWarps + warp;
+  // Before the programmatic-launch wait: L2 prefetches of this warp's first
+  // steps.  Weights are not outputs of the previous kernel, and L2 is the
+  // point of coherence, so the tensor copies issued after the wait still see
+  // any line that kernel writes; the prefetches only start the DRAM reads.
+  if (lane == 0) {
+    GtCur pc;
+    gt_set(a, R, gw, pc);
+    for (int k = 0; k < S && pc.u >= 0; ++k) {
+      gt_prefetch(a, pc);
+      gt_next(a, R, Wr, pc);
+    }
+  }
+  griddep_wait();  // programmatic launch: no global loads before the previous kernel completes
 
   unsigned char *ring = smem + (size_t)warp * S * kGtSlot;
   const uint32_t bars = smem_u32(smem + (size_t)kGtWarps * S * kGtSlot) + warp * S * 8;
@@ -596,7 +646,7 @@ __global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __g
     gt_next(a, R, Wr, ci);
   }
 
-  stage_x(R.x, R.lda, R.G, TT, xs, R.xstride, sums, R.sstride);
+  stage_x(R.x, R.lda, R.G, TT, reinterpret_cast<uint32_t *>(xs), R.xstride, sums, R.sstride);
   __syncthreads();
 
   float acc[kGvRows][TT];
@@ -623,16 +673,27 @@ __global__ void __launch_bounds__(kGtWarps * 32, 1) q4_gemv_tma_kernel(const __g
     const int g = cc.v * kGtGroups + lane;
     if (g < G) {
       const uint32_t sl = ring_s + slot * kGtSlot;
-      u64 cw[kGvRows][4];
+      // row i of the slot: 32 groups x 32 code bytes at i * 1024, then the
+      // scales (64 bytes a row) and the biases
+      uint4 cw[kGvRows][2];
       float s[kGvRows], b[kGvRows];
-#pragma unroll
-      for (int i = 0; i < kGvRows; ++i) {
-        const uint32_t row = sl + i * (kGtGroups * 32) + lane * 32;
-        lds_pairs(row, cw[i][0], cw[i][1]);
-        lds_pairs(row + 16, cw[i][2], cw[i][3]);
-        s[i] = f16_to_f(lds_u16(sl + kGtCodeBytes + 2 * (i * kGtGroups + lane)));
-        b[i] = f16_to_f(lds_u16(sl + kGtCodeBytes + kGtSbBytes + 2 * (i * kGtGroups + lane)));
-      }
+      const uint32_t cb = sl + lane * 32, sbb = sl + kGtCodeBytes + 2 * lane;
+      cw[0][0] = lds_u4_at<0>(cb);
+      cw[0][1] = lds_u4_at<16>(cb);
+      cw[1][0] = lds_u4_at<1024>(cb);
+      cw[1][1] = lds_u4_at<1040>(cb);
+      cw[2][0] = lds_u4_at<2048>(cb);
+      cw[2][1] = lds_u4_at<2064>(cb);
+      cw[3][0] = lds_u4_at<3072>(cb);
+      cw[3][1] = lds_u4_at<3088>(cb);
+      s[0] = f16_to_f(lds_u16_at<0>(sbb));
+      s[1] = f16_to_f(lds_u16_at<64>(sbb));
+      s[2] = f16_to_f(lds_u16_at<128>(sbb));
+      s[3] = f16_to_f(lds_u16_at<192>(sbb));
+      b[0] = f16_to_f(lds_u16_at<kGtSbBytes>(sbb));
+      b[1] = f16_to_f(lds_u16_at<kGtSbBytes + 64>(sbb));
+      b[2] = f16_to_f(lds_u16_at<kGtSbBytes + 128>(sbb));
+      b[3] = f16_to_f(lds_u16_at<kGtSbBytes + 192>(sbb));
       group_dot<TT>(cw, s, b, g, xs_s, R.xstride, sums_s, R.sstride, acc);
     }
     if (cc.v + 1 == cc.ns) {
@@ -698,13 +759,14 @@ std::mutex g_gv_mu;
 
 bool al16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
-// Staged-x floats for K = 64*G and T tokens: the x block and the three
-// per-group arrays; sets the per-token strides.
+// Staged-x 32-bit words for K = 64*G and T tokens: the integer x block (two
+// 16-bit values a word) and the three per-group float arrays; sets the
+// per-token strides.
 int64_t stage_floats(int G, int T, int *xstride, int *sstride) {
   const int gp = (G + 31) / 32 * 32;
-  *xstride = gp * 64;
+  *xstride = gp * 32;
   *sstride = gp;
-  return (int64_t)T * ((int64_t)gp * 64 + 3 * (int64_t)gp);
+  return (int64_t)T * ((int64_t)gp * 32 + 3 * (int64_t)gp);
 }
 
 template <typename K, typename A>
@@ -724,11 +786,12 @@ int launch_one(K kern, const A &args, int grid, int threads, size_t smem, int sm
 }
 
 // The TMA-fed launch; leaves *handled false for problems it does not take.
+template <int MP>
 int launch_gemv_tma(const Problem &p, int T, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx) {
   int nparts = 0;  // one past the highest part index in use
   for (int j = 0; j < p.njobs; ++j)
     if (p.jobs[j].part0 + p.jobs[j].nparts > nparts) nparts = p.jobs[j].part0 + p.jobs[j].nparts;
-  if (nparts > kGtMaxParts || p.njobs > kGtMaxParts) return TP_OK;
+  if (nparts > MP || p.njobs > MP) return TP_OK;
   for (int j = 0; j < p.njobs; ++j)
     for (int q = 0; q < p.jobs[j].nparts; ++q) {
       const Part &P = p.parts[p.jobs[j].part0 + q];
@@ -736,7 +799,7 @@ int launch_gemv_tma(const Problem &p, int T, cudaStream_t s, bool *handled, GvWo
           (P.lda % 8))
         return TP_OK;
     }
-  static GtArgs args;
+  static GtArgs<MP> args;
   memset(&args, 0, sizeof(args));
   // regions: distinct (x, K, lda)
   int reg_of[kMaxParts];
@@ -876,9 +939,9 @@ int launch_gemv_tma(const Problem &p, int T, cudaStream_t s, bool *handled, GvWo
   }
   const size_t smem = (size_t)(per_stage * S + xfloats * 4);
   static bool done1[64] = {false}, done2[64] = {false};
-  const int rc = T == 1 ? launch_one(q4_gemv_tma_kernel<1>, args, cta, kGtWarps * 32, smem, kGtSmemMax, done1, s,
+  const int rc = T == 1 ? launch_one(q4_gemv_tma_kernel<1, MP>, args, cta, kGtWarps * 32, smem, kGtSmemMax, done1, s,
                                      "q4_gemv_tma_kernel")
-                        : launch_one(q4_gemv_tma_kernel<2>, args, cta, kGtWarps * 32, smem, kGtSmemMax, done2, s,
+                        : launch_one(q4_gemv_tma_kernel<2, MP>, args, cta, kGtWarps * 32, smem, kGtSmemMax, done2, s,
                                      "q4_gemv_tma_kernel");
   if (rc == TP_OK) *handled = true;
   return rc;
@@ -985,7 +1048,11 @@ int launch_q4_gemv(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceF
     }
   }
   std::lock_guard<std::mutex> lk(g_gv_mu);
-  int rc = launch_gemv_tma(p, (int)T, s, handled, get_ws, ctx);
+  int nparts = 0;
+  for (int j = 0; j < p.njobs; ++j)
+    if (p.jobs[j].part0 + p.jobs[j].nparts > nparts) nparts = p.jobs[j].part0 + p.jobs[j].nparts;
+  int rc = nparts <= 8 && p.njobs <= 8 ? launch_gemv_tma<8>(p, (int)T, s, handled, get_ws, ctx)
+                                       : launch_gemv_tma<kGtMaxParts>(p, (int)T, s, handled, get_ws, ctx);
   if (rc != TP_OK || *handled) return rc;
   return launch_gemv_ldg(p, (int)T, s, handled, get_ws, ctx);
 }

@@ -1,6 +1,6 @@
 """Host-side logic of bench.py that needs no GPU: the recorded DRAM traffic is
 reported only while the kernel sources it was captured with are unchanged, and
-the oracle's CPU sample is sized to its time budget."""
+the oracle's CPU sample is sized to its time budget and counts its own work."""
 import bench
 
 
@@ -28,33 +28,57 @@ def test_family_hash_covers_the_shared_split_sum():
 
 
 def test_oracle_sample_fills_its_budget_with_whole_passes(monkeypatch):
-    # a fake oracle run: 1 ms per row plus 50 ms per call
+    # a fake oracle leg whose sized sample takes 0.5 s a pass
     calls = []
 
-    class FakeMLP:
-        total_rows, per_row, desc = 512, 1.0, "rows"
+    class FakeLeg:
+        def __init__(self, config):
+            calls.append(("config", config))
 
-        def __init__(self):
-            import types
-            self.oracle = types.SimpleNamespace(num_threads=lambda: 4)
+        def size_for(self, budget_s):
+            calls.append(("size_for", budget_s))
+            return 0.25
 
-        def run(self, rows):
-            calls.append(rows)
-            return 0.05 + 0.001 * rows
+        def prepare(self, f):
+            calls.append(("prepare", f))
 
-        seconds_per_row = bench.OracleMLP.seconds_per_row
-        rows_for = bench.OracleMLP.rows_for
+        def run(self):
+            calls.append("run")
+            return 0.5
+
+        def value(self, seconds):
+            return 2.0 / seconds
+
+        def describe(self):
+            return "sample"
+
+        def cores(self):
+            return 4
 
     clock = iter(range(1000))
-    monkeypatch.setattr(bench, "OracleMLP", FakeMLP)
+    monkeypatch.setattr(bench, "OracleLeg", FakeLeg)
     monkeypatch.setattr(bench.time, "time", lambda: float(next(clock)))
-    value, secs, sample, cores = bench.oracle_sample(10.0)
-    # calibration: one 64-row pass (1.78 ms a row); 10 s covers the whole batch
-    # (512 rows, 0.91 s a pass by that estimate), so 10 whole passes follow
-    assert calls[0] == 64
-    assert calls[1:] == [512] * 10
-    assert sample.startswith("10 pass(es) of 512 of 512")
+    value, secs, sample, cores = bench.oracle_sample("q4_1", 10.0)
+    # half the budget sizes the sample, one pass measures it, then whole
+    # passes fill the other half: 5 s / 0.5 s = 10 passes
+    assert calls[:4] == [("config", "q4_1"), ("size_for", 5.0), ("prepare", 0.25), "run"]
+    assert calls[4:] == ["run"] * 10
+    assert sample.startswith("10 pass(es) of the sample")
     assert cores == 4 and secs > 0 and value > 0
+
+
+def test_oracle_leg_counts_the_work_of_its_sample():
+    # the MLP pair at a 1/64 sample: every shard of W1 keeps ceil(2752/64) = 43
+    # rows, W2 keeps ceil(4096/64) = 64 rows, all 512 token rows
+    leg = bench.OracleLeg("mlp")
+    leg.prepare(1.0 / 64)
+    T, D, F, N = 512, 4096, 11008, 4
+    assert leg.work == 2.0 * T * D * 43 * N + 2.0 * T * F * 64
+    assert leg.full == 2.0 * 2 * T * D * F
+    assert leg.unit() == "TFLOP/s"
+    assert leg.cores() >= 1
+    assert leg.run() > 0
+    assert leg.value(1.0) == leg.work / 1e12
 
 
 def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
