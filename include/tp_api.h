@@ -32,10 +32,13 @@
  *    has fewer 128-row tiles than the GPU has SMs) use a per-(device, stream)
  *    float32 workspace with zeroed counters, allocated (cudaMalloc) on first
  *    need and grown when a larger call needs more; the counters are back at
- *    zero when each kernel ends.  tp_shutdown() frees all of it.
+ *    zero when each kernel ends.  A workspace that grows keeps its old
+ *    buffers allocated (a graph captured earlier still addresses them) until
+ *    tp_shutdown(), which frees all of it.
  *    tp_q4_sharded_to_all_noalloc never allocates.  A call may therefore be
  *    captured into a CUDA graph once the same call has run on the capturing
- *    stream outside the capture.
+ *    stream outside the capture, and a later, larger call on that stream
+ *    does not invalidate the capture.
  *  - Kernels may be launched with programmatic stream serialization: their
  *    set-up can overlap the end of the previous kernel on the stream, but
  *    they read and write no global memory before it has completed.
@@ -81,9 +84,14 @@ const char *tp_last_error(void);
  * reduction).  Never fails. */
 int64_t tp_launch_count(void);
 
-/* Synchronizes `stream`, copies the current device's status word into
+/* Synchronizes `stream`, copies the current device's status words into
  * *device_status (0 = no error, else a tp_status such as TP_ERR_TIMEOUT)
- * and resets the word to 0.  Returns TP_OK or TP_ERR_CUDA. */
+ * and resets them to 0.  Two words are read: the library's own (written by
+ * every entry point but the next) and the one inside the fixed buffer of
+ * tp_q4_sharded_to_all_noalloc; the first nonzero one is reported.  After a
+ * nonzero word the split counters it concerns are cleared as well.  Allocates
+ * nothing (a word that was never created reads as 0).  Returns TP_OK or
+ * TP_ERR_CUDA. */
 int tp_query_status(tp_stream_t stream, int *device_status);
 
 /* Selects the kernel family for the calling process (default AUTO).  The SIMT
@@ -494,9 +502,12 @@ int tp_q4_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K,
  *    (an asynchronous memset on `stream`) before its kernel.  Calls that can
  *    overlap on the GPU (on different streams without ordering) race on the
  *    array and give undefined results: order them.
- *  - Device-side wait timeouts of this entry point are recorded in the
- *    array, not in the word tp_query_status() reads; after a timeout the
+ *  - Device-side wait timeouts of this entry point are recorded in a status
+ *    word inside the array; tp_query_status() reads and clears it (without
+ *    allocating) together with the library's own word.  After a timeout the
  *    output is unspecified.
+ *  - Under TP_POLICY_SIMT it runs the CUDA-core kernel, like every other
+ *    entry point; that kernel needs no scratch.
  */
 int tp_q4_sharded_to_all_noalloc(int N, const void *const *x, int64_t T, int64_t K,
                                  const uint32_t *const *wq, const void *const *scales,

@@ -54,6 +54,34 @@ int scratch_address(void **out) {
 bool aligned(const void *p, int a) { return ((uintptr_t)p % (uintptr_t)a) == 0; }
 
 }  // namespace
+
+int noalloc_status_take(cudaStream_t s, int *value) {
+  *value = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+  void *base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_addr_mu);
+    if (dev >= 0 && dev < 64) base = g_addr[dev];
+  }
+  if (!base) return TP_OK;  // no call of the entry point on this device yet
+  unsigned char *b = static_cast<unsigned char *>(base);
+  int v = 0;
+  e = cudaMemcpyAsync(&v, b, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_error(e, "read the fixed buffer's status word");
+  if (v != 0) {
+    // a kernel may have stopped before re-arming its split counters
+    e = cudaMemsetAsync(b + kStatusBytes, 0, kCounterBytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(b, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "clear the fixed buffer's status word");
+  }
+  *value = v;
+  return TP_OK;
+}
+
 }  // namespace tp
 
 using namespace tp;
@@ -106,9 +134,11 @@ extern "C" int tp_q4_sharded_to_all_noalloc(int N, const void *const *x, int64_t
   p.wait_ns = wait_limit_ns();
 
   bool handled = false;
-  rc = launch_q4_fixed_workspace(p, (cudaStream_t)stream, &handled, partials, kPartialBytes, counters,
-                                 kCounterBytes / sizeof(int));
-  if (rc != TP_OK || handled) return rc;
+  if (!simt_policy()) {
+    rc = launch_q4_fixed_workspace(p, (cudaStream_t)stream, &handled, partials, kPartialBytes, counters,
+                                   kCounterBytes / sizeof(int));
+    if (rc != TP_OK || handled) return rc;
+  }
   // Shapes the tensor-core kernel does not take run on the CUDA-core kernel,
   // which needs no scratch.
   return launch_simt(p, (cudaStream_t)stream);

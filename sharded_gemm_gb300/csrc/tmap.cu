@@ -5,6 +5,7 @@
 
 #include <map>
 #include <mutex>
+#include <vector>
 #include <unordered_map>
 
 #include "tp_internal.h"
@@ -96,6 +97,17 @@ void tmap_cache_clear() {
   g_maps.clear();
 }
 
+// Buffers a workspace outgrew.  A CUDA graph captured from an earlier call
+// still holds their addresses, so they stay allocated (and their counters
+// stay at zero) until split_workspace_free(): growing a workspace never
+// invalidates a capture.
+struct Retired {
+  int dev;
+  void *p;
+  size_t counter_bytes;  // > 0: a counter array (cleared by split_workspace_reset)
+};
+static std::vector<Retired> g_retired;
+
 int split_workspace(cudaStream_t s, size_t partial_bytes, size_t ncounters, float **partials,
                     int **counters) {
   int dev = 0;
@@ -103,23 +115,26 @@ int split_workspace(cudaStream_t s, size_t partial_bytes, size_t ncounters, floa
   std::lock_guard<std::mutex> lk(g_ws_mu);
   Workspace &w = g_ws[{dev, s}];
   if (w.pbytes < partial_bytes) {
-    if (w.partials) cudaFree(w.partials);
-    w.partials = nullptr;
-    w.pbytes = 0;
     size_t want = partial_bytes + partial_bytes / 4;
-    cudaError_t e = cudaMalloc(&w.partials, want);
+    float *np = nullptr;
+    cudaError_t e = cudaMalloc(&np, want);
     if (e != cudaSuccess) return cuda_error(e, "workspace allocation");
+    if (w.partials) g_retired.push_back(Retired{dev, w.partials, 0});
+    w.partials = np;
     w.pbytes = want;
   }
   if (w.ncnt < ncounters) {
-    if (w.counters) cudaFree(w.counters);
-    w.counters = nullptr;
-    w.ncnt = 0;
     size_t want = ncounters + 1024;
-    cudaError_t e = cudaMalloc(&w.counters, want * sizeof(int));
+    int *nc = nullptr;
+    cudaError_t e = cudaMalloc(&nc, want * sizeof(int));
     if (e != cudaSuccess) return cuda_error(e, "workspace allocation");
-    e = cudaMemsetAsync(w.counters, 0, want * sizeof(int), s);
-    if (e != cudaSuccess) return cuda_error(e, "workspace clear");
+    e = cudaMemsetAsync(nc, 0, want * sizeof(int), s);
+    if (e != cudaSuccess) {
+      cudaFree(nc);
+      return cuda_error(e, "workspace clear");
+    }
+    if (w.counters) g_retired.push_back(Retired{dev, w.counters, w.ncnt * sizeof(int)});
+    w.counters = nc;
     w.ncnt = want;
   }
   *partials = w.partials;
@@ -129,8 +144,19 @@ int split_workspace(cudaStream_t s, size_t partial_bytes, size_t ncounters, floa
 
 void split_workspace_reset() {
   std::lock_guard<std::mutex> lk(g_ws_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
   for (auto &kv : g_ws)
-    if (kv.second.counters) cudaMemset(kv.second.counters, 0, kv.second.ncnt * sizeof(int));
+    if (kv.second.counters) {
+      cudaSetDevice(kv.first.first);
+      cudaMemset(kv.second.counters, 0, kv.second.ncnt * sizeof(int));
+    }
+  for (auto &r : g_retired)
+    if (r.counter_bytes) {
+      cudaSetDevice(r.dev);
+      cudaMemset(r.p, 0, r.counter_bytes);
+    }
+  cudaSetDevice(cur);
 }
 
 void split_workspace_free() {
@@ -143,6 +169,11 @@ void split_workspace_free() {
     if (kv.second.counters) cudaFree(kv.second.counters);
   }
   g_ws.clear();
+  for (auto &r : g_retired) {
+    cudaSetDevice(r.dev);
+    cudaFree(r.p);
+  }
+  g_retired.clear();
   cudaSetDevice(cur);
 }
 

@@ -40,6 +40,7 @@ int cuda_error(cudaError_t e, const char *what) {
 int64_t wait_limit_ns() { return g_wait_ns.load(); }
 
 bool pair_policy_allowed() { return g_policy.load() != TP_POLICY_SINGLE_SM; }
+bool simt_policy() { return g_policy.load() == TP_POLICY_SIMT; }
 
 void trace_buffer(unsigned long long **buf, int64_t *cap_records) {
   *buf = g_trace.load();
@@ -123,15 +124,28 @@ int tp_query_status(tp_stream_t stream, int *device_status) {
   if (!device_status) return set_error(TP_ERR_INVALID_ARG, "device_status is NULL");
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_error(e, "cudaStreamSynchronize");
-  int *w = device_status_word();
-  if (!w) return set_error(TP_ERR_CUDA, "cannot allocate the device status word");
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+  int *w = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (dev >= 0 && dev < 64) w = g_status[dev];  // never allocated here
+  }
   int v = 0;
-  e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_error(e, "read status word");
-  e = cudaMemset(w, 0, sizeof(int));
-  if (e != cudaSuccess) return cuda_error(e, "clear status word");
-  if (v != 0) split_workspace_reset();  // a kernel may have stopped mid-reduction
-  *device_status = v;
+  if (w) {
+    e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_error(e, "read status word");
+    if (v != 0) {
+      e = cudaMemset(w, 0, sizeof(int));
+      if (e != cudaSuccess) return cuda_error(e, "clear status word");
+      split_workspace_reset();  // a kernel may have stopped mid-reduction
+    }
+  }
+  int v2 = 0;
+  int rc = noalloc_status_take((cudaStream_t)stream, &v2);
+  if (rc) return rc;
+  *device_status = v != 0 ? v : v2;
   return TP_OK;
 }
 

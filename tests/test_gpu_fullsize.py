@@ -79,7 +79,7 @@ def test_full_mlp_backward():
     check_close(to_host(bw.dx)[rows], oracle.all_to_sharded_dx([d[rows] for d in dh], w1), "dx")
     h = [to_host(m) for m in bw.fwd.mid]
     x = bf16(cfg["x"])
-    for r in (0, N - 1):
+    for r in range(N):
         o2 = sample_rows(D, 16, seed=r)
         check_close(to_host(bw.dw2[r])[o2], oracle.sharded_dw([dyv[:, o2]], [h[r]])[0], "dW2 %d" % r)
         o1 = sample_rows(dh[r].shape[1], 16, seed=10 + r)
@@ -118,12 +118,18 @@ def test_full_summa(q):
     s.step()
     assert tp.tp_query_status() == 0
     bm = cfg["M"] // q
-    rows = sample_rows(bm, 4, seed=q)
-    Xb = [bf16(b)[rows] for b in oracle.blocks(cfg["X"], q)]
+    Xb = [bf16(b) for b in oracle.blocks(cfg["X"], q)]
     Ab = [bf16(b) for b in oracle.blocks(cfg["A"], q)]
-    ref = oracle.summa(Xb, Ab, q)  # Y_ij restricted to the sampled local rows
-    for b in range(q * q):
-        check_close(to_host(s.Y[b])[rows], ref[b], "block %d" % b)
+    # a seeded sample of 256 local rows per block row i: Y_ij for every j on
+    # those rows (the first and last row of the block always included)
+    for i in range(q):
+        rows = sample_rows(bm, 256, seed=17 * q + i)
+        for j in range(q):
+            ref = None
+            for t in range(q):
+                p = oracle.matmul(Xb[i * q + t][rows], Ab[t * q + j])
+                ref = p if ref is None else ref + p
+            check_close(to_host(s.Y[i * q + j])[rows], ref, "block (%d, %d)" % (i, j))
 
 
 @pytest.mark.parametrize("T", [1, 16, 2048])
@@ -138,7 +144,7 @@ def test_full_qkv(T):
     # fused QKV: shard r holds rows {s*D + r*D/N + i} of W_qkv
     wq = oracle.shard(cfg["w_qkv"], 0, 3, N)
     bq = oracle.shard(cfg["b_qkv"], 0, 3, N)
-    for r in (0, N - 1):
+    for r in range(N):
         check_close(to_host(w.qkv[r])[rows], oracle.linear(x, bf16(wq[r]), bq[r]), "qkv shard %d" % r)
     # W_o: row-parallel over x's column slices
     xs = oracle.shard(cfg["x"], -1, 1, N)
@@ -163,9 +169,9 @@ def test_full_q4_pair(T):
     assert tp.tp_query_status() == 0
     rows = sample_rows(T, 6)
     x = bf16(cfg["x"])[rows]
-    # up: column-parallel, sampled output columns of shards 0 and N-1
-    for r in (0, N - 1):
-        cols = sample_rows(F // N, 96, seed=r)
+    # up: column-parallel, sampled output columns of every shard
+    for r in range(N):
+        cols = sample_rows(F // N, 64, seed=r)
         g = [a[r * (F // N):(r + 1) * (F // N)][cols] for a in up]
         ref = oracle.q4_all_to_sharded(x, [g[0]], [g[1]], [g[2]], 64)[0]
         check_close(to_host(w.mid[r])[rows][:, cols], ref, "q4 up shard %d" % r)
@@ -188,7 +194,7 @@ def test_full_mx_pair(T):
     assert tp.tp_query_status() == 0
     rows = sample_rows(T, 6)
     x = bf16(cfg["x"])[rows]
-    for r in (0, N - 1):
+    for r in range(N):
         cols = sample_rows(F // N, 96, seed=r)
         sl = slice(r * (F // N), (r + 1) * (F // N))
         ref = oracle.mx_all_to_sharded(x, [up[0][sl][cols]], [up[1][sl][cols]])[0]

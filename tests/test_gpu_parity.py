@@ -233,6 +233,48 @@ def test_small_batch_calls_replay_in_a_cuda_graph():
         assert torch.equal(a, b)
 
 
+def test_graph_replay_survives_a_larger_call_on_the_same_stream():
+    # A captured call holds the addresses of its stream's split workspace.  A
+    # later call with a larger split (more tiles, more tokens, a 4-bit row-
+    # parallel sum) grows that workspace; the buffers the graph addresses must
+    # stay allocated and the replay must still give the captured result.
+    T, K, O, N = 1, 4096, 4096, 8
+    x = to_device(rand_bf16((T, K)), "bf16")
+    w = tp.tp_shard_weight(to_device(rand_bf16((O, K), 0.05), "bf16"), -1, 1, N)
+    xs = [x[:, r * (K // N):(r + 1) * (K // N)] for r in range(N)]
+    y = torch.empty((T, O), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            tp.tp_sharded_to_all(xs, w, None, out=y, stream=s)
+    s.synchronize()
+    ref = y.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tp.tp_sharded_to_all(xs, w, None, out=y, stream=s)
+    # larger splits on the same stream, outside the capture
+    T2, K2, O2 = 16, 8192, 8192
+    x2 = to_device(rand_bf16((T2, K2)), "bf16")
+    w2 = tp.tp_shard_weight(to_device(rand_bf16((O2, K2), 0.05), "bf16"), -1, 1, N)
+    x2s = [x2[:, r * (K2 // N):(r + 1) * (K2 // N)] for r in range(N)]
+    y2 = torch.empty((T2, O2), dtype=torch.float32, device="cuda")
+    pq, ps, pb = _q4_host(O2, K2, 5)
+    q4x = tp.tp_shard_weight(x2[:1].contiguous(), -1, 1, N)
+    q4w = [tp.tp_shard_weight(to_device(a, k), -1, 1, N) for a, k in ((pq, "u32"), (ps, "f16"), (pb, "f16"))]
+    with torch.cuda.stream(s):
+        tp.tp_sharded_to_all(x2s, w2, None, out=y2, stream=s)
+        tp.tp_q4_sharded_to_all(q4x, *q4w, stream=s)
+    s.synchronize()
+    y.zero_()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    _status_ok()
+    assert torch.equal(y, ref)
+
+
 def test_sharded_to_all_strided_input_columns(policy):
     # W_o style: x split by columns as strided views of one (T, K) buffer
     T, K, O, N = 48, 512, 192, 8
