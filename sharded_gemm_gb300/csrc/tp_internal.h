@@ -76,6 +76,12 @@ __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + _
 int *device_status_word();  // per current device; nullptr on failure
 int64_t wait_limit_ns();
 bool pair_policy_allowed();  // false under TP_POLICY_SINGLE_SM (no pairs, no rank clusters)
+bool simt_policy();          // true under TP_POLICY_SIMT (CUDA-core kernel only)
+// The status word of the no-allocation entry point's fixed buffer on the
+// current device: read into *value and, if nonzero, cleared (with the split
+// counters) on `s`.  0 if that entry point has not run on this device.
+// Allocates nothing.
+int noalloc_status_take(cudaStream_t s, int *value);
 void trace_buffer(unsigned long long **buf, int64_t *cap_records);
 int set_error(int code, const char *fmt, ...);
 void note_launch();  // counts one kernel launch of the calling thread (tp_launch_count)
@@ -115,6 +121,9 @@ typedef int (*GvWorkspaceFn)(void *ctx, size_t bytes, size_t ncounters, float **
 // CUDA-core 4-bit GEMV for decode batches of one or two tokens; leaves
 // *handled false (and returns TP_OK) for problems it does not take.
 int launch_q4_gemv(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx);
+// Tensor-core 4-bit decode with 8-bit operands for up to 16 tokens (k_q4dec.cu);
+// leaves *handled false (and returns TP_OK) for problems it does not take.
+int launch_q4_dec8(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx);
 int launch_shard(const void *w, int64_t rows, int64_t cols, int elem_bytes, int axis,
                  int segments, int N, void *const *shards, cudaStream_t s);
 int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void *scales,
