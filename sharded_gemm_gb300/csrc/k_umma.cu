@@ -37,6 +37,12 @@
 namespace tp {
 
 constexpr int kMaxMaps = 64;
+// k-blocks of the weight operand the row-parallel cluster kernel pulls into
+// L2 beyond its operand ring (cp.async.bulk.prefetch), so its tensor copies
+// find their lines in L2 (measured 53.6 -> 52.2 us on the MLP's W2; the same
+// prefetch slowed the pair kernels, whose weight tiles are shared by two
+// pairs, and is not used there).
+constexpr int kPrefetchKb = 6;
 constexpr int kMaxCMaps = 16;  // output maps of the TMA-store epilogue
 constexpr int BM = 128;
 constexpr int BK = 64;
@@ -680,6 +686,34 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
   griddep_launch_dependents();
+  // L2 prefetch of a unit part's B (weight) k-block, the boxes this CTA loads
+  auto prefetch_b = [&](const UPart &P, int rowB0, int kb) {
+    if (kb >= P.kblocks) return;
+    if constexpr (B_MN) {
+#pragma unroll
+      for (int sub = 0; sub < NSUB; ++sub)
+#pragma unroll
+        for (int c = 0; c < BNH / 64; ++c)
+          tma_prefetch_l2_2d(&a.mapB[P.bmap], rowB0 + sub * BNH + c * 64, kb * BK);
+    } else if constexpr (GATED) {
+      tma_prefetch_l2_2d(&a.mapB[P.bmap], kb * BK, rowB0);
+      tma_prefetch_l2_2d(&a.mapB[P.bmap2], kb * BK, rowB0);
+    } else {
+      tma_prefetch_l2_2d(&a.mapB[P.bmap], kb * BK, rowB0);
+    }
+  };
+  auto unit_rowB0 = [&](const UJob &J, int u) {
+    const int tb = (u - J.unit_begin) / J.tilesA;
+    return GATED ? tb * BN + (int)rank * BNH : tb * NSUB * BN + (int)rank * (NSUB == 2 ? BN : BNH);
+  };
+  // The weights are not outputs of the previous kernel, and L2 is the point
+  // of coherence: the first unit's first k-blocks are pulled into L2 before
+  // the programmatic-launch wait, which only starts the DRAM reads early.
+  if (warp == 0 && lane == 0 && !A_MN && pair < a.total_units) {
+    const UJob &J = a.jobs[find_job(a, pair)];
+    const UPart P = a.parts[J.part0];
+    for (int kb = 0; kb < STAGES; ++kb) prefetch_b(P, unit_rowB0(J, pair), kb);
+  }
   griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
 
   if (warp == 0) {
@@ -949,6 +983,20 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
   griddep_launch_dependents();
+  // The weights (B) are not outputs of the previous kernel, and L2 is the
+  // point of coherence: their first k-blocks are pulled into L2 before the
+  // programmatic-launch wait, which only starts the DRAM reads early.
+  auto prefetch_b = [&](int kb) {
+    if (kb >= P.kblocks) return;
+    if constexpr (B_MN) {
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) tma_prefetch_l2_2d(&a.mapB[P.bmap], rowB0 + c * 64, kb * BK);
+    } else {
+      tma_prefetch_l2_2d(&a.mapB[P.bmap], kb * BK, rowB0);
+    }
+  };
+  if (warp == 0 && lane == 0)
+    for (int kb = 0; kb < STAGES + kPrefetchKb; ++kb) prefetch_b(kb);
   griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
 
   if (warp == 0) {
@@ -979,6 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
         } else {
           tma_load_2d(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
         }
+        prefetch_b(kb + STAGES + kPrefetchKb);  // keeps the weight stream ahead of the ring
         used[stage] = true;
         last_phase[stage] = phase;
         if (++stage == STAGES) {
