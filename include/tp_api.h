@@ -107,7 +107,17 @@ int tp_set_wait_limit_ns(int64_t limit_ns);
  * aligned, caller owned), CTA 0 of every later tensor-core q4 decode launch
  * writes the globaltimer value (ns) of event e at stage sequence number s
  * (s < 1024, e < 32) into 64-bit word 16 + e*1024 + s, with plain stores.
- * NULL switches tracing off.  Events: 1 producer issued the stage's loads;
+ * NULL switches tracing off.
+ * 8-bit decode kernel (every part's K a multiple of 512): 1 the codes of the
+ * stage were issued; 2 the MMA thread had the stage's operands, 5 it issued
+ * the stage's commit; 6 converter warp 2 had the codes and a free A half, 8
+ * its tensor-memory stores completed; 9 epilogue warp 6 saw the stage's first
+ * accumulator pair, 11 it finished the stage.  Per accumulator pair p of
+ * stage s, at word index 4s + p: 17/18 the MMA thread issued / committed it,
+ * 12/13/14 epilogue warp 6 saw it / had loaded it / had applied it.  Per CTA
+ * b, at index b: 28 the SM id + 1, 30/31 the CTA's start / end, and 29 the
+ * start of block b of the activation pre-pass.
+ * 16-bit decode kernel (other shapes): 1 producer issued the stage's loads;
  * 2/3/4 the MMA thread saw the stage's data / A operand / free accumulator,
  * 5 it committed the stage; 6/7 converter warp 2 saw the data / a free A
  * slot, 12 finished the x reorder, 13 its tensor-memory stores completed, 8
@@ -492,8 +502,10 @@ int tp_q4_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K,
  * 64 KiB hold the split counters and 8 MiB - 64.25 KiB the float32 split
  * partials; a call whose split needs more (large T or many output rows)
  * returns TP_ERR_UNSUPPORTED with the sizes in the message and launches
- * nothing.  Decode-sized calls (T <= 16) of an 8192 x 28672 layer split 8
- * ways need about 4.4 MB.
+ * nothing.  For decode-sized calls (T <= 16) the K split is chosen to fit
+ * the array: the down projection of an 8192 x 28672 layer split 8 ways
+ * (T = 16) takes 8.31 MB, its prepared activations and 14 partials per
+ * 128-row tile.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, no allocation); make that first call before any
  *    stream capture.

@@ -1114,7 +1114,7 @@ int choose_chunks(const Problem &p, int tiles_total_parts, int groups, int sms) 
 // Builds the launch of `p` and runs it.  `get_ws(bytes, ncounters, &ws, &cnt)`
 // supplies the split-reduction workspace when the launch needs one.
 template <class WsFn>
-int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws) {
+int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws, size_t ws_cap) {
   *handled = false;
   if (p.in_dt != TP_BF16) return TP_OK;
   int64_t maxT = 0;
@@ -1130,11 +1130,17 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws)
   // One or two tokens: the CUDA-core GEMV (HBM-bound; the tensor-core decode
   // below is bound by its MMA issue rate there).  TP_POLICY_SINGLE_SM keeps
   // the tensor-core decode.
+  GvWorkspaceFn thunk = [](void *ctx, size_t bytes, size_t ncnt, float **ws, int **cnt) -> int {
+    return (*static_cast<WsFn *>(ctx))(bytes, ncnt, ws, cnt);
+  };
   if (maxT <= 2 && pair_policy_allowed()) {
-    GvWorkspaceFn thunk = [](void *ctx, size_t bytes, size_t ncnt, float **ws, int **cnt) -> int {
-      return (*static_cast<WsFn *>(ctx))(bytes, ncnt, ws, cnt);
-    };
     int rc = launch_q4_gemv(p, s, handled, thunk, &get_ws);
+    if (rc != TP_OK || *handled) return rc;
+  }
+  // Up to 16 tokens: the 8-bit tensor-core decode (k_q4dec.cu) where its
+  // shape rules hold, else the 16-bit one below.
+  if (maxT <= 16) {
+    int rc = launch_q4_dec8(p, s, handled, thunk, &get_ws, ws_cap);
     if (rc != TP_OK || *handled) return rc;
   }
   const bool decode = maxT <= 16;
@@ -1276,9 +1282,10 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws)
 }  // namespace
 
 int launch_q4(const Problem &p, cudaStream_t s, bool *handled) {
-  return launch_q4_impl(p, s, handled, [s](size_t bytes, size_t ncnt, float **ws, int **cnt) -> int {
-    return split_workspace(s, bytes, ncnt, ws, cnt);
-  });
+  return launch_q4_impl(
+      p, s, handled,
+      [s](size_t bytes, size_t ncnt, float **ws, int **cnt) -> int { return split_workspace(s, bytes, ncnt, ws, cnt); },
+      SIZE_MAX);
 }
 
 int launch_q4_fixed_workspace(const Problem &p, cudaStream_t s, bool *handled, float *ws,
@@ -1294,7 +1301,7 @@ int launch_q4_fixed_workspace(const Problem &p, cudaStream_t s, bool *handled, f
     *w = ws;
     *c = cnt;
     return TP_OK;
-  });
+  }, ws_bytes);
 }
 
 }  // namespace tp

@@ -92,6 +92,46 @@ int make_tmap_2d(CUtensorMap *out, const void *ptr, CUtensorMapDataType dt, int 
   return TP_OK;
 }
 
+// 3-D view of a row-major (rows, ld) matrix as (chunk, rows, chunks): dim 0
+// the chunk_elems elements of one chunk of a row, dim 1 the rows (stride
+// ld_elems), dim 2 the row's chunks (stride chunk_elems); a box of
+// (chunk_elems, box_rows, box_chunks) lands in shared memory as box_chunks
+// consecutive (box_rows x chunk) tiles -- one tensor copy where 2-D boxes
+// would need box_chunks.
+int make_tmap_3d_chunks(CUtensorMap *out, const void *ptr, CUtensorMapDataType dt, int elem_bytes,
+                        uint64_t row_elems, uint64_t rows, uint64_t ld_elems, uint32_t chunk_elems,
+                        uint32_t box_rows, uint32_t box_chunks, CUtensorMapSwizzle swz) {
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  if (!g_encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return set_error(TP_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled");
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  }
+  // cached under a key no 2-D map can have (box1 carries the chunk count in its top bits)
+  MapKey key{(uint64_t)(uintptr_t)ptr, row_elems, rows, ld_elems, chunk_elems,
+             box_rows | (box_chunks << 16) | 0x80000000u, (uint32_t)dt, (uint32_t)swz};
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *out = it->second;
+    return TP_OK;
+  }
+  cuuint64_t dims[3] = {chunk_elems, rows, row_elems / chunk_elems};
+  cuuint64_t strides[2] = {ld_elems * (uint64_t)elem_bytes, (uint64_t)chunk_elems * elem_bytes};
+  cuuint32_t box[3] = {chunk_elems, box_rows, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(out, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
+  if (g_maps.size() > 8192) g_maps.clear();
+  g_maps.emplace(key, *out);
+  return TP_OK;
+}
+
 void tmap_cache_clear() {
   std::lock_guard<std::mutex> lk(g_map_mu);
   g_maps.clear();

@@ -123,7 +123,9 @@ typedef int (*GvWorkspaceFn)(void *ctx, size_t bytes, size_t ncounters, float **
 int launch_q4_gemv(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx);
 // Tensor-core 4-bit decode with 8-bit operands for up to 16 tokens (k_q4dec.cu);
 // leaves *handled false (and returns TP_OK) for problems it does not take.
-int launch_q4_dec8(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx);
+// ws_cap: the most workspace bytes get_ws can supply (the split is chosen to fit).
+int launch_q4_dec8(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx,
+                   size_t ws_cap);
 int launch_shard(const void *w, int64_t rows, int64_t cols, int elem_bytes, int axis,
                  int segments, int N, void *const *shards, cudaStream_t s);
 int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void *scales,
@@ -150,6 +152,11 @@ int sm_count();
 int make_tmap_2d(CUtensorMap *out, const void *ptr, CUtensorMapDataType dt, int elem_bytes,
                  uint64_t inner, uint64_t outer, uint64_t ld_elems, uint32_t box0, uint32_t box1,
                  CUtensorMapSwizzle swz);
+// 3-D (chunk, rows, chunks) view of a row-major matrix whose boxes cover
+// several consecutive chunks of every row in one tensor copy (tmap.cu).
+int make_tmap_3d_chunks(CUtensorMap *out, const void *ptr, CUtensorMapDataType dt, int elem_bytes,
+                        uint64_t row_elems, uint64_t rows, uint64_t ld_elems, uint32_t chunk_elems,
+                        uint32_t box_rows, uint32_t box_chunks, CUtensorMapSwizzle swz);
 void tmap_cache_clear();
 // Per-(device, stream) workspace of the split-tile reductions: float partials and
 // int arrival counters (zero between calls).  Grows on demand.

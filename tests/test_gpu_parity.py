@@ -737,8 +737,12 @@ def _q4_host(rows, K, seed):
 
 # (2, 1088, 37, 3): two tokens, 34 items of 32 per row (a ragged second slab),
 # 37 rows (a ragged last block of 4); (1, 64, 1, 1): one group, one row.
+# (3, 1024, 200, 2), (9, 1536, 129, 3), (16, 512, 200, 4): the 8-bit tensor-core
+# decode (whole 512-element stages; 8- and 16-token operand widths; a ragged
+# last 128-row tile); (2, 1024, 300, 2) under single_sm takes it at two tokens.
 @pytest.mark.parametrize("T,K,On,N", [(1, 256, 128, 2), (2, 1088, 37, 3), (1, 64, 1, 1), (16, 512, 200, 4),
-                                      (40, 1024, 136, 8), (256, 128, 64, 1)])
+                                      (40, 1024, 136, 8), (256, 128, 64, 1), (3, 1024, 200, 2),
+                                      (9, 1536, 129, 3), (2, 1024, 300, 2), (13, 8192, 128, 1)])
 def test_q4_all_to_sharded(policy, T, K, On, N):
     x = rand_bf16((T, K))
     pq, ps, pb = _q4_host(On * N, K, T + K)
@@ -753,8 +757,12 @@ def test_q4_all_to_sharded(policy, T, K, On, N):
 
 # (2, 192, 75, 5): two tokens, 6 items per rank, 75 rows; (1, 2112, 130, 3):
 # 66 items per rank (three slabs, ragged), 130 rows.
+# (5, 512, 300, 4), (16, 3584, 200, 2), (8, 1024, 129, 8): the 8-bit decode's
+# row-parallel sums (rank partials, and split chunks of a rank's groups, added
+# in order by the last arriving warp).
 @pytest.mark.parametrize("T,Kn,O,N", [(1, 128, 256, 2), (2, 192, 75, 5), (1, 2112, 130, 3), (16, 64, 130, 8),
-                                      (33, 256, 72, 4), (256, 192, 128, 2)])
+                                      (33, 256, 72, 4), (256, 192, 128, 2), (5, 512, 300, 4),
+                                      (16, 3584, 200, 2), (8, 1024, 129, 8)])
 def test_q4_sharded_to_all(policy, T, Kn, O, N):
     x = rand_bf16((T, Kn * N))
     pq, ps, pb = _q4_host(O, Kn * N, O + Kn)
