@@ -374,18 +374,6 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
     }
     mbar_init(smem_u32(&drain_bar), 1);
     fence_mbar_init();
-    // Weights are never outputs of the previous kernel and L2 is the point
-    // of coherence: prefetching the first unit's codes into L2 before the
-    // programmatic-launch wait only starts the DRAM reads early.
-    if ((int)blockIdx.x < a.total_units) {
-      D8Unit ui;
-      d8_unit(a, blockIdx.x, ui);
-      for (int k = 0; k < ui.nst && k < C::CSTAGES; ++k) {
-        int gs;
-        const D8Part &P = a.parts[d8_stage_part(a, a.jobs[ui.job], ui.s0 + k, gs)];
-        tma_prefetch_3d(&a.cmaps[P.cmap], 0, ui.tile * 128, gs / 4);
-      }
-    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_sh), 512);
@@ -394,6 +382,19 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Weights are never outputs of the previous kernel and L2 is the point of
+  // coherence: prefetching the first unit's codes into L2 before the
+  // programmatic-launch wait only starts the DRAM reads early.  An epilogue
+  // thread issues it, so the producers start at once.
+  if (warp == 6 && lane == 0 && (int)blockIdx.x < a.total_units) {
+    D8Unit ui;
+    d8_unit(a, blockIdx.x, ui);
+    for (int k = 0; k < ui.nst && k < C::CSTAGES; ++k) {
+      int gs;
+      const D8Part &P = a.parts[d8_stage_part(a, a.jobs[ui.job], ui.s0 + k, gs)];
+      tma_prefetch_3d(&a.cmaps[P.cmap], 0, ui.tile * 128, gs / 4);
+    }
+  }
   griddep_wait();  // programmatic launch: no global loads before the previous kernel completes
   const uint32_t tmem = tmem_base_sh;
 

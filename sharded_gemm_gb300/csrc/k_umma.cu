@@ -73,12 +73,15 @@ struct UPart {
 struct UmmaArgs {
   CUtensorMap mapA[kMaxMaps];
   CUtensorMap mapB[kMaxMaps];
-  CUtensorMap mapC[kMaxCMaps];  // float32 outputs, 32 x 32 boxes, 128-byte swizzle
+  // TMA-store epilogues: float32 outputs in 32 x 32 boxes, 128-byte swizzle
+  // (TSTORE), or a warp's 32 rows x its columns, unswizzled (rstore)
+  CUtensorMap mapC[kMaxCMaps];
   UJob jobs[kMaxJobs];
   UPart parts[kMaxParts];
   int njobs, total_units, nmapA, nmapB;
   int chain, out_dt, vec_ok;
   int cluster_n;  // ranks per cluster (row-parallel cluster kernel)
+  int rstore;     // pair kernel: a CTA's last unit is stored through its drained operand ring
   unsigned long long *trace;  // optional timeline of CTA 0 (tp_set_trace)
   uint32_t idesc;
   int *status;
@@ -90,6 +93,18 @@ struct UmmaArgs {
 // Records the time of (event, k-block sequence) for CTA 0 when tracing.
 __device__ __forceinline__ void umma_trace(const UmmaArgs &a, int event, int seq) {
   if (a.trace != nullptr && blockIdx.x == 0 && seq < 1024) a.trace[16 + event * 1024 + seq] = globaltimer_ns();
+}
+
+// When tracing, every CTA b (< 1024) records its SM id + 1 (event 28) and its
+// start (30) and end (31) times at word index b.
+__device__ __forceinline__ void umma_cta_trace(const UmmaArgs &a, int event) {
+  if (a.trace == nullptr || threadIdx.x != 0 || blockIdx.x >= 1024) return;
+  if (event == 30) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    a.trace[16 + 28 * 1024 + blockIdx.x] = smid + 1;
+  }
+  a.trace[16 + event * 1024 + blockIdx.x] = globaltimer_ns();
 }
 
 __device__ __forceinline__ int find_job(const UmmaArgs &a, int u) {
@@ -138,6 +153,32 @@ __device__ __forceinline__ uint32_t pack_f16(float x, float y) {
   __half2 h = __floats2half2_rn(x, y);
   return *reinterpret_cast<uint32_t *>(&h);
 }
+
+// The bias of a warp's contiguous output columns [col0, col0 + 32 NW): lane l
+// holds columns col0 + 32 j + l.  Loaded before the warp waits for its
+// accumulator; loaded per output chunk instead, the bias reads (L1 misses
+// behind a full operand stream, about a microsecond each) serialized the
+// epilogue: 10 us for a 128 x 320 tile.
+template <int NW>
+struct WarpBias {
+  float v[NW];
+  __device__ __forceinline__ void load(const float *bias, int col0, int ncols, int lane) {
+#pragma unroll
+    for (int j = 0; j < NW; ++j) {
+      const int c = col0 + j * 32 + lane;
+      v[j] = (bias != nullptr && c < ncols) ? __ldg(bias + c) : 0.f;
+    }
+  }
+  // The bias of column col0 + o (o a compile-time constant after unrolling).
+  __device__ __forceinline__ float at(int o) const { return __shfl_sync(0xffffffffu, v[o >> 5], o & 31); }
+  // v[i] += bias of column col0 + o0 + i, when the job has a bias.
+  template <int CH>
+  __device__ __forceinline__ void add(bool has_bias, int o0, float (&x)[CH]) const {
+    if (!has_bias) return;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) x[i] += at(o0 + i);
+  }
+};
 
 // Stores CH consecutive output values of one thread (row-major, normal mode).
 template <int CH, bool BIAS = true>
@@ -196,12 +237,7 @@ __device__ __forceinline__ void tstore_chunk(const UmmaArgs &a, const UJob &J, i
   // A chunk wholly outside the output (ragged last tile) is skipped outright:
   // it neither stores nor writes the staging buffer, which is rewritten only
   // after the store issued from it has read it.
-  if (row0 >= J.rowsA || col0 >= J.rowsB) return;
-  if (J.bias) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < J.rowsB) v[i] += __ldg(J.bias + col0 + i);
-  }
+  if (row0 >= J.rowsA || col0 >= J.rowsB) return;  // the caller has added the bias
   if (cnt >= 1) {  // the previous store has read the buffer
     if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
@@ -223,13 +259,38 @@ __device__ __forceinline__ void tstore_chunk(const UmmaArgs &a, const UJob &J, i
   ++cnt;
 }
 
+// Ring-staged store: CH values of the thread's row go to its row of the
+// warp's staging block (32 rows x `pitch` bytes, unswizzled), converted to
+// the output type; o0 is the chunk's first column within the block.
+template <int CH>
+__device__ __forceinline__ void stage_row_chunk(int out_dt, uint32_t rowbuf, int o0, const float (&v)[CH]) {
+  if (out_dt == TP_F32) {
+#pragma unroll
+    for (int i = 0; i < CH; i += 4)
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(rowbuf + (uint32_t)((o0 + i) * 4)), "f"(v[i]),
+                   "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
+                   : "memory");
+  } else {
+    const bool bf = out_dt == TP_BF16;
+#pragma unroll
+    for (int i = 0; i < CH; i += 8) {
+      uint32_t q[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        q[k] = bf ? pack_bf16(v[i + 2 * k], v[i + 2 * k + 1]) : pack_f16(v[i + 2 * k], v[i + 2 * k + 1]);
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(rowbuf + (uint32_t)((o0 + i) * 2)), "r"(q[0]),
+                   "r"(q[1]), "r"(q[2]), "r"(q[3])
+                   : "memory");
+    }
+  }
+}
+
 // Swap-AB store: the thread's A row is output column `row`; its values are
 // tokens col0.. of that column.
 template <int CH>
 __device__ __forceinline__ void store_col_chunk(const UmmaArgs &a, const UJob &J, int row, int col0,
-                                                const float (&v)[CH]) {
+                                                const float (&v)[CH], float b) {
   if (row >= J.rowsA) return;
-  const float b = J.bias ? __ldg(J.bias + row) : 0.f;
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
     const int t = col0 + i;
@@ -291,7 +352,7 @@ __device__ __forceinline__ void split_finish(const UmmaArgs &a, const UJob &J, c
     for (int i = 0; i < HALF; ++i)
       if (i < ncol) v[i] += __ldcg(sj + (cl0 + i) * 128);
   }
-  store_col_chunk<HALF>(a, J, row, q.tb * BN + cl0, v);
+  store_col_chunk<HALF>(a, J, row, q.tb * BN + cl0, v, (J.bias && row < J.rowsA) ? __ldg(J.bias + row) : 0.f);
   __syncwarp();
   if (lane == 0) *cnt = 0;
 }
@@ -535,6 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       const int colb = q.tb * BN + half * HALF;
       const bool split = SWAP && J.splits > 1;
       const int nep = (a.chain || split) ? 1 : J.nparts;
+      // bias: swap mode, one per thread (its output column); else the warp's columns
+      const float rbias = (SWAP && J.bias && row < J.rowsA) ? __ldg(J.bias + row) : 0.f;
+      WarpBias<(HALF + 31) / 32> wb;
+      if constexpr (!SWAP && !PARTIALS) wb.load(J.bias, colb, J.rowsB, lane);
       for (int pe = 0; pe < nep; ++pe) {
         // warp-uniform: every lane must take the same path into tcgen05.ld
         const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, lim, a.status, &abort_sh);
@@ -558,9 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
               if (split)
                 store_slot_chunk<CH, BN>(a, J, q, quarter * 32 + lane, half * HALF + c * CH, v);
               else
-                store_col_chunk<CH>(a, J, row, colb + c * CH, v);
+                store_col_chunk<CH>(a, J, row, colb + c * CH, v, rbias);
             } else {
-              store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+              wb.add<CH>(J.bias != nullptr, c * CH, v);
+              store_row_chunk<CH, false>(a, J, row, colb + c * CH, v);
             }
           }
         }
@@ -583,8 +649,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
               if (split)
                 store_slot_chunk<CH, BN>(a, J, q, quarter * 32 + lane, half * HALF + c * CH, v);
               else
-                store_col_chunk<CH>(a, J, row, colb + c * CH, v);
+                store_col_chunk<CH>(a, J, row, colb + c * CH, v, rbias);
             } else {
+              // bias read per chunk: a preloaded copy beside the partial sums spills
               store_row_chunk<CH>(a, J, row, colb + c * CH, v);
             }
           }
@@ -631,6 +698,7 @@ template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false,
           bool TSTORE = false>
 __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_constant__ UmmaArgs a) {
   static_assert(!A_MN || NSUB == 1, "M-major A with one-tile units");
+  umma_cta_trace(a, 30);
   static_assert(!TSTORE || (!GATED && ChunkOf<BN / 2>::v == 32), "TMA stores of 32-column float32 chunks");
   static_assert(!GATED || (NSUB == 2 && NACC == 1), "gated units are two accumulators of one tile");
   constexpr int BNH = BN / 2;
@@ -684,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
   __syncthreads();
   cluster_sync_all();  // both CTAs' barriers exist before any remote use
   tc_fence_after();
+  if (threadIdx.x == 0) umma_trace(a, 8, 0);
   const uint32_t tmem_base = tmem_base_sh;
   griddep_launch_dependents();
   // L2 prefetch of a unit part's B (weight) k-block, the boxes this CTA loads
@@ -709,12 +778,15 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
   // The weights are not outputs of the previous kernel, and L2 is the point
   // of coherence: the first unit's first k-blocks are pulled into L2 before
   // the programmatic-launch wait, which only starts the DRAM reads early.
-  if (warp == 0 && lane == 0 && !A_MN && pair < a.total_units) {
+  // (issued by an epilogue thread, idle until the first accumulator is ready:
+  // the prefetch instructions held back the producer's first copies by 2 us)
+  if (warp == 2 && lane == 0 && !A_MN && pair < a.total_units) {
     const UJob &J = a.jobs[find_job(a, pair)];
     const UPart P = a.parts[J.part0];
     for (int kb = 0; kb < STAGES; ++kb) prefetch_b(P, unit_rowB0(J, pair), kb);
   }
   griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
+  if (threadIdx.x == 0) umma_trace(a, 8, 1);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -848,6 +920,21 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
       const int local = u - J.unit_begin;
       const int ta = local % J.tilesA, tb = local / J.tilesA;
       const int row = ta * 2 * BM + (int)rank * BM + quarter * 32 + lane;
+      // the warp's output columns: [wcol0, wcol0 + BN) of the two accumulators
+      // (NSUB = 2, not gated), else [wcol0, wcol0 + HALF)
+      constexpr int WCOLS = (NSUB == 2 && !GATED) ? BN : HALF;
+      const int wcol0 = (NSUB == 2 && !GATED) ? tb * 2 * BN + half * BN : tb * BN + half * HALF;
+      WarpBias<(WCOLS + 31) / 32> wb, wb2;
+      wb.load(J.bias, wcol0, J.rowsB, lane);
+      if constexpr (GATED) wb2.load(J.bias2, wcol0, J.rowsB, lane);
+      // The pair's last unit: its operand ring has drained once the
+      // accumulator is complete, so the warp stages its 32 x WCOLS block
+      // there and writes it with one tensor store (a warp's row-chunk stores
+      // touch 32 rows each: 0.5 us per 16 columns).
+      const bool rs = !A_MN && !TSTORE && a.rstore && u + npairs >= a.total_units;
+      const int oes = a.out_dt == TP_F32 ? 4 : 2;
+      const uint32_t rs_buf = sbase + (uint32_t)(ew * 32 * WCOLS * oes);
+      const uint32_t rs_row = rs_buf + (uint32_t)(lane * WCOLS * oes);
       const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, lim, a.status, &abort_sh);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
@@ -864,15 +951,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
           tmem_load_chunk<CH>(g_addr + c * CH, g);
           tmem_load_chunk<CH>(g_addr + BN + c * CH, v);
           tmem_wait_ld();
+          wb.add<CH>(J.bias != nullptr, c * CH, g);
+          wb2.add<CH>(J.bias2 != nullptr, c * CH, v);
 #pragma unroll
-          for (int i = 0; i < CH; ++i) {
-            const int col = colb + c * CH + i;
-            const bool in = col < J.rowsB;
-            const float gb = (J.bias && in) ? g[i] + __ldg(J.bias + col) : g[i];
-            const float ub = (J.bias2 && in) ? v[i] + __ldg(J.bias2 + col) : v[i];
-            v[i] = silu_f(gb) * ub;
-          }
-          store_row_chunk<CH, false>(a, J, row, colb + c * CH, v);
+          for (int i = 0; i < CH; ++i) v[i] = silu_f(g[i]) * v[i];
+          if (rs)
+            stage_row_chunk<CH>(a.out_dt, rs_row, c * CH, v);
+          else
+            store_row_chunk<CH, false>(a, J, row, colb + c * CH, v);
         }
       }
 #pragma unroll
@@ -885,10 +971,23 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
           float v[CH];
           tmem_load_chunk<CH>(tb_addr + c * CH, v);
           tmem_wait_ld();
+          if (ew == 0 && lane == 0) umma_trace(a, 6, (eseq * NSUB + sub) * 32 + c);
+          wb.add<CH>(J.bias != nullptr, (NSUB == 2 ? sub * BNH : 0) + c * CH, v);
           if constexpr (TSTORE)
             tstore_chunk(a, J, find_job(a, u), row - lane, colb + c * CH, v, ts_bufs, ts_cnt, lane);
+          else if (rs)
+            stage_row_chunk<CH>(a.out_dt, rs_row, (NSUB == 2 && !GATED ? sub * BNH : 0) + c * CH, v);
           else
-            store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+            store_row_chunk<CH, false>(a, J, row, colb + c * CH, v);
+          if (ew == 0 && lane == 0) umma_trace(a, 7, (eseq * NSUB + sub) * 32 + c);
+        }
+      }
+      if (rs) {  // the block is staged: one tensor store (the map clips rows and columns outside)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row - lane < J.rowsA && wcol0 < J.rowsB) {
+          tma_store_2d(&a.mapC[find_job(a, u)], rs_buf, wcol0, row - lane);
+          bulk_commit_group();
         }
       }
       if (ew == 0 && lane == 0) umma_trace(a, 5, eseq);
@@ -901,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
         acc_phase ^= 1;
       }
     }
-    if constexpr (TSTORE) {
+    if (TSTORE || a.rstore) {
       if (lane == 0) bulk_wait_group_all();  // the tile stores have finished
       __syncwarp();
     }
@@ -915,6 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, TCOLS);
   }
+  umma_cta_trace(a, 31);
 }
 
 // ====================================================================== rank clusters
@@ -934,6 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
 template <int BN, int STAGES, int MSUB, bool B_MN = false>
 __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __grid_constant__ UmmaArgs a) {
   static_assert(!B_MN || BN % 64 == 0, "M/N-major B needs 64-column boxes");
+  umma_cta_trace(a, 30);
   constexpr int A_SUB = BM * BK * 2;
   constexpr int A_BYTES = MSUB * A_SUB;
   constexpr int B_BYTES = BN * BK * 2;
@@ -995,9 +1096,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
       tma_prefetch_l2_2d(&a.mapB[P.bmap], kb * BK, rowB0);
     }
   };
-  if (warp == 0 && lane == 0)
+  if (warp == 2 && lane == 0)  // an epilogue thread: the producer starts its copies at once
     for (int kb = 0; kb < STAGES + kPrefetchKb; ++kb) prefetch_b(kb);
   griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
+  if (threadIdx.x == 0) umma_trace(a, 8, 1);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1028,6 +1130,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
           tma_load_2d(sb, &a.mapB[P.bmap], fb, kb * BK, rowB0);
         }
         prefetch_b(kb + STAGES + kPrefetchKb);  // keeps the weight stream ahead of the ring
+        umma_trace(a, 1, kb);
         used[stage] = true;
         last_phase[stage] = phase;
         if (++stage == STAGES) {
@@ -1045,6 +1148,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
       uint32_t phase = 0;
       for (int kb = 0; kb < P.kblocks; ++kb) {
         if (!mbar_wait(smem_u32(&full_bar[stage]), phase, lim, a.status, &abort_sh)) break;
+        umma_trace(a, 2, kb);
         tc_fence_after();
         const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
@@ -1055,6 +1159,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
                      B_MN ? umma_desc_sw128(sb + kk * 2048, 8192, 1024) : umma_desc_sw128(sb + kk * 32, 16, 1024),
                      a.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
         umma_commit(smem_u32(&empty_bar[stage]));
+        umma_trace(a, 3, kb);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
@@ -1071,11 +1176,24 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
   // order and store, cluster barrier (peers are done reading before the next
   // sub-tile is parked over it).
   bool got = true;
+  // The 4 bias values of the columns an epilogue thread stores: with 256
+  // threads over rows of BN / N / 4 items the column is the same for every
+  // item of the thread, so they are loaded once, before the wait.
+  const int slice = BN / N;
+  const int per_row = slice / 4;
+  const int tcol = (int)rank * slice + (((int)threadIdx.x - 64) % per_row) * 4;
+  float bcol[4] = {0.f, 0.f, 0.f, 0.f};
+  if (warp >= 2 && J.bias) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (rowB0 + tcol + i < J.rowsB) bcol[i] = __ldg(J.bias + rowB0 + tcol + i);
+  }
   if (warp >= 2) {
     got = mbar_wait(smem_u32(&tfull_bar), 0, lim, a.status, &abort_sh);
     got = __all_sync(0xffffffffu, got);
   }
   for (int m = 0; m < MSUB; ++m) {
+    if (warp == 2 && lane == 0) umma_trace(a, 4, m);
     if (warp >= 2 && got) {
       const int quarter = warp & 3;
       const int half = (warp - 2) >> 2;
@@ -1099,11 +1217,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // every rank's partial of sub-tile m is parked
+    if (warp == 2 && lane == 0) umma_trace(a, 9, m);
 
     if (warp >= 2) {
       // column slice `rank` of the sub-tile: sum over ranks 0..N-1 in order, then bias
-      const int slice = BN / N;
-      const int per_row = slice / 4;
       const int t = threadIdx.x - 64;
       for (int idx = t; idx < BM * per_row; idx += 256) {
         const int r = idx / per_row;
@@ -1118,8 +1235,19 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
           acc.w += v.w;
         }
         float o[4] = {acc.x, acc.y, acc.z, acc.w};
-        store_row_chunk<4>(a, J, rowA0 + m * BM + r, rowB0 + c, o);
+        if (J.bias) {
+          if (c == tcol) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] += bcol[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (rowB0 + c + i < J.rowsB) o[i] += __ldg(J.bias + rowB0 + c + i);
+          }
+        }
+        store_row_chunk<4, false>(a, J, rowA0 + m * BM + r, rowB0 + c, o);
       }
+      if (warp == 2 && lane == 0) umma_trace(a, 5, m);
     }
     if (m + 1 < MSUB) {
       __syncthreads();
@@ -1134,6 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
     tc_fence_after();
     tmem_dealloc(tmem_base, TCOLS);
   }
+  umma_cta_trace(a, 31);
 }
 
 // ====================================================================== host
@@ -1172,8 +1301,30 @@ template <int BN, bool B_MN, int STAGES, int NACC, int NSUB, bool GATED = false,
           bool TSTORE = false>
 int launch_pair(UmmaArgs &args, int sms, cudaStream_t s) {
   auto kern = umma_pair_kernel<BN, B_MN, STAGES, NACC, NSUB, GATED, A_MN, TSTORE>;
-  constexpr int smem = STAGES * (BM * BK * 2 + NSUB * (BN / 2) * BK * 2) + 1024 +
-                       (TSTORE ? kEpiWarps * kTsWarpBytes : 0);
+  constexpr int ring = STAGES * (BM * BK * 2 + NSUB * (BN / 2) * BK * 2);
+  constexpr int smem = ring + 1024 + (TSTORE ? kEpiWarps * kTsWarpBytes : 0);
+  // Ring-staged tensor stores of each pair's last unit: a warp's block is 32
+  // rows x WCOLS columns (the warp's columns, as in the epilogue); every
+  // warp's block must fit the ring, and every output's base and rows must
+  // allow tensor stores.
+  args.rstore = 0;
+  if (!A_MN && !TSTORE && args.njobs <= kMaxCMaps) {
+    constexpr int WCOLS = (NSUB == 2 && !GATED) ? BN : BN / 2;
+    const int oes = args.out_dt == TP_F32 ? 4 : 2;
+    bool ok = kEpiWarps * 32 * WCOLS * oes <= ring && (WCOLS * oes) % 16 == 0;
+    for (int j = 0; ok && j < args.njobs; ++j)
+      ok = ((uintptr_t)args.jobs[j].C % 16) == 0 && (args.jobs[j].ldc * oes) % 16 == 0;
+    for (int j = 0; ok && j < args.njobs; ++j) {
+      const UJob &J = args.jobs[j];
+      const CUtensorMapDataType dt = args.out_dt == TP_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : args.out_dt == TP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      if (make_tmap_2d(&args.mapC[j], J.C, dt, oes, (uint64_t)J.rowsB, (uint64_t)J.rowsA, (uint64_t)J.ldc,
+                       (uint32_t)WCOLS, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+        ok = false;
+    }
+    args.rstore = ok ? 1 : 0;
+  }
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
