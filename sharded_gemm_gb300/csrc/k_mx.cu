@@ -429,14 +429,17 @@ __device__ __forceinline__ uint32_t mt_scale_pair(const uint8_t *row, int kb, in
   return v;
 }
 
-__device__ __forceinline__ void mt_store(const MtArgs &a, const MtJob &J, int t, int orow, float v) {
-  const int64_t idx = (int64_t)t * J.ldc + orow;
-  if (a.out_dt == TP_F32)
-    static_cast<float *>(J.C)[idx] = v;
-  else if (a.out_dt == TP_BF16)
-    static_cast<__nv_bfloat16 *>(J.C)[idx] = __float2bfloat16_rn(v);
+// y[t][orow] of an output whose pointer and row stride the caller holds in
+// registers (read through the kernel-parameter block, they would be reloaded
+// after every store: the compiler cannot tell the output from the parameters).
+__device__ __forceinline__ void mt_store(int out_dt, void *C, int64_t ldc, int t, int orow, float v) {
+  const int64_t idx = (int64_t)t * ldc + orow;
+  if (out_dt == TP_F32)
+    static_cast<float *>(C)[idx] = v;
+  else if (out_dt == TP_BF16)
+    static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
   else
-    static_cast<__half *>(J.C)[idx] = __float2half_rn(v);
+    static_cast<__half *>(C)[idx] = __float2half_rn(v);
 }
 
 #define MT_WAIT_ALL(bar, par, okvar)                                   \
@@ -491,6 +494,9 @@ __device__ __forceinline__ void mt_epilogue(const MtArgs &a, uint32_t tmem, uint
     const float bias = (valid && J.bias) ? __ldg(J.bias + orow) : 0.f;
     const int t0 = ui.ntile * BN;
     const bool split = J.splits > 1;
+    void *const oC = J.C;
+    const int64_t oldc = J.ldc;
+    const int oT = J.T, odt = a.out_dt;
     float *slot = split ? a.ws + (J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 * BN + m : nullptr;
 #pragma unroll 1
     for (int c = 0; c < BN / C::CHK; ++c) {
@@ -507,7 +513,7 @@ __device__ __forceinline__ void mt_epilogue(const MtArgs &a, uint32_t tmem, uint
 #pragma unroll
         for (int i = 0; i < C::CHK; ++i) {
           const int t = t0 + c * C::CHK + i;
-          if (t < J.T) mt_store(a, J, t, orow, v[i] + bias);
+          if (t < oT) mt_store(odt, oC, oldc, t, orow, v[i] + bias);
         }
       }
     }

@@ -128,6 +128,7 @@ struct Q4Job {
 struct Q4Args {
   CUtensorMap cmaps[kMaxParts];
   CUtensorMap xmaps[kMaxParts];
+  const float *xfac[kMaxParts];  // prefill: per x map, 2^-c of every token (x was scaled by 2^c)
   Q4Job jobs[kMaxJobs];
   Q4Part parts[kMaxParts];
   int njobs, total_units, ncm, nxm;
@@ -255,14 +256,25 @@ __device__ __forceinline__ void codes_to_values_f16_blocked(uint32_t w, uint32_t
   o[3] = hfma2_u32(hsub2_u32(((w >> 12) & 0x000F000Fu) | m, m), s2, b2);
 }
 
-__device__ __forceinline__ void q4_store(const Q4Args &a, const Q4Job &J, int t, int orow, float v) {
-  const int64_t idx = (int64_t)t * J.ldc + orow;
-  if (a.out_dt == TP_F32)
-    static_cast<float *>(J.C)[idx] = v;
-  else if (a.out_dt == TP_BF16)
-    static_cast<uint16_t *>(J.C)[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+// A job's output, copied to registers once per unit.  Read through the
+// kernel-parameter block instead, every field is reloaded after every store
+// (the compiler cannot tell the output from the parameters): one dependent
+// load per element, 54 us for a 128 x 256 prefill tile.
+struct Q4Out {
+  void *C;
+  int64_t ldc;
+  int T, dt;
+};
+__device__ __forceinline__ Q4Out q4_out(const Q4Args &a, const Q4Job &J) { return Q4Out{J.C, J.ldc, J.T, a.out_dt}; }
+
+__device__ __forceinline__ void q4_store(const Q4Out &o, int t, int orow, float v) {
+  const int64_t idx = (int64_t)t * o.ldc + orow;
+  if (o.dt == TP_F32)
+    static_cast<float *>(o.C)[idx] = v;
+  else if (o.dt == TP_BF16)
+    static_cast<uint16_t *>(o.C)[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   else
-    static_cast<uint16_t *>(J.C)[idx] = __half_as_ushort(__float2half_rn(v));
+    static_cast<uint16_t *>(o.C)[idx] = __half_as_ushort(__float2half_rn(v));
 }
 
 #define Q4_WAIT_ALL(bar, par, okvar)                                                   \
@@ -273,8 +285,103 @@ __device__ __forceinline__ void q4_store(const Q4Args &a, const Q4Job &J, int t,
     }                                                                                  \
   }
 
+
+// ---------------------------------------------------------------- prefill x pre-pass
+// The prefill MMA takes both operands in float16 (the dequantized weights
+// s*q + b are formed in f16, one rounding), in the weights' blocked order
+// inside every 8-element block of K (0,4,1,5,2,6,3,7; a dot product does not
+// depend on the order of its terms).  Each activation row x[t] is
+// scaled by a power of two 2^c (its largest |x| lands in [2^14, 2^15)) and
+// rounded to f16 once, here, instead of in every CTA that reads it; the
+// epilogue multiplies the token's column by 2^-c.  Every bfloat16 x with
+// |x 2^c| >= 2^-14 (within 2^28 of its row's largest) keeps all 8 of its
+// significant bits; smaller ones become f16 subnormals, off by at most
+// 2^-25 in the scaled unit (2^-39 of the row's largest).  So the whole
+// bfloat16 range is kept: |x| > 65504 and rows of tiny values included.
+struct XsRegion {
+  const uint16_t *x;  // bf16 rows, stride lda
+  int64_t lda;
+  uint16_t *xs;       // f16 rows, stride K
+  float *fac;         // 2^-c per row
+  int K, row_begin;
+};
+struct XsArgs {
+  XsRegion r[kMaxParts];
+  int nregions;
+};
+
+__global__ void __launch_bounds__(256) q4_xs_prep_kernel(const __grid_constant__ XsArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();  // x may be the previous kernel's output
+  __shared__ uint32_t red[8];
+  const int row = blockIdx.x;
+  int ri = 0;
+  while (ri + 1 < a.nregions && row >= a.r[ri + 1].row_begin) ++ri;
+  const XsRegion &R = a.r[ri];
+  const int t = row - R.row_begin;
+  const uint4 *src = reinterpret_cast<const uint4 *>(R.x + (int64_t)t * R.lda);
+  const int n16 = R.K / 8;
+  // the largest |x| of the row, as float32 bits (ordered like the values)
+  uint32_t mx = 0;
+  for (int i = threadIdx.x; i < n16; i += 256) {
+    const uint4 w = src[i];
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      mx = max(mx, (wv[k] & 0x7FFFu) << 16);
+      mx = max(mx, wv[k] & 0x7FFF0000u);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) mx = max(mx, red[i]);
+  // biased exponent E of the largest |x| (1 for zero or subnormal rows):
+  // max * 2^(141 - E) lies in [2^14, 2^15); c is kept where 2^c and 2^-c
+  // are normal floats
+  const int E = max((int)(mx >> 23), 1);
+  const int c = min(max(141 - E, -125), 125);
+  const float sc = __uint_as_float((uint32_t)(127 + c) << 23);
+  uint4 *dst = reinterpret_cast<uint4 *>(R.xs + (int64_t)t * R.K);
+  for (int i = threadIdx.x; i < n16; i += 256) {
+    const uint4 w = src[i];
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float e[8];  // the block's 8 elements, scaled
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      e[2 * k] = __uint_as_float(wv[k] << 16) * sc;
+      e[2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u) * sc;
+    }
+    // the weights' blocked K order inside the block: (0,4), (1,5), (2,6), (3,7)
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h = __floats2half2_rn(e[k], e[k + 4]);
+      o[k] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) R.fac[t] = __uint_as_float((uint32_t)(127 - c) << 23);
+}
+
+// When tracing, every CTA b (< 1024) records its SM id + 1 (event 28) and its
+// start (30) and end (31) times at word index b.
+__device__ __forceinline__ void q4_cta_trace(const Q4Args &a, int event) {
+  if (a.trace == nullptr || threadIdx.x != 0 || blockIdx.x >= 1024) return;
+  if (event == 30) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    a.trace[16 + 28 * 1024 + blockIdx.x] = smid + 1;
+  }
+  a.trace[16 + event * 1024 + blockIdx.x] = globaltimer_ns();
+}
+
 template <bool DECODE>
 __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_constant__ Q4Args a) {
+  q4_cta_trace(a, 30);
   griddep_launch_dependents();
   griddep_wait();  // programmatic launch: no global memory before the previous kernel completes
   using C = Q4Cfg<DECODE>;
@@ -322,7 +429,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
-      int st = 0;
+      int st = 0, pseq = 0;
       uint32_t ph = 0;
       bool used[C::STAGES];
       uint32_t lastph[C::STAGES];
@@ -346,6 +453,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
           for (int gi = 0; gi < C::GS; ++gi)
             tma_load_2d(base + C::CODES_BYTES + gi * C::XBOX, &a.xmaps[P.xmap], fb, (gs + gi) * 64,
                         ui.ntile * C::BN);
+          q4_trace(a, 1, 1, pseq++);
           used[st] = true;
           lastph[st] = ph;
           if (++st == C::STAGES) {
@@ -361,7 +469,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int st = 0, as = 0, ds = 0;
+      int st = 0, as = 0, ds = 0, mseq = 0;
       uint32_t ph = 0, aph = 0, dph = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
@@ -373,6 +481,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
             ok = false;
             break;
           }
+          q4_trace(a, 2, 2, mseq);
           tc_fence_after();
           const uint32_t base = sbase + st * STAGE_BYTES;
           const int ng = min(C::GS, ui.g1 - gs);
@@ -412,6 +521,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
           }
           if (!ok) break;
           umma_commit(smem_u32(&empty_bar[st]));
+          q4_trace(a, 2, 5, mseq++);
           if (++st == C::STAGES) {
             st = 0;
             ph ^= 1;
@@ -427,6 +537,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
       }
       umma_commit(smem_u32(&drain_bar));
       mbar_wait(smem_u32(&drain_bar), 0, lim, a.status, nullptr);
+      if (a.trace != nullptr && blockIdx.x < 1024) a.trace[16 + 27 * 1024 + blockIdx.x] = globaltimer_ns();
     }
   } else if (warp < 10) {
     // ---------------------------------------------------------- converters
@@ -435,7 +546,8 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
     const bool ones = DECODE && lane == 31;
     const int srow = DECODE ? quarter * 31 + lane : quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    int st = 0, as = 0;
+    const bool tr = warp == 2 && lane == 0;
+    int st = 0, as = 0, cseq = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
@@ -447,11 +559,13 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
       for (int gs = ui.g0; ok && gs < ui.g1; gs += C::GS) {
         Q4_WAIT_ALL(smem_u32(&full_bar[st]), ph, ok);
         if (!ok) break;
+        if (tr) q4_trace(a, 3, 6, cseq);
         const uint32_t base = sbase + st * STAGE_BYTES;
         const int ng = min(C::GS, ui.g1 - gs);
         for (int gi = 0; gi < ng; ++gi) {
           Q4_WAIT_ALL(smem_u32(&aempty_bar[as]), aph ^ 1, ok);
           if (!ok) break;
+          if (tr) q4_trace(a, 3, 7, cseq);
           tc_fence_after();
           uint32_t out[16];
           if (DECODE) {
@@ -467,22 +581,8 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
               codes_to_int_bf16(w.w, out + 12);
             }
           } else {
-            // x tile of this group (BN rows x 64): bf16 -> f16 in place, blocked
-            // K order, so both MMA operands are f16 (exact for |x| in the f16
-            // normal range).
-            const int cid = (warp - 2) * 32 + lane;
-#pragma unroll 2
-            for (int k = 0; k < C::BN * 8 / 256; ++k) {
-              const uint32_t addr = base + C::CODES_BYTES + gi * C::XBOX + ((cid + k * 256) << 4);
-              const uint4 v = lds128(addr);
-              uint4 o;
-              o.x = f32x2_to_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.z << 16));
-              o.y = f32x2_to_f16x2(__uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.z & 0xFFFF0000u));
-              o.z = f32x2_to_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.w << 16));
-              o.w = f32x2_to_f16x2(__uint_as_float(v.y & 0xFFFF0000u), __uint_as_float(v.w & 0xFFFF0000u));
-              sts128(addr, o);
-            }
-            fence_proxy_async_smem();
+            // the x tile is already f16 in the blocked K order (pre-pass)
+            if (tr) q4_trace(a, 3, 12, cseq);
             uint32_t s2 = 0, b2 = 0;
             if (orow < J.rows) {
               const int64_t gi64 = (int64_t)orow * P.groups + gs + gi;
@@ -498,9 +598,11 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
           }
           tmem_st16(tmem + lane_off + C::A_COL0 + as * 32 + half * 16, out);
           tmem_wait_st();
+          if (tr) q4_trace(a, 3, 13, cseq);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&afull_bar[as]));
+          if (tr) q4_trace(a, 3, 8, cseq++);
           if (++as == C::NA) {
             as = 0;
             aph ^= 1;
@@ -519,7 +621,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
     const bool ones = DECODE && lane == 31;
     const int srow = DECODE ? quarter * 31 + lane : m;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    int ds = 0;
+    int ds = 0, eseq = 0;
     uint32_t dph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < a.total_units; u += gridDim.x) {
@@ -527,6 +629,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
       q4_decode_unit(a, u, ui);
       const Q4Part &P = a.parts[ui.part];
       const Q4Job &J = a.jobs[ui.job];
+      const Q4Out o = q4_out(a, J);
       const int orow = ui.tile * C::ROWS + srow;
       const bool valid = !ones && orow < J.rows;
       if constexpr (DECODE) {
@@ -565,7 +668,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
             const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
 #pragma unroll
             for (int t = 0; t < 16; ++t)
-              if (t < J.T) q4_store(a, J, t, orow, acc[t] + bias);
+              if (t < o.T) q4_store(o, t, orow, acc[t] + bias);
           }
         } else {
           // Split tile: every warp owns its 32 rows; the warp that arrives last
@@ -607,29 +710,41 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
               const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
 #pragma unroll
               for (int t = 0; t < 16; ++t)
-                if (t < J.T) q4_store(a, J, t, orow, sum[t] + bias);
+                if (t < o.T) q4_store(o, t, orow, sum[t] + bias);
             }
             __syncwarp();
             if (lane == 0) *cnt = 0;  // ready for the next call
           }
         }
       } else {
+        const int t0 = ui.ntile * C::BN;
+        // 2^-c of the unit's tokens (lane l: tokens t0 + 32 j + l), loaded
+        // before the accumulator is waited on
+        const float *fac = a.xfac[P.xmap];
+        float fw[C::BN / 32];
+#pragma unroll
+        for (int j = 0; j < C::BN / 32; ++j) {
+          const int t = t0 + 32 * j + lane;
+          fw[j] = t < J.T ? __ldg(fac + t) : 0.f;
+        }
+        const float bias = (valid && J.bias) ? __ldg(J.bias + orow) : 0.f;
         Q4_WAIT_ALL(smem_u32(&dfull_bar[ds]), dph, ok);
         if (!ok) break;
+        if (warp == 10 && lane == 0) q4_trace(a, 4, 9, eseq);
         tc_fence_after();
-        const float bias = (valid && J.bias) ? __ldg(J.bias + orow) : 0.f;
-        const int t0 = ui.ntile * C::BN;
         // split tiles: float32 partials to column-major workspace slots (a
         // warp's 32 rows of one column are one 128-byte line); a second launch
         // adds each tile's slots in split (rank) order, then the bias
         const bool split = J.splits > 1;
         float *slot = split ? a.ws + (J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 * C::BN + m
                             : nullptr;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < C::BN / 32; ++c) {
           float v[32];
           tmem_ld32(tmem + lane_off + C::D_COL0 + ds * C::BN + c * 32, v);
           tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= __shfl_sync(0xffffffffu, fw[c], i);  // undo the x scaling (exact)
           if (split) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) __stcg(slot + (c * 32 + i) * 128, v[i]);
@@ -637,10 +752,12 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int t = t0 + c * 32 + i;
-              if (t < J.T) q4_store(a, J, t, orow, v[i] + bias);
+              if (t < o.T) q4_store(o, t, orow, v[i] + bias);
             }
           }
+          if (warp == 10 && lane == 0) q4_trace(a, 4, 10, eseq * 8 + c);
         }
+        ++eseq;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&dempty_bar[ds]));
@@ -652,6 +769,8 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
     }
   }
 
+  if (a.trace != nullptr && warp == 10 && lane == 0 && blockIdx.x < 1024)
+    a.trace[16 + 26 * 1024 + blockIdx.x] = globaltimer_ns();  // first epilogue warp done
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -659,6 +778,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  q4_cta_trace(a, 31);
 }
 
 // ---------------------------------------------------------------- decode kernel
@@ -931,6 +1051,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_decode_kernel(const __grid_co
       q4_decode_unit(a, u, ui);
       const Q4Part &P = a.parts[ui.part];
       const Q4Job &J = a.jobs[ui.job];
+      const Q4Out o = q4_out(a, J);
       const int orow = ui.tile * C::ROWS + srow;
       const bool valid = !ones && orow < J.rows;
       float acc[TCAP];
@@ -1003,7 +1124,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_decode_kernel(const __grid_co
           const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
 #pragma unroll
           for (int t = 0; t < TCAP; ++t)
-            if (t < J.T) q4_store(a, J, t, orow, acc[t] + bias);
+            if (t < o.T) q4_store(o, t, orow, acc[t] + bias);
         }
       } else {
         float *slot = a.ws + ((J.ws_base + (int64_t)ui.tile_lin * J.splits + ui.sidx) * 128 + m) * 16;
@@ -1030,7 +1151,7 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_decode_kernel(const __grid_co
             const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
 #pragma unroll
             for (int t = 0; t < TCAP; ++t)
-              if (t < J.T) q4_store(a, J, t, orow, sum[t] + bias);
+              if (t < o.T) q4_store(o, t, orow, sum[t] + bias);
           }
           __syncwarp();
           if (lane == 0) *cnt = 0;  // ready for the next call
@@ -1168,6 +1289,7 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws,
   const int c = decode ? choose_chunks(p, (int)tiles_parts, groups_max, sms) : 1;
 
   const void *cptr[kMaxParts], *xptr[kMaxParts];
+  int64_t xK[kMaxParts], xlda[kMaxParts], xT[kMaxParts];
   int ncm = 0, nxm = 0;
   int64_t units = 0, slots = 0;
   int counters = 0;
@@ -1200,7 +1322,7 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws,
       for (int i = 0; i < ncm; ++i)
         if (cptr[i] == P.B) ic = i;
       for (int i = 0; i < nxm; ++i)
-        if (xptr[i] == P.A) ix = i;
+        if (xptr[i] == P.A && xK[i] == P.K && xlda[i] == P.lda && xT[i] == J.M) ix = i;
       int rc;
       if (ic < 0) {
         rc = make_tmap_2d(&args.cmaps[ncm], P.B, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (uint64_t)(P.K / 8),
@@ -1211,10 +1333,16 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws,
         ic = ncm++;
       }
       if (ix < 0) {
-        rc = make_tmap_2d(&args.xmaps[nxm], P.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)P.K,
-                          (uint64_t)Q.T, (uint64_t)P.lda, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B);
-        if (rc) return rc;
+        // prefill: the map is made over the pre-pass's f16 copy, once the workspace is known
+        if (decode) {
+          rc = make_tmap_2d(&args.xmaps[nxm], P.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)P.K,
+                            (uint64_t)Q.T, (uint64_t)P.lda, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B);
+          if (rc) return rc;
+        }
         xptr[nxm] = P.A;
+        xK[nxm] = P.K;
+        xlda[nxm] = P.lda;
+        xT[nxm] = J.M;
         ix = nxm++;
       }
       QP.cmap = (int16_t)ic;
@@ -1236,9 +1364,38 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws,
     return TP_OK;
   }
   if (units > INT32_MAX) return TP_OK;
-  if (slots > 0) {
-    int rc = get_ws((size_t)slots * 128 * BN * sizeof(float), (size_t)counters * 4, &args.ws, &args.cnt);
+  // workspace: split partial slots, then (prefill) each x region's f16 copy and factors
+  const size_t slot_bytes = (size_t)slots * 128 * BN * sizeof(float);
+  size_t prep_off[kMaxParts], prep_bytes = 0;
+  if (!decode)
+    for (int r = 0; r < nxm; ++r) {
+      prep_off[r] = slot_bytes + prep_bytes;
+      prep_bytes += ((size_t)xT[r] * xK[r] * 2 + (size_t)xT[r] * 4 + 255) / 256 * 256;
+    }
+  static XsArgs xa;
+  memset(&xa, 0, sizeof(xa));
+  int xs_rows = 0;
+  if (slot_bytes + prep_bytes > 0) {
+    int rc = get_ws(slot_bytes + prep_bytes, (size_t)counters * 4, &args.ws, &args.cnt);
     if (rc) return rc;
+  }
+  if (!decode) {
+    uint8_t *wsb = reinterpret_cast<uint8_t *>(args.ws);
+    for (int r = 0; r < nxm; ++r) {
+      XsRegion &R = xa.r[r];
+      R.x = static_cast<const uint16_t *>(xptr[r]);
+      R.lda = xlda[r];
+      R.K = (int)xK[r];
+      R.xs = reinterpret_cast<uint16_t *>(wsb + prep_off[r]);
+      R.fac = reinterpret_cast<float *>(wsb + prep_off[r] + (size_t)xT[r] * xK[r] * 2);
+      R.row_begin = xs_rows;
+      xs_rows += (int)xT[r];
+      args.xfac[r] = R.fac;
+      int rc = make_tmap_2d(&args.xmaps[r], R.xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)xK[r],
+                            (uint64_t)xT[r], (uint64_t)xK[r], 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+    }
+    xa.nregions = nxm;
   }
   args.njobs = p.njobs;
   args.total_units = (int)units;
@@ -1259,7 +1416,14 @@ int launch_q4_impl(const Problem &p, cudaStream_t s, bool *handled, WsFn get_ws,
   args.sb_vec = sbv;
   int rc;
   if (!decode) {
-    rc = q4_launch_cfg<false>(args, sms, s);
+    rc = TP_OK;
+    if (xs_rows > 0) {
+      cudaError_t e = launch_pdl(q4_xs_prep_kernel, dim3((unsigned)xs_rows), dim3(256), 0, s, xa);
+      note_launch();
+      if (e == cudaSuccess) e = cudaGetLastError();
+      if (e != cudaSuccess) rc = cuda_error(e, "q4_xs_prep_kernel launch");
+    }
+    if (rc == TP_OK) rc = q4_launch_cfg<false>(args, sms, s);
     if (rc == TP_OK && slots > 0) {  // ordered sums of the split tiles
       SplitJob sj[kMaxJobs];
       for (int j = 0; j < p.njobs; ++j) {

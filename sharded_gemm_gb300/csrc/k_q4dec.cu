@@ -277,14 +277,17 @@ __device__ __forceinline__ void mul2(float &a0, float &a1, float b0, float b1) {
       : "f"(b0), "f"(b1));
 }
 
-__device__ __forceinline__ void d8_store(int out_dt, const D8Job &J, int t, int orow, float v) {
-  const int64_t idx = (int64_t)t * J.ldc + orow;
+// y[t][orow] of an output whose pointer and row stride the caller holds in
+// registers (read through the kernel-parameter block, they would be reloaded
+// after every store: the compiler cannot tell the output from the parameters).
+__device__ __forceinline__ void d8_store(int out_dt, void *C, int64_t ldc, int t, int orow, float v) {
+  const int64_t idx = (int64_t)t * ldc + orow;
   if (out_dt == TP_F32)
-    static_cast<float *>(J.C)[idx] = v;
+    static_cast<float *>(C)[idx] = v;
   else if (out_dt == TP_BF16)
-    static_cast<uint16_t *>(J.C)[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    static_cast<uint16_t *>(C)[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   else
-    static_cast<uint16_t *>(J.C)[idx] = __half_as_ushort(__float2half_rn(v));
+    static_cast<uint16_t *>(C)[idx] = __half_as_ushort(__float2half_rn(v));
 }
 
 #define D8_WAIT(bar, par, okvar)                                           \
@@ -714,9 +717,12 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
       if (J.splits == 1) {
         if (valid) {
           const float bias = J.bias ? __ldg(J.bias + orow) : 0.f;
+          void *const oC = J.C;
+          const int64_t oldc = J.ldc;
+          const int oT = J.T, odt = a.out_dt;
 #pragma unroll
           for (int t = 0; t < TP; ++t)
-            if (t < J.T) d8_store(a.out_dt, J, t, orow, acc[t] + bias);
+            if (t < oT) d8_store(odt, oC, oldc, t, orow, acc[t] + bias);
         }
       } else {
         // A split tile: the partial goes to the unit's workspace slot,

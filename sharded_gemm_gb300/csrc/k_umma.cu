@@ -180,10 +180,24 @@ struct WarpBias {
   }
 };
 
+// A job's output, copied to registers once per unit: read through the
+// kernel-parameter block, the fields are reloaded after every store and every
+// tensor-memory load (the compiler cannot tell the output, or the asm
+// statements' memory, from the parameters), a dependent load per chunk.
+struct UOut {
+  void *C;
+  const float *bias;
+  int64_t ldc;
+  int rowsA, rowsB;
+  int out_dt, vec_ok;
+};
+__device__ __forceinline__ UOut uout(const UmmaArgs &a, const UJob &J) {
+  return UOut{J.C, J.bias, J.ldc, J.rowsA, J.rowsB, a.out_dt, a.vec_ok};
+}
+
 // Stores CH consecutive output values of one thread (row-major, normal mode).
 template <int CH, bool BIAS = true>
-__device__ __forceinline__ void store_row_chunk(const UmmaArgs &a, const UJob &J, int row, int col0,
-                                                float (&v)[CH]) {
+__device__ __forceinline__ void store_row_chunk(const UOut &J, int row, int col0, float (&v)[CH]) {
   if (row >= J.rowsA) return;
   if (BIAS && J.bias) {
 #pragma unroll
@@ -191,8 +205,8 @@ __device__ __forceinline__ void store_row_chunk(const UmmaArgs &a, const UJob &J
       if (col0 + i < J.rowsB) v[i] += __ldg(J.bias + col0 + i);
   }
   const int64_t base = (int64_t)row * J.ldc + col0;
-  const bool full = a.vec_ok && (col0 + CH <= J.rowsB);
-  if (a.out_dt == TP_F32) {
+  const bool full = J.vec_ok && (col0 + CH <= J.rowsB);
+  if (J.out_dt == TP_F32) {
     float *C = static_cast<float *>(J.C) + base;
     if (full && (CH % 4 == 0)) {
 #pragma unroll
@@ -205,7 +219,7 @@ __device__ __forceinline__ void store_row_chunk(const UmmaArgs &a, const UJob &J
     }
   } else {
     uint16_t *C = static_cast<uint16_t *>(J.C) + base;
-    const bool bf = a.out_dt == TP_BF16;
+    const bool bf = J.out_dt == TP_BF16;
     if (full && (CH % 8 == 0)) {
 #pragma unroll
       for (int i = 0; i < CH; i += 8) {
@@ -288,8 +302,7 @@ __device__ __forceinline__ void stage_row_chunk(int out_dt, uint32_t rowbuf, int
 // Swap-AB store: the thread's A row is output column `row`; its values are
 // tokens col0.. of that column.
 template <int CH>
-__device__ __forceinline__ void store_col_chunk(const UmmaArgs &a, const UJob &J, int row, int col0,
-                                                const float (&v)[CH], float b) {
+__device__ __forceinline__ void store_col_chunk(const UOut &J, int row, int col0, const float (&v)[CH], float b) {
   if (row >= J.rowsA) return;
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
@@ -297,9 +310,9 @@ __device__ __forceinline__ void store_col_chunk(const UmmaArgs &a, const UJob &J
     if (t >= J.rowsB) break;
     const int64_t idx = (int64_t)t * J.ldc + row;
     const float x = v[i] + b;
-    if (a.out_dt == TP_F32)
+    if (J.out_dt == TP_F32)
       static_cast<float *>(J.C)[idx] = x;
-    else if (a.out_dt == TP_BF16)
+    else if (J.out_dt == TP_BF16)
       static_cast<uint16_t *>(J.C)[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
     else
       static_cast<uint16_t *>(J.C)[idx] = __half_as_ushort(__float2half_rn(x));
@@ -352,7 +365,7 @@ __device__ __forceinline__ void split_finish(const UmmaArgs &a, const UJob &J, c
     for (int i = 0; i < HALF; ++i)
       if (i < ncol) v[i] += __ldcg(sj + (cl0 + i) * 128);
   }
-  store_col_chunk<HALF>(a, J, row, q.tb * BN + cl0, v, (J.bias && row < J.rowsA) ? __ldg(J.bias + row) : 0.f);
+  store_col_chunk<HALF>(uout(a, J), row, q.tb * BN + cl0, v, (J.bias && row < J.rowsA) ? __ldg(J.bias + row) : 0.f);
   __syncwarp();
   if (lane == 0) *cnt = 0;
 }
@@ -598,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       const int nep = (a.chain || split) ? 1 : J.nparts;
       // bias: swap mode, one per thread (its output column); else the warp's columns
       const float rbias = (SWAP && J.bias && row < J.rowsA) ? __ldg(J.bias + row) : 0.f;
+      const UOut uo = uout(a, J);
       WarpBias<(HALF + 31) / 32> wb;
       if constexpr (!SWAP && !PARTIALS) wb.load(J.bias, colb, J.rowsB, lane);
       for (int pe = 0; pe < nep; ++pe) {
@@ -623,10 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
               if (split)
                 store_slot_chunk<CH, BN>(a, J, q, quarter * 32 + lane, half * HALF + c * CH, v);
               else
-                store_col_chunk<CH>(a, J, row, colb + c * CH, v, rbias);
+                store_col_chunk<CH>(uo, row, colb + c * CH, v, rbias);
             } else {
               wb.add<CH>(J.bias != nullptr, c * CH, v);
-              store_row_chunk<CH, false>(a, J, row, colb + c * CH, v);
+              store_row_chunk<CH, false>(uo, row, colb + c * CH, v);
             }
           }
         }
@@ -649,10 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
               if (split)
                 store_slot_chunk<CH, BN>(a, J, q, quarter * 32 + lane, half * HALF + c * CH, v);
               else
-                store_col_chunk<CH>(a, J, row, colb + c * CH, v, rbias);
+                store_col_chunk<CH>(uo, row, colb + c * CH, v, rbias);
             } else {
               // bias read per chunk: a preloaded copy beside the partial sums spills
-              store_row_chunk<CH>(a, J, row, colb + c * CH, v);
+              store_row_chunk<CH>(uo, row, colb + c * CH, v);
             }
           }
         }
@@ -924,6 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
       // (NSUB = 2, not gated), else [wcol0, wcol0 + HALF)
       constexpr int WCOLS = (NSUB == 2 && !GATED) ? BN : HALF;
       const int wcol0 = (NSUB == 2 && !GATED) ? tb * 2 * BN + half * BN : tb * BN + half * HALF;
+      const UOut uo = uout(a, J);
       WarpBias<(WCOLS + 31) / 32> wb, wb2;
       wb.load(J.bias, wcol0, J.rowsB, lane);
       if constexpr (GATED) wb2.load(J.bias2, wcol0, J.rowsB, lane);
@@ -958,7 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
           if (rs)
             stage_row_chunk<CH>(a.out_dt, rs_row, c * CH, v);
           else
-            store_row_chunk<CH, false>(a, J, row, colb + c * CH, v);
+            store_row_chunk<CH, false>(uo, row, colb + c * CH, v);
         }
       }
 #pragma unroll
@@ -978,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_pair_kernel(const __grid_con
           else if (rs)
             stage_row_chunk<CH>(a.out_dt, rs_row, (NSUB == 2 && !GATED ? sub * BNH : 0) + c * CH, v);
           else
-            store_row_chunk<CH, false>(a, J, row, colb + c * CH, v);
+            store_row_chunk<CH, false>(uo, row, colb + c * CH, v);
           if (ew == 0 && lane == 0) umma_trace(a, 7, (eseq * NSUB + sub) * 32 + c);
         }
       }
@@ -1183,6 +1198,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
   const int per_row = slice / 4;
   const int tcol = (int)rank * slice + (((int)threadIdx.x - 64) % per_row) * 4;
   float bcol[4] = {0.f, 0.f, 0.f, 0.f};
+  const UOut uo = uout(a, J);
   if (warp >= 2 && J.bias) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -1245,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_row_cluster_kernel(const __g
               if (rowB0 + c + i < J.rowsB) o[i] += __ldg(J.bias + rowB0 + c + i);
           }
         }
-        store_row_chunk<4, false>(a, J, rowA0 + m * BM + r, rowB0 + c, o);
+        store_row_chunk<4, false>(uo, rowA0 + m * BM + r, rowB0 + c, o);
       }
       if (warp == 2 && lane == 0) umma_trace(a, 5, m);
     }

@@ -776,6 +776,64 @@ def test_q4_sharded_to_all(policy, T, Kn, O, N):
     check_close(to_host(y), ref, "q4 row")
 
 
+def _range_rows(T, K, seed):
+    """Activation rows spanning the bfloat16 range, for the 4-bit prefill
+    (T > 16): rows far above the float16 maximum (|x| ~ 1e6 > 65504), rows of
+    tiny values (~1e-30, below the float16 subnormals), ordinary rows, an
+    all-zero row, a row mixing 1e5 and 1 inside it, and rows near 3e4."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, K))
+    scale = np.ones(T)
+    scale[0:8] = 1e6
+    scale[8:16] = 1e-30
+    scale[24] = 0.0
+    scale[26:T] = 3e4
+    x = x * scale[:, None]
+    x[25, ::2] *= 1e5
+    return synth.f32_to_bf16_bits(x.astype(np.float32))
+
+
+def _check_rows(got, ref, what):
+    # Row by row (one token per row), each row divided by its largest |ref|
+    # first: the shared bound |d| <= ATOL (|ref| + 1) is written for outputs
+    # of order one, and on a 1e6-scale row its absolute floor vanishes, so
+    # outputs that cancel to near zero would be held to a bound that the
+    # rounding of the row's large terms exceeds.
+    for t in range(ref.shape[0]):
+        s = float(np.abs(ref[t]).max())
+        s = s if s > 0 else 1.0
+        check_close(np.asarray(got[t], np.float64) / s, ref[t] / s, "%s token %d" % (what, t))
+
+
+@pytest.mark.parametrize("T,K,On,N", [(40, 512, 72, 2), (300, 256, 130, 1)])
+def test_q4_prefill_keeps_bf16_range_col(policy, T, K, On, N):
+    # the prefill takes x in float16 after a per-row power-of-two scaling:
+    # rows beyond the float16 range or below its subnormals must come out
+    # as the oracle computes them from the bfloat16 values
+    x = _range_rows(T, K, T + K)
+    pq, ps, pb = _q4_host(On * N, K, 5 + K)
+    shards = [tp.tp_shard_weight(to_device(a, k), 0, 1, N) for a, k in ((pq, "u32"), (ps, "f16"), (pb, "f16"))]
+    ys = tp.tp_q4_all_to_sharded(to_device(x, "bf16"), *shards, out_dtype=torch.float32)
+    _status_ok()
+    ref = oracle.q4_all_to_sharded(bf16(x), oracle.shard(pq, 0, 1, N), oracle.shard(ps, 0, 1, N),
+                                   oracle.shard(pb, 0, 1, N), 64)
+    for r in range(N):
+        _check_rows(to_host(ys[r]), ref[r], "q4 prefill range, shard %d" % r)
+
+
+def test_q4_prefill_keeps_bf16_range_row(policy):
+    T, Kn, O, N = 40, 256, 136, 4
+    x = _range_rows(T, Kn * N, 77)
+    pq, ps, pb = _q4_host(O, Kn * N, 91)
+    xs = tp.tp_shard_weight(to_device(x, "bf16"), -1, 1, N)
+    shards = [tp.tp_shard_weight(to_device(a, k), -1, 1, N) for a, k in ((pq, "u32"), (ps, "f16"), (pb, "f16"))]
+    y = tp.tp_q4_sharded_to_all(xs, *shards, out_dtype=torch.float32)
+    _status_ok()
+    ref = oracle.q4_sharded_to_all([bf16(p) for p in oracle.shard(x, -1, 1, N)], oracle.shard(pq, -1, 1, N),
+                                   oracle.shard(ps, -1, 1, N), oracle.shard(pb, -1, 1, N), 64, None)
+    _check_rows(to_host(y), ref, "q4 prefill range, row-parallel")
+
+
 # ------------------------------------------------------------------ determinism, faults
 def _digest(ts):
     h = hashlib.sha256()
