@@ -593,7 +593,9 @@ __global__ void __launch_bounds__(kMtThreads, 1) mx_umma_kernel(const __grid_con
           const uint32_t fb = smem_u32(&full_bar[st]);
           mbar_arrive_expect_tx(fb, C::X_BYTES + C::C_BYTES);
           tma_load_2d(base + C::A_BYTES, &a.xmaps[P.xmap], fb, kb * 64, ui.ntile * BN);
-          tma_load_2d(base + C::A_BYTES + C::X_BYTES, &a.cmaps[P.cmap], fb, kb * 64, ui.tile * 128);
+          // the weights are read once: evicted first, so x and the split partials stay in L2
+          tma_load_2d_hint(base + C::A_BYTES + C::X_BYTES, &a.cmaps[P.cmap], fb, kb * 64, ui.tile * 128,
+                           l2_policy_evict_first());
           used[st] = true;
           lastph[st] = ph;
           if (++st == STAGES) {
@@ -1002,12 +1004,17 @@ int launch_mx_tc(const Problem &p, cudaStream_t s, bool *handled) {
   static MtArgs args;
   memset(&args, 0, sizeof(args));
   // k-block chunks per part: the same count for every part, chosen to fill
-  // the SMs with the fewest k-blocks per unit (plus a small cost per split)
+  // the SMs with the fewest k-blocks per unit, plus, for split tiles, the
+  // ordered split sum that reads every float32 partial back (measured about
+  // 4.3 TB/s) and, where the partials outgrow what L2 keeps beside the
+  // streamed weights (about 48 MB), their write to DRAM and read back.
+  // Costs in k-block times (about 0.64 us at 256 tokens).
   int64_t tiles_parts = 0;
-  int kb_max = 0;
+  int kb_max = 0, parts_max = 1;
   for (int j = 0; j < p.njobs; ++j) {
     const Job &J = p.jobs[j];
     tiles_parts += ((J.N + 127) / 128) * ((J.M + BN - 1) / BN) * J.nparts;
+    parts_max = std::max(parts_max, J.nparts);
     for (int q = 0; q < J.nparts; ++q) kb_max = std::max(kb_max, (int)((p.parts[J.part0 + q].K + 63) / 64));
   }
   int chunks = 1;
@@ -1015,7 +1022,12 @@ int launch_mx_tc(const Problem &p, cudaStream_t s, bool *handled) {
   for (int c = 1; c <= 16 && c <= kb_max; ++c) {
     const int ck = (kb_max + c - 1) / c;
     const int64_t units = tiles_parts * ((kb_max + ck - 1) / ck);
-    const double cost = (double)((units + sms - 1) / sms) * (ck + 4.0) + (c > 1 ? 2.0 : 0.0);
+    const bool split = c > 1 || parts_max > 1;
+    const double slot_mb = split ? (double)units * 128.0 * BN * 4.0 / 1e6 : 0.0;
+    const double kb_us = 0.64;
+    const double cost = (double)((units + sms - 1) / sms) * (ck + 4.0) +
+                        (split ? 2.0 + slot_mb / 4.3 / kb_us + (slot_mb > 48.0 ? 2.0 * slot_mb / 6.8 / kb_us : 0.0)
+                               : 0.0);
     if (cost < best - 1e-9) {
       best = cost;
       chunks = c;

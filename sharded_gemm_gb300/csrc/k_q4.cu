@@ -448,7 +448,8 @@ __global__ void __launch_bounds__(kQThreads, 1) q4_umma_kernel(const __grid_cons
           const uint32_t base = sbase + st * STAGE_BYTES;
           const uint32_t fb = smem_u32(&full_bar[st]);
           mbar_arrive_expect_tx(fb, C::CODES_TX + C::X_TX);
-          tma_load_2d(base, &a.cmaps[P.cmap], fb, gs * 8, ui.tile * C::ROWS);
+          // the codes are read once: evicted first, so x and the split partials stay in L2
+          tma_load_2d_hint(base, &a.cmaps[P.cmap], fb, gs * 8, ui.tile * C::ROWS, l2_policy_evict_first());
 #pragma unroll
           for (int gi = 0; gi < C::GS; ++gi)
             tma_load_2d(base + C::CODES_BYTES + gi * C::XBOX, &a.xmaps[P.xmap], fb, (gs + gi) * 64,

@@ -63,6 +63,9 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const __grid_constant
   griddep_wait();  // the slots are written by the kernel before this one
   const int per_tile4 = a.BN * 32;  // items per 128 x BN tile
   const int64_t per_tile = (int64_t)a.BN * 128;
+  // Every item count is a multiple of 32 and so is the stride: the 32 lanes
+  // of a warp take the 32 items of one column of one tile together (its 128
+  // rows: four 128-byte slot lines per split, eight lanes per line).
   for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < a.nitems;
        it += (int64_t)gridDim.x * blockDim.x) {
     int j = 0;
@@ -75,23 +78,33 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const __grid_constant
     const int tile = (int)(tile_lin % J.tiles), ntile = (int)(tile_lin / J.tiles);
     const int orow = tile * 128 + m;
     const int t = ntile * a.BN + c;
-    if (orow >= J.rows || t >= J.T) continue;  // slots past the tokens or rows may be unwritten
-    const float *s0 = a.ws + (J.ws_base + tile_lin * J.splits) * per_tile + (int64_t)c * 128 + m;
-    float4 acc = __ldcg(reinterpret_cast<const float4 *>(s0));
+    const int splits = J.splits;
+    const float *s0 = a.ws + (J.ws_base + tile_lin * splits) * per_tile + (int64_t)c * 128 + m;
+    // slots past the tokens or rows may be unwritten: not read, not stored
+    const bool in = orow < J.rows && t < J.T;
+    if (in) {
+      float4 acc = __ldcg(reinterpret_cast<const float4 *>(s0));
 #pragma unroll 8
-    for (int sp = 1; sp < J.splits; ++sp) {
-      const float4 f = __ldcg(reinterpret_cast<const float4 *>(s0 + (int64_t)sp * per_tile));
-      acc.x += f.x;
-      acc.y += f.y;
-      acc.z += f.z;
-      acc.w += f.w;
+      for (int sp = 1; sp < splits; ++sp) {
+        const float4 f = __ldcg(reinterpret_cast<const float4 *>(s0 + (int64_t)sp * per_tile));
+        acc.x += f.x;
+        acc.y += f.y;
+        acc.z += f.z;
+        acc.w += f.w;
+      }
+      float v[4] = {acc.x, acc.y, acc.z, acc.w};
+      const int n = J.rows - orow < 4 ? J.rows - orow : 4;
+      if (J.bias) {
+        for (int i = 0; i < n; ++i) v[i] += __ldg(J.bias + orow + i);
+      }
+      sr_store4<DT>(J.C, (int64_t)t * J.ldc + orow, v, n, a.vec_out != 0);
     }
-    float v[4] = {acc.x, acc.y, acc.z, acc.w};
-    const int n = J.rows - orow < 4 ? J.rows - orow : 4;
-    if (J.bias) {
-      for (int i = 0; i < n; ++i) v[i] += __ldg(J.bias + orow + i);
-    }
-    sr_store4<DT>(J.C, (int64_t)t * J.ldc + orow, v, n, a.vec_out != 0);
+    // The slots are scratch: once every lane of the warp has read its part,
+    // the first lane of each line drops the line from L2 without a write-back
+    // (the partials never need to reach DRAM).
+    __syncwarp();
+    if ((m & 31) == 0)
+      for (int sp = 0; sp < splits; ++sp) l2_discard_line(s0 + (int64_t)sp * per_tile);
   }
 }
 

@@ -96,6 +96,30 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// An L2 policy for data read once (streamed weights): its lines are the
+// first to be evicted, so data that is still to be read again stays.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy for the lines it reads.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// Drops the 128-byte L2 line at `addr` (128-byte aligned) without writing it
+// back: for scratch data that has been read for the last time.
+__device__ __forceinline__ void l2_discard_line(const void *addr) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(addr) : "memory");
+}
+
 // Tile store shared -> global through the tensor map (bulk-group completion);
 // elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
