@@ -71,56 +71,56 @@ def load_peaks() -> dict:
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per call (summed over
-# the kernels the call launches), from one ncu capture of `python bench.py --config C --steps 3
-# --warmup 3 --no-cpu-baseline` (the summary is in profiles/dram_traffic_by_config.md).
+# the kernels the call launches, one step), from one ncu capture per config of
+# `python bench.py --config C --steps 1 --warmup 3 --no-cpu-baseline --no-q4-decode`
+# with --cache-control none (caches kept between launches, as in a real step).
 # An entry is reported only while its kernel family's sources hash to the value
 # in TRAFFIC_SOURCES, since a changed kernel needs a new capture (the hash covers
 # the code, not the comments).
-TRAFFIC_SOURCES = {"umma": "30f51ba1b9f2321f", "q4": "f74999c1f4c8dc46", "mx": "1b2195dd2eed474d"}
+TRAFFIC_SOURCES = {"umma": "9c42b579d88c39d3", "q4": "15328bb74f90e3a9", "mx": "36edcb50399fb9e7"}
 TRAFFIC = {
-    ("mlp", "tp_all_to_sharded"): 97284096,
-    ("mlp", "tp_sharded_to_all"): 102735104,
-    ("mlp_ag_rs", "tp_gathered_to_sharded"): 97700864,
-    ("mlp_ag_rs", "tp_sharded_to_sharded"): 102843136,
-    ("ffn_gated", "tp_gated_all_to_sharded"): 196570880,
-    ("ffn_gated", "tp_sharded_to_all"): 102977024,
-    ("summa2", "tp_summa"): 1088304640,
-    ("summa4", "tp_summa"): 1122663936,
-    ("qkv1", "tp_all_to_sharded(qkv)"): 103928832,
-    ("qkv1", "tp_sharded_to_all(o)"): 33627904,
-    ("qkv1", "tp_all_to_sharded(lm_head)"): 412323072,
-    ("qkv16", "tp_all_to_sharded(qkv)"): 104060160,
-    ("qkv16", "tp_sharded_to_all(o)"): 33751296,
-    ("qkv16", "tp_all_to_sharded(lm_head)"): 414397440,
-    ("qkv2048", "tp_all_to_sharded(qkv)"): 152982272,
-    ("qkv2048", "tp_sharded_to_all(o)"): 51164160,
-    ("qkv2048", "tp_all_to_sharded(lm_head)"): 938591488,
-    ("q4_1", "tp_q4_all_to_sharded"): 135356928,
-    ("q4_1", "tp_q4_sharded_to_all"): 132429312,
-    ("q4_16", "tp_q4_all_to_sharded"): 136966656,
-    ("q4_16", "tp_q4_sharded_to_all"): 134494464,
-    ("q4_256", "tp_q4_all_to_sharded"): 141629952,
-    ("q4_256", "tp_q4_sharded_to_all"): 261504512,
-    ("mx_1", "tp_mx_all_to_sharded"): 245041920,
-    ("mx_1", "tp_mx_sharded_to_all"): 242436352,
-    ("mx_16", "tp_mx_all_to_sharded"): 259156480,
-    ("mx_16", "tp_mx_sharded_to_all"): 248046848,
-    ("mx_256", "tp_mx_all_to_sharded"): 508315904,
-    ("mx_256", "tp_mx_sharded_to_all"): 347982080,
-    ("mlp_bwd", "tp_sharded_dw(w1)"): 135337472,
-    ("mlp_bwd", "tp_bias_grad(b1)"): 11290880,
-    ("mlp_bwd", "tp_sharded_to_all_dx"): 94629376,
-    ("mlp_bwd", "tp_sharded_dw(w2)"): 131244800,
-    ("mlp_bwd", "tp_bias_grad(b2)"): 4213248,
-    ("mlp_bwd", "tp_all_to_sharded_dx"): 102053376,
+    ("mlp", "tp_all_to_sharded"): 94351616,
+    ("mlp", "tp_sharded_to_all"): 104192256,
+    ("mlp_ag_rs", "tp_gathered_to_sharded"): 93484032,
+    ("mlp_ag_rs", "tp_sharded_to_sharded"): 104566272,
+    ("ffn_gated", "tp_gated_all_to_sharded"): 192219648,
+    ("ffn_gated", "tp_sharded_to_all"): 104792320,
+    ("summa2", "tp_summa"): 1087090432,
+    ("summa4", "tp_summa"): 1121469184,
+    ("qkv1", "tp_all_to_sharded(qkv)"): 101331456,
+    ("qkv1", "tp_sharded_to_all(o)"): 33677056,
+    ("qkv1", "tp_all_to_sharded(lm_head)"): 413271552,
+    ("qkv16", "tp_all_to_sharded(qkv)"): 101381376,
+    ("qkv16", "tp_sharded_to_all(o)"): 33777920,
+    ("qkv16", "tp_all_to_sharded(lm_head)"): 418281472,
+    ("qkv2048", "tp_all_to_sharded(qkv)"): 148572928,
+    ("qkv2048", "tp_sharded_to_all(o)"): 65743104,
+    ("qkv2048", "tp_all_to_sharded(lm_head)"): 960369664,
+    ("q4_1", "tp_q4_all_to_sharded"): 132354560,
+    ("q4_1", "tp_q4_sharded_to_all"): 132802304,
+    ("q4_16", "tp_q4_all_to_sharded"): 135540224,
+    ("q4_16", "tp_q4_sharded_to_all"): 138573824,
+    ("q4_256", "tp_q4_all_to_sharded"): 164937984,
+    ("q4_256", "tp_q4_sharded_to_all"): 232049408,
+    ("mx_1", "tp_mx_all_to_sharded"): 242231040,
+    ("mx_1", "tp_mx_sharded_to_all"): 242233088,
+    ("mx_16", "tp_mx_all_to_sharded"): 245936128,
+    ("mx_16", "tp_mx_sharded_to_all"): 253933568,
+    ("mx_256", "tp_mx_all_to_sharded"): 292743424,
+    ("mx_256", "tp_mx_sharded_to_all"): 320696064,
+    ("mlp_bwd", "tp_sharded_to_all_dx"): 93768448,
+    ("mlp_bwd", "tp_sharded_dw(w2)"): 139603968,
+    ("mlp_bwd", "tp_bias_grad(b2)"): 2398720,
+    ("mlp_bwd", "tp_all_to_sharded_dx"): 163256320,
+    ("mlp_bwd", "tp_sharded_dw(w1)"): 137828864,
+    ("mlp_bwd", "tp_bias_grad(b1)"): 12615424,
 }
-
 
 # The sources each family of kernels is built from (the shared host code and
 # headers belong to every family).
 COMMON_SOURCES = ["tp_api.cu", "tp_internal.h", "ptx.cuh", "tmap.cu", "k_split.cu"]
-FAMILY_SOURCES = {"umma": ["k_umma.cu", "k_colsum.cu", "k_simt.cu"], "q4": ["k_q4.cu", "k_q4gemv.cu"],
-                  "mx": ["k_mx.cu"]}
+FAMILY_SOURCES = {"umma": ["k_umma.cu", "k_colsum.cu", "k_simt.cu"],
+                  "q4": ["k_q4.cu", "k_q4gemv.cu", "k_q4dec.cu"], "mx": ["k_mx.cu"]}
 
 
 def config_family(config: str) -> str:
