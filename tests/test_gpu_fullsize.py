@@ -27,7 +27,8 @@ def test_full_mlp_pair():
     pair = MLPPair(cfg)
     pair.step()
     assert tp.tp_query_status() == 0
-    rows = sample_rows(cfg["T"], 12)
+    # 64 of the 512 token rows (both 256-row token tiles), every output column
+    rows = sample_rows(cfg["T"], 64)
     x = bf16(cfg["x"])[rows]
     N = cfg["N"]
     w1 = [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, N)]
@@ -46,7 +47,7 @@ def test_full_gated_ffn():
     ffn = GatedFFN(cfg)
     ffn.step()
     assert tp.tp_query_status() == 0
-    rows = sample_rows(cfg["T"], 10)
+    rows = sample_rows(cfg["T"], 48)
     x = bf16(cfg["x"])[rows]
     N = cfg["N"]
     sh = lambda a: [bf16(p) for p in oracle.shard(cfg[a], 0, 1, N)]
@@ -68,7 +69,7 @@ def test_full_mlp_backward():
     bw = MLPBackward(cfg, dy)
     bw.step()
     assert tp.tp_query_status() == 0
-    rows = sample_rows(T, 8)
+    rows = sample_rows(T, 32)
     dyv = bf16(dy)
     w1 = [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, N)]
     w2 = [bf16(p) for p in oracle.shard(cfg["w2"], -1, 1, N)]
@@ -80,9 +81,9 @@ def test_full_mlp_backward():
     h = [to_host(m) for m in bw.fwd.mid]
     x = bf16(cfg["x"])
     for r in range(N):
-        o2 = sample_rows(D, 16, seed=r)
+        o2 = sample_rows(D, 64, seed=r)
         check_close(to_host(bw.dw2[r])[o2], oracle.sharded_dw([dyv[:, o2]], [h[r]])[0], "dW2 %d" % r)
-        o1 = sample_rows(dh[r].shape[1], 16, seed=10 + r)
+        o1 = sample_rows(dh[r].shape[1], 64, seed=10 + r)
         check_close(to_host(bw.dw1[r])[o1], oracle.sharded_dw([dh[r][:, o1]], [x])[0], "dW1 %d" % r)
     check_close(to_host(bw.db2[0]), oracle.bias_grad([[dyv]])[0], "db2")
     for r, g in enumerate(oracle.bias_grad([[d] for d in dh])):
@@ -96,7 +97,7 @@ def test_full_mlp_gather_scatter():
     ffn = MLPGatherScatter(cfg)
     ffn.step()
     assert tp.tp_query_status() == 0
-    rows = sample_rows(cfg["T"], 12)
+    rows = sample_rows(cfg["T"], 64)
     N = cfg["N"]
     xs = [bf16(p)[rows] for p in oracle.shard(cfg["x"], -1, 1, N)]
     w1 = [bf16(p) for p in oracle.shard(cfg["w1"], 0, 1, N)]
@@ -139,7 +140,7 @@ def test_full_qkv(T):
     w.step()
     assert tp.tp_query_status() == 0
     N, D = cfg["N"], cfg["D"]
-    rows = sample_rows(T, 8)
+    rows = sample_rows(T, 16 if T <= 16 else 48)  # every token row for T <= 16
     x = bf16(cfg["x"])[rows]
     # fused QKV: shard r holds rows {s*D + r*D/N + i} of W_qkv
     wq = oracle.shard(cfg["w_qkv"], 0, 3, N)
@@ -167,7 +168,7 @@ def test_full_q4_pair(T):
     w = Q4Pair(cfg, quantized=(up, down))
     w.step()
     assert tp.tp_query_status() == 0
-    rows = sample_rows(T, 6)
+    rows = sample_rows(T, 16 if T <= 16 else 48)  # every token row for T <= 16
     x = bf16(cfg["x"])[rows]
     # up: column-parallel, sampled output columns of every shard
     for r in range(N):
@@ -192,7 +193,7 @@ def test_full_mx_pair(T):
     w = MXPair(cfg, quantized=(up, down))
     w.step()
     assert tp.tp_query_status() == 0
-    rows = sample_rows(T, 6)
+    rows = sample_rows(T, 16 if T <= 16 else 48)  # every token row for T <= 16
     x = bf16(cfg["x"])[rows]
     for r in range(N):
         cols = sample_rows(F // N, 96, seed=r)
