@@ -115,8 +115,8 @@ int tp_set_wait_limit_ns(int64_t limit_ns);
  * accumulator pair, 11 it finished the stage.  Per accumulator pair p of
  * stage s, at word index 4s + p: 17/18 the MMA thread issued / committed it,
  * 12/13/14 epilogue warp 6 saw it / had loaded it / had applied it.  Per CTA
- * b, at index b: 28 the SM id + 1, 30/31 the CTA's start / end, and 29 the
- * start of block b of the activation pre-pass.
+ * b, at index b: 28 the SM id + 1, 30/31 the CTA's start / end, and 29/10
+ * the start / end of its share of the activation pre-pass.
  * 16-bit decode kernel (other shapes): 1 producer issued the stage's loads;
  * 2/3/4 the MMA thread saw the stage's data / A operand / free accumulator,
  * 5 it committed the stage; 6/7 converter warp 2 saw the data / a free A

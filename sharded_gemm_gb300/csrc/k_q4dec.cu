@@ -33,7 +33,12 @@
 // core's accumulator and the groups are added in float32 in a fixed order.
 //
 // Roles (one CTA per SM, persistent over units = (tile of 128 output rows,
-// range of stages)).  Warp 0 issues the tensor copy of a stage's packed
+// range of stages)).  The pre-pass runs inside this kernel: at the start the
+// epilogue warps of every CTA write their share of the prepared activations
+// and count themselves done on a launch-wide counter; once it is full (or,
+// after a short wait, once this CTA has prepared every item itself) the
+// activation stream starts.  The codes stream starts at once with its first
+// stage.  Warp 0 issues the tensor copy of a stage's packed
 // codes (8 groups) into the codes ring; warp 10 the stage's activation tile,
 // scales, biases and per-group factors into the operand ring.  Warps 2-5
 // expand a stage's codes into one of two halves of the A operand in TMEM
@@ -72,6 +77,14 @@ constexpr int kD8GroupsPerStage = 8;
 // the other roles through a ring in shared memory.
 constexpr int kUnitRing = 4;
 constexpr int kUnitReaders = 1 + 1 + 4 + 4;  // operand producer, MMA, converters, epilogue
+// Codes stages a CTA issues before the prepared activations are ready: the
+// first stage's DRAM latency then overlaps the pre-pass, and the pre-pass's
+// reads of x still meet short DRAM queues.
+constexpr int kD8PreStages = 1;
+// How long a CTA waits for the other CTAs' shares of the pre-pass before it
+// prepares every item itself (identical values, so the duplicate writes are
+// harmless).  The launch does not require all CTAs to be resident together.
+constexpr uint64_t kD8PrepAloneNs = 30000;
 
 template <int TP>
 struct D8Cfg {
@@ -81,7 +94,7 @@ struct D8Cfg {
   // stages ahead of the MMAs.
   static constexpr int CODES_BOX = 128 * 128;         // 4 groups x 128 rows, 128B-swizzled
   static constexpr int CODES_BYTES = 2 * CODES_BOX;
-  static constexpr int CSTAGES = 4;
+  static constexpr int CSTAGES = TP == 16 ? 5 : 4;
   // Operand ring: the stage's activation tile (released by the MMA's
   // commit) with its scales, biases and per-group factors and sums
   // (released by the epilogue, which reads them a few groups behind).
@@ -93,7 +106,7 @@ struct D8Cfg {
   static constexpr int GX_BYTES = kD8GroupsPerStage * 2 * TP * 4;
   static constexpr int OP_BYTES = (GX_OFF + GX_BYTES + 1023) / 1024 * 1024;
   static constexpr int OP_TX = 4 * B_BOX + 4096 + GX_BYTES;
-  static constexpr int OSTAGES = TP == 16 ? 4 : 6;
+  static constexpr int OSTAGES = TP == 16 ? 3 : 6;
   static constexpr int A_COL0 = 0;                    // A: two halves of 128 columns (a stage's 8 groups each)
   static constexpr int D_COL0 = 256;                  // D: 4 pair slots of 2N columns (2 groups each)
   static constexpr int NDP = 4, DP_COLS = 2 * N;
@@ -103,6 +116,14 @@ struct D8Cfg {
   static_assert(SMEM <= 227 * 1024 - 1024, "shared memory (dynamic, leaving room for the static barriers)");
 };
 
+// A region of the activation pre-pass: one distinct activation block.
+struct PrepRegion {
+  const uint16_t *x;  // bfloat16 (T, K), row stride lda
+  int64_t lda;
+  uint8_t *xq;        // (2 TP, K) bytes
+  float *gx;          // (groups, 2, TP)
+  int K, groups, T, item_begin;
+};
 struct D8Part {
   int16_t cmap, smap, qmap, region;
   int groups;
@@ -128,10 +149,13 @@ struct D8Args {
   D8Job jobs[MP];
   D8Part parts[MP];
   const float *gx[MP];                          // per region: [groups][2][TP] floats
+  PrepRegion prep[MP];                          // per region: the pre-pass's input and outputs
+  int nprep, prep_items;
   int njobs, total_units, out_dt;
   uint32_t idesc;
   float *ws;
   int *work, *done;  // unit dispenser and finished-CTA count (zero between launches)
+  int *prepped;      // CTAs done with their share of the pre-pass (zero between launches)
   int *status;
   uint64_t wait_ns;
   unsigned long long *trace;  // optional role timeline of CTA 0 (tp_set_trace)
@@ -231,20 +255,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int32_t x, int32_t y, int32_t z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -324,6 +334,94 @@ __device__ __forceinline__ void d8_store(int out_dt, void *C, int64_t ldc, int t
     }                                                                                  \
   }
 
+// ------------------------------------------------------------------ pre-pass
+// One item per (region, token t < TP, group g): the group's 64 bfloat16 x
+// scaled by 2^c, c = 7 - floor(log2 max|x|) (clamped so 2^(9-c) stays a
+// normal float), written as E4M3 hi and lo terms into rows t and TP + t of
+// the region's (2 TP, K) byte matrix in the K order of the expanded codes,
+// and gx[g][0][t] = 2^(9-c), gx[g][1][t] = the group's plain ascending sum.
+// Tokens T <= t < TP get zero rows and zero factors.  The decode kernel's
+// CTAs share the items out at their start (see the kernel).
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {  // lo -> byte 0, hi -> byte 1
+  unsigned short d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ void e4m3x2_value(uint32_t v, float &lo, float &hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)v));
+  lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+}
+
+template <int TP, int MP>
+__device__ __forceinline__ void d8_prep_item(const PrepRegion (&regs)[MP], int nregions, int item) {
+  int ri = 0;
+  while (ri + 1 < nregions && item >= regs[ri + 1].item_begin) ++ri;
+  const PrepRegion &R = regs[ri];
+  const int local = item - R.item_begin;
+  const int t = local / R.groups, g = local - t * R.groups;
+  uint32_t hiw[16], low[16];
+  float fac = 0.f, sum = 0.f;
+  if (t < R.T) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(R.x + (int64_t)t * R.lda + 64 * (int64_t)g);
+    float v[64];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 w = src[c];
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        v[8 * c + 2 * m] = __uint_as_float(wv[m] << 16);
+        v[8 * c + 2 * m + 1] = __uint_as_float(wv[m] & 0xFFFF0000u);
+      }
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+      sum += v[k];
+      mx = fmaxf(mx, fabsf(v[k]));
+    }
+    int e = mx == 0.f ? 0 : (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;  // floor(log2 mx), normal mx
+    e = e < -120 ? -120 : (e > 120 ? 120 : e);
+    const int c = 7 - e;                                 // in [-113, 127]
+    const float scale = __uint_as_float((uint32_t)(c + 127) << 23);
+    fac = __uint_as_float((uint32_t)(2 + e + 127) << 23);  // 2^(9-c)
+    // K order inside each block of eight: 0, 2, 4, 6, 1, 3, 5, 7
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      uint32_t hp[4], lp[4];  // byte pairs (element ord[2i], element ord[2i+1])
+      constexpr int ord[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float x0 = v[8 * m + ord[2 * i]] * scale, x1 = v[8 * m + ord[2 * i + 1]] * scale;
+        const uint32_t h = e4m3x2(x0, x1);
+        float h0, h1;
+        e4m3x2_value(h, h0, h1);
+        hp[i] = h;
+        lp[i] = e4m3x2(x0 - h0, x1 - h1);
+      }
+      hiw[2 * m] = hp[0] | (hp[1] << 16);
+      hiw[2 * m + 1] = hp[2] | (hp[3] << 16);
+      low[2 * m] = lp[0] | (lp[1] << 16);
+      low[2 * m + 1] = lp[2] | (lp[3] << 16);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) hiw[i] = low[i] = 0u;
+  }
+  uint4 *dh = reinterpret_cast<uint4 *>(R.xq + (int64_t)t * R.K + 64 * (int64_t)g);
+  uint4 *dl = reinterpret_cast<uint4 *>(R.xq + (int64_t)(TP + t) * R.K + 64 * (int64_t)g);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    dh[i] = make_uint4(hiw[4 * i], hiw[4 * i + 1], hiw[4 * i + 2], hiw[4 * i + 3]);
+    dl[i] = make_uint4(low[4 * i], low[4 * i + 1], low[4 * i + 2], low[4 * i + 3]);
+  }
+  R.gx[((int64_t)g * 2) * TP + t] = fac;
+  R.gx[((int64_t)g * 2 + 1) * TP + t] = sum;
+}
+
+
 // ------------------------------------------------------------------ kernel
 template <int TP, int MP>
 __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_constant__ D8Args<MP> a) {
@@ -345,6 +443,8 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
   __shared__ __align__(8) uint64_t ufull_bar[kUnitRing], uempty_bar[kUnitRing];  // unit indices to every role
   __shared__ int unit_ring[kUnitRing];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t xready_bar;  // the prepared activations of every region are written
+  __shared__ int prep_alone_sh;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -376,6 +476,7 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
       mbar_init(smem_u32(&uempty_bar[i]), kUnitReaders);  // every other role read it
     }
     mbar_init(smem_u32(&drain_bar), 1);
+    mbar_init(smem_u32(&xready_bar), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -385,19 +486,6 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // Weights are never outputs of the previous kernel and L2 is the point of
-  // coherence: prefetching the first unit's codes into L2 before the
-  // programmatic-launch wait only starts the DRAM reads early.  An epilogue
-  // thread issues it, so the producers start at once.
-  if (warp == 6 && lane == 0 && (int)blockIdx.x < a.total_units) {
-    D8Unit ui;
-    d8_unit(a, blockIdx.x, ui);
-    for (int k = 0; k < ui.nst && k < C::CSTAGES; ++k) {
-      int gs;
-      const D8Part &P = a.parts[d8_stage_part(a, a.jobs[ui.job], ui.s0 + k, gs)];
-      tma_prefetch_3d(&a.cmaps[P.cmap], 0, ui.tile * 128, gs / 4);
-    }
-  }
   griddep_wait();  // programmatic launch: no global loads before the previous kernel completes
   const uint32_t tmem = tmem_base_sh;
 
@@ -417,6 +505,7 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
       int us = 0;
       uint32_t uph = 0;
       int next = (int)blockIdx.x < a.total_units ? (int)blockIdx.x : -1;  // the codes producer's unit to publish
+      bool prep_ok = false;
       while (ok) {
         int u;
         if (codes) {
@@ -448,6 +537,16 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
               (!codes && !mbar_wait(smem_u32(&sdone_bar[st]), ph ^ 1, lim, a.status, &abort_sh))) {
             ok = false;
             break;
+          }
+          // The activation stream waits for the prepared activations; the
+          // codes stream issues its first stages before that.
+          if (!prep_ok && (!codes || seq >= kD8PreStages)) {
+            if (!mbar_wait(smem_u32(&xready_bar), 0, lim, a.status, &abort_sh)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();  // the tensor copies below read what other threads wrote
+            prep_ok = true;
           }
           const uint32_t fb = smem_u32(&fullb[st]);
           if (codes) {
@@ -503,24 +602,30 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
           tc_fence_after();
           const uint32_t base = obase + os * C::OP_BYTES;
           const uint32_t abase = tmem + C::A_COL0 + h * 128;
-          for (int p = 0; p < C::NDP; ++p) {  // groups 2p, 2p+1 of the stage
-            if (!mbar_wait(smem_u32(&dempty_bar[p]), dph ^ 1, lim, a.status, &abort_sh)) {
+          // Per half-stage (pairs 2hp, 2hp+1: 4 accumulators), the 4 first K-steps
+          // and then the 4 second ones, so that no MMA follows the one it adds to.
+          for (int hp = 0; hp < 2; ++hp) {
+            if (!mbar_wait(smem_u32(&dempty_bar[2 * hp]), dph ^ 1, lim, a.status, &abort_sh) ||
+                !mbar_wait(smem_u32(&dempty_bar[2 * hp + 1]), dph ^ 1, lim, a.status, &abort_sh)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            d8_trace(a, 17, seq * 4 + p);
+            d8_trace(a, 17, seq * 4 + 2 * hp);
 #pragma unroll
-            for (int gg = 0; gg < 2; ++gg) {
-              const uint32_t d = tmem + C::D_COL0 + p * C::DP_COLS + gg * C::N;
-              const uint32_t bb = base + C::B_OFF + p * C::B_BOX + gg * 64;
+            for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-              for (int kk = 0; kk < 2; ++kk)
-                umma_f8_ts(d, abase + p * 32 + gg * 16 + kk * 8, umma_desc_sw128(bb + kk * 32, 16, 1024), a.idesc,
-                           kk > 0 ? 1u : 0u);
-            }
-            if (p & 1) umma_commit(smem_u32(&dfull_bar[p >> 1]));
-            d8_trace(a, 18, seq * 4 + p);
+              for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+                for (int gg = 0; gg < 2; ++gg) {
+                  const int p = 2 * hp + pp;
+                  const uint32_t d = tmem + C::D_COL0 + p * C::DP_COLS + gg * C::N;
+                  const uint32_t bb = base + C::B_OFF + p * C::B_BOX + gg * 64;
+                  umma_f8_ts(d, abase + p * 32 + gg * 16 + kk * 8, umma_desc_sw128(bb + kk * 32, 16, 1024), a.idesc,
+                             kk > 0 ? 1u : 0u);
+                }
+            umma_commit(smem_u32(&dfull_bar[hp]));
+            d8_trace(a, 18, seq * 4 + 2 * hp);
           }
           if (!ok) break;
           umma_commit(smem_u32(&sdone_bar[os]));  // frees A half h and the stage's B tile
@@ -606,6 +711,47 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
     tmem_wait_st();  // no store may still be in flight when the CTA tears down
   } else if (warp < 10) {
     // ------------------------------------------------------------ epilogue
+    {
+      // First this CTA's share of the activation pre-pass (a contiguous run
+      // of items), one arrival on the launch-wide count, and a short wait
+      // for the other CTAs' shares; a CTA that waits in vain (the others are
+      // not resident) prepares every item itself.  Then the producers go.
+      const int per = (a.prep_items + (int)gridDim.x - 1) / (int)gridDim.x;
+      const int i0 = (int)blockIdx.x * per;
+      const int i1 = min(a.prep_items, i0 + per);
+      const int et = (warp - 6) * 32 + lane;
+      const bool tr = a.trace != nullptr && warp == 6 && lane == 0 && blockIdx.x < 1024;
+      if (tr) a.trace[16 + 29 * 1024 + blockIdx.x] = globaltimer_ns();
+      for (int it = i0 + et; it < i1; it += 128) d8_prep_item<TP, MP>(a.prep, a.nprep, it);
+      fence_proxy_async_global();  // the tensor copies of every CTA read what this thread wrote
+      __threadfence();
+      named_barrier(1, 128);
+      if (warp == 6 && lane == 0) {
+        atomicAdd(a.prepped, 1);
+        const uint64_t t0 = globaltimer_ns();
+        int all = 0;
+        for (;;) {
+          int v;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.prepped) : "memory");
+          if (v >= (int)gridDim.x) {
+            all = 1;
+            break;
+          }
+          if (globaltimer_ns() - t0 > kD8PrepAloneNs || abort_sh) break;
+          __nanosleep(64);
+        }
+        prep_alone_sh = !all;
+      }
+      named_barrier(1, 128);
+      if (prep_alone_sh) {
+        for (int it = et; it < a.prep_items; it += 128) d8_prep_item<TP, MP>(a.prep, a.nprep, it);
+        fence_proxy_async_global();
+        __threadfence();
+        named_barrier(1, 128);
+      }
+      if (warp == 6 && lane == 0) mbar_arrive(smem_u32(&xready_bar));
+      if (tr) a.trace[16 + 10 * 1024 + blockIdx.x] = globaltimer_ns();
+    }
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -749,113 +895,10 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
     if (atomicAdd(a.done, 1) == (int)gridDim.x - 1) {
       atomicExch(a.work, 0);
       atomicExch(a.done, 0);
+      atomicExch(a.prepped, 0);
     }
   }
   if (a.trace != nullptr && threadIdx.x == 0 && blockIdx.x < 1024) a.trace[16 + 31 * 1024 + blockIdx.x] = globaltimer_ns();
-}
-
-// ------------------------------------------------------------------ pre-pass
-// One thread per (region, token t < TP, group g): the group's 64 bfloat16 x
-// scaled by 2^c, c = 7 - floor(log2 max|x|) (clamped so 2^(9-c) stays a
-// normal float), written as E4M3 hi and lo terms into rows t and TP + t of
-// the region's (2 TP, K) byte matrix in the K order of the expanded codes,
-// and gx[g][0][t] = 2^(9-c), gx[g][1][t] = the group's plain ascending sum.
-// Tokens T <= t < TP get zero rows and zero factors.
-struct PrepRegion {
-  const uint16_t *x;  // bfloat16 (T, K), row stride lda
-  int64_t lda;
-  uint8_t *xq;        // (2 TP, K) bytes
-  float *gx;          // (groups, 2, TP)
-  int K, groups, T, item_begin;
-};
-struct PrepArgs {
-  PrepRegion r[kMaxParts];
-  int nregions, items;
-  unsigned long long *trace;  // optional: block start times (event 29)
-};
-
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {  // lo -> byte 0, hi -> byte 1
-  unsigned short d;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-__device__ __forceinline__ void e4m3x2_value(uint32_t v, float &lo, float &hi) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)v));
-  lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
-  hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
-}
-
-template <int TP>
-__global__ void __launch_bounds__(256) q4_dec8_prep_kernel(const __grid_constant__ PrepArgs a) {
-  griddep_launch_dependents();
-  griddep_wait();  // x may be the previous kernel's output
-  if (a.trace != nullptr && threadIdx.x == 0 && blockIdx.x < 1024) a.trace[16 + 29 * 1024 + blockIdx.x] = globaltimer_ns();
-  const int item = blockIdx.x * blockDim.x + threadIdx.x;
-  if (item >= a.items) return;
-  int ri = 0;
-  while (ri + 1 < a.nregions && item >= a.r[ri + 1].item_begin) ++ri;
-  const PrepRegion &R = a.r[ri];
-  const int local = item - R.item_begin;
-  const int t = local / R.groups, g = local - t * R.groups;
-  uint32_t hiw[16], low[16];
-  float fac = 0.f, sum = 0.f;
-  if (t < R.T) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(R.x + (int64_t)t * R.lda + 64 * (int64_t)g);
-    float v[64];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 w = src[c];
-      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        v[8 * c + 2 * m] = __uint_as_float(wv[m] << 16);
-        v[8 * c + 2 * m + 1] = __uint_as_float(wv[m] & 0xFFFF0000u);
-      }
-    }
-    float mx = 0.f;
-#pragma unroll
-    for (int k = 0; k < 64; ++k) {
-      sum += v[k];
-      mx = fmaxf(mx, fabsf(v[k]));
-    }
-    int e = mx == 0.f ? 0 : (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;  // floor(log2 mx), normal mx
-    e = e < -120 ? -120 : (e > 120 ? 120 : e);
-    const int c = 7 - e;                                 // in [-113, 127]
-    const float scale = __uint_as_float((uint32_t)(c + 127) << 23);
-    fac = __uint_as_float((uint32_t)(2 + e + 127) << 23);  // 2^(9-c)
-    // K order inside each block of eight: 0, 2, 4, 6, 1, 3, 5, 7
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      uint32_t hp[4], lp[4];  // byte pairs (element ord[2i], element ord[2i+1])
-      constexpr int ord[8] = {0, 2, 4, 6, 1, 3, 5, 7};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float x0 = v[8 * m + ord[2 * i]] * scale, x1 = v[8 * m + ord[2 * i + 1]] * scale;
-        const uint32_t h = e4m3x2(x0, x1);
-        float h0, h1;
-        e4m3x2_value(h, h0, h1);
-        hp[i] = h;
-        lp[i] = e4m3x2(x0 - h0, x1 - h1);
-      }
-      hiw[2 * m] = hp[0] | (hp[1] << 16);
-      hiw[2 * m + 1] = hp[2] | (hp[3] << 16);
-      low[2 * m] = lp[0] | (lp[1] << 16);
-      low[2 * m + 1] = lp[2] | (lp[3] << 16);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) hiw[i] = low[i] = 0u;
-  }
-  uint4 *dh = reinterpret_cast<uint4 *>(R.xq + (int64_t)t * R.K + 64 * (int64_t)g);
-  uint4 *dl = reinterpret_cast<uint4 *>(R.xq + (int64_t)(TP + t) * R.K + 64 * (int64_t)g);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    dh[i] = make_uint4(hiw[4 * i], hiw[4 * i + 1], hiw[4 * i + 2], hiw[4 * i + 3]);
-    dl[i] = make_uint4(low[4 * i], low[4 * i + 1], low[4 * i + 2], low[4 * i + 3]);
-  }
-  R.gx[((int64_t)g * 2) * TP + t] = fac;
-  R.gx[((int64_t)g * 2 + 1) * TP + t] = sum;
 }
 
 // ------------------------------------------------------------------ host
@@ -904,9 +947,7 @@ template <int TP, int MP>
 int launch_dec8_t(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx, size_t ws_cap) {
   using C = D8Cfg<TP>;
   static D8Args<MP> args;
-  static PrepArgs prep;
   memset(&args, 0, sizeof(args));
-  memset(&prep, 0, sizeof(prep));
   const int sms = sm_count();
 
   // regions: distinct activation blocks (x, K, lda)
@@ -923,11 +964,11 @@ int launch_dec8_t(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn
       const int G = (int)(P.K / 64);
       int r = -1;
       for (int i = 0; i < nreg; ++i)
-        if (prep.r[i].x == P.A && prep.r[i].K == (int)P.K && prep.r[i].lda == P.lda) r = i;
+        if (args.prep[i].x == P.A && args.prep[i].K == (int)P.K && args.prep[i].lda == P.lda) r = i;
       if (r < 0) {
         if (nreg >= MP) return TP_OK;
         r = nreg++;
-        PrepRegion &R = prep.r[r];
+        PrepRegion &R = args.prep[r];
         R.x = static_cast<const uint16_t *>(P.A);
         R.lda = P.lda;
         R.K = (int)P.K;
@@ -1021,11 +1062,11 @@ int launch_dec8_t(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn
   const int64_t slot_floats = slots * 128 * TP;
   float *ws = nullptr;
   int *cnt = nullptr;
-  int rc = get_ws(ctx, (size_t)prep_bytes + (size_t)slot_floats * sizeof(float), 2, &ws, &cnt);
+  int rc = get_ws(ctx, (size_t)prep_bytes + (size_t)slot_floats * sizeof(float), 3, &ws, &cnt);
   if (rc) return rc;
   uint8_t *wsb = reinterpret_cast<uint8_t *>(ws);
   for (int r = 0; r < nreg; ++r) {
-    PrepRegion &R = prep.r[r];
+    PrepRegion &R = args.prep[r];
     R.xq = wsb + reg_off[r];
     R.gx = reinterpret_cast<float *>(wsb + reg_off[r] + (int64_t)2 * TP * R.K);
     args.gx[r] = R.gx;
@@ -1037,24 +1078,22 @@ int launch_dec8_t(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn
   }
   int64_t trace_cap = 0;
   trace_buffer(&args.trace, &trace_cap);
-  prep.nregions = nreg;
-  prep.items = items;
-  prep.trace = args.trace;
+  args.nprep = nreg;
+  args.prep_items = items;
   args.njobs = p.njobs;
   args.total_units = (int)units;
   args.out_dt = p.out_dt;
   args.ws = reinterpret_cast<float *>(wsb + prep_bytes);
   args.work = cnt;
   args.done = cnt + 1;
+  args.prepped = cnt + 2;
   args.status = p.status;
   args.wait_ns = (uint64_t)p.wait_ns;
   // kind::f8f6f4 instruction descriptor: D f32, A and B E4M3 (format 0), both
   // K-major, M = 128, N = 2 TP
   args.idesc = (1u << 4) | ((uint32_t)(C::N >> 3) << 17) | ((128u >> 4) << 24);
 
-  static bool pdone[64] = {false}, kdone[64] = {false};
-  rc = d8_launch(q4_dec8_prep_kernel<TP>, prep, (items + 255) / 256, 256, 0, pdone, s, "q4_dec8_prep_kernel");
-  if (rc) return rc;
+  static bool kdone[64] = {false};
   const int grid = args.total_units < sms ? args.total_units : sms;
   rc = d8_launch(q4_dec8_kernel<TP, MP>, args, grid, kD8Threads, C::SMEM, kdone, s, "q4_dec8_kernel");
   if (rc == TP_OK && slots > 0) {  // ordered sums of the split tiles

@@ -139,6 +139,12 @@ __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.b
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// The same for global memory: generic-proxy accesses before it are ordered
+// before later tensor or bulk copies (async proxy) of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
