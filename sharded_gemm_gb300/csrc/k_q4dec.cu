@@ -538,9 +538,9 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
             ok = false;
             break;
           }
-          // The activation stream waits for the prepared activations; the
-          // codes stream issues its first stages before that.
-          if (!prep_ok && (!codes || seq >= kD8PreStages)) {
+          // The codes stream issues its first stages before the prepared
+          // activations are ready, then waits for them too.
+          if (!prep_ok && codes && seq >= kD8PreStages) {
             if (!mbar_wait(smem_u32(&xready_bar), 0, lim, a.status, &abort_sh)) {
               ok = false;
               break;
@@ -561,9 +561,15 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
           } else {
             const uint32_t base = obase + st * C::OP_BYTES;
             mbar_arrive_expect_tx(fb, C::OP_TX);
-            tma_load_3d(base + C::B_OFF, &a.xmaps[P.region], fb, 0, 0, gs / 2);  // chunks gs/2 .. gs/2 + 3
             tma_load_2d(base + C::S_OFF, &a.smaps[P.smap], fb, gs, y);
             tma_load_2d(base + C::Q_OFF, &a.qmaps[P.qmap], fb, gs, y);
+            if (!prep_ok) {  // the scales and biases above need no prepared activations
+              if (!mbar_wait(smem_u32(&xready_bar), 0, lim, a.status, &abort_sh))
+                ok = false;  // the copies below are still issued: the stage completes before teardown
+              fence_proxy_async_global();  // the tensor copies below read what other threads wrote
+              prep_ok = true;
+            }
+            tma_load_3d(base + C::B_OFF, &a.xmaps[P.region], fb, 0, 0, gs / 2);  // chunks gs/2 .. gs/2 + 3
             bulk_load(base + C::GX_OFF, a.gx[P.region] + (int64_t)gs * 2 * TP, C::GX_BYTES, fb);
           }
           usedmask |= 1u << st;
@@ -572,6 +578,7 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
             st = 0;
             ph ^= 1;
           }
+          if (!ok) break;
         }
       }
       if (!ok)  // let the copies in flight land before the CTA's memory goes away
