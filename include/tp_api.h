@@ -536,6 +536,17 @@ int tp_q4_sharded_to_all_noalloc(int N, const void *const *x, int64_t T, int64_t
  */
 int tp_debug_wait_timeout(int64_t limit_ns, tp_stream_t stream);
 
+/*
+ * Check of the 8-bit 4-bit decode's fallback (no counterpart on the pages).
+ * With on != 0, every later launch of that kernel (T <= 16, tp_q4_* calls)
+ * has each CTA prepare every activation item itself instead of waiting for
+ * the launch-wide count of the other CTAs' shares: the path a CTA takes when
+ * its peers are not resident.  The prepared values are the same either way,
+ * so the outputs are bit-identical.  on = 0 restores the default.  Process
+ * wide; returns TP_OK.
+ */
+int tp_debug_prep_alone(int on);
+
 #ifdef __cplusplus
 }
 #endif

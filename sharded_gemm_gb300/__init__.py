@@ -106,6 +106,7 @@ def _load() -> ctypes.CDLL:
             "tp_q4_all_to_sharded": ([i32, vp, i64, i64, vpp, vpp, vpp, i32, i64, vpp, vpp, i64, i32, vp], i32),
             "tp_q4_sharded_to_all": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
             "tp_debug_wait_timeout": ([i64, vp], i32),
+            "tp_debug_prep_alone": ([i32], i32),
             "tp_set_trace": ([vp, i64], i32),
             "tp_q4_sharded_to_all_noalloc": ([i32, vpp, i64, i64, vpp, vpp, vpp, i32, i64, vp, vp, i64, i32, vp], i32),
         }
@@ -279,6 +280,10 @@ def tp_query_status(stream=None) -> int:
 
 def tp_debug_wait_timeout(limit_ns: int, stream=None) -> None:
     _check(lib().tp_debug_wait_timeout(limit_ns, _stream(stream)))
+
+
+def tp_debug_prep_alone(on: bool) -> None:
+    _check(lib().tp_debug_prep_alone(1 if on else 0))
 
 
 def tp_shard_weight(w, axis: int, segments: int, N: int, shards=None, stream=None):

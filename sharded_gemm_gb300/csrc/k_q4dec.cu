@@ -60,6 +60,7 @@
 #include <cuda_fp16.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -151,6 +152,7 @@ struct D8Args {
   const float *gx[MP];                          // per region: [groups][2][TP] floats
   PrepRegion prep[MP];                          // per region: the pre-pass's input and outputs
   int nprep, prep_items;
+  uint64_t prep_alone_ns;  // wait for the other CTAs' shares at most this long (0: not at all)
   int njobs, total_units, out_dt;
   uint32_t idesc;
   float *ws;
@@ -737,14 +739,14 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
         atomicAdd(a.prepped, 1);
         const uint64_t t0 = globaltimer_ns();
         int all = 0;
-        for (;;) {
+        for (; a.prep_alone_ns > 0;) {
           int v;
           asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.prepped) : "memory");
           if (v >= (int)gridDim.x) {
             all = 1;
             break;
           }
-          if (globaltimer_ns() - t0 > kD8PrepAloneNs || abort_sh) break;
+          if (globaltimer_ns() - t0 > a.prep_alone_ns || abort_sh) break;
           __nanosleep(64);
         }
         prep_alone_sh = !all;
@@ -910,6 +912,7 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
 
 // ------------------------------------------------------------------ host
 std::mutex g_d8_mu;
+std::atomic<bool> g_d8_prep_alone{false};
 
 bool al16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
@@ -1086,6 +1089,7 @@ int launch_dec8_t(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn
   int64_t trace_cap = 0;
   trace_buffer(&args.trace, &trace_cap);
   args.nprep = nreg;
+  args.prep_alone_ns = g_d8_prep_alone.load() ? 0 : kD8PrepAloneNs;
   args.prep_items = items;
   args.njobs = p.njobs;
   args.total_units = (int)units;
@@ -1116,6 +1120,8 @@ int launch_dec8_t(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn
 }
 
 }  // namespace
+
+void set_dec8_prep_alone(bool on) { g_d8_prep_alone.store(on); }
 
 int launch_q4_dec8(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx,
                    size_t ws_cap) {

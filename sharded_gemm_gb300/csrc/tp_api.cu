@@ -763,6 +763,11 @@ int tp_q4_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K,
   return dispatch(p, (cudaStream_t)stream);
 }
 
+int tp_debug_prep_alone(int on) {
+  set_dec8_prep_alone(on != 0);
+  return TP_OK;
+}
+
 int tp_debug_wait_timeout(int64_t limit_ns, tp_stream_t stream) {
   if (limit_ns < 1000000LL || limit_ns > 60000000000LL)
     return set_error(TP_ERR_INVALID_ARG, "limit %lld ns outside [1e6, 6e10]", (long long)limit_ns);

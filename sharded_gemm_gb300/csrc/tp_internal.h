@@ -126,6 +126,9 @@ int launch_q4_gemv(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceF
 // ws_cap: the most workspace bytes get_ws can supply (the split is chosen to fit).
 int launch_q4_dec8(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn get_ws, void *ctx,
                    size_t ws_cap);
+// Debug: every CTA of later 8-bit decode launches prepares all activation
+// items itself instead of waiting for the launch-wide count (tp_debug_prep_alone).
+void set_dec8_prep_alone(bool on);
 int launch_shard(const void *w, int64_t rows, int64_t cols, int elem_bytes, int axis,
                  int segments, int N, void *const *shards, cudaStream_t s);
 int launch_quantize(const float *w, int64_t rows, int64_t K, uint32_t *wq, void *scales,

@@ -776,6 +776,41 @@ def test_q4_sharded_to_all(policy, T, Kn, O, N):
     check_close(to_host(y), ref, "q4 row")
 
 
+# The 8-bit decode's fallback for CTAs whose peers are not resident: each CTA
+# prepares every activation item itself instead of waiting for the launch-wide
+# count.  The prepared values are the same, so the outputs must be the same
+# bytes as the default path's; both sides span several 128-row tiles, ragged
+# last tiles and (row-parallel) range splits across rank boundaries.
+@pytest.mark.parametrize("layer,T", [("col", 16), ("col", 5), ("row", 16), ("row", 8)])
+def test_q4_dec8_prepare_alone_bit_identical(layer, T):
+    N = 4
+    if layer == "col":
+        K, On = 1536, 200
+        x = to_device(rand_bf16((T, K)), "bf16")
+        pq, ps, pb = _q4_host(On * N, K, 7 + T)
+        shards = [tp.tp_shard_weight(to_device(a, k), 0, 1, N) for a, k in ((pq, "u32"), (ps, "f16"), (pb, "f16"))]
+        run = lambda: torch.cat(tp.tp_q4_all_to_sharded(x, *shards, out_dtype=torch.float32), dim=1)
+    else:
+        Kn, O = 3584, 300
+        xs = tp.tp_shard_weight(to_device(rand_bf16((T, Kn * N)), "bf16"), -1, 1, N)
+        pq, ps, pb = _q4_host(O, Kn * N, 11 + T)
+        shards = [tp.tp_shard_weight(to_device(a, k), -1, 1, N) for a, k in ((pq, "u32"), (ps, "f16"), (pb, "f16"))]
+        b = to_device((RNG.standard_normal(O) * 0.1).astype(np.float32), "f32")
+        run = lambda: tp.tp_q4_sharded_to_all(xs, *shards, bias=b)
+    y0 = run().clone()
+    _status_ok()
+    try:
+        tp.tp_debug_prep_alone(True)
+        y1 = run().clone()
+        _status_ok()
+    finally:
+        tp.tp_debug_prep_alone(False)
+    y2 = run().clone()
+    _status_ok()
+    assert to_host(y1).tobytes() == to_host(y0).tobytes()
+    assert to_host(y2).tobytes() == to_host(y0).tobytes()
+
+
 def _range_rows(T, K, seed):
     """Activation rows spanning the bfloat16 range, for the 4-bit prefill
     (T > 16): rows far above the float16 maximum (|x| ~ 1e6 > 65504), rows of
