@@ -77,43 +77,43 @@ def load_peaks() -> dict:
 # An entry is reported only while its kernel family's sources hash to the value
 # in TRAFFIC_SOURCES, since a changed kernel needs a new capture (the hash covers
 # the code, not the comments).
-TRAFFIC_SOURCES = {"umma": "9c42b579d88c39d3", "q4": "15328bb74f90e3a9", "mx": "36edcb50399fb9e7"}
+TRAFFIC_SOURCES = {"umma": "4a2be1735e5dffc0", "q4": "917dbf235150a0de", "mx": "635f7418c2053a66"}
 TRAFFIC = {
-    ("mlp", "tp_all_to_sharded"): 94351616,
-    ("mlp", "tp_sharded_to_all"): 104192256,
-    ("mlp_ag_rs", "tp_gathered_to_sharded"): 93484032,
-    ("mlp_ag_rs", "tp_sharded_to_sharded"): 104566272,
-    ("ffn_gated", "tp_gated_all_to_sharded"): 192219648,
-    ("ffn_gated", "tp_sharded_to_all"): 104792320,
-    ("summa2", "tp_summa"): 1087090432,
-    ("summa4", "tp_summa"): 1121469184,
-    ("qkv1", "tp_all_to_sharded(qkv)"): 101331456,
-    ("qkv1", "tp_sharded_to_all(o)"): 33677056,
-    ("qkv1", "tp_all_to_sharded(lm_head)"): 413271552,
-    ("qkv16", "tp_all_to_sharded(qkv)"): 101381376,
-    ("qkv16", "tp_sharded_to_all(o)"): 33777920,
-    ("qkv16", "tp_all_to_sharded(lm_head)"): 418281472,
-    ("qkv2048", "tp_all_to_sharded(qkv)"): 148572928,
-    ("qkv2048", "tp_sharded_to_all(o)"): 65743104,
-    ("qkv2048", "tp_all_to_sharded(lm_head)"): 960369664,
-    ("q4_1", "tp_q4_all_to_sharded"): 132354560,
-    ("q4_1", "tp_q4_sharded_to_all"): 132802304,
-    ("q4_16", "tp_q4_all_to_sharded"): 135540224,
-    ("q4_16", "tp_q4_sharded_to_all"): 138573824,
-    ("q4_256", "tp_q4_all_to_sharded"): 164937984,
-    ("q4_256", "tp_q4_sharded_to_all"): 232049408,
-    ("mx_1", "tp_mx_all_to_sharded"): 242231040,
-    ("mx_1", "tp_mx_sharded_to_all"): 242233088,
-    ("mx_16", "tp_mx_all_to_sharded"): 245936128,
-    ("mx_16", "tp_mx_sharded_to_all"): 253933568,
-    ("mx_256", "tp_mx_all_to_sharded"): 292743424,
-    ("mx_256", "tp_mx_sharded_to_all"): 320696064,
-    ("mlp_bwd", "tp_sharded_to_all_dx"): 93768448,
-    ("mlp_bwd", "tp_sharded_dw(w2)"): 139603968,
-    ("mlp_bwd", "tp_bias_grad(b2)"): 2398720,
-    ("mlp_bwd", "tp_all_to_sharded_dx"): 163256320,
-    ("mlp_bwd", "tp_sharded_dw(w1)"): 137828864,
-    ("mlp_bwd", "tp_bias_grad(b1)"): 12615424,
+    ("mlp", "tp_all_to_sharded"): 94262528,
+    ("mlp", "tp_sharded_to_all"): 103596288,
+    ("mlp_ag_rs", "tp_gathered_to_sharded"): 93495808,
+    ("mlp_ag_rs", "tp_sharded_to_sharded"): 104035328,
+    ("ffn_gated", "tp_gated_all_to_sharded"): 192644864,
+    ("ffn_gated", "tp_sharded_to_all"): 104138752,
+    ("summa2", "tp_summa"): 1087345664,
+    ("summa4", "tp_summa"): 1121416960,
+    ("qkv1", "tp_all_to_sharded(qkv)"): 101042176,
+    ("qkv1", "tp_sharded_to_all(o)"): 33658624,
+    ("qkv1", "tp_all_to_sharded(lm_head)"): 413223680,
+    ("qkv16", "tp_all_to_sharded(qkv)"): 101409792,
+    ("qkv16", "tp_sharded_to_all(o)"): 33768960,
+    ("qkv16", "tp_all_to_sharded(lm_head)"): 417971200,
+    ("qkv2048", "tp_all_to_sharded(qkv)"): 149106944,
+    ("qkv2048", "tp_sharded_to_all(o)"): 65795072,
+    ("qkv2048", "tp_all_to_sharded(lm_head)"): 962912768,
+    ("q4_1", "tp_q4_all_to_sharded"): 132643072,
+    ("q4_1", "tp_q4_sharded_to_all"): 132956416,
+    ("q4_16", "tp_q4_all_to_sharded"): 134749696,
+    ("q4_16", "tp_q4_sharded_to_all"): 138810880,
+    ("q4_256", "tp_q4_all_to_sharded"): 164696320,
+    ("q4_256", "tp_q4_sharded_to_all"): 234857728,
+    ("mx_1", "tp_mx_all_to_sharded"): 242230784,
+    ("mx_1", "tp_mx_sharded_to_all"): 242233600,
+    ("mx_16", "tp_mx_all_to_sharded"): 246192384,
+    ("mx_16", "tp_mx_sharded_to_all"): 253548288,
+    ("mx_256", "tp_mx_all_to_sharded"): 290115328,
+    ("mx_256", "tp_mx_sharded_to_all"): 321110784,
+    ("mlp_bwd", "tp_sharded_to_all_dx"): 94145792,
+    ("mlp_bwd", "tp_sharded_dw(w2)"): 140020224,
+    ("mlp_bwd", "tp_bias_grad(b2)"): 2395904,
+    ("mlp_bwd", "tp_all_to_sharded_dx"): 163216896,
+    ("mlp_bwd", "tp_sharded_dw(w1)"): 137746944,
+    ("mlp_bwd", "tp_bias_grad(b1)"): 12583936,
 }
 
 # The sources each family of kernels is built from (the shared host code and
