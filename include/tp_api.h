@@ -116,7 +116,9 @@ int tp_set_wait_limit_ns(int64_t limit_ns);
  * stage s, at word index 4s + p: 17/18 the MMA thread issued / committed it,
  * 12/13/14 epilogue warp 6 saw it / had loaded it / had applied it.  Per CTA
  * b, at index b: 28 the SM id + 1, 30/31 the CTA's start / end, and 29/10
- * the start / end of its share of the activation pre-pass.
+ * the start / end of its share of the activation pre-pass.  The ordered split
+ * sum that follows a split launch (4-bit and mxfp8): per block b, 21/22 its
+ * start (after the programmatic-launch wait) and end.
  * 16-bit decode kernel (other shapes): 1 producer issued the stage's loads;
  * 2/3/4 the MMA thread saw the stage's data / A operand / free accumulator,
  * 5 it committed the stage; 6/7 converter warp 2 saw the data / a free A

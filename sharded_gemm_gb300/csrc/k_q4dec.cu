@@ -45,8 +45,8 @@
 // (tcgen05.st, one wait per stage), so the next stage is expanded while the
 // MMAs read this one.  Warp 1 issues the stage's 16 MMAs (A from TMEM, B
 // from shared memory) into 4 accumulator slots of two groups each, with 6
-// barrier waits and 6 commits per stage: per-group handshakes cost more
-// than the MMAs they guard.  Warps 6-9 load a slot's accumulators while the
+// barrier waits and 3 commits per stage (one per half-stage, one for the
+// stage): per-group handshakes cost more than the MMAs they guard.  Warps 6-9 load a slot's accumulators while the
 // previous slot's are applied and release it.  At a unit's end a unit that
 // covers its whole job stores y; otherwise the epilogue warps store its
 // float32 partial to the unit's workspace slot and go on, and a second
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(kD8Threads, 1) q4_dec8_kernel(const __grid_con
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // One stage = A half h (8 groups in TMEM), the stage's activation tile,
-    // and the 4 D pair slots: 6 barrier waits and 6 commits for 16 MMAs.
+    // and the 4 D pair slots: 6 barrier waits and 3 commits for 16 MMAs.
     if (lane == 0) {
       int os = 0, h = 0, seq = 0, us = 0;
       uint32_t oph = 0, hph = 0, dph = 0, uph = 0;
