@@ -77,7 +77,7 @@ def load_peaks() -> dict:
 # An entry is reported only while its kernel family's sources hash to the value
 # in TRAFFIC_SOURCES, since a changed kernel needs a new capture (the hash covers
 # the code, not the comments).
-TRAFFIC_SOURCES = {"umma": "4a2be1735e5dffc0", "q4": "917dbf235150a0de", "mx": "635f7418c2053a66"}
+TRAFFIC_SOURCES = {"umma": "4a2be1735e5dffc0", "q4": "56407a1fb0151c48", "mx": "635f7418c2053a66"}
 TRAFFIC = {
     ("mlp", "tp_all_to_sharded"): 94262528,
     ("mlp", "tp_sharded_to_all"): 103596288,
@@ -96,12 +96,12 @@ TRAFFIC = {
     ("qkv2048", "tp_all_to_sharded(qkv)"): 149106944,
     ("qkv2048", "tp_sharded_to_all(o)"): 65795072,
     ("qkv2048", "tp_all_to_sharded(lm_head)"): 962912768,
-    ("q4_1", "tp_q4_all_to_sharded"): 132643072,
-    ("q4_1", "tp_q4_sharded_to_all"): 132956416,
-    ("q4_16", "tp_q4_all_to_sharded"): 134749696,
-    ("q4_16", "tp_q4_sharded_to_all"): 138810880,
-    ("q4_256", "tp_q4_all_to_sharded"): 164696320,
-    ("q4_256", "tp_q4_sharded_to_all"): 234857728,
+    ("q4_1", "tp_q4_all_to_sharded"): 132331520,
+    ("q4_1", "tp_q4_sharded_to_all"): 132838912,
+    ("q4_16", "tp_q4_all_to_sharded"): 132990208,
+    ("q4_16", "tp_q4_sharded_to_all"): 136736256,
+    ("q4_256", "tp_q4_all_to_sharded"): 163230976,
+    ("q4_256", "tp_q4_sharded_to_all"): 235825408,
     ("mx_1", "tp_mx_all_to_sharded"): 242230784,
     ("mx_1", "tp_mx_sharded_to_all"): 242233600,
     ("mx_16", "tp_mx_all_to_sharded"): 246192384,

@@ -506,7 +506,7 @@ int tp_q4_sharded_to_all(int N, const void *const *x, int64_t T, int64_t K,
  * returns TP_ERR_UNSUPPORTED with the sizes in the message and launches
  * nothing.  For decode-sized calls (T <= 16) the K split is chosen to fit
  * the array: the down projection of an 8192 x 28672 layer split 8 ways
- * (T = 16) takes 8.31 MB, its prepared activations and 14 partials per
+ * (T = 16) takes 4.64 MB, its prepared activations and 7 partials per
  * 128-row tile.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, no allocation); make that first call before any

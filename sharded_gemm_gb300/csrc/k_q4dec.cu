@@ -60,7 +60,9 @@
 #include <cuda_fp16.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -916,25 +918,37 @@ std::atomic<bool> g_d8_prep_alone{false};
 
 bool al16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
-// Ranges per tile.  Units are dispensed at run time, so the time is about
-// the even share of all stages plus a per-unit cost, plus the last unit (the
-// tail) and, with more than one range, the ordered split sum launch; all in
-// stage times (a stage streams 36 KB of codes, scales and biases).
+// Ranges per tile.  Units are dispensed at run time, but the SMs stream at
+// about the same rate, so the time is about the whole rounds of units the
+// SMs run (units / SMs rounded up, times the longest unit plus a per-unit
+// cost of 0.3 stage times), or the even share of all stages where that is
+// larger; then, with more than one range, the ordered split sum: a fixed
+// part and a part that grows with the float32 partials it reads back (about
+// 0.39 stage times per MB).  All in stage times (a stage streams 36 KB of
+// codes, scales and biases per SM).  Fitted to a sweep of the ranges at
+// T = 16: the column layer's 16 stages a tile in 2 ranges took 1.2 us less
+// per call than in 4 (3, 6, 8 slower); the row layer's 56 in 7 ranges as
+// long as in 14, in 8, 10, 19 or 28 longer (8 ranges: 4 rounds of 7 stages
+// against 3 of 8).
 struct D8Split {
   int ranges;
   double cost;
 };
-D8Split d8_ranges(const int64_t *tiles, const int *nst, int njobs, int sms, int c) {
-  double stages = 0, units = 0;
+D8Split d8_ranges(const int64_t *tiles, const int *nst, int njobs, int sms, int c, int TP) {
+  double stages = 0, units = 0, slots = 0;
   int longest = 0;
   for (int j = 0; j < njobs; ++j) {
     const int len = (nst[j] + c - 1) / c;
     const int r = (nst[j] + len - 1) / len;
     stages += (double)tiles[j] * nst[j];
     units += (double)tiles[j] * r;
+    if (r > 1) slots += (double)tiles[j] * r;
     if (len > longest) longest = len;
   }
-  return D8Split{c, (stages + 0.5 * units) / sms + longest + (c > 1 ? 1.5 : 0.0)};
+  const double share = (stages + 0.3 * units) / sms;
+  const double rounds = std::ceil(units / sms) * (longest + 0.3);
+  const double slot_mb = slots * 128.0 * TP * 4.0 / 1e6;
+  return D8Split{c, std::max(share, rounds) + (c > 1 ? 1.5 + 0.39 * slot_mb : 0.0)};
 }
 
 template <typename K, typename A>
@@ -1015,7 +1029,7 @@ int launch_dec8_t(const Problem &p, cudaStream_t s, bool *handled, GvWorkspaceFn
     }
     if (!useful) continue;
     if (cc > 1 && (size_t)prep_bytes + (size_t)sl * 128 * TP * sizeof(float) > ws_cap) continue;
-    const D8Split d = d8_ranges(tiles_j, nst_j, p.njobs, sms, cc);
+    const D8Split d = d8_ranges(tiles_j, nst_j, p.njobs, sms, cc, TP);
     if (d.cost < best - 1e-9) {
       best = d.cost;
       c = cc;
